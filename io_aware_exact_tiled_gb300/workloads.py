@@ -1,0 +1,124 @@
+"""Seeded synthetic inputs for exact tiled attention.
+
+This module only draws random tensors and structure (key lengths, tile masks).
+It holds none of the attention arithmetic, so both the CUDA path and the CPU
+oracle can take their inputs from here without sharing any of the method.
+
+Workloads (shapes follow the BERT-large / GPT-2 / long-context / block-sparse
+settings used to evaluate fused exact attention; weights and datasets are not
+needed because attention inputs are drawn directly):
+
+  tiny      [1, 1, 128, 64]    fp32, no mask
+  bert      [8, 16, 512, 64]   bf16, key padding, valid length ~ U{256..512}
+  gpt2      [8, 12, 1024, 64]  bf16, causal
+  long4k    [1, 32, 4096, 128] bf16, causal, K rows scaled by 2
+  long8k    [1, 32, 8192, 128] bf16, causal, K rows scaled by 2
+  sparse16k [2, 16, 16384, 128] bf16, 128x128 tile mask: the diagonal plus
+            floor(0.125 * (T*T - T)) other tiles, T = N / 128
+
+Recipe: one CPU ``torch.Generator`` seeded with ``seed`` draws standard normal
+fp32 tensors in the order Q, K, V, dO; then the key lengths; then the tile
+mask. K is multiplied by ``k_scale`` (exact in bf16) and all four tensors are
+rounded to the working dtype with round-to-nearest-even.
+"""
+
+from __future__ import annotations
+
+import dataclasses
+import math
+from typing import Optional
+
+import torch
+
+TILE = 128
+
+
+@dataclasses.dataclass(frozen=True)
+class Workload:
+    name: str
+    B: int
+    H: int
+    N: int
+    d: int
+    dtype: str = "bf16"          # "bf16" or "fp32"
+    causal: bool = False
+    kv_len_range: Optional[tuple] = None   # inclusive (lo, hi) for key padding
+    block_density: Optional[float] = None  # fraction of off-diagonal tiles kept
+    k_scale: float = 1.0
+    backward: bool = True
+
+    @property
+    def scale(self) -> float:
+        return 1.0 / math.sqrt(self.d)
+
+    @property
+    def torch_dtype(self):
+        return torch.bfloat16 if self.dtype == "bf16" else torch.float32
+
+    def with_(self, **kw) -> "Workload":
+        return dataclasses.replace(self, **kw)
+
+
+WORKLOADS = {
+    "tiny": Workload("tiny", 1, 1, 128, 64, dtype="fp32", backward=False),
+    "bert": Workload("bert", 8, 16, 512, 64, kv_len_range=(256, 512)),
+    "gpt2": Workload("gpt2", 8, 12, 1024, 64, causal=True),
+    "long4k": Workload("long4k", 1, 32, 4096, 128, causal=True, k_scale=2.0),
+    "long8k": Workload("long8k", 1, 32, 8192, 128, causal=True, k_scale=2.0),
+    "sparse16k": Workload("sparse16k", 2, 16, 16384, 128, block_density=0.125),
+}
+
+
+def make_blockmask(T: int, density: float, gen: torch.Generator) -> torch.Tensor:
+    """uint8 [T, T] tile mask: every diagonal tile kept plus exactly
+    floor(density * (T*T - T)) off-diagonal tiles chosen uniformly without
+    replacement (one seeded permutation of the off-diagonal positions)."""
+    keep = torch.eye(T, dtype=torch.uint8)
+    off = [(i, j) for i in range(T) for j in range(T) if i != j]
+    n_keep = int(math.floor(density * len(off)))
+    perm = torch.randperm(len(off), generator=gen)[:n_keep]
+    for p in perm.tolist():
+        i, j = off[p]
+        keep[i, j] = 1
+    return keep
+
+
+@dataclasses.dataclass
+class Inputs:
+    q: torch.Tensor
+    k: torch.Tensor
+    v: torch.Tensor
+    do: torch.Tensor
+    kv_len: Optional[torch.Tensor]    # int32 [B] or None
+    blockmask: Optional[torch.Tensor]  # uint8 [T, T] or None
+    scale: float
+    causal: bool
+
+
+def make_inputs(w: Workload, seed: int = 0, device: str = "cpu") -> Inputs:
+    """Draw the seeded inputs of workload ``w``.
+
+    ``device="cpu"`` follows the recipe above exactly. ``device="cuda"`` draws
+    the same distributions with a CUDA generator (different numbers, same
+    recipe), which is much faster for the largest shapes; whichever device
+    draws, both sides of a comparison receive the same tensors.
+    """
+    gen = torch.Generator(device=device)
+    gen.manual_seed(seed)
+    shape = (w.B, w.H, w.N, w.d)
+    q = torch.randn(shape, generator=gen, device=device, dtype=torch.float32)
+    k = torch.randn(shape, generator=gen, device=device, dtype=torch.float32)
+    v = torch.randn(shape, generator=gen, device=device, dtype=torch.float32)
+    do = torch.randn(shape, generator=gen, device=device, dtype=torch.float32)
+    if w.k_scale != 1.0:
+        k.mul_(w.k_scale)
+    kv_len = None
+    blockmask = None
+    cpu_gen = gen if device == "cpu" else torch.Generator().manual_seed(seed + 1)
+    if w.kv_len_range is not None:
+        lo, hi = w.kv_len_range
+        kv_len = torch.randint(lo, hi + 1, (w.B,), generator=cpu_gen, dtype=torch.int64).to(torch.int32)
+    if w.block_density is not None:
+        blockmask = make_blockmask(w.N // TILE, w.block_density, cpu_gen)
+    dt = w.torch_dtype
+    return Inputs(q.to(dt), k.to(dt), v.to(dt), do.to(dt), kv_len, blockmask, w.scale, w.causal)
