@@ -1,0 +1,135 @@
+/*
+ * fa.h -- C ABI of libfa.so: fused, tiled, exact softmax attention on GB300
+ * (sm_103a), forward and backward.
+ *
+ * What is computed ("FlashAttention: making attention IO-aware", sections
+ * "Attention is memory-bound", "Tiling: never materialise S", "Online
+ * softmax", "The backward pass: recompute, don't store"):
+ *
+ *   S = scale * Q K^T (+ mask),  P = softmax(S) row-wise,  O = P V,
+ *   L = m + log(l) per query row (natural log; m = row max, l = sum exp(S - m))
+ *
+ * and, for the backward pass, the gradients of <dO, O>:
+ *
+ *   D = rowsum(dO * O),  dV = P^T dO,  dP = dO V^T,  dS = P * (dP - D),
+ *   dQ = scale * dS K,  dK = scale * dS^T Q,
+ *
+ * with P recomputed tile by tile from Q, K and L. No N x N matrix is ever
+ * written to device memory.
+ *
+ * Masks (all optional, combined with AND): causal (key j visible to query i
+ * iff j <= i; "FlashAttention-2" section: tiles above the diagonal are
+ * skipped), key padding (key j visible iff j < kv_len[b]; "Why is
+ * FlashAttention faster?", "Extra computation can still finish sooner"), and
+ * a 128 x 128 tile mask shared by every (batch, head) (block-sparse
+ * attention, "Counting the IO": masked tiles are skipped entirely). A query
+ * row that sees no key gets O = 0, L = -inf and contributes no gradient.
+ *
+ * Conventions shared by every entry point
+ * ---------------------------------------
+ * Layout: Q, K, V, O, dO, dQ, dK, dV are contiguous [B, H, N, d] row-major
+ *   arrays in device memory, all of the element type `dtype`; lse is a
+ *   contiguous float32 [B, H, N] array. Base pointers must be 16-byte aligned.
+ * Types: FA_BF16 (bfloat16 in and out, bf16 tensor-core products with fp32
+ *   accumulation) or FA_FP32 (float32 in and out, tf32 tensor-core products
+ *   with fp32 accumulation; forward pass only).
+ * Supported sizes: d in {64, 128}; N a positive multiple of 128;
+ *   B * H * N < 2^31. Other sizes return FA_ERR_UNSUPPORTED.
+ * blockmask: NULL or a device uint8 array [N/128, N/128]; entry [i][j] != 0
+ *   keeps the tile of query block i and key block j.
+ * kv_len: NULL or a device int32 array [B] with 0 <= kv_len[b] <= N.
+ * Ownership: the caller allocates and frees every buffer, including the
+ *   workspace; the library allocates no device memory and keeps no pointer
+ *   after a call returns.
+ * Streams: `stream` is a cudaStream_t (NULL = legacy default stream). Calls
+ *   are asynchronous with respect to the host: argument checks run on the host
+ *   and return an error before anything is launched; launch failures return
+ *   FA_ERR_CUDA; a device-side wait that gives up (a bounded wait that expired)
+ *   is reported by fa_get_status on the workspace of that call.
+ * Workspace: a device buffer of at least the size the matching
+ *   *_workspace_size function returns, 256-byte aligned. Its contents need not
+ *   be initialised. Two calls in flight at the same time need two workspaces.
+ */
+#ifndef FA_H_
+#define FA_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    FA_OK = 0,
+    FA_ERR_INVALID_ARG = 1, /* null pointer, bad alignment, negative size, ... */
+    FA_ERR_UNSUPPORTED = 2, /* valid request outside the supported sizes/types */
+    FA_ERR_CUDA = 3,        /* a CUDA runtime call or launch failed */
+    FA_ERR_TIMEOUT = 4      /* a device-side bounded wait gave up */
+} fa_status;
+
+typedef enum { FA_BF16 = 0, FA_FP32 = 1 } fa_dtype;
+
+/* Bytes of workspace fa_fwd needs for these sizes: the status word, plus
+ * room for a transposed fp32 copy of V, which FA_FP32 calls use (tf32
+ * tensor-core operands must be K-major). FA_BF16 calls need only 256 bytes
+ * but accept the full size. */
+size_t fa_fwd_workspace_size(int B, int H, int N, int d);
+
+/* Bytes of workspace fa_bwd needs: D = rowsum(dO * O) and L in log2 units
+ * (fp32 [B,H,N] each), the fp32 dQ accumulator [B,H,N,d] and the status
+ * word. */
+size_t fa_bwd_workspace_size(int B, int H, int N, int d);
+
+/*
+ * Forward pass ("Online softmax"; the tiled forward of "FlashAttention:
+ * making attention IO-aware"): writes O [B,H,N,d] and lse = L [B,H,N].
+ *   q, k, v   in,  device, [B,H,N,d] of `dtype`
+ *   o         out, device, [B,H,N,d] of `dtype`
+ *   lse       out, device, float32 [B,H,N], natural-log logsumexp of the
+ *             scaled, masked scores of each row
+ *   scale     multiplies Q K^T before the softmax (usually 1/sqrt(d))
+ *   causal    0 or 1
+ *   blockmask, kv_len  optional masks (see above)
+ *   workspace, ws_bytes  device scratch of fa_fwd_workspace_size bytes
+ * Errors: FA_ERR_INVALID_ARG, FA_ERR_UNSUPPORTED (nothing launched),
+ *         FA_ERR_CUDA (launch failed).
+ */
+fa_status fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int N, int d,
+                 float scale, int causal, const uint8_t* blockmask, const int32_t* kv_len, fa_dtype dtype,
+                 void* workspace, size_t ws_bytes, void* stream);
+
+/*
+ * Backward pass ("The backward pass: recompute, don't store"): given the
+ * forward inputs, its outputs O and lse, and dO, writes dQ, dK, dV.
+ *   q, k, v, o, dout  in,  device, [B,H,N,d] of `dtype` (FA_BF16 only)
+ *   lse               in,  device, float32 [B,H,N] from fa_fwd
+ *   dq, dk, dv        out, device, [B,H,N,d] of `dtype`
+ *   the remaining arguments as for fa_fwd; the masks must be the ones the
+ *   forward pass used.
+ * Runs three kernels on `stream`: D = rowsum(dO * O) (and zeroing of the dQ
+ * accumulator), the fused key-block kernel, and the dQ conversion.
+ */
+fa_status fa_bwd(const void* q, const void* k, const void* v, const void* o, const float* lse, const void* dout,
+                 void* dq, void* dk, void* dv, int B, int H, int N, int d, float scale, int causal,
+                 const uint8_t* blockmask, const int32_t* kv_len, fa_dtype dtype, void* workspace, size_t ws_bytes,
+                 void* stream);
+
+/* Synchronises `stream`, then reads and clears the device status word of
+ * `workspace` (of the fa_fwd or fa_bwd call that used it). Returns FA_OK or
+ * FA_ERR_TIMEOUT (a device-side wait gave up; the outputs are then invalid),
+ * or FA_ERR_CUDA if the stream reported an error. */
+fa_status fa_get_status(void* workspace, void* stream);
+
+/* Static, human-readable name of a status code. */
+const char* fa_status_string(fa_status s);
+
+/* Number of kernels the last successful fa_fwd / fa_bwd call launched on
+ * this host thread (for accounting in benchmarks). */
+int fa_last_launch_count(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* FA_H_ */

@@ -1,5 +1,17 @@
 """Fused, tiled, exact softmax attention for GB300 (sm_103a).
 
-The compute path is the C-ABI library ``libfa.so`` built from ``csrc/``; the
-Python layer only marshals arguments (see ``binding``).
+The compute path is the C-ABI library ``libfa.so`` built from ``csrc/``
+(declared in ``include/fa.h``); :mod:`.binding` only marshals arguments.
 """
+
+from .binding import (  # noqa: F401
+    FAError,
+    forward,
+    backward,
+    fwd_workspace_size,
+    bwd_workspace_size,
+    get_status,
+    last_launch_count,
+    load,
+    workspace,
+)

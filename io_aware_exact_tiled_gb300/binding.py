@@ -1,0 +1,177 @@
+"""ctypes binding of libfa.so (include/fa.h), argument marshalling only.
+
+Every step of the attention path runs in the CUDA kernels behind the C ABI;
+this module checks tensor properties, allocates outputs and workspace with
+PyTorch when the caller does not pass them, and forwards raw device pointers
+and the current CUDA stream. There is no fallback: if the library is missing
+or a call fails, an exception is raised.
+"""
+
+from __future__ import annotations
+
+import ctypes
+import math
+import os
+import re
+from typing import Optional
+
+import torch
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "libfa.so")
+HEADER_PATH = os.path.join(os.path.dirname(_PKG), "include", "fa.h")
+
+FA_OK, FA_ERR_INVALID_ARG, FA_ERR_UNSUPPORTED, FA_ERR_CUDA, FA_ERR_TIMEOUT = range(5)
+FA_BF16, FA_FP32 = 0, 1
+
+
+class FAError(RuntimeError):
+    def __init__(self, code: int, what: str):
+        self.code = code
+        super().__init__(f"{what}: {status_string(code)} ({code})")
+
+
+_lib = None
+
+
+def load(path: str = LIB_PATH) -> ctypes.CDLL:
+    """Load libfa.so and declare the C signatures. Raises if it is missing."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(path):
+        raise RuntimeError(
+            f"{path} is missing: build it first (python -c 'import __graft_entry__ as g; g.build()')")
+    lib = ctypes.CDLL(path)
+    vp, sz, i, f = ctypes.c_void_p, ctypes.c_size_t, ctypes.c_int, ctypes.c_float
+    lib.fa_fwd_workspace_size.argtypes = [i, i, i, i]
+    lib.fa_fwd_workspace_size.restype = sz
+    lib.fa_bwd_workspace_size.argtypes = [i, i, i, i]
+    lib.fa_bwd_workspace_size.restype = sz
+    lib.fa_fwd.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, f, i, vp, vp, i, vp, sz, vp]
+    lib.fa_fwd.restype = i
+    lib.fa_bwd.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, i, i, i, i, f, i, vp, vp, i, vp, sz, vp]
+    lib.fa_bwd.restype = i
+    lib.fa_get_status.argtypes = [vp, vp]
+    lib.fa_get_status.restype = i
+    lib.fa_status_string.argtypes = [i]
+    lib.fa_status_string.restype = ctypes.c_char_p
+    lib.fa_last_launch_count.argtypes = []
+    lib.fa_last_launch_count.restype = i
+    _lib = lib
+    return lib
+
+
+def declared_functions(header: str = HEADER_PATH):
+    """Names of the functions include/fa.h declares."""
+    text = open(header).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(fa_[a-z0-9_]+)\s*\(", text)))
+
+
+def status_string(code: int) -> str:
+    return load().fa_status_string(code).decode()
+
+
+def _ptr(t: Optional[torch.Tensor]):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream_handle(stream: Optional[torch.cuda.Stream]):
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+def _check_qkv(*ts: torch.Tensor):
+    q = ts[0]
+    for t in ts:
+        if t.device.type != "cuda":
+            raise ValueError("tensors must be on a CUDA device")
+        if not t.is_contiguous():
+            raise ValueError("tensors must be contiguous [B, H, N, d]")
+        if t.shape != q.shape or t.dtype != q.dtype:
+            raise ValueError("q, k, v (and o, dO) must share shape and dtype")
+    if q.dim() != 4:
+        raise ValueError("expected [B, H, N, d] tensors")
+    if q.dtype == torch.bfloat16:
+        return FA_BF16
+    if q.dtype == torch.float32:
+        return FA_FP32
+    raise ValueError("dtype must be bfloat16 or float32")
+
+
+def _mask_ptrs(blockmask, kv_len, q):
+    if blockmask is not None:
+        T = q.shape[2] // 128
+        if blockmask.dtype != torch.uint8 or blockmask.shape != (T, T) or not blockmask.is_contiguous():
+            raise ValueError(f"blockmask must be a contiguous uint8 [{T}, {T}] tensor")
+        if blockmask.device != q.device:
+            raise ValueError("blockmask must be on the same device")
+    if kv_len is not None:
+        if kv_len.dtype != torch.int32 or kv_len.shape != (q.shape[0],) or kv_len.device != q.device:
+            raise ValueError("kv_len must be an int32 [B] tensor on the same device")
+    return _ptr(blockmask), _ptr(kv_len)
+
+
+def fwd_workspace_size(B, H, N, d) -> int:
+    return load().fa_fwd_workspace_size(B, H, N, d)
+
+
+def bwd_workspace_size(B, H, N, d) -> int:
+    return load().fa_bwd_workspace_size(B, H, N, d)
+
+
+def workspace(nbytes: int, device) -> torch.Tensor:
+    """A device buffer usable as workspace (256-byte aligned by the allocator)."""
+    return torch.empty(max(256, nbytes), dtype=torch.uint8, device=device)
+
+
+def forward(q, k, v, scale: Optional[float] = None, causal: bool = False, blockmask=None, kv_len=None,
+            out=None, lse=None, ws=None, stream=None):
+    """O, L = fa_fwd(...). Returns (o [B,H,N,d], lse fp32 [B,H,N])."""
+    lib = load()
+    dtype = _check_qkv(q, k, v)
+    B, H, N, d = q.shape
+    scale = 1.0 / math.sqrt(d) if scale is None else float(scale)
+    o = torch.empty_like(q) if out is None else out
+    L = torch.empty((B, H, N), dtype=torch.float32, device=q.device) if lse is None else lse
+    if ws is None:
+        ws = workspace(lib.fa_fwd_workspace_size(B, H, N, d) if dtype == FA_FP32 else 256, q.device)
+    bm, kl = _mask_ptrs(blockmask, kv_len, q)
+    rc = lib.fa_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(L), B, H, N, d, scale, int(bool(causal)), bm, kl,
+                    dtype, _ptr(ws), ws.numel(), _stream_handle(stream))
+    if rc != FA_OK:
+        raise FAError(rc, "fa_fwd")
+    return o, L
+
+
+def backward(q, k, v, o, lse, do, scale: Optional[float] = None, causal: bool = False, blockmask=None,
+             kv_len=None, dq=None, dk=None, dv=None, ws=None, stream=None):
+    """dQ, dK, dV = fa_bwd(...). Returns (dq, dk, dv)."""
+    lib = load()
+    dtype = _check_qkv(q, k, v, o, do)
+    B, H, N, d = q.shape
+    if lse.dtype != torch.float32 or lse.shape != (B, H, N) or not lse.is_contiguous():
+        raise ValueError("lse must be a contiguous float32 [B, H, N] tensor")
+    scale = 1.0 / math.sqrt(d) if scale is None else float(scale)
+    dq = torch.empty_like(q) if dq is None else dq
+    dk = torch.empty_like(k) if dk is None else dk
+    dv = torch.empty_like(v) if dv is None else dv
+    if ws is None:
+        ws = workspace(lib.fa_bwd_workspace_size(B, H, N, d), q.device)
+    bm, kl = _mask_ptrs(blockmask, kv_len, q)
+    rc = lib.fa_bwd(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), _ptr(do), _ptr(dq), _ptr(dk), _ptr(dv),
+                    B, H, N, d, scale, int(bool(causal)), bm, kl, dtype, _ptr(ws), ws.numel(),
+                    _stream_handle(stream))
+    if rc != FA_OK:
+        raise FAError(rc, "fa_bwd")
+    return dq, dk, dv
+
+
+def get_status(ws: torch.Tensor, stream=None) -> int:
+    """Synchronise and read (then clear) the device status word of a workspace."""
+    return load().fa_get_status(_ptr(ws), _stream_handle(stream))
+
+
+def last_launch_count() -> int:
+    return load().fa_last_launch_count()

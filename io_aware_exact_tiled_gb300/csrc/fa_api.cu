@@ -1,0 +1,161 @@
+// C ABI of libfa.so (declared in include/fa.h): argument checks, workspace
+// carving, status word handling and dispatch to the kernel launchers.
+#include <cuda_runtime.h>
+#include <math.h>
+#include <stdint.h>
+#include <string.h>
+
+#include "fa.h"
+#include "fa_launch.h"
+
+namespace {
+
+constexpr size_t kStatusBytes = 256;
+thread_local int g_last_launches = 0;
+
+size_t align256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
+
+bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+// Shape checks shared by both passes.
+fa_status check_shape(int B, int H, int N, int d, float scale) {
+    if (B <= 0 || H <= 0 || N <= 0 || d <= 0) return FA_ERR_INVALID_ARG;
+    if (!(scale > 0.f) || !isfinite(scale)) return FA_ERR_INVALID_ARG;
+    if (d != 64 && d != 128) return FA_ERR_UNSUPPORTED;
+    if (N % 128 != 0) return FA_ERR_UNSUPPORTED;
+    if (static_cast<long long>(B) * H * N >= (1LL << 31)) return FA_ERR_UNSUPPORTED;
+    if (B > 65535 || (N / 128 + 1) / 2 > 65535) return FA_ERR_UNSUPPORTED;
+    return FA_OK;
+}
+
+fa_status map_cuda(cudaError_t e) { return e == cudaSuccess ? FA_OK : FA_ERR_CUDA; }
+
+}  // namespace
+
+extern "C" {
+
+size_t fa_fwd_workspace_size(int B, int H, int N, int d) {
+    if (B <= 0 || H <= 0 || N <= 0 || d <= 0) return 0;
+    // status word + room for an fp32 transposed copy of V (fp32 inputs only)
+    return kStatusBytes + align256(static_cast<size_t>(B) * H * N * d * sizeof(float));
+}
+
+size_t fa_bwd_workspace_size(int B, int H, int N, int d) {
+    if (B <= 0 || H <= 0 || N <= 0 || d <= 0) return 0;
+    const size_t rows = static_cast<size_t>(B) * H * N;
+    return kStatusBytes + 2 * align256(rows * sizeof(float)) + align256(rows * d * sizeof(float));
+}
+
+fa_status fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int N, int d,
+                 float scale, int causal, const uint8_t* blockmask, const int32_t* kv_len, fa_dtype dtype,
+                 void* workspace, size_t ws_bytes, void* stream) {
+    if (!q || !k || !v || !o || !lse || !workspace) return FA_ERR_INVALID_ARG;
+    if (dtype != FA_BF16 && dtype != FA_FP32) return FA_ERR_INVALID_ARG;
+    if (causal != 0 && causal != 1) return FA_ERR_INVALID_ARG;
+    fa_status st = check_shape(B, H, N, d, scale);
+    if (st != FA_OK) return st;
+    if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(o, 16) || !aligned(lse, 4) ||
+        !aligned(workspace, 256) || (kv_len && !aligned(kv_len, 4)))
+        return FA_ERR_INVALID_ARG;
+    if (dtype == FA_FP32 && d != 64) return FA_ERR_UNSUPPORTED;
+    const size_t need = dtype == FA_FP32 ? fa_fwd_workspace_size(B, H, N, d) : kStatusBytes;
+    if (ws_bytes < need) return FA_ERR_INVALID_ARG;
+
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    fa::FwdArgs a;
+    a.q = q;
+    a.k = k;
+    a.v = v;
+    a.o = o;
+    a.lse = lse;
+    a.B = B;
+    a.H = H;
+    a.N = N;
+    a.d = d;
+    a.scale = scale;
+    a.causal = causal;
+    a.blockmask = blockmask;
+    a.kv_len = kv_len;
+    a.fp32 = dtype == FA_FP32;
+    a.status = static_cast<int*>(workspace);
+    a.vt_scratch = static_cast<char*>(workspace) + kStatusBytes;
+    if (cudaMemsetAsync(a.status, 0, sizeof(int) * 4, s) != cudaSuccess) return FA_ERR_CUDA;
+    int n = 0;
+    st = map_cuda(fa::launch_fwd(a, s, &n));
+    if (st == FA_OK) g_last_launches = n;
+    return st;
+}
+
+fa_status fa_bwd(const void* q, const void* k, const void* v, const void* o, const float* lse, const void* dout,
+                 void* dq, void* dk, void* dv, int B, int H, int N, int d, float scale, int causal,
+                 const uint8_t* blockmask, const int32_t* kv_len, fa_dtype dtype, void* workspace, size_t ws_bytes,
+                 void* stream) {
+    if (!q || !k || !v || !o || !lse || !dout || !dq || !dk || !dv || !workspace) return FA_ERR_INVALID_ARG;
+    if (dtype != FA_BF16 && dtype != FA_FP32) return FA_ERR_INVALID_ARG;
+    if (causal != 0 && causal != 1) return FA_ERR_INVALID_ARG;
+    fa_status st = check_shape(B, H, N, d, scale);
+    if (st != FA_OK) return st;
+    if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(o, 16) || !aligned(dout, 16) ||
+        !aligned(dq, 16) || !aligned(dk, 16) || !aligned(dv, 16) || !aligned(lse, 16) ||
+        !aligned(workspace, 256) || (kv_len && !aligned(kv_len, 4)))
+        return FA_ERR_INVALID_ARG;
+    if (dtype != FA_BF16) return FA_ERR_UNSUPPORTED;
+    if (ws_bytes < fa_bwd_workspace_size(B, H, N, d)) return FA_ERR_INVALID_ARG;
+
+    const size_t rows = static_cast<size_t>(B) * H * N;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    fa::BwdArgs a;
+    a.q = q;
+    a.k = k;
+    a.v = v;
+    a.o = o;
+    a.dout = dout;
+    a.lse = lse;
+    a.dq = dq;
+    a.dk = dk;
+    a.dv = dv;
+    a.B = B;
+    a.H = H;
+    a.N = N;
+    a.d = d;
+    a.scale = scale;
+    a.causal = causal;
+    a.blockmask = blockmask;
+    a.kv_len = kv_len;
+    char* ws = static_cast<char*>(workspace);
+    a.status = reinterpret_cast<int*>(ws);
+    a.delta = reinterpret_cast<float*>(ws + kStatusBytes);
+    a.lse2 = reinterpret_cast<float*>(ws + kStatusBytes + align256(rows * sizeof(float)));
+    a.dq_accum = reinterpret_cast<float*>(ws + kStatusBytes + 2 * align256(rows * sizeof(float)));
+    if (cudaMemsetAsync(a.status, 0, sizeof(int) * 4, s) != cudaSuccess) return FA_ERR_CUDA;
+    int n = 0;
+    st = map_cuda(fa::launch_bwd(a, s, &n));
+    if (st == FA_OK) g_last_launches = n;
+    return st;
+}
+
+fa_status fa_get_status(void* workspace, void* stream) {
+    if (!workspace) return FA_ERR_INVALID_ARG;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (cudaStreamSynchronize(s) != cudaSuccess) return FA_ERR_CUDA;
+    int word = 0;
+    if (cudaMemcpy(&word, workspace, sizeof(int), cudaMemcpyDeviceToHost) != cudaSuccess) return FA_ERR_CUDA;
+    if (word == 0) return FA_OK;
+    if (cudaMemset(workspace, 0, sizeof(int)) != cudaSuccess) return FA_ERR_CUDA;
+    return (word & 0xFF) == FA_ERR_TIMEOUT ? FA_ERR_TIMEOUT : FA_ERR_CUDA;
+}
+
+const char* fa_status_string(fa_status s) {
+    switch (s) {
+        case FA_OK: return "FA_OK";
+        case FA_ERR_INVALID_ARG: return "FA_ERR_INVALID_ARG: invalid argument";
+        case FA_ERR_UNSUPPORTED: return "FA_ERR_UNSUPPORTED: unsupported size or type";
+        case FA_ERR_CUDA: return "FA_ERR_CUDA: CUDA runtime or launch error";
+        case FA_ERR_TIMEOUT: return "FA_ERR_TIMEOUT: a device-side wait gave up";
+    }
+    return "unknown fa_status";
+}
+
+int fa_last_launch_count(void) { return g_last_launches; }
+
+}  // extern "C"

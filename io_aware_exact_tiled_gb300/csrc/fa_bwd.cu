@@ -1,0 +1,504 @@
+// Backward pass of fused, tiled, exact softmax attention on sm_103a.
+//
+// What it computes ("FlashAttention: making attention IO-aware", section
+// "The backward pass: recompute, don't store"): the forward pass kept only O
+// and L = m + log l. Each score tile is recomputed from Q and K, the
+// probabilities come back already normalised as P = exp(S - L), and the
+// softmax-gradient row sum is the closed form D = rowsum(dO * O). With these,
+// the gradients of <dO, O> are (textbook derivative of the definition):
+//   dV = P^T dO,  dP = dO V^T,  dS = P * (dP - D),
+//   dQ = scale * dS K,  dK = scale * dS^T Q,
+// and no N x N matrix is written to device memory.
+//
+// Kernels (all on the caller's stream):
+//   fa_bwd_pre_kernel   D = rowsum(dO * O) (fp32, shuffle reduction over the
+//                       threads that share a row) and zeroing of the fp32 dQ
+//                       accumulator
+//   fa_bwd_kernel       one CTA per (batch, head, 128-key block j): K_j and
+//                       V_j stay in shared memory while the query blocks i
+//                       stream through a two-stage TMA ring; five tcgen05
+//                       GEMMs per tile with dK_j and dV_j accumulated in TMEM;
+//                       dQ_i = dS K_j is added into the fp32 accumulator with
+//                       vector atomics
+//   fa_bwd_dq_kernel    fp32 dQ accumulator -> dQ in bf16
+//
+// Warp roles of fa_bwd_kernel (384 threads):
+//   warp 0      TMA producer (K_j, V_j once; Q_i, dO_i, L_i, D_i per stage)
+//   warp 1      TMEM allocation; lane 0 issues the MMAs
+//   warps 4-7   thread r owns key r of the block: P^T and dS^T rows
+//   warps 8-11  thread r owns query r of the current block: dQ drain
+// TMEM columns: [0,128) S^T, overwritten by P^T (bf16); [128,256) dP^T, then
+// dQ_i; [256, 256+d) dV_j; [256+d, 256+2d) dK_j.
+#include <math_constants.h>
+
+#include "fa_common.cuh"
+#include "fa_launch.h"
+#include "tmap.h"
+
+namespace fa {
+
+template <int D>
+struct BwdCfg {
+    static constexpr int ROWB = D * 2;
+    static constexpr int NREG = ROWB / 128;
+    static constexpr int TILE_BYTES = kTile * ROWB;  // 128 rows of Q, K, V or dO
+    static constexpr int STAGES = 2;
+    static constexpr int K_OFF = 0;
+    static constexpr int V_OFF = K_OFF + TILE_BYTES;
+    static constexpr int Q_OFF = V_OFF + TILE_BYTES;                  // [STAGES]
+    static constexpr int DO_OFF = Q_OFF + STAGES * TILE_BYTES;        // [STAGES]
+    static constexpr int DS_OFF = DO_OFF + STAGES * TILE_BYTES;       // dS^T, 128 x 128 bf16
+    static constexpr int LSE_OFF = DS_OFF + 32768;                    // [STAGES][128] fp32
+    static constexpr int DEL_OFF = LSE_OFF + STAGES * 512;            // [STAGES][128] fp32
+    static constexpr int BAR_OFF = DEL_OFF + STAGES * 512;
+    static constexpr int USED = BAR_OFF + 256;
+    static constexpr int SMEM = USED + 1024 <= 232448 ? USED + 1024 : 232448;
+    static constexpr uint32_t ID_SQ = idesc_make(128, 128, kFmtBF16, false, false);  // S^T, dP^T
+    static constexpr uint32_t ID_KN = idesc_make(128, D, kFmtBF16, false, true);     // dV, dK
+    static constexpr uint32_t ID_DQ = idesc_make(128, D, kFmtBF16, true, true);      // dQ
+    static constexpr int COL_S = 0, COL_DP = 128, COL_DQ = 128, COL_DV = 256, COL_DK = 256 + D;
+};
+
+struct BwdParams {
+    int B, H, N;
+    float scale;
+    float scale_log2;
+    MaskArgs mask;
+    const float* lse2;   // L * log2(e), +inf where L = -inf
+    const float* delta;
+    void* dk;
+    void* dv;
+    float* dq_accum;
+    int* status;
+};
+
+constexpr float kLog2e = 1.4426950408889634f;
+
+template <int D>
+__global__ void __launch_bounds__(384, 1)
+    fa_bwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
+                  const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmdO,
+                  const BwdParams p) {
+    using C = BwdCfg<D>;
+    extern __shared__ __align__(1024) uint8_t smem_raw[];
+    uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    // The carve-up needs the dynamic shared window to start within the slack
+    // reserved for alignment; report instead of overrunning if it does not.
+    if ((sm - smem_raw) + C::USED > C::SMEM) {
+        if (tid == 0 && p.status) atomicCAS(p.status, 0, FA_DEV_TIMEOUT | (99 << 8));
+        return;
+    }
+    uint64_t* bars = reinterpret_cast<uint64_t*>(sm + C::BAR_OFF);
+    uint64_t* kv_full = bars + 0;
+    uint64_t* qd_full = bars + 1;                 // [STAGES]
+    uint64_t* qd_empty = qd_full + C::STAGES;     // [STAGES]
+    uint64_t* s_full = qd_empty + C::STAGES;
+    uint64_t* dp_full = s_full + 1;
+    uint64_t* p_ready = dp_full + 1;
+    uint64_t* ds_ready = p_ready + 1;
+    uint64_t* dq_full = ds_ready + 1;
+    uint64_t* dq_free = dq_full + 1;
+    uint64_t* dkv_done = dq_free + 1;
+    uint64_t* drain = dkv_done + 1;
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+    const WaitCtx cx{abort_flag, p.status};
+
+    const int h = blockIdx.x, b = blockIdx.y, j = blockIdx.z;
+    const int N = p.N, T = p.mask.T;
+    const int bh = b * p.H + h;
+    const int kvalid = keys_valid(p.mask, b, N);
+    const int lo = p.mask.causal ? j : 0;
+    auto visible_i = [&](int i) -> bool { return tile_visible(p.mask, i, j, kvalid); };
+
+    if (tid == 0) {
+        *abort_flag = 0;
+        mbar_init(kv_full, 1);
+        for (int s = 0; s < C::STAGES; ++s) {
+            mbar_init(&qd_full[s], 1);
+            mbar_init(&qd_empty[s], 1);
+        }
+        mbar_init(s_full, 1);
+        mbar_init(dp_full, 1);
+        mbar_init(p_ready, 128);
+        mbar_init(ds_ready, 128);
+        mbar_init(dq_full, 1);
+        mbar_init(dq_free, 128);
+        mbar_init(dkv_done, 1);
+        mbar_init(drain, 1);
+        fence_barrier_init();
+    }
+    if (warp == 0 && lane == 0) {
+        tma_prefetch_desc(&tmQ);
+        tma_prefetch_desc(&tmK);
+        tma_prefetch_desc(&tmV);
+        tma_prefetch_desc(&tmdO);
+    }
+    if (warp == 1) {
+        tmem_alloc(tmem_slot, 512);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tm = *tmem_slot;
+
+    if (warp == 0) {
+        // ------------------------------------------------------------ producer
+        if (lane == 0) {
+            int u = 0;
+            bool kv_issued = false;
+            for (int i = lo; i < T; ++i) {
+                if (!visible_i(i)) continue;
+                if (!kv_issued) {
+                    mbar_arrive_expect_tx(kv_full, 2 * C::TILE_BYTES);
+                    for (int r = 0; r < C::NREG; ++r) {
+                        tma_load_2d(sm + C::K_OFF + r * 16384, &tmK, r * 64, bh * N + j * kTile, kv_full);
+                        tma_load_2d(sm + C::V_OFF + r * 16384, &tmV, r * 64, bh * N + j * kTile, kv_full);
+                    }
+                    kv_issued = true;
+                }
+                const int st = u % C::STAGES;
+                const uint32_t ph = (u / C::STAGES) & 1;
+                if (!mbar_wait(&qd_empty[st], ph ^ 1, cx, 11)) break;
+                mbar_arrive_expect_tx(&qd_full[st], 2 * C::TILE_BYTES + 1024);
+                const int row = bh * N + i * kTile;
+                for (int r = 0; r < C::NREG; ++r) {
+                    tma_load_2d(sm + C::Q_OFF + st * C::TILE_BYTES + r * 16384, &tmQ, r * 64, row, &qd_full[st]);
+                    tma_load_2d(sm + C::DO_OFF + st * C::TILE_BYTES + r * 16384, &tmdO, r * 64, row, &qd_full[st]);
+                }
+                bulk_load(sm + C::LSE_OFF + st * 512, p.lse2 + row, 512, &qd_full[st]);
+                bulk_load(sm + C::DEL_OFF + st * 512, p.delta + row, 512, &qd_full[st]);
+                ++u;
+            }
+            if (kv_issued) mbar_wait_teardown(kv_full, 0, 200000000ull);
+            for (int s = 0; s < C::STAGES && s < u; ++s) {
+                const int last = s + ((u - 1 - s) / C::STAGES) * C::STAGES;
+                mbar_wait_teardown(&qd_full[s], (last / C::STAGES) & 1, 200000000ull);
+            }
+        }
+    } else if (warp == 1) {
+        // ------------------------------------------------------------ MMA issuer
+        if (lane == 0) {
+            const uint32_t kb = smem_u32(sm + C::K_OFF), vb = smem_u32(sm + C::V_OFF);
+            const uint32_t dsb = smem_u32(sm + C::DS_OFF);
+            bool ok = true;
+            int u = 0;
+            for (int i = lo; ok && i < T; ++i) {
+                if (!visible_i(i)) continue;
+                if (u == 0) {
+                    if (!(ok = mbar_wait(kv_full, 0, cx, 12))) break;
+                }
+                const int st = u % C::STAGES;
+                const uint32_t ph = (u / C::STAGES) & 1;
+                if (!(ok = mbar_wait(&qd_full[st], ph, cx, 13))) break;
+                tc_fence_after();
+                const uint32_t qb = smem_u32(sm + C::Q_OFF + st * C::TILE_BYTES);
+                const uint32_t dob = smem_u32(sm + C::DO_OFF + st * C::TILE_BYTES);
+                // S^T = K_j Q_i^T
+#pragma unroll
+                for (int kk = 0; kk < D / 16; ++kk) {
+                    const uint32_t off = (kk / 4) * 16384 + (kk % 4) * 32;
+                    umma_ss<false>(tm + C::COL_S, sdesc_sw128(kb + off, 16, 1024), sdesc_sw128(qb + off, 16, 1024),
+                                   C::ID_SQ, kk > 0);
+                }
+                umma_commit(s_full);
+                // dP^T = V_j dO_i^T (its columns held dQ of the previous block)
+                if (u > 0 && !(ok = mbar_wait(dq_free, (u - 1) & 1, cx, 14))) break;
+                tc_fence_after();
+#pragma unroll
+                for (int kk = 0; kk < D / 16; ++kk) {
+                    const uint32_t off = (kk / 4) * 16384 + (kk % 4) * 32;
+                    umma_ss<false>(tm + C::COL_DP, sdesc_sw128(vb + off, 16, 1024), sdesc_sw128(dob + off, 16, 1024),
+                                   C::ID_SQ, kk > 0);
+                }
+                umma_commit(dp_full);
+                // dV_j += P^T dO_i
+                if (!(ok = mbar_wait(p_ready, u & 1, cx, 15))) break;
+                tc_fence_after();
+#pragma unroll
+                for (int kk = 0; kk < 8; ++kk)
+                    umma_ts<false>(tm + C::COL_DV, tm + C::COL_S + kk * 8, sdesc_sw128(dob + kk * 2048, 16384, 1024),
+                                   C::ID_KN, (u > 0 || kk > 0) ? 1u : 0u);
+                // dK_j += dS^T Q_i ; dQ_i = dS K_j
+                if (!(ok = mbar_wait(ds_ready, u & 1, cx, 16))) break;
+                tc_fence_after();
+#pragma unroll
+                for (int kk = 0; kk < 8; ++kk) {
+                    const uint32_t off = (kk / 4) * 16384 + (kk % 4) * 32;
+                    umma_ss<false>(tm + C::COL_DK, sdesc_sw128(dsb + off, 16, 1024),
+                                   sdesc_sw128(qb + kk * 2048, 16384, 1024), C::ID_KN, (u > 0 || kk > 0) ? 1u : 0u);
+                }
+#pragma unroll
+                for (int kk = 0; kk < 8; ++kk)
+                    umma_ss<false>(tm + C::COL_DQ, sdesc_sw128(dsb + kk * 2048, 16384, 1024),
+                                   sdesc_sw128(kb + kk * 2048, 16384, 1024), C::ID_DQ, kk > 0 ? 1u : 0u);
+                umma_commit(dq_full);
+                umma_commit(&qd_empty[st]);
+                ++u;
+            }
+            if (ok && u > 0) umma_commit(dkv_done);
+            umma_commit(drain);
+            mbar_wait_teardown(drain, 0, 200000000ull);
+        }
+    } else if (warp >= 4 && warp < 8) {
+        // ------------------------------------------------------------ P^T, dS^T (thread = key)
+        const int r = (warp & 3) * 32 + lane;
+        const uint32_t tl = tm + (static_cast<uint32_t>((warp & 3) * 32) << 16);
+        const int key = j * kTile + r;
+        const bool key_ok = key < kvalid;
+        const float c2 = p.scale_log2;
+        uint8_t* ds_row = sm + C::DS_OFF + r * 128;
+        bool ok = true;
+        int u = 0;
+        for (int i = lo; i < T; ++i) {
+            if (!visible_i(i)) continue;
+            const int st = u % C::STAGES;
+            const uint32_t ph = (u / C::STAGES) & 1;
+            const float* lse_s = reinterpret_cast<const float*>(sm + C::LSE_OFF + st * 512);
+            const float* del_s = reinterpret_cast<const float*>(sm + C::DEL_OFF + st * 512);
+            ok = mbar_wait(&qd_full[st], ph, cx, 17);
+            ok = __all_sync(0xffffffffu, ok);
+            if (!ok) break;
+            ok = mbar_wait(s_full, u & 1, cx, 18);
+            ok = __all_sync(0xffffffffu, ok);
+            if (!ok) break;
+            tc_fence_after();
+            const bool diag = p.mask.causal && i == j;
+            uint32_t pk[64];  // P^T row as bf16 pairs
+#pragma unroll
+            for (int c = 0; c < 4; ++c) {
+                uint32_t sr[32];
+                tmem_ld32(tl + C::COL_S + c * 32, sr);
+                tmem_ld_wait(sr);
+#pragma unroll
+                for (int g = 0; g < 8; ++g) {
+                    const float4 L4 = reinterpret_cast<const float4*>(lse_s)[c * 8 + g];
+                    float pv[4];
+                    pv[0] = ex2_approx(fmaf(__uint_as_float(sr[4 * g + 0]), c2, -L4.x));
+                    pv[1] = ex2_approx(fmaf(__uint_as_float(sr[4 * g + 1]), c2, -L4.y));
+                    pv[2] = ex2_approx(fmaf(__uint_as_float(sr[4 * g + 2]), c2, -L4.z));
+                    pv[3] = ex2_approx(fmaf(__uint_as_float(sr[4 * g + 3]), c2, -L4.w));
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        const int q = c * 32 + 4 * g + e;
+                        if (!key_ok || (diag && q < r)) pv[e] = 0.f;
+                    }
+                    pk[c * 16 + 2 * g] = pack_bf16x2(pv[0], pv[1]);
+                    pk[c * 16 + 2 * g + 1] = pack_bf16x2(pv[2], pv[3]);
+                }
+                tmem_st16(tl + C::COL_S + c * 16, &pk[c * 16]);
+            }
+            tmem_st_wait();
+            tc_fence_before();
+            mbar_arrive(p_ready);
+            // dS^T = P^T * (dP^T - D) * scale, staged in shared memory
+            ok = mbar_wait(dp_full, u & 1, cx, 19);
+            ok = __all_sync(0xffffffffu, ok);
+            if (!ok) break;
+            if (u > 0) {
+                // the previous dS^T must have been consumed by its dK / dQ GEMMs
+                ok = mbar_wait(dq_full, (u - 1) & 1, cx, 20);
+                ok = __all_sync(0xffffffffu, ok);
+                if (!ok) break;
+            }
+            tc_fence_after();
+#pragma unroll
+            for (int c = 0; c < 4; ++c) {
+                uint32_t dr[32];
+                tmem_ld32(tl + C::COL_DP + c * 32, dr);
+                tmem_ld_wait(dr);
+#pragma unroll
+                for (int g = 0; g < 4; ++g) {  // 8 queries = one 16-byte chunk
+                    const int q0 = c * 32 + 8 * g;
+                    const float4 d0 = reinterpret_cast<const float4*>(del_s)[q0 / 4];
+                    const float4 d1 = reinterpret_cast<const float4*>(del_s)[q0 / 4 + 1];
+                    const float dd[8] = {d0.x, d0.y, d0.z, d0.w, d1.x, d1.y, d1.z, d1.w};
+                    uint32_t w[4];
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        const uint32_t pp = pk[q0 / 2 + e];
+                        const float pa = __uint_as_float(pp << 16), pb = __uint_as_float(pp & 0xFFFF0000u);
+                        const float sa = pa * (__uint_as_float(dr[8 * g + 2 * e]) - dd[2 * e]) * p.scale;
+                        const float sb = pb * (__uint_as_float(dr[8 * g + 2 * e + 1]) - dd[2 * e + 1]) * p.scale;
+                        w[e] = pack_bf16x2(sa, sb);
+                    }
+                    const int chunk = q0 / 8;            // 0..15
+                    const int region = chunk >> 3;       // 64 queries per swizzle region
+                    const int cc = (chunk & 7) ^ (r & 7);
+                    *reinterpret_cast<uint4*>(ds_row + region * 16384 + cc * 16) = make_uint4(w[0], w[1], w[2], w[3]);
+                }
+            }
+            fence_proxy_async_smem();
+            tc_fence_before();
+            mbar_arrive(ds_ready);
+            ++u;
+        }
+        // ------------------------------------------------------------ dK, dV epilogue
+        if (ok && u > 0) {
+            ok = mbar_wait(dkv_done, 0, cx, 21);
+            ok = __all_sync(0xffffffffu, ok);
+            if (ok) tc_fence_after();
+        }
+        if (ok) {
+            const size_t orow = (static_cast<size_t>(bh) * N + key) * D;
+#pragma unroll
+            for (int which = 0; which < 2; ++which) {
+                uint16_t* out = static_cast<uint16_t*>(which == 0 ? p.dv : p.dk) + orow;
+                const uint32_t col = which == 0 ? C::COL_DV : C::COL_DK;
+#pragma unroll
+                for (int c = 0; c < D / 32; ++c) {
+                    uint32_t v[32];
+                    if (u > 0) {
+                        tmem_ld32(tl + col + c * 32, v);
+                        tmem_ld_wait(v);
+                    } else {
+#pragma unroll
+                        for (int e = 0; e < 32; ++e) v[e] = 0u;
+                    }
+                    uint4* dst = reinterpret_cast<uint4*>(out + c * 32);
+#pragma unroll
+                    for (int q = 0; q < 4; ++q)
+                        dst[q] = make_uint4(pack_bf16x2(__uint_as_float(v[8 * q]), __uint_as_float(v[8 * q + 1])),
+                                            pack_bf16x2(__uint_as_float(v[8 * q + 2]), __uint_as_float(v[8 * q + 3])),
+                                            pack_bf16x2(__uint_as_float(v[8 * q + 4]), __uint_as_float(v[8 * q + 5])),
+                                            pack_bf16x2(__uint_as_float(v[8 * q + 6]), __uint_as_float(v[8 * q + 7])));
+                }
+            }
+        }
+    } else if (warp >= 8) {
+        // ------------------------------------------------------------ dQ drain (thread = query)
+        const int r = (warp & 3) * 32 + lane;
+        const uint32_t tl = tm + (static_cast<uint32_t>((warp & 3) * 32) << 16);
+        int u = 0;
+        for (int i = lo; i < T; ++i) {
+            if (!visible_i(i)) continue;
+            bool ok = mbar_wait(dq_full, u & 1, cx, 22);
+            ok = __all_sync(0xffffffffu, ok);
+            if (!ok) break;
+            tc_fence_after();
+            float4* acc = reinterpret_cast<float4*>(p.dq_accum + (static_cast<size_t>(bh) * N + i * kTile + r) * D);
+#pragma unroll
+            for (int c = 0; c < D / 32; ++c) {
+                uint32_t v[32];
+                tmem_ld32(tl + C::COL_DQ + c * 32, v);
+                tmem_ld_wait(v);
+#pragma unroll
+                for (int q = 0; q < 8; ++q)
+                    atomicAdd(acc + c * 8 + q, make_float4(__uint_as_float(v[4 * q]), __uint_as_float(v[4 * q + 1]),
+                                                           __uint_as_float(v[4 * q + 2]),
+                                                           __uint_as_float(v[4 * q + 3])));
+            }
+            tc_fence_before();
+            mbar_arrive(dq_free);
+            ++u;
+        }
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        tc_fence_after();
+        tmem_dealloc(tm, 512);
+    }
+}
+
+// D[row] = sum_k dO[row, k] * O[row, k] in fp32; also zeroes dQ_accum[row, :]
+// and writes L in log2 units (L * log2 e; +inf for a row that saw no key, so
+// that its recomputed probabilities are 0). D/8 threads share a row (16 bytes
+// of O and of dO each) and reduce with warp shuffles.
+template <int D>
+__global__ void __launch_bounds__(256) fa_bwd_pre_kernel(const uint16_t* __restrict__ o, const uint16_t* __restrict__ dout,
+                                                         const float* __restrict__ lse, float* __restrict__ delta,
+                                                         float* __restrict__ lse2, float* __restrict__ dq_accum,
+                                                         long long rows) {
+    constexpr int TPR = D / 8;  // threads per row
+    const long long row = (static_cast<long long>(blockIdx.x) * 256 + threadIdx.x) / TPR;
+    const int part = threadIdx.x % TPR;
+    float acc = 0.f;
+    if (row < rows) {
+        const uint4 a = *reinterpret_cast<const uint4*>(o + row * D + part * 8);
+        const uint4 g = *reinterpret_cast<const uint4*>(dout + row * D + part * 8);
+        const uint32_t av[4] = {a.x, a.y, a.z, a.w}, gv[4] = {g.x, g.y, g.z, g.w};
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+            acc = fmaf(__uint_as_float(av[e] << 16), __uint_as_float(gv[e] << 16), acc);
+            acc = fmaf(__uint_as_float(av[e] & 0xFFFF0000u), __uint_as_float(gv[e] & 0xFFFF0000u), acc);
+        }
+        float4* z = reinterpret_cast<float4*>(dq_accum + row * D + part * 8);
+        z[0] = make_float4(0.f, 0.f, 0.f, 0.f);
+        z[1] = make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+#pragma unroll
+    for (int off = TPR / 2; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
+    if (row < rows && part == 0) {
+        delta[row] = acc;
+        const float L = lse[row];
+        lse2[row] = L == -CUDART_INF_F ? CUDART_INF_F : L * kLog2e;
+    }
+}
+
+// dQ (bf16) <- dQ_accum (fp32), 8 elements per thread.
+__global__ void __launch_bounds__(256) fa_bwd_dq_kernel(const float* __restrict__ acc, uint16_t* __restrict__ dq,
+                                                        long long n8) {
+    for (long long i = static_cast<long long>(blockIdx.x) * 256 + threadIdx.x; i < n8;
+         i += static_cast<long long>(gridDim.x) * 256) {
+        const float4 a = reinterpret_cast<const float4*>(acc)[2 * i];
+        const float4 c = reinterpret_cast<const float4*>(acc)[2 * i + 1];
+        reinterpret_cast<uint4*>(dq)[i] =
+            make_uint4(pack_bf16x2(a.x, a.y), pack_bf16x2(a.z, a.w), pack_bf16x2(c.x, c.y), pack_bf16x2(c.z, c.w));
+    }
+}
+
+template <int D>
+static cudaError_t launch_bwd_t(const BwdArgs& a, cudaStream_t stream, int* nlaunch) {
+    using C = BwdCfg<D>;
+    const uint64_t rows = static_cast<uint64_t>(a.B) * a.H * a.N;
+    CUtensorMap tq, tk, tv, tdo;
+    if (!make_tmap_2d_sw128(&tq, a.q, rows, D, 2, kTile, 64) || !make_tmap_2d_sw128(&tk, a.k, rows, D, 2, kTile, 64) ||
+        !make_tmap_2d_sw128(&tv, a.v, rows, D, 2, kTile, 64) ||
+        !make_tmap_2d_sw128(&tdo, a.dout, rows, D, 2, kTile, 64))
+        return cudaErrorInvalidValue;
+    static bool attr_set = false;
+    if (!attr_set) {
+        cudaError_t e = cudaFuncSetAttribute(fa_bwd_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
+        if (e != cudaSuccess) return e;
+        attr_set = true;
+    }
+    const long long nrows = static_cast<long long>(rows);
+    const long long pre_threads = nrows * (D / 8);
+    fa_bwd_pre_kernel<D><<<static_cast<unsigned>((pre_threads + 255) / 256), 256, 0, stream>>>(
+        static_cast<const uint16_t*>(a.o), static_cast<const uint16_t*>(a.dout), a.lse, a.delta, a.lse2, a.dq_accum,
+        nrows);
+    BwdParams p;
+    p.B = a.B;
+    p.H = a.H;
+    p.N = a.N;
+    p.scale = a.scale;
+    p.scale_log2 = a.scale * kLog2e;
+    p.mask.blockmask = a.blockmask;
+    p.mask.kv_len = a.kv_len;
+    p.mask.causal = a.causal;
+    p.mask.T = a.N / kTile;
+    p.lse2 = a.lse2;
+    p.delta = a.delta;
+    p.dk = a.dk;
+    p.dv = a.dv;
+    p.dq_accum = a.dq_accum;
+    p.status = a.status;
+    dim3 grid(a.H, a.B, a.N / kTile);
+    fa_bwd_kernel<D><<<grid, 384, C::SMEM, stream>>>(tq, tk, tv, tdo, p);
+    const long long n8 = nrows * D / 8;
+    long long blocks = (n8 + 255) / 256;
+    if (blocks > 152 * 16) blocks = 152 * 16;
+    fa_bwd_dq_kernel<<<static_cast<unsigned>(blocks), 256, 0, stream>>>(a.dq_accum, static_cast<uint16_t*>(a.dq), n8);
+    *nlaunch = 3;
+    return cudaGetLastError();
+}
+
+cudaError_t launch_bwd(const BwdArgs& a, cudaStream_t stream, int* nlaunch) {
+    if (a.d == 64) return launch_bwd_t<64>(a, stream, nlaunch);
+    return launch_bwd_t<128>(a, stream, nlaunch);
+}
+
+}  // namespace fa

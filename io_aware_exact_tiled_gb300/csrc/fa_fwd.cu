@@ -1,0 +1,474 @@
+// Forward pass of fused, tiled, exact softmax attention on sm_103a.
+//
+// What it computes ("FlashAttention: making attention IO-aware", sections
+// "Tiling: never materialise S" and "Online softmax", and the page's tiled
+// forward listing): for each query tile Q_i it streams key/value tiles
+// (K_j, V_j), forms S_ij = scale * Q_i K_j^T on the tensor cores, updates a
+// running row maximum m, a running sum l of exp(S - m) and an unnormalised
+// output o (rescaled by exp(m_old - m_new) when the maximum grows), and at the
+// end writes O = o / l and L = m + log l. Tiles that the causal mask, the key
+// padding or the tile mask remove are never loaded or computed
+// ("FlashAttention-2": tiles above the diagonal are skipped; "Counting the
+// IO": block-sparse attention skips masked tiles).
+//
+// GB300 design (one CTA per pair of 128-row query tiles of one head):
+//   warp 0      TMA producer: both Q tiles once, then K/V tiles through a
+//               multi-stage shared-memory ring guarded by mbarriers
+//   warp 1      allocates TMEM; lane 0 issues every tcgen05.mma and commit
+//   warps 4-7   softmax warpgroup of Q tile 0 (thread r owns row r, which is
+//               TMEM lane r, so row max and row sum are in-thread)
+//   warps 8-11  softmax warpgroup of Q tile 1
+// TMEM (512 columns): per Q tile, S (128 fp32 columns, P overwrites it as
+// bf16) and the O accumulator (d columns). The MMA warp interleaves the two
+// Q tiles so that one tile's softmax overlaps the other tile's GEMMs.
+// The online-softmax reference maximum is only moved (and O rescaled) when
+// the row maximum grows by more than 2^8 in the exp2 domain; otherwise the
+// stale maximum is kept, which is exact because o and l always share it.
+// The running sum l adds the probabilities after their rounding to bf16, i.e.
+// exactly the weights the P V product uses, so that O = o / l is a convex
+// combination of rows of V even in bf16.
+#include <math_constants.h>
+
+#include "fa_common.cuh"
+#include "fa_launch.h"
+#include "tmap.h"
+
+namespace fa {
+
+template <bool TF32, int D>
+struct FwdCfg {
+    static constexpr int ELEM = TF32 ? 4 : 2;
+    static constexpr int ROWB = D * ELEM;              // bytes per row of Q/K/V
+    static constexpr int NREG = ROWB / 128;            // 128-byte swizzle regions per row
+    static constexpr int TILE_BYTES = kTile * ROWB;    // one 128-row tile
+    static constexpr int STAGES = TILE_BYTES <= 16384 ? 4 : 2;
+    static constexpr int NQ = 2;                       // query tiles per CTA
+    static constexpr int Q_OFF = 0;
+    static constexpr int K_OFF = Q_OFF + NQ * TILE_BYTES;
+    static constexpr int V_OFF = K_OFF + STAGES * TILE_BYTES;
+    static constexpr int BAR_OFF = V_OFF + STAGES * TILE_BYTES;
+    static constexpr int SMEM = BAR_OFF + 256 + 1024;  // + barriers + alignment slack
+    static constexpr int KSTEP = 32 / ELEM;            // K elements per MMA instruction
+    static constexpr int S_KSTEPS = D / KSTEP;
+    static constexpr int PV_KSTEPS = kTile / KSTEP;
+    static constexpr int THREADS = 384;
+    static constexpr int BOXC = 128 / ELEM;            // elements per swizzle row
+    static constexpr uint32_t ID_S = idesc_make(128, 128, TF32 ? kFmtTF32 : kFmtBF16, false, false);
+    // bf16: V is read MN-major straight from its [keys][d] layout;
+    // tf32 operands must be K-major, so V arrives transposed ([d][keys]).
+    static constexpr uint32_t ID_PV = idesc_make(128, D, TF32 ? kFmtTF32 : kFmtBF16, false, !TF32);
+    static_assert(SMEM <= 232448, "shared memory budget");
+};
+
+struct FwdParams {
+    int B, H, N;
+    float scale_log2;  // scale * log2(e)
+    MaskArgs mask;
+    void* o;
+    float* lse;
+    int* status;
+};
+
+constexpr float kRescaleThreshold = 8.0f;  // log2 units
+constexpr float kLn2 = 0.69314718055994530942f;
+
+template <bool TF32, int D>
+__global__ void __launch_bounds__(384, 1)
+    fa_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
+                  const __grid_constant__ CUtensorMap tmV, const FwdParams p) {
+    using C = FwdCfg<TF32, D>;
+    extern __shared__ __align__(1024) uint8_t smem_raw[];
+    uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    uint64_t* bars = reinterpret_cast<uint64_t*>(sm + C::BAR_OFF);
+    uint64_t* bar_q = bars + 0;
+    uint64_t* k_full = bars + 1;
+    uint64_t* v_full = k_full + C::STAGES;
+    uint64_t* kv_empty = v_full + C::STAGES;
+    uint64_t* s_full = kv_empty + C::STAGES;  // [2]
+    uint64_t* p_full = s_full + 2;            // [2]
+    uint64_t* o_done = p_full + 2;            // [2]
+    uint64_t* drain = o_done + 2;
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+    const WaitCtx cx{abort_flag, p.status};
+
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int h = blockIdx.x, b = blockIdx.y;
+    const int T = p.mask.T;
+    const int npairs = (T + 1) >> 1;
+    const int qp = npairs - 1 - static_cast<int>(blockIdx.z);  // longest causal work first
+    const int qb0 = 2 * qp, qb1 = 2 * qp + 1;
+    const bool act1 = qb1 < T;
+    const int N = p.N;
+    const int bh = b * p.H + h;
+    const int kvalid = keys_valid(p.mask, b, N);
+    int hi = T;
+    if (p.mask.causal) hi = min(hi, (act1 ? qb1 : qb0) + 1);
+    hi = min(hi, (kvalid + kTile - 1) / kTile);
+
+    if (tid == 0) {
+        *abort_flag = 0;
+        mbar_init(bar_q, 1);
+        for (int i = 0; i < C::STAGES; ++i) {
+            mbar_init(&k_full[i], 1);
+            mbar_init(&v_full[i], 1);
+            mbar_init(&kv_empty[i], 1);
+        }
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(&s_full[i], 1);
+            mbar_init(&p_full[i], 128);
+            mbar_init(&o_done[i], 1);
+        }
+        mbar_init(drain, 1);
+        fence_barrier_init();
+    }
+    if (warp == 0 && lane == 0) {
+        tma_prefetch_desc(&tmQ);
+        tma_prefetch_desc(&tmK);
+        tma_prefetch_desc(&tmV);
+    }
+    if (warp == 1) {
+        tmem_alloc(tmem_slot, 512);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tm = *tmem_slot;
+
+    // which Q tiles of this CTA need key tile t (bit s = Q tile s)
+    auto need_of = [&](int t) -> uint32_t {
+        uint32_t nd = tile_visible(p.mask, qb0, t, kvalid) ? 1u : 0u;
+        if (act1 && tile_visible(p.mask, qb1, t, kvalid)) nd |= 2u;
+        return nd;
+    };
+
+    if (warp == 0) {
+        // ------------------------------------------------------------ producer
+        if (lane == 0) {
+            const int qrow0 = bh * N + qb0 * kTile;
+            mbar_arrive_expect_tx(bar_q, (act1 ? 2 : 1) * C::TILE_BYTES);
+            for (int s = 0; s < (act1 ? 2 : 1); ++s)
+                for (int r = 0; r < C::NREG; ++r)
+                    tma_load_2d(sm + C::Q_OFF + s * C::TILE_BYTES + r * 16384, &tmQ, r * C::BOXC,
+                                qrow0 + s * kTile, bar_q);
+            int u = 0;
+            for (int t = 0; t < hi; ++t) {
+                if (!need_of(t)) continue;
+                const int stage = u % C::STAGES;
+                const uint32_t ph = (u / C::STAGES) & 1;
+                if (!mbar_wait(&kv_empty[stage], ph ^ 1, cx, 1)) break;
+                uint8_t* sk = sm + C::K_OFF + stage * C::TILE_BYTES;
+                uint8_t* sv = sm + C::V_OFF + stage * C::TILE_BYTES;
+                mbar_arrive_expect_tx(&k_full[stage], C::TILE_BYTES);
+                for (int r = 0; r < C::NREG; ++r)
+                    tma_load_2d(sk + r * 16384, &tmK, r * C::BOXC, bh * N + t * kTile, &k_full[stage]);
+                mbar_arrive_expect_tx(&v_full[stage], C::TILE_BYTES);
+                if constexpr (!TF32) {
+                    for (int r = 0; r < C::NREG; ++r)
+                        tma_load_2d(sv + r * 16384, &tmV, r * C::BOXC, bh * N + t * kTile, &v_full[stage]);
+                } else {
+                    // V^T [d][keys]: four 32-key swizzle regions of [d][32]
+                    for (int r = 0; r < 4; ++r)
+                        tma_load_2d(sv + r * D * 128, &tmV, t * kTile + r * 32, bh * D, &v_full[stage]);
+                }
+                ++u;
+            }
+            // let every copy in flight land before the CTA can exit
+            mbar_wait_teardown(bar_q, 0, 200000000ull);
+            for (int i = 0; i < C::STAGES && i < u; ++i) {
+                const int last = i + ((u - 1 - i) / C::STAGES) * C::STAGES;
+                const uint32_t ph = (last / C::STAGES) & 1;
+                mbar_wait_teardown(&k_full[i], ph, 200000000ull);
+                mbar_wait_teardown(&v_full[i], ph, 200000000ull);
+            }
+        }
+    } else if (warp == 1) {
+        // ------------------------------------------------------------ MMA issuer
+        if (lane == 0) {
+            bool ok = mbar_wait(bar_q, 0, cx, 2);
+            if (ok) tc_fence_after();
+            int pend_stage[2] = {-1, -1};
+            uint32_t pend_ph[2] = {0, 0};
+            int nP[2] = {0, 0};
+            int nPV[2] = {0, 0};
+            uint32_t rem = 0;  // 2 bits per stage: users still to finish
+            const uint32_t qbase = smem_u32(sm + C::Q_OFF);
+            const uint32_t kbase = smem_u32(sm + C::K_OFF);
+            const uint32_t vbase = smem_u32(sm + C::V_OFF);
+
+            auto issue_pv = [&](int s) -> bool {
+                const int ps = pend_stage[s];
+                if (!mbar_wait(&p_full[s], nP[s] & 1, cx, 3)) return false;
+                ++nP[s];
+                if (!mbar_wait(&v_full[ps], pend_ph[s], cx, 4)) return false;
+                tc_fence_after();
+                const uint32_t vst = vbase + ps * C::TILE_BYTES;
+#pragma unroll
+                for (int kk = 0; kk < C::PV_KSTEPS; ++kk) {
+                    uint64_t bd;
+                    if constexpr (!TF32)
+                        bd = sdesc_sw128(vst + kk * 2048, 16384, 1024);
+                    else
+                        bd = sdesc_sw128(vst + (kk / 4) * (D * 128) + (kk % 4) * 32, 16, 1024);
+                    umma_ts<TF32>(tm + s * 256 + 128, tm + s * 256 + kk * 8, bd, C::ID_PV,
+                                  (nPV[s] > 0 || kk > 0) ? 1u : 0u);
+                }
+                ++nPV[s];
+                umma_commit(&o_done[s]);
+                uint32_t r = (rem >> (2 * ps)) & 3u;
+                r -= 1;
+                rem = (rem & ~(3u << (2 * ps))) | (r << (2 * ps));
+                if (r == 0) umma_commit(&kv_empty[ps]);
+                pend_stage[s] = -1;
+                return true;
+            };
+
+            int u = 0;
+            for (int t = 0; ok && t < hi; ++t) {
+                const uint32_t nd = need_of(t);
+                if (!nd) continue;
+                const int stage = u % C::STAGES;
+                const uint32_t ph = (u / C::STAGES) & 1;
+                if (!mbar_wait(&k_full[stage], ph, cx, 5)) { ok = false; break; }
+                tc_fence_after();
+                rem = (rem & ~(3u << (2 * stage))) | ((uint32_t)__popc(nd) << (2 * stage));
+#pragma unroll
+                for (int s = 0; s < 2; ++s) {
+                    if (!(nd & (1u << s))) continue;
+                    if (pend_stage[s] >= 0 && !issue_pv(s)) { ok = false; break; }
+                    const uint32_t qs = qbase + s * C::TILE_BYTES;
+                    const uint32_t ks = kbase + stage * C::TILE_BYTES;
+#pragma unroll
+                    for (int kk = 0; kk < C::S_KSTEPS; ++kk) {
+                        const uint32_t off = (kk / 4) * 16384 + (kk % 4) * 32;
+                        umma_ss<TF32>(tm + s * 256, sdesc_sw128(qs + off, 16, 1024), sdesc_sw128(ks + off, 16, 1024),
+                                      C::ID_S, kk > 0 ? 1u : 0u);
+                    }
+                    umma_commit(&s_full[s]);
+                    pend_stage[s] = stage;
+                    pend_ph[s] = ph;
+                }
+                ++u;
+            }
+            for (int s = 0; ok && s < 2; ++s)
+                if (pend_stage[s] >= 0 && !issue_pv(s)) ok = false;
+            // wait for every MMA issued so far before TMEM can be released
+            umma_commit(drain);
+            mbar_wait_teardown(drain, 0, 200000000ull);
+        }
+    } else if (warp >= 4) {
+        // ------------------------------------------------------------ softmax
+        const int s = (warp - 4) >> 2;
+        const int wq = warp & 3;
+        const int r = wq * 32 + lane;
+        const bool active = (s == 0) || act1;
+        const int qb = s == 0 ? qb0 : qb1;
+        const int grow = qb * kTile + r;  // query row within the sequence
+        const uint32_t tl = tm + (static_cast<uint32_t>(wq * 32) << 16) + s * 256;
+        const float c2 = p.scale_log2;
+        float m_hat = -CUDART_INF_F, l = 0.f;
+        int n = 0;
+        bool ok = true;
+        if (active) {
+            for (int t = 0; t < hi; ++t) {
+                const uint32_t nd = need_of(t);
+                if (!(nd & (1u << s))) continue;
+                ok = mbar_wait(&s_full[s], n & 1, cx, 6);
+                ok = __all_sync(0xffffffffu, ok);
+                if (!ok) break;
+                tc_fence_after();
+                uint32_t sr[4][32];
+#pragma unroll
+                for (int c = 0; c < 4; ++c) tmem_ld32(tl + c * 32, sr[c]);
+#pragma unroll
+                for (int c = 0; c < 4; ++c) tmem_ld_wait(sr[c]);
+                if (tile_partial(p.mask, qb, t, kvalid)) {
+                    const int lim = min(kvalid - t * kTile, p.mask.causal && t == qb ? r + 1 : kTile);
+#pragma unroll
+                    for (int c = 0; c < 4; ++c)
+#pragma unroll
+                        for (int i = 0; i < 32; ++i)
+                            if (c * 32 + i >= lim) sr[c][i] = __float_as_uint(-CUDART_INF_F);
+                }
+                float mx = -CUDART_INF_F;
+#pragma unroll
+                for (int c = 0; c < 4; ++c)
+#pragma unroll
+                    for (int i = 0; i < 32; ++i) mx = fmaxf(mx, __uint_as_float(sr[c][i]));
+                const float m_new = fmaxf(m_hat, mx * c2);
+                const bool resc = (m_new - m_hat) > kRescaleThreshold;
+                float alpha = 1.f;
+                if (resc) {
+                    alpha = ex2_approx(m_hat - m_new);
+                    m_hat = m_new;
+                    l *= alpha;
+                }
+                const float mu = (m_hat == -CUDART_INF_F) ? 0.f : m_hat;
+                float rs = 0.f;
+#pragma unroll
+                for (int c = 0; c < 4; ++c) {
+                    if constexpr (!TF32) {
+                        uint32_t pk[16];
+#pragma unroll
+                        for (int i = 0; i < 16; ++i) {
+                            const float p0 = ex2_approx(fmaf(__uint_as_float(sr[c][2 * i]), c2, -mu));
+                            const float p1 = ex2_approx(fmaf(__uint_as_float(sr[c][2 * i + 1]), c2, -mu));
+                            pk[i] = pack_bf16x2(p0, p1);
+                            // l sums the bf16 weights that the PV product uses
+                            rs += __uint_as_float(pk[i] << 16) + __uint_as_float(pk[i] & 0xFFFF0000u);
+                        }
+                        tmem_st16(tl + c * 16, pk);
+                    } else {
+                        uint32_t pk[32];
+#pragma unroll
+                        for (int i = 0; i < 32; ++i) {
+                            const float p0 = ex2_approx(fmaf(__uint_as_float(sr[c][i]), c2, -mu));
+                            rs += p0;
+                            pk[i] = __float_as_uint(p0);
+                        }
+                        tmem_st32(tl + c * 32, pk);
+                    }
+                }
+                l += rs;
+                tmem_st_wait();
+                if (__any_sync(0xffffffffu, resc) && n > 0) {
+                    // O holds the previous tiles' sum: wait for their last PV,
+                    // then bring it to the new reference maximum.
+                    ok = mbar_wait(&o_done[s], (n - 1) & 1, cx, 7);
+                    ok = __all_sync(0xffffffffu, ok);
+                    if (!ok) break;
+                    tc_fence_after();
+#pragma unroll
+                    for (int c = 0; c < D / 32; ++c) {
+                        uint32_t ov[32];
+                        tmem_ld32(tl + 128 + c * 32, ov);
+                        tmem_ld_wait(ov);
+#pragma unroll
+                        for (int i = 0; i < 32; ++i) ov[i] = __float_as_uint(__uint_as_float(ov[i]) * alpha);
+                        tmem_st32(tl + 128 + c * 32, ov);
+                    }
+                    tmem_st_wait();
+                }
+                tc_fence_before();
+                mbar_arrive(&p_full[s]);
+                ++n;
+            }
+            // ------------------------------------------------------------ epilogue
+            if (ok && n > 0) {
+                ok = mbar_wait(&o_done[s], (n - 1) & 1, cx, 8);
+                ok = __all_sync(0xffffffffu, ok);
+                if (ok) tc_fence_after();
+            }
+            if (ok) {
+                const float inv = l > 0.f ? 1.f / l : 0.f;
+                const size_t orow = (static_cast<size_t>(bh) * N + grow) * D;
+#pragma unroll
+                for (int c = 0; c < D / 32; ++c) {
+                    uint32_t ov[32];
+                    if (n > 0) {
+                        tmem_ld32(tl + 128 + c * 32, ov);
+                        tmem_ld_wait(ov);
+                    } else {
+#pragma unroll
+                        for (int i = 0; i < 32; ++i) ov[i] = 0u;
+                    }
+                    if constexpr (!TF32) {
+                        uint4* dst = reinterpret_cast<uint4*>(static_cast<uint16_t*>(p.o) + orow + c * 32);
+#pragma unroll
+                        for (int j = 0; j < 4; ++j) {
+                            uint4 w;
+                            w.x = pack_bf16x2(__uint_as_float(ov[8 * j + 0]) * inv, __uint_as_float(ov[8 * j + 1]) * inv);
+                            w.y = pack_bf16x2(__uint_as_float(ov[8 * j + 2]) * inv, __uint_as_float(ov[8 * j + 3]) * inv);
+                            w.z = pack_bf16x2(__uint_as_float(ov[8 * j + 4]) * inv, __uint_as_float(ov[8 * j + 5]) * inv);
+                            w.w = pack_bf16x2(__uint_as_float(ov[8 * j + 6]) * inv, __uint_as_float(ov[8 * j + 7]) * inv);
+                            dst[j] = w;
+                        }
+                    } else {
+                        float4* dst = reinterpret_cast<float4*>(static_cast<float*>(p.o) + orow + c * 32);
+#pragma unroll
+                        for (int j = 0; j < 8; ++j)
+                            dst[j] = make_float4(__uint_as_float(ov[4 * j]) * inv, __uint_as_float(ov[4 * j + 1]) * inv,
+                                                 __uint_as_float(ov[4 * j + 2]) * inv,
+                                                 __uint_as_float(ov[4 * j + 3]) * inv);
+                    }
+                }
+                p.lse[static_cast<size_t>(bh) * N + grow] = l > 0.f ? (m_hat + log2f(l)) * kLn2 : -CUDART_INF_F;
+            }
+        }
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        tc_fence_after();
+        tmem_dealloc(tm, 512);
+    }
+}
+
+// V [BH][N][d] fp32 -> V^T [BH][d][N] (tf32 operands of tcgen05 must be K-major)
+__global__ void fa_transpose_v_kernel(const float* __restrict__ v, float* __restrict__ vt, int N, int D) {
+    __shared__ float tile[32][33];
+    const int bh = blockIdx.z;
+    const int n0 = blockIdx.x * 32, d0 = blockIdx.y * 32;
+    const float* src = v + static_cast<size_t>(bh) * N * D;
+    float* dst = vt + static_cast<size_t>(bh) * N * D;
+    for (int i = threadIdx.y; i < 32; i += blockDim.y) tile[i][threadIdx.x] = src[(size_t)(n0 + i) * D + d0 + threadIdx.x];
+    __syncthreads();
+    for (int i = threadIdx.y; i < 32; i += blockDim.y) dst[(size_t)(d0 + i) * N + n0 + threadIdx.x] = tile[threadIdx.x][i];
+}
+
+template <bool TF32, int D>
+static cudaError_t launch_fwd_t(const FwdArgs& a, cudaStream_t stream, int* nlaunch) {
+    using C = FwdCfg<TF32, D>;
+    const int elem = TF32 ? 4 : 2;
+    const uint64_t rows = static_cast<uint64_t>(a.B) * a.H * a.N;
+    CUtensorMap tq, tk, tv;
+    if (!make_tmap_2d_sw128(&tq, a.q, rows, D, elem, kTile, C::BOXC)) return cudaErrorInvalidValue;
+    if (!make_tmap_2d_sw128(&tk, a.k, rows, D, elem, kTile, C::BOXC)) return cudaErrorInvalidValue;
+    int launches = 0;
+    if constexpr (TF32) {
+        float* vt = static_cast<float*>(a.vt_scratch);
+        dim3 g(a.N / 32, D / 32, a.B * a.H);
+        fa_transpose_v_kernel<<<g, dim3(32, 8), 0, stream>>>(static_cast<const float*>(a.v), vt, a.N, D);
+        ++launches;
+        if (!make_tmap_2d_sw128(&tv, vt, static_cast<uint64_t>(a.B) * a.H * D, a.N, elem, D, C::BOXC))
+            return cudaErrorInvalidValue;
+    } else {
+        if (!make_tmap_2d_sw128(&tv, a.v, rows, D, elem, kTile, C::BOXC)) return cudaErrorInvalidValue;
+    }
+    static bool attr_set = false;
+    if (!attr_set) {
+        cudaError_t e = cudaFuncSetAttribute(fa_fwd_kernel<TF32, D>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
+        if (e != cudaSuccess) return e;
+        attr_set = true;
+    }
+    FwdParams p;
+    p.B = a.B;
+    p.H = a.H;
+    p.N = a.N;
+    p.scale_log2 = a.scale * 1.4426950408889634f;
+    p.mask.blockmask = a.blockmask;
+    p.mask.kv_len = a.kv_len;
+    p.mask.causal = a.causal;
+    p.mask.T = a.N / kTile;
+    p.o = a.o;
+    p.lse = a.lse;
+    p.status = a.status;
+    const int T = a.N / kTile;
+    dim3 grid(a.H, a.B, (T + 1) / 2);
+    fa_fwd_kernel<TF32, D><<<grid, C::THREADS, C::SMEM, stream>>>(tq, tk, tv, p);
+    ++launches;
+    *nlaunch = launches;
+    return cudaGetLastError();
+}
+
+cudaError_t launch_fwd(const FwdArgs& a, cudaStream_t stream, int* nlaunch) {
+    if (a.fp32) {
+        if (a.d == 64) return launch_fwd_t<true, 64>(a, stream, nlaunch);
+        return cudaErrorInvalidValue;  // fp32 d=128 exceeds the shared-memory budget of this kernel
+    }
+    if (a.d == 64) return launch_fwd_t<false, 64>(a, stream, nlaunch);
+    return launch_fwd_t<false, 128>(a, stream, nlaunch);
+}
+
+}  // namespace fa

@@ -1,0 +1,42 @@
+// Internal interface between the C-ABI layer (fa_api.cu) and the kernel
+// launchers (fa_fwd.cu, fa_bwd.cu). Arguments are already validated.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace fa {
+
+struct FwdArgs {
+    const void *q, *k, *v;
+    void* o;
+    float* lse;
+    int B, H, N, d;
+    float scale;
+    int causal;
+    const uint8_t* blockmask;
+    const int32_t* kv_len;
+    int fp32;
+    void* vt_scratch;  // fp32 only: [B,H,d,N] transposed V
+    int* status;
+};
+
+struct BwdArgs {
+    const void *q, *k, *v, *o, *dout;
+    const float* lse;
+    void *dq, *dk, *dv;
+    int B, H, N, d;
+    float scale;
+    int causal;
+    const uint8_t* blockmask;
+    const int32_t* kv_len;
+    float* delta;     // [B,H,N] scratch: D = rowsum(dO * O)
+    float* lse2;      // [B,H,N] scratch: L in log2 units
+    float* dq_accum;  // [B,H,N,d] fp32 scratch
+    int* status;
+};
+
+cudaError_t launch_fwd(const FwdArgs& a, cudaStream_t stream, int* nlaunch);
+cudaError_t launch_bwd(const BwdArgs& a, cudaStream_t stream, int* nlaunch);
+
+}  // namespace fa

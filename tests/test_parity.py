@@ -1,0 +1,111 @@
+"""GPU parity: the CUDA path (through the C ABI) against the fp64 oracle on the
+same seeded inputs. Small shapes span several tiles and the edge cases; the
+full workload shapes are checked on whole sampled heads."""
+
+import numpy as np
+import pytest
+import torch
+
+import io_aware_exact_tiled_gb300 as fa
+from io_aware_exact_tiled_gb300 import workloads as W
+
+from parity import check, errors, run_gpu
+
+pytestmark = pytest.mark.gpu
+
+
+def small(name, **kw):
+    return W.WORKLOADS[name].with_(**kw)
+
+
+SWEEP = []
+for d in (64, 128):
+    for N in (128, 384, 1024):
+        SWEEP.append(W.Workload(f"dense-{N}-{d}", 2, 2, N, d))
+        SWEEP.append(W.Workload(f"causal-{N}-{d}", 2, 2, N, d, causal=True))
+        SWEEP.append(W.Workload(f"kvlen-{N}-{d}", 3, 2, N, d, kv_len_range=(1, N)))
+        SWEEP.append(W.Workload(f"sparse-{N}-{d}", 1, 2, N, d, block_density=0.3))
+SWEEP.append(W.Workload("causal-kvlen-sparse-768-128", 2, 2, 768, 128, causal=True, kv_len_range=(200, 700),
+                        block_density=0.5))
+SWEEP.append(W.Workload("wide-scores-512-128", 1, 2, 512, 128, causal=True, k_scale=4.0))
+
+
+@pytest.mark.parametrize("w", SWEEP, ids=lambda w: w.name)
+def test_sweep(cuda_device, w):
+    x = W.make_inputs(w, seed=3)
+    g = run_gpu(x, cuda_device)
+    check(errors(x, g))
+
+
+def test_tiny_fp32_forward(cuda_device):
+    w = W.WORKLOADS["tiny"]
+    x = W.make_inputs(w, seed=0)
+    g = run_gpu(x, cuda_device, backward=False)
+    e = errors(x, g, backward=False)
+    check(e)
+    assert e["lse"] <= 1e-3
+
+
+def test_bert_full(cuda_device):
+    x = W.make_inputs(W.WORKLOADS["bert"], seed=0)
+    check(errors(x, run_gpu(x, cuda_device)))
+
+
+def test_gpt2_full(cuda_device):
+    x = W.make_inputs(W.WORKLOADS["gpt2"], seed=0)
+    check(errors(x, run_gpu(x, cuda_device)))
+
+
+@pytest.mark.parametrize("name", ["long4k", "long8k"])
+def test_long_context_sampled_heads(cuda_device, name):
+    w = W.WORKLOADS[name]
+    x = W.make_inputs(w, seed=0)
+    g = run_gpu(x, cuda_device)
+    heads = [(0, 0), (0, 17), (0, w.H - 1)]
+    check(errors(x, g, heads=heads))
+
+
+def test_block_sparse_sampled_heads(cuda_device):
+    w = W.WORKLOADS["sparse16k"]
+    x = W.make_inputs(w, seed=0)
+    g = run_gpu(x, cuda_device)
+    check(errors(x, g, heads=[(0, 0), (w.B - 1, w.H - 1)]))
+
+
+def test_fully_masked_rows_and_empty_key_blocks(cuda_device):
+    # kv_len = 0 for one batch element: every row sees no key (O = 0,
+    # L = -inf, zero gradients); a tile mask with an empty query row and an
+    # empty key column.
+    w = W.Workload("edge", 2, 2, 384, 64)
+    x = W.make_inputs(w, seed=5)
+    x.kv_len = torch.tensor([0, 300], dtype=torch.int32)
+    bm = torch.ones(3, 3, dtype=torch.uint8)
+    bm[1, :] = 0
+    bm[:, 2] = 0
+    x.blockmask = bm
+    g = run_gpu(x, cuda_device)
+    check(errors(x, g))
+    assert (g["o"][0] == 0).all() and np.isneginf(g["lse"][0]).all()
+    assert (g["dk"][0] == 0).all() and (g["dv"][0] == 0).all() and (g["dq"][0] == 0).all()
+    assert (g["o"][1, :, 128:256] == 0).all()
+    assert (g["dk"][:, :, 256:] == 0).all() and (g["dv"][:, :, 256:] == 0).all()
+
+
+def test_forward_deterministic(cuda_device):
+    w = W.Workload("det", 1, 4, 1024, 128, causal=True)
+    x = W.make_inputs(w, seed=1)
+    a = run_gpu(x, cuda_device, backward=False)
+    b = run_gpu(x, cuda_device, backward=False)
+    assert np.array_equal(a["o"], b["o"]) and np.array_equal(a["lse"], b["lse"])
+
+
+def test_status_word_clear_after_calls(cuda_device):
+    w = W.Workload("st", 1, 2, 256, 128, causal=True)
+    x = W.make_inputs(w, seed=2)
+    q, k, v, do = (t.to(cuda_device) for t in (x.q, x.k, x.v, x.do))
+    ws = fa.workspace(fa.bwd_workspace_size(1, 2, 256, 128), cuda_device)
+    o, lse = fa.forward(q, k, v, causal=True, ws=ws)
+    assert fa.get_status(ws) == 0
+    fa.backward(q, k, v, o, lse, do, causal=True, ws=ws)
+    assert fa.get_status(ws) == 0
+    assert fa.last_launch_count() == 3
