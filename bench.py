@@ -1,0 +1,432 @@
+#!/usr/bin/env python
+"""Benchmark of fused exact attention (forward + backward) on GB300.
+
+One step is one pass of the whole path over one batch: fa_fwd (O, L) then
+fa_bwd (D preprocess, fused key-block backward, dQ conversion) on seeded
+synthetic inputs already resident in HBM. Prints one JSON line (rank 0).
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--workload long8k]
+  python bench.py --impl reference ...   # the fp64 CPU oracle on a sample
+
+Multi-GPU (torchrun, one rank per GPU): every rank runs an independent
+replica of the workload (heads are independent; no data exchange), the
+timing is the maximum over ranks and the value is the total over ranks.
+"""
+
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "attention fwd and fwd+bwd TFLOP/s on 1 GB300; % of dense BF16 tensor peak"
+DEFAULT_WORKLOAD = "long8k"
+FALLBACK_PEAKS = {"bf16_tflops": 1900.0, "hbm_gbs": 6800.0, "bf16_tflops_sustained": 1700.0}
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    return ap.parse_args()
+
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        d = json.load(open(p))
+        return d, "measured"
+    return dict(FALLBACK_PEAKS), "fallback"
+
+
+def describe(w):
+    mask = "causal" if w.causal else ("key padding U{%d..%d}" % w.kv_len_range if w.kv_len_range else
+                                       ("128x128 tile mask, diagonal + %.1f%% of other tiles" % (100 * w.block_density)
+                                        if w.block_density else "no mask"))
+    ks = ", K rows x%g" % w.k_scale if w.k_scale != 1.0 else ""
+    return f"{w.name}: attention fwd+bwd, B={w.B} H={w.H} N={w.N} d={w.d} {w.dtype}, {mask}{ks}"
+
+
+# ------------------------------------------------------------------ clocks
+class ClockSampler:
+    """Samples nvidia-smi clocks and throttle reasons every 100 ms."""
+
+    FIELDS = ("index,uuid,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, uuid=None):
+        self.uuid = uuid
+        self.rows = []
+        self.proc = None
+        self.thread = None
+
+    def start(self):
+        cmd = ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits", "-lms", "100"]
+        if self.uuid:
+            cmd[1:1] = ["-i", self.uuid]
+        try:
+            self.proc = subprocess.Popen(cmd, stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+            return
+        self.t0 = None
+
+        def reader():
+            for line in self.proc.stdout:
+                self.rows.append((time.time(), [c.strip() for c in line.split(",")]))
+
+        self.thread = threading.Thread(target=reader, daemon=True)
+        self.thread.start()
+        time.sleep(0.6)
+
+    def stop(self):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self, t_begin, t_end):
+        rows = [r for (t, r) in self.rows if t_begin <= t <= t_end + 0.05 and len(r) >= 10]
+        if not rows:
+            rows = [r for (_, r) in self.rows if len(r) >= 10][-3:]
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unavailable"], "samples": 0}
+
+        def num(x):
+            try:
+                return float(x)
+            except ValueError:
+                return None
+
+        sm = [num(r[2]) for r in rows if num(r[2]) is not None]
+        reasons = set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for r in rows:
+            for k, name in enumerate(names):
+                if r[6 + k].lower().startswith("active"):
+                    reasons.add(name)
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": num(rows[0][3]), "reasons": sorted(reasons), "samples": len(rows),
+                "power_w_max": max((num(r[4]) or 0.0) for r in rows)}
+
+
+# ------------------------------------------------------------------ helpers
+def kernel_source_sha():
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "io_aware_exact_tiled_gb300", "csrc")
+    for f in sorted(os.listdir(csrc)):
+        h.update(open(os.path.join(csrc, f), "rb").read())
+    return h.hexdigest()[:16]
+
+
+def recorded_traffic(kernel: str, workload: str):
+    """DRAM bytes per launch of `kernel` from the committed ncu summary, if
+    the kernel sources have not changed since it was taken."""
+    p = os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.exists(p):
+        return None
+    try:
+        d = json.load(open(p))
+        e = d.get(kernel, {}).get(workload)
+        if e and e.get("source_sha") == kernel_source_sha():
+            return e["dram_bytes_per_launch"]
+    except (ValueError, KeyError, TypeError):
+        return None
+    return None
+
+
+def oracle_sample(w, x, budget_s=12.0, max_heads=8):
+    """Time the fp64 CPU oracle (forward + backward) on whole heads of the
+    workload until about `budget_s` seconds have been spent."""
+    import oracle
+    from io_aware_exact_tiled_gb300 import accounting as acc
+    heads = [(b, h) for b in range(w.B) for h in range(w.H)]
+    done, flop, t_used = [], 0.0, 0.0
+    kl = None if x.kv_len is None else x.kv_len.cpu()
+    bm = None if x.blockmask is None else x.blockmask.cpu()
+    q, k, v, do = (t.cpu() for t in (x.q, x.k, x.v, x.do))
+    for (b, h) in heads[:max_heads]:
+        qs, ks, vs, dos = (t[b:b + 1, h:h + 1] for t in (q, k, v, do))
+        kls = None if kl is None else kl[b:b + 1]
+        t0 = time.perf_counter()
+        oracle.forward(qs, ks, vs, x.scale, causal=x.causal, kv_len=kls, blockmask=bm)
+        oracle.backward(qs, ks, vs, dos, x.scale, causal=x.causal, kv_len=kls, blockmask=bm)
+        t_used += time.perf_counter() - t0
+        pb = acc.pairs_per_batch(w.N, w.causal, None if kl is None else kl.tolist(),
+                                 None if bm is None else bm.numpy(), w.B)[b]
+        flop += 14.0 * w.d * pb
+        done.append((b, h))
+        if t_used >= budget_s:
+            break
+    return flop, t_used, done
+
+
+# ------------------------------------------------------------------ reference arm
+def oracle_rows(w, x, R):
+    """Time the oracle on the last R query rows of head (0, 0) (the rows with
+    the most visible keys under a causal mask); returns (flops, seconds)."""
+    import numpy as np
+    import oracle
+    from oracle.attention import visible
+    kl = None if x.kv_len is None else x.kv_len[:1]
+    bm = None if x.blockmask is None else x.blockmask
+    rows = (w.N - R, w.N)
+    q, k, v, do = (t[:1, :1] for t in (x.q, x.k, x.v, x.do))   # head (0, 0)
+    t0 = time.perf_counter()
+    oracle.forward(q, k, v, x.scale, causal=x.causal, kv_len=kl, blockmask=bm, rows=rows)
+    oracle.backward(q, k, v, do, x.scale, causal=x.causal, kv_len=kl, blockmask=bm, rows=rows)
+    t = time.perf_counter() - t0
+    vis = visible(w.N, x.causal, None if kl is None else int(kl[0]), bm, np.arange(*rows))
+    return 14.0 * w.d * float(vis.sum()), t
+
+
+def run_reference(args, rank, world):
+    if rank != 0:
+        return
+    from io_aware_exact_tiled_gb300 import workloads as W
+    w = W.WORKLOADS[args.workload]
+    x = W.make_inputs(w, seed=0)
+    # size each step so that warm-up + timed steps stay within a few minutes
+    budget = min(5.0, 150.0 / max(1, args.steps + args.warmup))
+    f1, t1 = oracle_rows(w, x, 128)
+    R = int(min(w.N, max(128, 128 * math.floor(budget / max(t1, 1e-6)))))
+    times, flops = [], []
+    for i in range(args.warmup + args.steps):
+        f, t = oracle_rows(w, x, R)
+        if i >= args.warmup:
+            times.append(t)
+            flops.append(f)
+    total_t = sum(times)
+    value = sum(flops) / total_t / 1e12
+    cores = os.cpu_count()
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * total_t / len(times),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": describe(w)},
+        "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
+                         "sample": f"each step: fp64 NumPy forward + backward of the last {R} query rows of head "
+                                   f"(0, 0) (N={w.N}, d={w.d}) on the host cores (BLAS threads = all cores; exp "
+                                   f"single-threaded)"},
+        "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+# ------------------------------------------------------------------ our arm
+def main():
+    args = parse()
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if args.impl == "reference":
+        return run_reference(args, rank, world)
+
+    import torch
+    import torch.distributed as dist
+
+    import io_aware_exact_tiled_gb300 as fa
+    from io_aware_exact_tiled_gb300 import accounting as acc
+    from io_aware_exact_tiled_gb300 import workloads as W
+
+    if world > 1:
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl")
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    fa.load()
+
+    w = W.WORKLOADS[args.workload]
+    x = W.make_inputs(w, seed=rank, device="cuda")
+    q, k, v, do = (t.to(dev) for t in (x.q, x.k, x.v, x.do))
+    bm = None if x.blockmask is None else x.blockmask.to(dev)
+    kl = None if x.kv_len is None else x.kv_len.to(dev)
+    B, H, N, d = q.shape
+    o = torch.empty_like(q)
+    lse = torch.empty((B, H, N), dtype=torch.float32, device=dev)
+    dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+    ws_f = fa.workspace(256, dev)
+    ws_b = fa.workspace(fa.bwd_workspace_size(B, H, N, d), dev)
+    kw = dict(scale=x.scale, causal=x.causal, blockmask=bm, kv_len=kl)
+    fwd_flop, bwd_flop = acc.flops(B, H, N, d, x.causal, None if kl is None else x.kv_len.tolist(),
+                                   None if bm is None else x.blockmask.numpy())
+    launches = [0]
+
+    def step():
+        fa.forward(q, k, v, out=o, lse=lse, ws=ws_f, **kw)
+        launches[0] += fa.last_launch_count()
+        fa.backward(q, k, v, o, lse, do, dq=dq, dk=dk, dv=dv, ws=ws_b, **kw)
+        launches[0] += fa.last_launch_count()
+
+    for _ in range(max(3, args.warmup)):
+        step()
+    torch.cuda.synchronize()
+    if fa.get_status(ws_f) != 0 or fa.get_status(ws_b) != 0:
+        raise RuntimeError("device status word reports a timed-out wait")
+
+    # per-kernel events (the library records them around its main kernels)
+    K = args.steps
+    ev = lambda: torch.cuda.Event(enable_timing=True)
+    fb_ev = [(ev(), ev()) for _ in range(K)]
+    bb_ev = [(ev(), ev()) for _ in range(K)]
+    for a, b in fb_ev + bb_ev:   # materialise the event handles
+        a.record()
+        b.record()
+    t_start, t_stop = ev(), ev()
+    torch.cuda.synchronize()
+
+    uuid = None
+    try:
+        uuid = "GPU-" + str(torch.cuda.get_device_properties(dev).uuid)
+    except Exception:
+        uuid = None
+    sampler = ClockSampler(uuid)
+    if rank == 0:
+        sampler.start()
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    launches[0] = 0
+    wall0 = time.time()
+    t_start.record()
+    for i in range(K):
+        fa.set_timing_events(*fb_ev[i])
+        fa.forward(q, k, v, out=o, lse=lse, ws=ws_f, **kw)
+        launches[0] += fa.last_launch_count()
+        fa.set_timing_events(*bb_ev[i])
+        fa.backward(q, k, v, o, lse, do, dq=dq, dk=dk, dv=dv, ws=ws_b, **kw)
+        launches[0] += fa.last_launch_count()
+    t_stop.record()
+    fa.set_timing_events(None, None)
+    torch.cuda.synchronize()
+    wall1 = time.time()
+    if world > 1:
+        dist.barrier()
+    sampler.stop()
+    st_f, st_b = fa.get_status(ws_f), fa.get_status(ws_b)
+    if st_f != 0 or st_b != 0:
+        raise RuntimeError("device status word reports a timed-out wait")
+    ms = t_start.elapsed_time(t_stop)
+    fwd_ms = sum(a.elapsed_time(b) for a, b in fb_ev) / K
+    bwd_ms = sum(a.elapsed_time(b) for a, b in bb_ev) / K
+    if world > 1:
+        t = torch.tensor([ms, fwd_ms, bwd_ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms, fwd_ms, bwd_ms = t.tolist()
+    ms_step = ms / K
+    total_flop = (fwd_flop + bwd_flop) * world
+    value = total_flop / (ms_step * 1e-3) / 1e12
+
+    # ---------------- end to end through the public API with host buffers
+    e2e = None
+    if not args.no_e2e:
+        hq, hk, hv, hdo = (t.cpu().pin_memory() for t in (q, k, v, do))
+        ho, hlse = torch.empty_like(hq).pin_memory(), torch.empty(lse.shape, dtype=torch.float32).pin_memory()
+        hdq, hdk, hdv = (torch.empty_like(hq).pin_memory() for _ in range(3))
+        dq_, dk_, dv_ = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+        qd, kd, vd, dod = (torch.empty_like(q) for _ in range(4))
+
+        def e2e_step():
+            qd.copy_(hq, non_blocking=True)
+            kd.copy_(hk, non_blocking=True)
+            vd.copy_(hv, non_blocking=True)
+            dod.copy_(hdo, non_blocking=True)
+            fa.forward(qd, kd, vd, out=o, lse=lse, ws=ws_f, **kw)
+            fa.backward(qd, kd, vd, o, lse, dod, dq=dq_, dk=dk_, dv=dv_, ws=ws_b, **kw)
+            ho.copy_(o, non_blocking=True)
+            hlse.copy_(lse, non_blocking=True)
+            hdq.copy_(dq_, non_blocking=True)
+            hdk.copy_(dk_, non_blocking=True)
+            hdv.copy_(dv_, non_blocking=True)
+
+        for _ in range(3):
+            e2e_step()
+        torch.cuda.synchronize()
+        K2 = max(3, min(K, 30))
+        e0, e1 = ev(), ev()
+        if world > 1:
+            dist.barrier()
+        e0.record()
+        for _ in range(K2):
+            e2e_step()
+        e1.record()
+        torch.cuda.synchronize()
+        ems = e0.elapsed_time(e1)
+        if world > 1:
+            t = torch.tensor([ems], device=dev)
+            dist.all_reduce(t, op=dist.ReduceOp.MAX)
+            ems = t.item()
+        h2d = sum(t.numel() * t.element_size() for t in (hq, hk, hv, hdo))
+        d2h = sum(t.numel() * t.element_size() for t in (ho, hlse, hdq, hdk, hdv))
+        e2e = {"value": total_flop / (ems / K2 * 1e-3) / 1e12, "unit": "TFLOP/s", "h2d_bytes_per_step": h2d,
+               "d2h_bytes_per_step": d2h, "ms_per_step": ems / K2}
+
+    if rank != 0:
+        if world > 1:
+            dist.destroy_process_group()
+        return
+
+    peaks, peaks_src = load_peaks()
+    peak = float(peaks["bf16_tflops"])
+    fwd_tf = fwd_flop / (fwd_ms * 1e-3) / 1e12
+    bwd_tf = bwd_flop / (bwd_ms * 1e-3) / 1e12
+    dominant = "fa_bwd_kernel" if bwd_ms >= fwd_ms else "fa_fwd_kernel"
+    dom_tf = bwd_tf if dominant == "fa_bwd_kernel" else fwd_tf
+    roofline = {"bound": "tensor", "achieved": dom_tf, "peak": peak, "unit": "TFLOP/s", "frac": dom_tf / peak,
+                "traffic": recorded_traffic(dominant, args.workload), "kernel": dominant,
+                "peak_source": f"{peaks_src} bf16 dense burst (MEASURED_PEAKS.json bf16_tflops)"
+                if peaks_src == "measured" else "fallback 1.9 PFLOP/s bf16 burst"}
+    clocks = sampler.summary(wall0, wall1)
+
+    cpu = None
+    if world == 1 and not args.no_cpu_baseline:
+        xs = W.make_inputs(w, seed=0)
+        f, t, heads = oracle_sample(w, xs)
+        cpu = {"value": f / t / 1e12, "unit": "TFLOP/s", "cores": os.cpu_count(), "kind": "oracle",
+               "sample": f"fp64 NumPy forward + backward of {len(heads)} whole head(s) {heads} of the workload "
+                         f"({t:.1f} s; BLAS threads = all cores, exp single-threaded)"}
+
+    line = {
+        "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": K, "warmup": args.warmup,
+        "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic (seeded N(0,1) Q, K, V, dO in bf16)",
+        "config": {"workload": describe(w), "B": B, "H": H, "N": N, "d": d, "causal": bool(x.causal),
+                   "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
+                   "l2": "inputs larger than L2 (Q, K, V, O, dO = %d MiB each vs 129 MB L2)"
+                         % (q.numel() * q.element_size() >> 20)},
+        "fwd": {"ms": fwd_ms, "tflops": fwd_tf, "pct_peak": 100 * fwd_tf / peak},
+        "bwd": {"ms": bwd_ms, "tflops": bwd_tf, "pct_peak": 100 * bwd_tf / peak,
+                "note": "fa_bwd_kernel alone; the D preprocess and dQ conversion kernels are in ms_per_step"},
+        "pct_peak_step": 100 * value / world / peak,
+        "roofline": roofline,
+        "cpu_baseline": cpu,
+        "e2e": e2e,
+        "gpu_launches": launches[0],
+        "clocks": clocks,
+        "peak_memory_bytes": torch.cuda.max_memory_allocated(dev),
+    }
+    print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -31,8 +31,9 @@
  *   arrays in device memory, all of the element type `dtype`; lse is a
  *   contiguous float32 [B, H, N] array. Base pointers must be 16-byte aligned.
  * Types: FA_BF16 (bfloat16 in and out, bf16 tensor-core products with fp32
- *   accumulation) or FA_FP32 (float32 in and out, tf32 tensor-core products
- *   with fp32 accumulation; forward pass only).
+ *   accumulation) or FA_FP32 (float32 in and out; S from three tf32
+ *   tensor-core products of high/low parts, P V in tf32, fp32 accumulation;
+ *   forward pass with d = 64 only).
  * Supported sizes: d in {64, 128}; N a positive multiple of 128;
  *   B * H * N < 2^31. Other sizes return FA_ERR_UNSUPPORTED.
  * blockmask: NULL or a device uint8 array [N/128, N/128]; entry [i][j] != 0
@@ -70,10 +71,11 @@ typedef enum {
 
 typedef enum { FA_BF16 = 0, FA_FP32 = 1 } fa_dtype;
 
-/* Bytes of workspace fa_fwd needs for these sizes: the status word, plus
- * room for a transposed fp32 copy of V, which FA_FP32 calls use (tf32
- * tensor-core operands must be K-major). FA_BF16 calls need only 256 bytes
- * but accept the full size. */
+/* Bytes of workspace fa_fwd needs for these sizes: the status word, plus,
+ * for FA_FP32 calls, a transposed copy of V (tf32 tensor-core operands must
+ * be K-major) and the tf32 high and low parts of Q and K (S is formed from
+ * three tf32 products to keep fp32 accuracy). FA_BF16 calls need only 256
+ * bytes but accept the full size. */
 size_t fa_fwd_workspace_size(int B, int H, int N, int d);
 
 /* Bytes of workspace fa_bwd needs: D = rowsum(dO * O) and L in log2 units
@@ -127,6 +129,14 @@ const char* fa_status_string(fa_status s);
 /* Number of kernels the last successful fa_fwd / fa_bwd call launched on
  * this host thread (for accounting in benchmarks). */
 int fa_last_launch_count(void);
+
+/* Profiling hook: for the following fa_fwd / fa_bwd calls made by this host
+ * thread, record the CUDA event `begin` (a cudaEvent_t) on the call's stream
+ * immediately before the main attention kernel and `end` immediately after
+ * it, so that a caller can time that kernel alone. Passing NULL for both
+ * turns the hook off. The events are owned by the caller. Returns
+ * FA_ERR_INVALID_ARG if exactly one of them is NULL. */
+fa_status fa_set_timing_events(void* begin, void* end);
 
 #ifdef __cplusplus
 }

@@ -13,5 +13,6 @@ from .binding import (  # noqa: F401
     get_status,
     last_launch_count,
     load,
+    set_timing_events,
     workspace,
 )

@@ -58,6 +58,8 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.fa_status_string.restype = ctypes.c_char_p
     lib.fa_last_launch_count.argtypes = []
     lib.fa_last_launch_count.restype = i
+    lib.fa_set_timing_events.argtypes = [vp, vp]
+    lib.fa_set_timing_events.restype = i
     _lib = lib
     return lib
 
@@ -175,3 +177,13 @@ def get_status(ws: torch.Tensor, stream=None) -> int:
 
 def last_launch_count() -> int:
     return load().fa_last_launch_count()
+
+
+def set_timing_events(begin=None, end=None):
+    """Record torch.cuda.Event `begin`/`end` around the main attention kernel
+    of the following calls on this thread (None, None turns it off)."""
+    b = None if begin is None else ctypes.c_void_p(begin.cuda_event)
+    e = None if end is None else ctypes.c_void_p(end.cuda_event)
+    rc = load().fa_set_timing_events(b, e)
+    if rc != FA_OK:
+        raise FAError(rc, "fa_set_timing_events")

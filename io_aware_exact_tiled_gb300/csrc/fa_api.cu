@@ -12,6 +12,7 @@ namespace {
 
 constexpr size_t kStatusBytes = 256;
 thread_local int g_last_launches = 0;
+thread_local cudaEvent_t g_ev_begin = nullptr, g_ev_end = nullptr;
 
 size_t align256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
 
@@ -36,8 +37,8 @@ extern "C" {
 
 size_t fa_fwd_workspace_size(int B, int H, int N, int d) {
     if (B <= 0 || H <= 0 || N <= 0 || d <= 0) return 0;
-    // status word + room for an fp32 transposed copy of V (fp32 inputs only)
-    return kStatusBytes + align256(static_cast<size_t>(B) * H * N * d * sizeof(float));
+    // status word + fp32 inputs only: V^T and the tf32 high/low parts of Q, K
+    return kStatusBytes + 5 * align256(static_cast<size_t>(B) * H * N * d * sizeof(float));
 }
 
 size_t fa_bwd_workspace_size(int B, int H, int N, int d) {
@@ -78,7 +79,9 @@ fa_status fa_fwd(const void* q, const void* k, const void* v, void* o, float* ls
     a.kv_len = kv_len;
     a.fp32 = dtype == FA_FP32;
     a.status = static_cast<int*>(workspace);
-    a.vt_scratch = static_cast<char*>(workspace) + kStatusBytes;
+    a.fp32_scratch = static_cast<char*>(workspace) + kStatusBytes;
+    a.ev_begin = g_ev_begin;
+    a.ev_end = g_ev_end;
     if (cudaMemsetAsync(a.status, 0, sizeof(int) * 4, s) != cudaSuccess) return FA_ERR_CUDA;
     int n = 0;
     st = map_cuda(fa::launch_fwd(a, s, &n));
@@ -127,6 +130,8 @@ fa_status fa_bwd(const void* q, const void* k, const void* v, const void* o, con
     a.delta = reinterpret_cast<float*>(ws + kStatusBytes);
     a.lse2 = reinterpret_cast<float*>(ws + kStatusBytes + align256(rows * sizeof(float)));
     a.dq_accum = reinterpret_cast<float*>(ws + kStatusBytes + 2 * align256(rows * sizeof(float)));
+    a.ev_begin = g_ev_begin;
+    a.ev_end = g_ev_end;
     if (cudaMemsetAsync(a.status, 0, sizeof(int) * 4, s) != cudaSuccess) return FA_ERR_CUDA;
     int n = 0;
     st = map_cuda(fa::launch_bwd(a, s, &n));
@@ -157,5 +162,12 @@ const char* fa_status_string(fa_status s) {
 }
 
 int fa_last_launch_count(void) { return g_last_launches; }
+
+fa_status fa_set_timing_events(void* begin, void* end) {
+    if ((begin == nullptr) != (end == nullptr)) return FA_ERR_INVALID_ARG;
+    g_ev_begin = static_cast<cudaEvent_t>(begin);
+    g_ev_end = static_cast<cudaEvent_t>(end);
+    return FA_OK;
+}
 
 }  // extern "C"

@@ -487,7 +487,9 @@ static cudaError_t launch_bwd_t(const BwdArgs& a, cudaStream_t stream, int* nlau
     p.dq_accum = a.dq_accum;
     p.status = a.status;
     dim3 grid(a.H, a.B, a.N / kTile);
+    if (a.ev_begin) cudaEventRecord(a.ev_begin, stream);
     fa_bwd_kernel<D><<<grid, 384, C::SMEM, stream>>>(tq, tk, tv, tdo, p);
+    if (a.ev_end) cudaEventRecord(a.ev_end, stream);
     const long long n8 = nrows * D / 8;
     long long blocks = (n8 + 255) / 256;
     if (blocks > 152 * 16) blocks = 152 * 16;

@@ -24,9 +24,10 @@
 // The online-softmax reference maximum is only moved (and O rescaled) when
 // the row maximum grows by more than 2^8 in the exp2 domain; otherwise the
 // stale maximum is kept, which is exact because o and l always share it.
-// The running sum l adds the probabilities after their rounding to bf16, i.e.
-// exactly the weights the P V product uses, so that O = o / l is a convex
-// combination of rows of V even in bf16.
+// Two running sums are kept: l over the fp32 probabilities, which gives L,
+// and lw over the same probabilities after their rounding to bf16, i.e. the
+// weights the P V product actually multiplies, which normalises O so that it
+// is a convex combination of rows of V even with bf16 weights.
 #include <math_constants.h>
 
 #include "fa_common.cuh"
@@ -41,11 +42,14 @@ struct FwdCfg {
     static constexpr int ROWB = D * ELEM;              // bytes per row of Q/K/V
     static constexpr int NREG = ROWB / 128;            // 128-byte swizzle regions per row
     static constexpr int TILE_BYTES = kTile * ROWB;    // one 128-row tile
-    static constexpr int STAGES = TILE_BYTES <= 16384 ? 4 : 2;
+    // fp32 inputs: S is formed from tf32 high and low parts of Q and K
+    // (Qh Kh^T + Qh Kl^T + Ql Kh^T), so Q and K tiles come in two copies.
+    static constexpr int SPLIT = TF32 ? 2 : 1;
+    static constexpr int STAGES = TF32 ? 1 : (TILE_BYTES <= 16384 ? 4 : 2);
     static constexpr int NQ = 2;                       // query tiles per CTA
     static constexpr int Q_OFF = 0;
-    static constexpr int K_OFF = Q_OFF + NQ * TILE_BYTES;
-    static constexpr int V_OFF = K_OFF + STAGES * TILE_BYTES;
+    static constexpr int K_OFF = Q_OFF + NQ * SPLIT * TILE_BYTES;
+    static constexpr int V_OFF = K_OFF + STAGES * SPLIT * TILE_BYTES;
     static constexpr int BAR_OFF = V_OFF + STAGES * TILE_BYTES;
     static constexpr int SMEM = BAR_OFF + 256 + 1024;  // + barriers + alignment slack
     static constexpr int KSTEP = 32 / ELEM;            // K elements per MMA instruction
@@ -75,7 +79,8 @@ constexpr float kLn2 = 0.69314718055994530942f;
 template <bool TF32, int D>
 __global__ void __launch_bounds__(384, 1)
     fa_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
-                  const __grid_constant__ CUtensorMap tmV, const FwdParams p) {
+                  const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmQlo,
+                  const __grid_constant__ CUtensorMap tmKlo, const FwdParams p) {
     using C = FwdCfg<TF32, D>;
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -126,6 +131,10 @@ __global__ void __launch_bounds__(384, 1)
         tma_prefetch_desc(&tmQ);
         tma_prefetch_desc(&tmK);
         tma_prefetch_desc(&tmV);
+        if constexpr (TF32) {
+            tma_prefetch_desc(&tmQlo);
+            tma_prefetch_desc(&tmKlo);
+        }
     }
     if (warp == 1) {
         tmem_alloc(tmem_slot, 512);
@@ -147,22 +156,28 @@ __global__ void __launch_bounds__(384, 1)
         // ------------------------------------------------------------ producer
         if (lane == 0) {
             const int qrow0 = bh * N + qb0 * kTile;
-            mbar_arrive_expect_tx(bar_q, (act1 ? 2 : 1) * C::TILE_BYTES);
+            mbar_arrive_expect_tx(bar_q, (act1 ? 2 : 1) * C::SPLIT * C::TILE_BYTES);
             for (int s = 0; s < (act1 ? 2 : 1); ++s)
-                for (int r = 0; r < C::NREG; ++r)
-                    tma_load_2d(sm + C::Q_OFF + s * C::TILE_BYTES + r * 16384, &tmQ, r * C::BOXC,
-                                qrow0 + s * kTile, bar_q);
+                for (int r = 0; r < C::NREG; ++r) {
+                    uint8_t* dq = sm + C::Q_OFF + s * C::SPLIT * C::TILE_BYTES + r * 16384;
+                    tma_load_2d(dq, &tmQ, r * C::BOXC, qrow0 + s * kTile, bar_q);
+                    if constexpr (TF32) tma_load_2d(dq + C::TILE_BYTES, &tmQlo, r * C::BOXC, qrow0 + s * kTile, bar_q);
+                }
             int u = 0;
             for (int t = 0; t < hi; ++t) {
                 if (!need_of(t)) continue;
                 const int stage = u % C::STAGES;
                 const uint32_t ph = (u / C::STAGES) & 1;
                 if (!mbar_wait(&kv_empty[stage], ph ^ 1, cx, 1)) break;
-                uint8_t* sk = sm + C::K_OFF + stage * C::TILE_BYTES;
+                uint8_t* sk = sm + C::K_OFF + stage * C::SPLIT * C::TILE_BYTES;
                 uint8_t* sv = sm + C::V_OFF + stage * C::TILE_BYTES;
-                mbar_arrive_expect_tx(&k_full[stage], C::TILE_BYTES);
-                for (int r = 0; r < C::NREG; ++r)
+                mbar_arrive_expect_tx(&k_full[stage], C::SPLIT * C::TILE_BYTES);
+                for (int r = 0; r < C::NREG; ++r) {
                     tma_load_2d(sk + r * 16384, &tmK, r * C::BOXC, bh * N + t * kTile, &k_full[stage]);
+                    if constexpr (TF32)
+                        tma_load_2d(sk + C::TILE_BYTES + r * 16384, &tmKlo, r * C::BOXC, bh * N + t * kTile,
+                                    &k_full[stage]);
+                }
                 mbar_arrive_expect_tx(&v_full[stage], C::TILE_BYTES);
                 if constexpr (!TF32) {
                     for (int r = 0; r < C::NREG; ++r)
@@ -230,6 +245,12 @@ __global__ void __launch_bounds__(384, 1)
                 if (!nd) continue;
                 const int stage = u % C::STAGES;
                 const uint32_t ph = (u / C::STAGES) & 1;
+                // The producer refills this stage only after every P V that
+                // reads its previous tile: issue those first.
+#pragma unroll
+                for (int s = 0; s < 2; ++s)
+                    if (ok && pend_stage[s] == stage && !issue_pv(s)) ok = false;
+                if (!ok) break;
                 if (!mbar_wait(&k_full[stage], ph, cx, 5)) { ok = false; break; }
                 tc_fence_after();
                 rem = (rem & ~(3u << (2 * stage))) | ((uint32_t)__popc(nd) << (2 * stage));
@@ -237,13 +258,19 @@ __global__ void __launch_bounds__(384, 1)
                 for (int s = 0; s < 2; ++s) {
                     if (!(nd & (1u << s))) continue;
                     if (pend_stage[s] >= 0 && !issue_pv(s)) { ok = false; break; }
-                    const uint32_t qs = qbase + s * C::TILE_BYTES;
-                    const uint32_t ks = kbase + stage * C::TILE_BYTES;
+                    const uint32_t qs = qbase + s * C::SPLIT * C::TILE_BYTES;
+                    const uint32_t ks = kbase + stage * C::SPLIT * C::TILE_BYTES;
+                    // bf16: one product; fp32: (Qh, Kh), (Qh, Kl), (Ql, Kh)
 #pragma unroll
-                    for (int kk = 0; kk < C::S_KSTEPS; ++kk) {
-                        const uint32_t off = (kk / 4) * 16384 + (kk % 4) * 32;
-                        umma_ss<TF32>(tm + s * 256, sdesc_sw128(qs + off, 16, 1024), sdesc_sw128(ks + off, 16, 1024),
-                                      C::ID_S, kk > 0 ? 1u : 0u);
+                    for (int part = 0; part < (TF32 ? 3 : 1); ++part) {
+                        const uint32_t qa = qs + (part == 2 ? C::TILE_BYTES : 0);
+                        const uint32_t kb2 = ks + (part == 1 ? C::TILE_BYTES : 0);
+#pragma unroll
+                        for (int kk = 0; kk < C::S_KSTEPS; ++kk) {
+                            const uint32_t off = (kk / 4) * 16384 + (kk % 4) * 32;
+                            umma_ss<TF32>(tm + s * 256, sdesc_sw128(qa + off, 16, 1024),
+                                          sdesc_sw128(kb2 + off, 16, 1024), C::ID_S, (part > 0 || kk > 0) ? 1u : 0u);
+                        }
                     }
                     umma_commit(&s_full[s]);
                     pend_stage[s] = stage;
@@ -267,7 +294,10 @@ __global__ void __launch_bounds__(384, 1)
         const int grow = qb * kTile + r;  // query row within the sequence
         const uint32_t tl = tm + (static_cast<uint32_t>(wq * 32) << 16) + s * 256;
         const float c2 = p.scale_log2;
-        float m_hat = -CUDART_INF_F, l = 0.f;
+        // l: running sum of the fp32 probabilities (gives L); lw: running sum
+        // of the same probabilities rounded to the bf16 weights that the P V
+        // product multiplies (normalises O)
+        float m_hat = -CUDART_INF_F, l = 0.f, lw = 0.f;
         int n = 0;
         bool ok = true;
         if (active) {
@@ -303,9 +333,10 @@ __global__ void __launch_bounds__(384, 1)
                     alpha = ex2_approx(m_hat - m_new);
                     m_hat = m_new;
                     l *= alpha;
+                    lw *= alpha;
                 }
                 const float mu = (m_hat == -CUDART_INF_F) ? 0.f : m_hat;
-                float rs = 0.f;
+                float rs = 0.f, rr = 0.f;
 #pragma unroll
                 for (int c = 0; c < 4; ++c) {
                     if constexpr (!TF32) {
@@ -315,8 +346,8 @@ __global__ void __launch_bounds__(384, 1)
                             const float p0 = ex2_approx(fmaf(__uint_as_float(sr[c][2 * i]), c2, -mu));
                             const float p1 = ex2_approx(fmaf(__uint_as_float(sr[c][2 * i + 1]), c2, -mu));
                             pk[i] = pack_bf16x2(p0, p1);
-                            // l sums the bf16 weights that the PV product uses
-                            rs += __uint_as_float(pk[i] << 16) + __uint_as_float(pk[i] & 0xFFFF0000u);
+                            rs += p0 + p1;
+                            rr += __uint_as_float(pk[i] << 16) + __uint_as_float(pk[i] & 0xFFFF0000u);
                         }
                         tmem_st16(tl + c * 16, pk);
                     } else {
@@ -327,10 +358,12 @@ __global__ void __launch_bounds__(384, 1)
                             rs += p0;
                             pk[i] = __float_as_uint(p0);
                         }
+                        rr = rs;
                         tmem_st32(tl + c * 32, pk);
                     }
                 }
                 l += rs;
+                lw += rr;
                 tmem_st_wait();
                 if (__any_sync(0xffffffffu, resc) && n > 0) {
                     // O holds the previous tiles' sum: wait for their last PV,
@@ -361,7 +394,7 @@ __global__ void __launch_bounds__(384, 1)
                 if (ok) tc_fence_after();
             }
             if (ok) {
-                const float inv = l > 0.f ? 1.f / l : 0.f;
+                const float inv = lw > 0.f ? 1.f / lw : 0.f;
                 const size_t orow = (static_cast<size_t>(bh) * N + grow) * D;
 #pragma unroll
                 for (int c = 0; c < D / 32; ++c) {
@@ -405,6 +438,24 @@ __global__ void __launch_bounds__(384, 1)
     }
 }
 
+// fp32 inputs: x = hi + lo with hi = x with its 13 low mantissa bits cleared
+// (exactly representable in tf32) and lo = x - hi (exact in fp32, |lo| <
+// 2^-10 |x|), so that products of tf32 parts recover S to about fp32 accuracy.
+__global__ void fa_split_tf32_kernel(const float4* __restrict__ x, float4* __restrict__ hi, float4* __restrict__ lo,
+                                     long long n4) {
+    for (long long i = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x; i < n4;
+         i += static_cast<long long>(gridDim.x) * blockDim.x) {
+        const float4 a = x[i];
+        float4 h;
+        h.x = __uint_as_float(__float_as_uint(a.x) & 0xFFFFE000u);
+        h.y = __uint_as_float(__float_as_uint(a.y) & 0xFFFFE000u);
+        h.z = __uint_as_float(__float_as_uint(a.z) & 0xFFFFE000u);
+        h.w = __uint_as_float(__float_as_uint(a.w) & 0xFFFFE000u);
+        hi[i] = h;
+        lo[i] = make_float4(a.x - h.x, a.y - h.y, a.z - h.z, a.w - h.w);
+    }
+}
+
 // V [BH][N][d] fp32 -> V^T [BH][d][N] (tf32 operands of tcgen05 must be K-major)
 __global__ void fa_transpose_v_kernel(const float* __restrict__ v, float* __restrict__ vt, int N, int D) {
     __shared__ float tile[32][33];
@@ -422,19 +473,35 @@ static cudaError_t launch_fwd_t(const FwdArgs& a, cudaStream_t stream, int* nlau
     using C = FwdCfg<TF32, D>;
     const int elem = TF32 ? 4 : 2;
     const uint64_t rows = static_cast<uint64_t>(a.B) * a.H * a.N;
-    CUtensorMap tq, tk, tv;
-    if (!make_tmap_2d_sw128(&tq, a.q, rows, D, elem, kTile, C::BOXC)) return cudaErrorInvalidValue;
-    if (!make_tmap_2d_sw128(&tk, a.k, rows, D, elem, kTile, C::BOXC)) return cudaErrorInvalidValue;
+    CUtensorMap tq, tk, tv, tql, tkl;
     int launches = 0;
     if constexpr (TF32) {
-        float* vt = static_cast<float*>(a.vt_scratch);
+        // scratch: V^T, Qh, Ql, Kh, Kl (each [B,H,N,d] fp32)
+        const size_t n = rows * D;
+        float* vt = static_cast<float*>(a.fp32_scratch);
+        float *qh = vt + n, *ql = qh + n, *kh = ql + n, *kl = kh + n;
         dim3 g(a.N / 32, D / 32, a.B * a.H);
         fa_transpose_v_kernel<<<g, dim3(32, 8), 0, stream>>>(static_cast<const float*>(a.v), vt, a.N, D);
-        ++launches;
-        if (!make_tmap_2d_sw128(&tv, vt, static_cast<uint64_t>(a.B) * a.H * D, a.N, elem, D, C::BOXC))
+        const long long n4 = static_cast<long long>(n / 4);
+        const unsigned blocks = static_cast<unsigned>(n4 < 152 * 32 * 256 ? (n4 + 255) / 256 : 152 * 32);
+        fa_split_tf32_kernel<<<blocks, 256, 0, stream>>>(static_cast<const float4*>(a.q), reinterpret_cast<float4*>(qh),
+                                                         reinterpret_cast<float4*>(ql), n4);
+        fa_split_tf32_kernel<<<blocks, 256, 0, stream>>>(static_cast<const float4*>(a.k), reinterpret_cast<float4*>(kh),
+                                                         reinterpret_cast<float4*>(kl), n4);
+        launches += 3;
+        if (!make_tmap_2d_sw128(&tv, vt, static_cast<uint64_t>(a.B) * a.H * D, a.N, elem, D, C::BOXC) ||
+            !make_tmap_2d_sw128(&tq, qh, rows, D, elem, kTile, C::BOXC) ||
+            !make_tmap_2d_sw128(&tql, ql, rows, D, elem, kTile, C::BOXC) ||
+            !make_tmap_2d_sw128(&tk, kh, rows, D, elem, kTile, C::BOXC) ||
+            !make_tmap_2d_sw128(&tkl, kl, rows, D, elem, kTile, C::BOXC))
             return cudaErrorInvalidValue;
     } else {
-        if (!make_tmap_2d_sw128(&tv, a.v, rows, D, elem, kTile, C::BOXC)) return cudaErrorInvalidValue;
+        if (!make_tmap_2d_sw128(&tq, a.q, rows, D, elem, kTile, C::BOXC) ||
+            !make_tmap_2d_sw128(&tk, a.k, rows, D, elem, kTile, C::BOXC) ||
+            !make_tmap_2d_sw128(&tv, a.v, rows, D, elem, kTile, C::BOXC))
+            return cudaErrorInvalidValue;
+        tql = tq;
+        tkl = tk;
     }
     static bool attr_set = false;
     if (!attr_set) {
@@ -456,7 +523,9 @@ static cudaError_t launch_fwd_t(const FwdArgs& a, cudaStream_t stream, int* nlau
     p.status = a.status;
     const int T = a.N / kTile;
     dim3 grid(a.H, a.B, (T + 1) / 2);
-    fa_fwd_kernel<TF32, D><<<grid, C::THREADS, C::SMEM, stream>>>(tq, tk, tv, p);
+    if (a.ev_begin) cudaEventRecord(a.ev_begin, stream);
+    fa_fwd_kernel<TF32, D><<<grid, C::THREADS, C::SMEM, stream>>>(tq, tk, tv, tql, tkl, p);
+    if (a.ev_end) cudaEventRecord(a.ev_end, stream);
     ++launches;
     *nlaunch = launches;
     return cudaGetLastError();

@@ -17,8 +17,9 @@ struct FwdArgs {
     const uint8_t* blockmask;
     const int32_t* kv_len;
     int fp32;
-    void* vt_scratch;  // fp32 only: [B,H,d,N] transposed V
+    void* fp32_scratch;  // fp32 only: V^T [B,H,d,N], then Qh, Ql, Kh, Kl [B,H,N,d]
     int* status;
+    cudaEvent_t ev_begin, ev_end;  // optional, recorded around the main kernel
 };
 
 struct BwdArgs {
@@ -34,6 +35,7 @@ struct BwdArgs {
     float* lse2;      // [B,H,N] scratch: L in log2 units
     float* dq_accum;  // [B,H,N,d] fp32 scratch
     int* status;
+    cudaEvent_t ev_begin, ev_end;  // optional, recorded around the main kernel
 };
 
 cudaError_t launch_fwd(const FwdArgs& a, cudaStream_t stream, int* nlaunch);

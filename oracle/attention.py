@@ -110,13 +110,14 @@ def _heads(q, kv_len):
 
 
 def forward(q, k, v, scale: float, causal: bool = False, kv_len=None,
-            blockmask=None, chunk: int = 1024, heads=None, tile: int = TILE):
+            blockmask=None, chunk: int = 1024, heads=None, tile: int = TILE, rows=None):
     """Exact attention forward on [B, H, N, d] inputs, in fp64.
 
     O = softmax(scale * Q K^T + mask) V and L = m + log(sum exp(S - m))
     per row (natural log). ``heads`` optionally restricts the work to a list
     of (b, h) pairs; the other heads of the outputs are left as NaN.
     ``tile`` is the edge of the square tiles that ``blockmask`` describes.
+    ``rows`` = (r0, r1) optionally restricts the work to those query rows.
     Returns (O [B,H,N,d], L [B,H,N]) as float64 numpy arrays.
     """
     q, k, v = _f64(q), _f64(k), _f64(v)
@@ -127,14 +128,15 @@ def forward(q, k, v, scale: float, causal: bool = False, kv_len=None,
     for b, h, kb in _heads(q, kv_len):
         if want is not None and (b, h) not in want:
             continue
-        for r0 in range(0, N, chunk):
-            rows = np.arange(r0, min(N, r0 + chunk))
-            vis = visible(N, causal, kb, blockmask, rows, tile)
-            s = scores(q[b, h, rows], k[b, h], scale, vis)
+        lo, hi = (0, N) if rows is None else rows
+        for r0 in range(lo, hi, chunk):
+            rr = np.arange(r0, min(hi, r0 + chunk))
+            vis = visible(N, causal, kb, blockmask, rr, tile)
+            s = scores(q[b, h, rr], k[b, h], scale, vis)
             p, m, lsum = probabilities(s)
-            O[b, h, rows] = p @ v[b, h]
+            O[b, h, rr] = p @ v[b, h]
             with np.errstate(divide="ignore"):
-                L[b, h, rows] = np.where(lsum > 0, m + np.log(np.where(lsum > 0, lsum, 1.0)), -np.inf)
+                L[b, h, rr] = np.where(lsum > 0, m + np.log(np.where(lsum > 0, lsum, 1.0)), -np.inf)
     return O, L
 
 
@@ -145,13 +147,15 @@ def row_stat_D(do, o) -> np.ndarray:
 
 
 def backward(q, k, v, do, scale: float, causal: bool = False, kv_len=None,
-             blockmask=None, chunk: int = 1024, heads=None, tile: int = TILE):
+             blockmask=None, chunk: int = 1024, heads=None, tile: int = TILE, rows=None):
     """Gradients of <dO, O> with respect to Q, K, V, in fp64.
 
     Plain derivative of the definition (not written on the pages):
     dV = P^T dO, dP = dO V^T, dS = P * (dP - rowsum(P * dP)),
     dQ = scale * dS K, dK = scale * dS^T Q. Masked entries have P = 0 and so
-    carry no gradient. Returns (dQ, dK, dV) as float64 numpy arrays.
+    carry no gradient. ``rows`` = (r0, r1) restricts the sum to those query
+    rows (dK, dV then hold only their contribution). Returns (dQ, dK, dV) as
+    float64 numpy arrays.
     """
     q, k, v, do = _f64(q), _f64(k), _f64(v), _f64(do)
     B, H, N, d = q.shape
@@ -164,16 +168,17 @@ def backward(q, k, v, do, scale: float, causal: bool = False, kv_len=None,
             continue
         dk_bh = np.zeros((N, d))
         dv_bh = np.zeros((N, d))
-        for r0 in range(0, N, chunk):
-            rows = np.arange(r0, min(N, r0 + chunk))
-            vis = visible(N, causal, kb, blockmask, rows, tile)
-            s = scores(q[b, h, rows], k[b, h], scale, vis)
+        lo, hi = (0, N) if rows is None else rows
+        for r0 in range(lo, hi, chunk):
+            rr = np.arange(r0, min(hi, r0 + chunk))
+            vis = visible(N, causal, kb, blockmask, rr, tile)
+            s = scores(q[b, h, rr], k[b, h], scale, vis)
             p, _, _ = probabilities(s)
-            do_c = do[b, h, rows]
+            do_c = do[b, h, rr]
             dp = do_c @ v[b, h].T
             ds = p * (dp - (p * dp).sum(axis=1, keepdims=True))
-            dq[b, h, rows] = scale * (ds @ k[b, h])
-            dk_bh += scale * (ds.T @ q[b, h, rows])
+            dq[b, h, rr] = scale * (ds @ k[b, h])
+            dk_bh += scale * (ds.T @ q[b, h, rr])
             dv_bh += p.T @ do_c
         dk[b, h] = dk_bh
         dv[b, h] = dv_bh

@@ -321,3 +321,21 @@ def test_heads_subset():
     dq, dk, dv = oracle.backward(q, k, v, do, 0.5, heads=[(0, 1)])
     gq, gk, gv = oracle.backward(q, k, v, do, 0.5)
     np.testing.assert_allclose(dk[0, 1], gk[0, 1], atol=0)
+
+
+def test_row_subsets_partition_the_work():
+    q, k, v, do = (rnd((1, 2, 300, 5), s) for s in (90, 91, 92, 93))
+    kw = dict(causal=True, kv_len=[250])
+    O, L = oracle.forward(q, k, v, 0.5, **kw)
+    dq, dk, dv = oracle.backward(q, k, v, do, 0.5, **kw)
+    parts = [(0, 128), (128, 200), (200, 300)]
+    acc_k, acc_v = 0, 0
+    for r in parts:
+        Os, Ls = oracle.forward(q, k, v, 0.5, rows=r, chunk=50, **kw)
+        np.testing.assert_allclose(Os[:, :, r[0]:r[1]], O[:, :, r[0]:r[1]], atol=1e-13)
+        gq, gk, gv = oracle.backward(q, k, v, do, 0.5, rows=r, chunk=50, **kw)
+        np.testing.assert_allclose(gq[:, :, r[0]:r[1]], dq[:, :, r[0]:r[1]], atol=1e-13)
+        acc_k = acc_k + gk
+        acc_v = acc_v + gv
+    np.testing.assert_allclose(acc_k, dk, atol=1e-12)
+    np.testing.assert_allclose(acc_v, dv, atol=1e-12)
