@@ -117,6 +117,31 @@ fa_status fa_bwd(const void* q, const void* k, const void* v, const void* o, con
                  const uint8_t* blockmask, const int32_t* kv_len, fa_dtype dtype, void* workspace, size_t ws_bytes,
                  void* stream);
 
+/*
+ * Backward pass without a caller-supplied workspace. The pages describe no
+ * counterpart of this call; it exists for callers that cannot allocate
+ * device memory when they run the backward pass (for example a plug-in whose
+ * host runtime gives it tensors but no allocator, or a latency-critical loop
+ * that must not call cudaMalloc / cudaFree because they can synchronise the
+ * device). Arguments and results are those of fa_bwd minus the workspace:
+ * the scratch fa_bwd would take from the workspace comes from a fixed 32 MiB
+ * device array inside the library, which every GPU that loads the library
+ * keeps until the process exits. Nothing is allocated.
+ *   - Requests with fa_bwd_workspace_size(B, H, N, d) > 32 MiB return
+ *     FA_ERR_UNSUPPORTED without launching anything.
+ *   - All calls on a device share that array and it keeps the previous call's
+ *     contents; each call re-zeroes what must start at zero. Calls that can
+ *     overlap on the GPU (other streams, unordered host threads) race on it:
+ *     serialise them on one stream.
+ *   - The first call on each device (with that device current) looks up the
+ *     array's device address; make that first call before any stream capture.
+ *   - Device-side wait time-outs are recorded in the array's status word,
+ *     which this entry point does not expose.
+ */
+fa_status fa_bwd_noalloc(const void* q, const void* k, const void* v, const void* o, const float* lse,
+                         const void* dout, void* dq, void* dk, void* dv, int B, int H, int N, int d, float scale,
+                         int causal, const uint8_t* blockmask, const int32_t* kv_len, fa_dtype dtype, void* stream);
+
 /* Synchronises `stream`, then reads and clears the device status word of
  * `workspace` (of the fa_fwd or fa_bwd call that used it). Returns FA_OK or
  * FA_ERR_TIMEOUT (a device-side wait gave up; the outputs are then invalid),

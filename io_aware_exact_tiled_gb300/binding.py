@@ -187,3 +187,29 @@ def set_timing_events(begin=None, end=None):
     rc = load().fa_set_timing_events(b, e)
     if rc != FA_OK:
         raise FAError(rc, "fa_set_timing_events")
+
+
+def backward_noalloc(q, k, v, o, lse, do, scale: Optional[float] = None, causal: bool = False, blockmask=None,
+                     kv_len=None, dq=None, dk=None, dv=None, stream=None):
+    """dQ, dK, dV = fa_bwd_noalloc(...): the backward pass with the library's
+    own fixed scratch instead of a workspace (for callers that cannot allocate
+    device memory). Outputs are allocated here only if not passed in."""
+    lib = load()
+    fn = lib.fa_bwd_noalloc
+    vp, i, f = ctypes.c_void_p, ctypes.c_int, ctypes.c_float
+    fn.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, i, i, i, i, f, i, vp, vp, i, vp]
+    fn.restype = i
+    dtype = _check_qkv(q, k, v, o, do)
+    B, H, N, d = q.shape
+    if lse.dtype != torch.float32 or lse.shape != (B, H, N) or not lse.is_contiguous():
+        raise ValueError("lse must be a contiguous float32 [B, H, N] tensor")
+    scale = 1.0 / math.sqrt(d) if scale is None else float(scale)
+    dq = torch.empty_like(q) if dq is None else dq
+    dk = torch.empty_like(k) if dk is None else dk
+    dv = torch.empty_like(v) if dv is None else dv
+    bm, kl = _mask_ptrs(blockmask, kv_len, q)
+    rc = fn(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), _ptr(do), _ptr(dq), _ptr(dk), _ptr(dv), B, H, N, d,
+            scale, int(bool(causal)), bm, kl, dtype, _stream_handle(stream))
+    if rc != FA_OK:
+        raise FAError(rc, "fa_bwd_noalloc")
+    return dq, dk, dv
