@@ -25,7 +25,8 @@ fa_status check_shape(int B, int H, int N, int d, float scale) {
     if (d != 64 && d != 128) return FA_ERR_UNSUPPORTED;
     if (N % 128 != 0) return FA_ERR_UNSUPPORTED;
     if (static_cast<long long>(B) * H * N >= (1LL << 31)) return FA_ERR_UNSUPPORTED;
-    if (B > 65535 || (N / 128 + 1) / 2 > 65535) return FA_ERR_UNSUPPORTED;
+    // grid limits: forward (H, B, pairs of query tiles), backward (N/128, H, B)
+    if (B > 65535 || H > 65535 || (N / 128 + 1) / 2 > 65535) return FA_ERR_UNSUPPORTED;
     return FA_OK;
 }
 

@@ -19,16 +19,13 @@
 //                       stream through a two-stage TMA ring; five tcgen05
 //                       GEMMs per tile with dK_j and dV_j accumulated in TMEM;
 //                       dQ_i = dS K_j is added into the fp32 accumulator with
-//                       vector atomics
+//                       TMA bulk reduce-adds staged through shared memory
 //   fa_bwd_dq_kernel    fp32 dQ accumulator -> dQ in bf16
 //
-// Warp roles of fa_bwd_kernel (384 threads):
-//   warp 0      TMA producer (K_j, V_j once; Q_i, dO_i, L_i, D_i per stage)
-//   warp 1      TMEM allocation; lane 0 issues the MMAs
-//   warps 4-7   thread r owns key r of the block: P^T and dS^T rows
-//   warps 8-11  thread r owns query r of the current block: dQ drain
-// TMEM columns: [0,128) S^T, overwritten by P^T (bf16); [128,256) dP^T, then
-// dQ_i; [256, 256+d) dV_j; [256+d, 256+2d) dK_j.
+// TMEM columns of fa_bwd_kernel: [0,128) S^T, then P^T (bf16), then dQ_i;
+// [128,256) dP^T; [256, 256+d) dV_j; [256+d, 256+2d) dK_j. The softmax
+// scale is applied once, to dK_j in the epilogue and to dQ in the conversion
+// kernel, instead of to every element of dS.
 #include <math_constants.h>
 
 #include "fa_common.cuh"
@@ -53,10 +50,12 @@ struct BwdCfg {
     static constexpr int BAR_OFF = DEL_OFF + STAGES * 512;
     static constexpr int USED = BAR_OFF + 256;
     static constexpr int SMEM = USED + 1024 <= 232448 ? USED + 1024 : 232448;
+    static constexpr int THREADS = 512;
     static constexpr uint32_t ID_SQ = idesc_make(128, 128, kFmtBF16, false, false);  // S^T, dP^T
     static constexpr uint32_t ID_KN = idesc_make(128, D, kFmtBF16, false, true);     // dV, dK
     static constexpr uint32_t ID_DQ = idesc_make(128, D, kFmtBF16, true, true);      // dQ
-    static constexpr int COL_S = 0, COL_DP = 128, COL_DQ = 128, COL_DV = 256, COL_DK = 256 + D;
+    // dQ_i reuses the S^T / P^T columns once dV_i has read P^T
+    static constexpr int COL_S = 0, COL_DQ = 0, COL_DP = 128, COL_DV = 256, COL_DK = 256 + D;
 };
 
 struct BwdParams {
@@ -68,17 +67,27 @@ struct BwdParams {
     const float* delta;
     void* dk;
     void* dv;
-    float* dq_accum;
     int* status;
 };
 
 constexpr float kLog2e = 1.4426950408889634f;
 
+// Warp roles (512 threads):
+//   warp 0        TMA producer (K_j, V_j once; Q_i, dO_i, L_i, D_i per stage)
+//   warp 1        TMEM allocation; lane 0 issues the MMAs
+//   warps 4-7     compute group 0: thread r owns key r, queries 0-63 of block i
+//   warps 8-11    compute group 1: key r, queries 64-127
+//   warps 12-15   dQ drain: thread r owns query r of block i
+// Per query block i the MMA thread issues, in this order:
+//   dP^T = V_j dO_i^T  (its columns were last read by the compute groups)
+//   S^T  = K_j Q_i^T   (after the drain has read dQ_{i-1} out of these columns)
+//   dV  += P^T dO_i    (P^T from TMEM, written by the compute groups)
+//   dK  += dS^T Q_i, dQ_i = dS K_j  (dS^T from shared memory)
 template <int D>
-__global__ void __launch_bounds__(384, 1)
+__global__ void __launch_bounds__(512, 1)
     fa_bwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                   const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmdO,
-                  const BwdParams p) {
+                  const __grid_constant__ CUtensorMap tmdQacc, const BwdParams p) {
     using C = BwdCfg<D>;
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -99,13 +108,17 @@ __global__ void __launch_bounds__(384, 1)
     uint64_t* ds_ready = p_ready + 1;
     uint64_t* dq_full = ds_ready + 1;
     uint64_t* dq_free = dq_full + 1;
-    uint64_t* dkv_done = dq_free + 1;
+    uint64_t* ds_free = dq_free + 1;   // dS^T buffer free again (drain done reading it)
+    uint64_t* dkv_done = ds_free + 1;
     uint64_t* drain = dkv_done + 1;
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
     const WaitCtx cx{abort_flag, p.status};
 
-    const int h = blockIdx.x, b = blockIdx.y, j = blockIdx.z;
+    // Head-major order: the key blocks of one head are adjacent in the grid
+    // (j = 0, the longest causal column, first), so the CTAs running at any
+    // time share the Q, dO and dQ-accumulator rows of a few heads in L2.
+    const int j = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
     const int N = p.N, T = p.mask.T;
     const int bh = b * p.H + h;
     const int kvalid = keys_valid(p.mask, b, N);
@@ -121,10 +134,11 @@ __global__ void __launch_bounds__(384, 1)
         }
         mbar_init(s_full, 1);
         mbar_init(dp_full, 1);
-        mbar_init(p_ready, 128);
-        mbar_init(ds_ready, 128);
+        mbar_init(p_ready, 256);
+        mbar_init(ds_ready, 256);
         mbar_init(dq_full, 1);
         mbar_init(dq_free, 128);
+        mbar_init(ds_free, 4);
         mbar_init(dkv_done, 1);
         mbar_init(drain, 1);
         fence_barrier_init();
@@ -134,6 +148,7 @@ __global__ void __launch_bounds__(384, 1)
         tma_prefetch_desc(&tmK);
         tma_prefetch_desc(&tmV);
         tma_prefetch_desc(&tmdO);
+        tma_prefetch_desc(&tmdQacc);
     }
     if (warp == 1) {
         tmem_alloc(tmem_slot, 512);
@@ -196,17 +211,7 @@ __global__ void __launch_bounds__(384, 1)
                 tc_fence_after();
                 const uint32_t qb = smem_u32(sm + C::Q_OFF + st * C::TILE_BYTES);
                 const uint32_t dob = smem_u32(sm + C::DO_OFF + st * C::TILE_BYTES);
-                // S^T = K_j Q_i^T
-#pragma unroll
-                for (int kk = 0; kk < D / 16; ++kk) {
-                    const uint32_t off = (kk / 4) * 16384 + (kk % 4) * 32;
-                    umma_ss<false>(tm + C::COL_S, sdesc_sw128(kb + off, 16, 1024), sdesc_sw128(qb + off, 16, 1024),
-                                   C::ID_SQ, kk > 0);
-                }
-                umma_commit(s_full);
-                // dP^T = V_j dO_i^T (its columns held dQ of the previous block)
-                if (u > 0 && !(ok = mbar_wait(dq_free, (u - 1) & 1, cx, 14))) break;
-                tc_fence_after();
+                // dP^T = V_j dO_i^T
 #pragma unroll
                 for (int kk = 0; kk < D / 16; ++kk) {
                     const uint32_t off = (kk / 4) * 16384 + (kk % 4) * 32;
@@ -214,13 +219,24 @@ __global__ void __launch_bounds__(384, 1)
                                    C::ID_SQ, kk > 0);
                 }
                 umma_commit(dp_full);
-                // dV_j += P^T dO_i
+                // S^T = K_j Q_i^T (these columns held dQ of the previous block)
+                if (u > 0 && !(ok = mbar_wait(dq_free, (u - 1) & 1, cx, 14))) break;
+                tc_fence_after();
+#pragma unroll
+                for (int kk = 0; kk < D / 16; ++kk) {
+                    const uint32_t off = (kk / 4) * 16384 + (kk % 4) * 32;
+                    umma_ss<false>(tm + C::COL_S, sdesc_sw128(kb + off, 16, 1024), sdesc_sw128(qb + off, 16, 1024),
+                                   C::ID_SQ, kk > 0);
+                }
+                umma_commit(s_full);
+                // dV_j += P^T dO_i ; P^T of queries 0-63 sits in columns 0-31
+                // and that of queries 64-127 in columns 64-95
                 if (!(ok = mbar_wait(p_ready, u & 1, cx, 15))) break;
                 tc_fence_after();
 #pragma unroll
                 for (int kk = 0; kk < 8; ++kk)
-                    umma_ts<false>(tm + C::COL_DV, tm + C::COL_S + kk * 8, sdesc_sw128(dob + kk * 2048, 16384, 1024),
-                                   C::ID_KN, (u > 0 || kk > 0) ? 1u : 0u);
+                    umma_ts<false>(tm + C::COL_DV, tm + C::COL_S + (kk >> 2) * 64 + (kk & 3) * 8,
+                                   sdesc_sw128(dob + kk * 2048, 16384, 1024), C::ID_KN, (u > 0 || kk > 0) ? 1u : 0u);
                 // dK_j += dS^T Q_i ; dQ_i = dS K_j
                 if (!(ok = mbar_wait(ds_ready, u & 1, cx, 16))) break;
                 tc_fence_after();
@@ -242,92 +258,87 @@ __global__ void __launch_bounds__(384, 1)
             umma_commit(drain);
             mbar_wait_teardown(drain, 0, 200000000ull);
         }
-    } else if (warp >= 4 && warp < 8) {
+    } else if (warp >= 4 && warp < 12) {
         // ------------------------------------------------------------ P^T, dS^T (thread = key)
+        const int g = (warp - 4) >> 2;       // query half: 64 g .. 64 g + 63
         const int r = (warp & 3) * 32 + lane;
         const uint32_t tl = tm + (static_cast<uint32_t>((warp & 3) * 32) << 16);
         const int key = j * kTile + r;
         const bool key_ok = key < kvalid;
         const float c2 = p.scale_log2;
-        uint8_t* ds_row = sm + C::DS_OFF + r * 128;
+        uint8_t* ds_row = sm + C::DS_OFF + g * 16384 + r * 128;
         bool ok = true;
         int u = 0;
         for (int i = lo; i < T; ++i) {
             if (!visible_i(i)) continue;
             const int st = u % C::STAGES;
             const uint32_t ph = (u / C::STAGES) & 1;
-            const float* lse_s = reinterpret_cast<const float*>(sm + C::LSE_OFF + st * 512);
-            const float* del_s = reinterpret_cast<const float*>(sm + C::DEL_OFF + st * 512);
+            const float* lse_s = reinterpret_cast<const float*>(sm + C::LSE_OFF + st * 512) + 64 * g;
+            const float* del_s = reinterpret_cast<const float*>(sm + C::DEL_OFF + st * 512) + 64 * g;
             ok = mbar_wait(&qd_full[st], ph, cx, 17);
-            ok = __all_sync(0xffffffffu, ok);
-            if (!ok) break;
-            ok = mbar_wait(s_full, u & 1, cx, 18);
-            ok = __all_sync(0xffffffffu, ok);
+            ok = __all_sync(0xffffffffu, ok) && __all_sync(0xffffffffu, mbar_wait(s_full, u & 1, cx, 18));
             if (!ok) break;
             tc_fence_after();
+            // masking is needed only on the diagonal tile (causal) or for
+            // padded keys
             const bool diag = p.mask.causal && i == j;
-            uint32_t pk[64];  // P^T row as bf16 pairs
+            const bool masked = diag || !key_ok;
+            uint32_t pk[32];  // P^T of this thread's 64 queries, bf16 pairs
 #pragma unroll
-            for (int c = 0; c < 4; ++c) {
+            for (int c = 0; c < 2; ++c) {
                 uint32_t sr[32];
-                tmem_ld32(tl + C::COL_S + c * 32, sr);
+                tmem_ld32(tl + C::COL_S + 64 * g + c * 32, sr);
                 tmem_ld_wait(sr);
 #pragma unroll
-                for (int g = 0; g < 8; ++g) {
-                    const float4 L4 = reinterpret_cast<const float4*>(lse_s)[c * 8 + g];
-                    float pv[4];
-                    pv[0] = ex2_approx(fmaf(__uint_as_float(sr[4 * g + 0]), c2, -L4.x));
-                    pv[1] = ex2_approx(fmaf(__uint_as_float(sr[4 * g + 1]), c2, -L4.y));
-                    pv[2] = ex2_approx(fmaf(__uint_as_float(sr[4 * g + 2]), c2, -L4.z));
-                    pv[3] = ex2_approx(fmaf(__uint_as_float(sr[4 * g + 3]), c2, -L4.w));
-#pragma unroll
-                    for (int e = 0; e < 4; ++e) {
-                        const int q = c * 32 + 4 * g + e;
-                        if (!key_ok || (diag && q < r)) pv[e] = 0.f;
+                for (int e = 0; e < 8; ++e) {
+                    const float4 L4 = reinterpret_cast<const float4*>(lse_s)[c * 8 + e];
+                    float pv0 = ex2_approx(fmaf(__uint_as_float(sr[4 * e + 0]), c2, -L4.x));
+                    float pv1 = ex2_approx(fmaf(__uint_as_float(sr[4 * e + 1]), c2, -L4.y));
+                    float pv2 = ex2_approx(fmaf(__uint_as_float(sr[4 * e + 2]), c2, -L4.z));
+                    float pv3 = ex2_approx(fmaf(__uint_as_float(sr[4 * e + 3]), c2, -L4.w));
+                    if (masked) {
+                        const int q = 64 * g + c * 32 + 4 * e;
+                        if (!key_ok || (diag && q + 0 < r)) pv0 = 0.f;
+                        if (!key_ok || (diag && q + 1 < r)) pv1 = 0.f;
+                        if (!key_ok || (diag && q + 2 < r)) pv2 = 0.f;
+                        if (!key_ok || (diag && q + 3 < r)) pv3 = 0.f;
                     }
-                    pk[c * 16 + 2 * g] = pack_bf16x2(pv[0], pv[1]);
-                    pk[c * 16 + 2 * g + 1] = pack_bf16x2(pv[2], pv[3]);
+                    pk[c * 16 + 2 * e] = pack_bf16x2(pv0, pv1);
+                    pk[c * 16 + 2 * e + 1] = pack_bf16x2(pv2, pv3);
                 }
-                tmem_st16(tl + C::COL_S + c * 16, &pk[c * 16]);
+                tmem_st16(tl + C::COL_S + 64 * g + c * 16, &pk[c * 16]);
             }
             tmem_st_wait();
             tc_fence_before();
             mbar_arrive(p_ready);
-            // dS^T = P^T * (dP^T - D) * scale, staged in shared memory
+            // dS^T = P^T * (dP^T - D) (the scale is applied to dK and dQ at the end)
             ok = mbar_wait(dp_full, u & 1, cx, 19);
+            if (u > 0) ok = ok && mbar_wait(ds_free, (u - 1) & 1, cx, 20);
             ok = __all_sync(0xffffffffu, ok);
             if (!ok) break;
-            if (u > 0) {
-                // the previous dS^T must have been consumed by its dK / dQ GEMMs
-                ok = mbar_wait(dq_full, (u - 1) & 1, cx, 20);
-                ok = __all_sync(0xffffffffu, ok);
-                if (!ok) break;
-            }
             tc_fence_after();
 #pragma unroll
-            for (int c = 0; c < 4; ++c) {
+            for (int c = 0; c < 2; ++c) {
                 uint32_t dr[32];
-                tmem_ld32(tl + C::COL_DP + c * 32, dr);
+                tmem_ld32(tl + C::COL_DP + 64 * g + c * 32, dr);
                 tmem_ld_wait(dr);
 #pragma unroll
-                for (int g = 0; g < 4; ++g) {  // 8 queries = one 16-byte chunk
-                    const int q0 = c * 32 + 8 * g;
+                for (int e = 0; e < 4; ++e) {  // 8 queries = one 16-byte chunk
+                    const int q0 = c * 32 + 8 * e;  // within this half
                     const float4 d0 = reinterpret_cast<const float4*>(del_s)[q0 / 4];
                     const float4 d1 = reinterpret_cast<const float4*>(del_s)[q0 / 4 + 1];
                     const float dd[8] = {d0.x, d0.y, d0.z, d0.w, d1.x, d1.y, d1.z, d1.w};
                     uint32_t w[4];
 #pragma unroll
-                    for (int e = 0; e < 4; ++e) {
-                        const uint32_t pp = pk[q0 / 2 + e];
+                    for (int t = 0; t < 4; ++t) {
+                        const uint32_t pp = pk[q0 / 2 + t];
                         const float pa = __uint_as_float(pp << 16), pb = __uint_as_float(pp & 0xFFFF0000u);
-                        const float sa = pa * (__uint_as_float(dr[8 * g + 2 * e]) - dd[2 * e]) * p.scale;
-                        const float sb = pb * (__uint_as_float(dr[8 * g + 2 * e + 1]) - dd[2 * e + 1]) * p.scale;
-                        w[e] = pack_bf16x2(sa, sb);
+                        const float sa = pa * (__uint_as_float(dr[8 * e + 2 * t]) - dd[2 * t]);
+                        const float sb = pb * (__uint_as_float(dr[8 * e + 2 * t + 1]) - dd[2 * t + 1]);
+                        w[t] = pack_bf16x2(sa, sb);
                     }
-                    const int chunk = q0 / 8;            // 0..15
-                    const int region = chunk >> 3;       // 64 queries per swizzle region
-                    const int cc = (chunk & 7) ^ (r & 7);
-                    *reinterpret_cast<uint4*>(ds_row + region * 16384 + cc * 16) = make_uint4(w[0], w[1], w[2], w[3]);
+                    const int chunk = q0 / 8;  // 0..7 within this 64-query swizzle region
+                    *reinterpret_cast<uint4*>(ds_row + ((chunk ^ (r & 7)) * 16)) = make_uint4(w[0], w[1], w[2], w[3]);
                 }
             }
             fence_proxy_async_smem();
@@ -336,41 +347,41 @@ __global__ void __launch_bounds__(384, 1)
             ++u;
         }
         // ------------------------------------------------------------ dK, dV epilogue
+        // group 0 writes dV_j, group 1 writes dK_j = scale * (dS^T Q)
         if (ok && u > 0) {
-            ok = mbar_wait(dkv_done, 0, cx, 21);
-            ok = __all_sync(0xffffffffu, ok);
+            ok = __all_sync(0xffffffffu, mbar_wait(dkv_done, 0, cx, 21));
             if (ok) tc_fence_after();
         }
         if (ok) {
             const size_t orow = (static_cast<size_t>(bh) * N + key) * D;
+            uint16_t* out = static_cast<uint16_t*>(g == 0 ? p.dv : p.dk) + orow;
+            const uint32_t col = g == 0 ? C::COL_DV : C::COL_DK;
+            const float mul = g == 0 ? 1.f : p.scale;
 #pragma unroll
-            for (int which = 0; which < 2; ++which) {
-                uint16_t* out = static_cast<uint16_t*>(which == 0 ? p.dv : p.dk) + orow;
-                const uint32_t col = which == 0 ? C::COL_DV : C::COL_DK;
+            for (int c = 0; c < D / 32; ++c) {
+                uint32_t v[32];
+                if (u > 0) {
+                    tmem_ld32(tl + col + c * 32, v);
+                    tmem_ld_wait(v);
+                } else {
 #pragma unroll
-                for (int c = 0; c < D / 32; ++c) {
-                    uint32_t v[32];
-                    if (u > 0) {
-                        tmem_ld32(tl + col + c * 32, v);
-                        tmem_ld_wait(v);
-                    } else {
-#pragma unroll
-                        for (int e = 0; e < 32; ++e) v[e] = 0u;
-                    }
-                    uint4* dst = reinterpret_cast<uint4*>(out + c * 32);
-#pragma unroll
-                    for (int q = 0; q < 4; ++q)
-                        dst[q] = make_uint4(pack_bf16x2(__uint_as_float(v[8 * q]), __uint_as_float(v[8 * q + 1])),
-                                            pack_bf16x2(__uint_as_float(v[8 * q + 2]), __uint_as_float(v[8 * q + 3])),
-                                            pack_bf16x2(__uint_as_float(v[8 * q + 4]), __uint_as_float(v[8 * q + 5])),
-                                            pack_bf16x2(__uint_as_float(v[8 * q + 6]), __uint_as_float(v[8 * q + 7])));
+                    for (int e = 0; e < 32; ++e) v[e] = 0u;
                 }
+                uint4* dst = reinterpret_cast<uint4*>(out + c * 32);
+#pragma unroll
+                for (int q = 0; q < 4; ++q)
+                    dst[q] = make_uint4(
+                        pack_bf16x2(__uint_as_float(v[8 * q]) * mul, __uint_as_float(v[8 * q + 1]) * mul),
+                        pack_bf16x2(__uint_as_float(v[8 * q + 2]) * mul, __uint_as_float(v[8 * q + 3]) * mul),
+                        pack_bf16x2(__uint_as_float(v[8 * q + 4]) * mul, __uint_as_float(v[8 * q + 5]) * mul),
+                        pack_bf16x2(__uint_as_float(v[8 * q + 6]) * mul, __uint_as_float(v[8 * q + 7]) * mul));
             }
         }
-    } else if (warp >= 8) {
+    } else if (warp >= 12) {
         // ------------------------------------------------------------ dQ drain (thread = query)
-        const int r = (warp & 3) * 32 + lane;
-        const uint32_t tl = tm + (static_cast<uint32_t>((warp & 3) * 32) << 16);
+        const int wq = warp & 3;
+        const uint32_t tl = tm + (static_cast<uint32_t>(wq * 32) << 16);
+        uint8_t* stage_buf = sm + C::DS_OFF + wq * 8192;  // two [32 x 32] fp32 boxes of 4 KiB
         int u = 0;
         for (int i = lo; i < T; ++i) {
             if (!visible_i(i)) continue;
@@ -378,22 +389,48 @@ __global__ void __launch_bounds__(384, 1)
             ok = __all_sync(0xffffffffu, ok);
             if (!ok) break;
             tc_fence_after();
-            float4* acc = reinterpret_cast<float4*>(p.dq_accum + (static_cast<size_t>(bh) * N + i * kTile + r) * D);
+            const int grow = bh * N + i * kTile + wq * 32;  // first accumulator row of this warp
 #pragma unroll
-            for (int c = 0; c < D / 32; ++c) {
-                uint32_t v[32];
-                tmem_ld32(tl + C::COL_DQ + c * 32, v);
-                tmem_ld_wait(v);
+            for (int half = 0; half < D / 64; ++half) {
+                uint32_t v[2][32];
+                tmem_ld32(tl + C::COL_DQ + half * 64, v[0]);
+                tmem_ld32(tl + C::COL_DQ + half * 64 + 32, v[1]);
+                tmem_ld_wait(v[0]);
+                tmem_ld_wait(v[1]);
+                if (half == D / 64 - 1) {
+                    // every TMEM read of dQ_i is done: its columns may be reused
+                    tc_fence_before();
+                    mbar_arrive(dq_free);
+                }
+                if (half > 0) {
+                    if (lane == 0) bulk_wait_group_read0();
+                    __syncwarp();
+                }
 #pragma unroll
-                for (int q = 0; q < 8; ++q)
-                    atomicAdd(acc + c * 8 + q, make_float4(__uint_as_float(v[4 * q]), __uint_as_float(v[4 * q + 1]),
-                                                           __uint_as_float(v[4 * q + 2]),
-                                                           __uint_as_float(v[4 * q + 3])));
+                for (int bx = 0; bx < 2; ++bx) {
+                    uint8_t* row = stage_buf + bx * 4096 + lane * 128;
+#pragma unroll
+                    for (int c = 0; c < 8; ++c)
+                        *reinterpret_cast<uint4*>(row + ((c ^ (lane & 7)) * 16)) =
+                            make_uint4(v[bx][4 * c], v[bx][4 * c + 1], v[bx][4 * c + 2], v[bx][4 * c + 3]);
+                }
+                fence_proxy_async_smem();
+                __syncwarp();
+                if (lane == 0) {
+                    tma_reduce_add_2d(&tmdQacc, half * 64, grow, stage_buf);
+                    tma_reduce_add_2d(&tmdQacc, half * 64 + 32, grow, stage_buf + 4096);
+                    bulk_commit_group();
+                }
             }
-            tc_fence_before();
-            mbar_arrive(dq_free);
+            if (lane == 0) {
+                bulk_wait_group_read0();
+                mbar_arrive(ds_free);
+            }
+            __syncwarp();
             ++u;
         }
+        if (lane == 0) bulk_wait_group0();
+        __syncwarp();
     }
     tc_fence_before();
     __syncthreads();
@@ -438,15 +475,17 @@ __global__ void __launch_bounds__(256) fa_bwd_pre_kernel(const uint16_t* __restr
     }
 }
 
-// dQ (bf16) <- dQ_accum (fp32), 8 elements per thread.
+// dQ (bf16) <- scale * dQ_accum (fp32), 8 elements per thread.
 __global__ void __launch_bounds__(256) fa_bwd_dq_kernel(const float* __restrict__ acc, uint16_t* __restrict__ dq,
-                                                        long long n8) {
+                                                        long long n8, float scale) {
     for (long long i = static_cast<long long>(blockIdx.x) * 256 + threadIdx.x; i < n8;
          i += static_cast<long long>(gridDim.x) * 256) {
         const float4 a = reinterpret_cast<const float4*>(acc)[2 * i];
         const float4 c = reinterpret_cast<const float4*>(acc)[2 * i + 1];
-        reinterpret_cast<uint4*>(dq)[i] =
-            make_uint4(pack_bf16x2(a.x, a.y), pack_bf16x2(a.z, a.w), pack_bf16x2(c.x, c.y), pack_bf16x2(c.z, c.w));
+        reinterpret_cast<uint4*>(dq)[i] = make_uint4(pack_bf16x2(a.x * scale, a.y * scale),
+                                                     pack_bf16x2(a.z * scale, a.w * scale),
+                                                     pack_bf16x2(c.x * scale, c.y * scale),
+                                                     pack_bf16x2(c.z * scale, c.w * scale));
     }
 }
 
@@ -454,10 +493,11 @@ template <int D>
 static cudaError_t launch_bwd_t(const BwdArgs& a, cudaStream_t stream, int* nlaunch) {
     using C = BwdCfg<D>;
     const uint64_t rows = static_cast<uint64_t>(a.B) * a.H * a.N;
-    CUtensorMap tq, tk, tv, tdo;
+    CUtensorMap tq, tk, tv, tdo, tdq;
     if (!make_tmap_2d_sw128(&tq, a.q, rows, D, 2, kTile, 64) || !make_tmap_2d_sw128(&tk, a.k, rows, D, 2, kTile, 64) ||
         !make_tmap_2d_sw128(&tv, a.v, rows, D, 2, kTile, 64) ||
-        !make_tmap_2d_sw128(&tdo, a.dout, rows, D, 2, kTile, 64))
+        !make_tmap_2d_sw128(&tdo, a.dout, rows, D, 2, kTile, 64) ||
+        !make_tmap_2d_sw128(&tdq, a.dq_accum, rows, D, 4, 32, 32))
         return cudaErrorInvalidValue;
     static bool attr_set = false;
     if (!attr_set) {
@@ -484,16 +524,16 @@ static cudaError_t launch_bwd_t(const BwdArgs& a, cudaStream_t stream, int* nlau
     p.delta = a.delta;
     p.dk = a.dk;
     p.dv = a.dv;
-    p.dq_accum = a.dq_accum;
     p.status = a.status;
-    dim3 grid(a.H, a.B, a.N / kTile);
+    dim3 grid(a.N / kTile, a.H, a.B);
     if (a.ev_begin) cudaEventRecord(a.ev_begin, stream);
-    fa_bwd_kernel<D><<<grid, 384, C::SMEM, stream>>>(tq, tk, tv, tdo, p);
+    fa_bwd_kernel<D><<<grid, C::THREADS, C::SMEM, stream>>>(tq, tk, tv, tdo, tdq, p);
     if (a.ev_end) cudaEventRecord(a.ev_end, stream);
     const long long n8 = nrows * D / 8;
     long long blocks = (n8 + 255) / 256;
     if (blocks > 152 * 16) blocks = 152 * 16;
-    fa_bwd_dq_kernel<<<static_cast<unsigned>(blocks), 256, 0, stream>>>(a.dq_accum, static_cast<uint16_t*>(a.dq), n8);
+    fa_bwd_dq_kernel<<<static_cast<unsigned>(blocks), 256, 0, stream>>>(a.dq_accum, static_cast<uint16_t*>(a.dq), n8,
+                                                                        a.scale);
     *nlaunch = 3;
     return cudaGetLastError();
 }

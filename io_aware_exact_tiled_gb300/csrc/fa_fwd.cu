@@ -98,10 +98,13 @@ __global__ void __launch_bounds__(384, 1)
     const WaitCtx cx{abort_flag, p.status};
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    // Longest-first order across all heads (the query-tile pair index is the
+    // slowest grid dimension): with causal masks the longest CTAs start first
+    // and the short ones fill the tail.
     const int h = blockIdx.x, b = blockIdx.y;
     const int T = p.mask.T;
     const int npairs = (T + 1) >> 1;
-    const int qp = npairs - 1 - static_cast<int>(blockIdx.z);  // longest causal work first
+    const int qp = npairs - 1 - static_cast<int>(blockIdx.z);
     const int qb0 = 2 * qp, qb1 = 2 * qp + 1;
     const bool act1 = qb1 < T;
     const int N = p.N;

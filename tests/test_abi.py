@@ -77,6 +77,7 @@ def test_fwd_rejects_bad_arguments(lib):
     assert fwd(lib, d=256) == fb.FA_ERR_UNSUPPORTED
     assert fwd(lib, N=100) == fb.FA_ERR_UNSUPPORTED
     assert fwd(lib, B=1 << 16) == fb.FA_ERR_UNSUPPORTED
+    assert fwd(lib, H=1 << 16) == fb.FA_ERR_UNSUPPORTED
     assert fwd(lib, B=4096, H=4096, N=256) == fb.FA_ERR_UNSUPPORTED
     assert fwd(lib, dtype=fb.FA_FP32, d=128) == fb.FA_ERR_UNSUPPORTED
     assert fwd(lib, dtype=fb.FA_FP32, wsb=1000) == fb.FA_ERR_INVALID_ARG
