@@ -63,8 +63,8 @@ struct BwdParams {
     float scale;
     float scale_log2;
     MaskArgs mask;
-    const float* lse2;   // L * log2(e), +inf where L = -inf
-    const float* delta;
+    const float* nlse2;   // -L * log2(e) (-inf where L = -inf, so that P = 0)
+    const float* ndelta;  // -D = -rowsum(dO * O)
     void* dk;
     void* dv;
     int* status;
@@ -90,7 +90,10 @@ __global__ void __launch_bounds__(512, 1)
                   const __grid_constant__ CUtensorMap tmdQacc, const BwdParams p) {
     using C = BwdCfg<D>;
     extern __shared__ __align__(1024) uint8_t smem_raw[];
-    uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    // 1024-byte aligned base for the swizzled tiles; offsetting the shared
+    // array itself (rather than casting through an integer) keeps the pointer
+    // in the shared address space, so accesses compile to shared loads/stores
+    uint8_t* sm = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     // The carve-up needs the dynamic shared window to start within the slack
     // reserved for alignment; report instead of overrunning if it does not.
@@ -158,7 +161,6 @@ __global__ void __launch_bounds__(512, 1)
     __syncthreads();
     tc_fence_after();
     const uint32_t tm = *tmem_slot;
-
     if (warp == 0) {
         // ------------------------------------------------------------ producer
         if (lane == 0) {
@@ -183,8 +185,8 @@ __global__ void __launch_bounds__(512, 1)
                     tma_load_2d(sm + C::Q_OFF + st * C::TILE_BYTES + r * 16384, &tmQ, r * 64, row, &qd_full[st]);
                     tma_load_2d(sm + C::DO_OFF + st * C::TILE_BYTES + r * 16384, &tmdO, r * 64, row, &qd_full[st]);
                 }
-                bulk_load(sm + C::LSE_OFF + st * 512, p.lse2 + row, 512, &qd_full[st]);
-                bulk_load(sm + C::DEL_OFF + st * 512, p.delta + row, 512, &qd_full[st]);
+                bulk_load(sm + C::LSE_OFF + st * 512, p.nlse2 + row, 512, &qd_full[st]);
+                bulk_load(sm + C::DEL_OFF + st * 512, p.ndelta + row, 512, &qd_full[st]);
                 ++u;
             }
             if (kv_issued) mbar_wait_teardown(kv_full, 0, 200000000ull);
@@ -196,8 +198,12 @@ __global__ void __launch_bounds__(512, 1)
     } else if (warp == 1) {
         // ------------------------------------------------------------ MMA issuer
         if (lane == 0) {
-            const uint32_t kb = smem_u32(sm + C::K_OFF), vb = smem_u32(sm + C::V_OFF);
-            const uint32_t dsb = smem_u32(sm + C::DS_OFF);
+            // descriptors are built once and advanced by constants per k-step
+            const uint64_t dK_k = sdesc_sw128(smem_u32(sm + C::K_OFF), 16, 1024);        // K_j, K-major
+            const uint64_t dV_k = sdesc_sw128(smem_u32(sm + C::V_OFF), 16, 1024);        // V_j, K-major
+            const uint64_t dK_mn = sdesc_sw128(smem_u32(sm + C::K_OFF), 16384, 1024);    // K_j, MN-major
+            const uint64_t dS_k = sdesc_sw128(smem_u32(sm + C::DS_OFF), 16, 1024);       // dS^T, K-major
+            const uint64_t dS_mn = sdesc_sw128(smem_u32(sm + C::DS_OFF), 16384, 1024);   // dS, MN-major
             bool ok = true;
             int u = 0;
             for (int i = lo; ok && i < T; ++i) {
@@ -211,12 +217,14 @@ __global__ void __launch_bounds__(512, 1)
                 tc_fence_after();
                 const uint32_t qb = smem_u32(sm + C::Q_OFF + st * C::TILE_BYTES);
                 const uint32_t dob = smem_u32(sm + C::DO_OFF + st * C::TILE_BYTES);
+                const uint64_t dQ_k = sdesc_sw128(qb, 16, 1024), dQ_mn = sdesc_sw128(qb, 16384, 1024);
+                const uint64_t dO_k = sdesc_sw128(dob, 16, 1024), dO_mn = sdesc_sw128(dob, 16384, 1024);
                 // dP^T = V_j dO_i^T
 #pragma unroll
                 for (int kk = 0; kk < D / 16; ++kk) {
                     const uint32_t off = (kk / 4) * 16384 + (kk % 4) * 32;
-                    umma_ss<false>(tm + C::COL_DP, sdesc_sw128(vb + off, 16, 1024), sdesc_sw128(dob + off, 16, 1024),
-                                   C::ID_SQ, kk > 0);
+                    umma_ss<false>(tm + C::COL_DP, sdesc_advance(dV_k, off), sdesc_advance(dO_k, off), C::ID_SQ,
+                                   kk > 0);
                 }
                 umma_commit(dp_full);
                 // S^T = K_j Q_i^T (these columns held dQ of the previous block)
@@ -225,8 +233,8 @@ __global__ void __launch_bounds__(512, 1)
 #pragma unroll
                 for (int kk = 0; kk < D / 16; ++kk) {
                     const uint32_t off = (kk / 4) * 16384 + (kk % 4) * 32;
-                    umma_ss<false>(tm + C::COL_S, sdesc_sw128(kb + off, 16, 1024), sdesc_sw128(qb + off, 16, 1024),
-                                   C::ID_SQ, kk > 0);
+                    umma_ss<false>(tm + C::COL_S, sdesc_advance(dK_k, off), sdesc_advance(dQ_k, off), C::ID_SQ,
+                                   kk > 0);
                 }
                 umma_commit(s_full);
                 // dV_j += P^T dO_i ; P^T of queries 0-63 sits in columns 0-31
@@ -236,20 +244,20 @@ __global__ void __launch_bounds__(512, 1)
 #pragma unroll
                 for (int kk = 0; kk < 8; ++kk)
                     umma_ts<false>(tm + C::COL_DV, tm + C::COL_S + (kk >> 2) * 64 + (kk & 3) * 8,
-                                   sdesc_sw128(dob + kk * 2048, 16384, 1024), C::ID_KN, (u > 0 || kk > 0) ? 1u : 0u);
+                                   sdesc_advance(dO_mn, kk * 2048), C::ID_KN, (u > 0 || kk > 0) ? 1u : 0u);
                 // dK_j += dS^T Q_i ; dQ_i = dS K_j
                 if (!(ok = mbar_wait(ds_ready, u & 1, cx, 16))) break;
                 tc_fence_after();
 #pragma unroll
                 for (int kk = 0; kk < 8; ++kk) {
                     const uint32_t off = (kk / 4) * 16384 + (kk % 4) * 32;
-                    umma_ss<false>(tm + C::COL_DK, sdesc_sw128(dsb + off, 16, 1024),
-                                   sdesc_sw128(qb + kk * 2048, 16384, 1024), C::ID_KN, (u > 0 || kk > 0) ? 1u : 0u);
+                    umma_ss<false>(tm + C::COL_DK, sdesc_advance(dS_k, off), sdesc_advance(dQ_mn, kk * 2048), C::ID_KN,
+                                   (u > 0 || kk > 0) ? 1u : 0u);
                 }
 #pragma unroll
                 for (int kk = 0; kk < 8; ++kk)
-                    umma_ss<false>(tm + C::COL_DQ, sdesc_sw128(dsb + kk * 2048, 16384, 1024),
-                                   sdesc_sw128(kb + kk * 2048, 16384, 1024), C::ID_DQ, kk > 0 ? 1u : 0u);
+                    umma_ss<false>(tm + C::COL_DQ, sdesc_advance(dS_mn, kk * 2048), sdesc_advance(dK_mn, kk * 2048),
+                                   C::ID_DQ, kk > 0 ? 1u : 0u);
                 umma_commit(dq_full);
                 umma_commit(&qd_empty[st]);
                 ++u;
@@ -265,16 +273,16 @@ __global__ void __launch_bounds__(512, 1)
         const uint32_t tl = tm + (static_cast<uint32_t>((warp & 3) * 32) << 16);
         const int key = j * kTile + r;
         const bool key_ok = key < kvalid;
-        const float c2 = p.scale_log2;
-        uint8_t* ds_row = sm + C::DS_OFF + g * 16384 + r * 128;
+        const uint64_t c2c2 = f2_make(p.scale_log2, p.scale_log2);
+        const uint32_t ds_row = smem_u32(sm + C::DS_OFF + g * 16384 + r * 128);
         bool ok = true;
         int u = 0;
         for (int i = lo; i < T; ++i) {
             if (!visible_i(i)) continue;
             const int st = u % C::STAGES;
             const uint32_t ph = (u / C::STAGES) & 1;
-            const float* lse_s = reinterpret_cast<const float*>(sm + C::LSE_OFF + st * 512) + 64 * g;
-            const float* del_s = reinterpret_cast<const float*>(sm + C::DEL_OFF + st * 512) + 64 * g;
+            const uint32_t nlse_s = smem_u32(sm + C::LSE_OFF + st * 512) + 256 * g;
+            const uint32_t ndel_s = smem_u32(sm + C::DEL_OFF + st * 512) + 256 * g;
             ok = mbar_wait(&qd_full[st], ph, cx, 17);
             ok = __all_sync(0xffffffffu, ok) && __all_sync(0xffffffffu, mbar_wait(s_full, u & 1, cx, 18));
             if (!ok) break;
@@ -283,19 +291,22 @@ __global__ void __launch_bounds__(512, 1)
             // padded keys
             const bool diag = p.mask.causal && i == j;
             const bool masked = diag || !key_ok;
-            uint32_t pk[32];  // P^T of this thread's 64 queries, bf16 pairs
 #pragma unroll
             for (int c = 0; c < 2; ++c) {
+                uint32_t pk[16];  // P^T of 32 queries, bf16 pairs
                 uint32_t sr[32];
                 tmem_ld32(tl + C::COL_S + 64 * g + c * 32, sr);
                 tmem_ld_wait(sr);
 #pragma unroll
                 for (int e = 0; e < 8; ++e) {
-                    const float4 L4 = reinterpret_cast<const float4*>(lse_s)[c * 8 + e];
-                    float pv0 = ex2_approx(fmaf(__uint_as_float(sr[4 * e + 0]), c2, -L4.x));
-                    float pv1 = ex2_approx(fmaf(__uint_as_float(sr[4 * e + 1]), c2, -L4.y));
-                    float pv2 = ex2_approx(fmaf(__uint_as_float(sr[4 * e + 2]), c2, -L4.z));
-                    float pv3 = ex2_approx(fmaf(__uint_as_float(sr[4 * e + 3]), c2, -L4.w));
+                    // x = S * scale * log2(e) - L * log2(e), two queries per instruction
+                    const float4 nL = lds128(nlse_s + (c * 8 + e) * 16);
+                    float x0, x1, x2, x3;
+                    f2_split(f2_fma(f2_make(__uint_as_float(sr[4 * e]), __uint_as_float(sr[4 * e + 1])), c2c2,
+                                    f2_make(nL.x, nL.y)), x0, x1);
+                    f2_split(f2_fma(f2_make(__uint_as_float(sr[4 * e + 2]), __uint_as_float(sr[4 * e + 3])), c2c2,
+                                    f2_make(nL.z, nL.w)), x2, x3);
+                    float pv0 = ex2_approx(x0), pv1 = ex2_approx(x1), pv2 = ex2_approx(x2), pv3 = ex2_approx(x3);
                     if (masked) {
                         const int q = 64 * g + c * 32 + 4 * e;
                         if (!key_ok || (diag && q + 0 < r)) pv0 = 0.f;
@@ -303,44 +314,49 @@ __global__ void __launch_bounds__(512, 1)
                         if (!key_ok || (diag && q + 2 < r)) pv2 = 0.f;
                         if (!key_ok || (diag && q + 3 < r)) pv3 = 0.f;
                     }
-                    pk[c * 16 + 2 * e] = pack_bf16x2(pv0, pv1);
-                    pk[c * 16 + 2 * e + 1] = pack_bf16x2(pv2, pv3);
+                    pk[2 * e] = pack_bf16x2(pv0, pv1);
+                    pk[2 * e + 1] = pack_bf16x2(pv2, pv3);
                 }
-                tmem_st16(tl + C::COL_S + 64 * g + c * 16, &pk[c * 16]);
+                tmem_st16(tl + C::COL_S + 64 * g + c * 16, pk);
             }
             tmem_st_wait();
             tc_fence_before();
             mbar_arrive(p_ready);
-            // dS^T = P^T * (dP^T - D) (the scale is applied to dK and dQ at the end)
-            ok = mbar_wait(dp_full, u & 1, cx, 19);
-            if (u > 0) ok = ok && mbar_wait(ds_free, (u - 1) & 1, cx, 20);
-            ok = __all_sync(0xffffffffu, ok);
+            // dS^T = P^T * (dP^T - D) (the scale is applied to dK and dQ at
+            // the end), computed into registers before the shared buffer is
+            // known to be free; P^T is read back from TMEM (bf16)
+            ok = __all_sync(0xffffffffu, mbar_wait(dp_full, u & 1, cx, 19));
             if (!ok) break;
             tc_fence_after();
+            uint32_t dsw[32];
 #pragma unroll
             for (int c = 0; c < 2; ++c) {
-                uint32_t dr[32];
+                uint32_t dr[32], pk[16];
                 tmem_ld32(tl + C::COL_DP + 64 * g + c * 32, dr);
+                tmem_ld16(tl + C::COL_S + 64 * g + c * 16, pk);
                 tmem_ld_wait(dr);
+                tmem_ld_wait(pk);
 #pragma unroll
-                for (int e = 0; e < 4; ++e) {  // 8 queries = one 16-byte chunk
-                    const int q0 = c * 32 + 8 * e;  // within this half
-                    const float4 d0 = reinterpret_cast<const float4*>(del_s)[q0 / 4];
-                    const float4 d1 = reinterpret_cast<const float4*>(del_s)[q0 / 4 + 1];
-                    const float dd[8] = {d0.x, d0.y, d0.z, d0.w, d1.x, d1.y, d1.z, d1.w};
-                    uint32_t w[4];
-#pragma unroll
-                    for (int t = 0; t < 4; ++t) {
-                        const uint32_t pp = pk[q0 / 2 + t];
-                        const float pa = __uint_as_float(pp << 16), pb = __uint_as_float(pp & 0xFFFF0000u);
-                        const float sa = pa * (__uint_as_float(dr[8 * e + 2 * t]) - dd[2 * t]);
-                        const float sb = pb * (__uint_as_float(dr[8 * e + 2 * t + 1]) - dd[2 * t + 1]);
-                        w[t] = pack_bf16x2(sa, sb);
-                    }
-                    const int chunk = q0 / 8;  // 0..7 within this 64-query swizzle region
-                    *reinterpret_cast<uint4*>(ds_row + ((chunk ^ (r & 7)) * 16)) = make_uint4(w[0], w[1], w[2], w[3]);
+                for (int e = 0; e < 8; ++e) {  // 4 queries
+                    const float4 nD = lds128(ndel_s + (c * 8 + e) * 16);
+                    const uint64_t t01 = f2_add(f2_make(__uint_as_float(dr[4 * e]), __uint_as_float(dr[4 * e + 1])),
+                                                f2_make(nD.x, nD.y));
+                    const uint64_t t23 = f2_add(f2_make(__uint_as_float(dr[4 * e + 2]), __uint_as_float(dr[4 * e + 3])),
+                                                f2_make(nD.z, nD.w));
+                    dsw[c * 16 + 2 * e] = bf16x2_from_f2(f2_mul(t01, f2_from_bf16x2(pk[2 * e])));
+                    dsw[c * 16 + 2 * e + 1] = bf16x2_from_f2(f2_mul(t23, f2_from_bf16x2(pk[2 * e + 1])));
                 }
             }
+            if (u > 0) {
+                // the previous dS^T must have been consumed by its dK / dQ
+                // GEMMs and the buffer released by the dQ drain
+                ok = __all_sync(0xffffffffu, mbar_wait(ds_free, (u - 1) & 1, cx, 20));
+                if (!ok) break;
+            }
+#pragma unroll
+            for (int chunk = 0; chunk < 8; ++chunk)  // 8 queries per 16-byte chunk
+                sts128(ds_row + ((chunk ^ (r & 7)) * 16), dsw[4 * chunk], dsw[4 * chunk + 1], dsw[4 * chunk + 2],
+                       dsw[4 * chunk + 3]);
             fence_proxy_async_smem();
             tc_fence_before();
             mbar_arrive(ds_ready);
@@ -390,6 +406,7 @@ __global__ void __launch_bounds__(512, 1)
             if (!ok) break;
             tc_fence_after();
             const int grow = bh * N + i * kTile + wq * 32;  // first accumulator row of this warp
+            const uint32_t sb = smem_u32(stage_buf);
 #pragma unroll
             for (int half = 0; half < D / 64; ++half) {
                 uint32_t v[2][32];
@@ -407,13 +424,12 @@ __global__ void __launch_bounds__(512, 1)
                     __syncwarp();
                 }
 #pragma unroll
-                for (int bx = 0; bx < 2; ++bx) {
-                    uint8_t* row = stage_buf + bx * 4096 + lane * 128;
+                for (int bx = 0; bx < 2; ++bx)
 #pragma unroll
-                    for (int c = 0; c < 8; ++c)
-                        *reinterpret_cast<uint4*>(row + ((c ^ (lane & 7)) * 16)) =
-                            make_uint4(v[bx][4 * c], v[bx][4 * c + 1], v[bx][4 * c + 2], v[bx][4 * c + 3]);
-                }
+                    for (int c = 0; c < 8; ++c) {
+                        const uint32_t* w = &v[bx][4 * c];
+                        sts128(sb + bx * 4096 + lane * 128 + ((c ^ (lane & 7)) * 16), w[0], w[1], w[2], w[3]);
+                    }
                 fence_proxy_async_smem();
                 __syncwarp();
                 if (lane == 0) {
@@ -440,14 +456,15 @@ __global__ void __launch_bounds__(512, 1)
     }
 }
 
-// D[row] = sum_k dO[row, k] * O[row, k] in fp32; also zeroes dQ_accum[row, :]
-// and writes L in log2 units (L * log2 e; +inf for a row that saw no key, so
-// that its recomputed probabilities are 0). D/8 threads share a row (16 bytes
-// of O and of dO each) and reduce with warp shuffles.
+// D[row] = sum_k dO[row, k] * O[row, k] in fp32, stored negated (-D); also
+// zeroes dQ_accum[row, :] and writes -L in log2 units (-L * log2 e; -inf for
+// a row that saw no key, so that its recomputed probabilities are 0). D/8
+// threads share a row (16 bytes of O and of dO each) and reduce with warp
+// shuffles.
 template <int D>
 __global__ void __launch_bounds__(256) fa_bwd_pre_kernel(const uint16_t* __restrict__ o, const uint16_t* __restrict__ dout,
-                                                         const float* __restrict__ lse, float* __restrict__ delta,
-                                                         float* __restrict__ lse2, float* __restrict__ dq_accum,
+                                                         const float* __restrict__ lse, float* __restrict__ ndelta,
+                                                         float* __restrict__ nlse2, float* __restrict__ dq_accum,
                                                          long long rows) {
     constexpr int TPR = D / 8;  // threads per row
     const long long row = (static_cast<long long>(blockIdx.x) * 256 + threadIdx.x) / TPR;
@@ -469,9 +486,9 @@ __global__ void __launch_bounds__(256) fa_bwd_pre_kernel(const uint16_t* __restr
 #pragma unroll
     for (int off = TPR / 2; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
     if (row < rows && part == 0) {
-        delta[row] = acc;
+        ndelta[row] = -acc;
         const float L = lse[row];
-        lse2[row] = L == -CUDART_INF_F ? CUDART_INF_F : L * kLog2e;
+        nlse2[row] = L == -CUDART_INF_F ? -CUDART_INF_F : -L * kLog2e;
     }
 }
 
@@ -520,8 +537,8 @@ static cudaError_t launch_bwd_t(const BwdArgs& a, cudaStream_t stream, int* nlau
     p.mask.kv_len = a.kv_len;
     p.mask.causal = a.causal;
     p.mask.T = a.N / kTile;
-    p.lse2 = a.lse2;
-    p.delta = a.delta;
+    p.nlse2 = a.lse2;
+    p.ndelta = a.delta;
     p.dk = a.dk;
     p.dv = a.dv;
     p.status = a.status;

@@ -83,7 +83,10 @@ __global__ void __launch_bounds__(384, 1)
                   const __grid_constant__ CUtensorMap tmKlo, const FwdParams p) {
     using C = FwdCfg<TF32, D>;
     extern __shared__ __align__(1024) uint8_t smem_raw[];
-    uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    // 1024-byte aligned base for the swizzled tiles; offsetting the shared
+    // array itself (rather than casting through an integer) keeps the pointer
+    // in the shared address space, so accesses compile to shared loads/stores
+    uint8_t* sm = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
     uint64_t* bars = reinterpret_cast<uint64_t*>(sm + C::BAR_OFF);
     uint64_t* bar_q = bars + 0;
     uint64_t* k_full = bars + 1;
@@ -211,9 +214,12 @@ __global__ void __launch_bounds__(384, 1)
             int nP[2] = {0, 0};
             int nPV[2] = {0, 0};
             uint32_t rem = 0;  // 2 bits per stage: users still to finish
-            const uint32_t qbase = smem_u32(sm + C::Q_OFF);
-            const uint32_t kbase = smem_u32(sm + C::K_OFF);
-            const uint32_t vbase = smem_u32(sm + C::V_OFF);
+            // descriptors are built once and advanced by constants per k-step
+            const uint64_t dQ0 = sdesc_sw128(smem_u32(sm + C::Q_OFF), 16, 1024);
+            const uint64_t dK0 = sdesc_sw128(smem_u32(sm + C::K_OFF), 16, 1024);
+            // bf16: V MN-major (LBO = distance between 64-column regions);
+            // tf32: V^T K-major
+            const uint64_t dV0 = sdesc_sw128(smem_u32(sm + C::V_OFF), TF32 ? 16 : 16384, 1024);
 
             auto issue_pv = [&](int s) -> bool {
                 const int ps = pend_stage[s];
@@ -221,15 +227,11 @@ __global__ void __launch_bounds__(384, 1)
                 ++nP[s];
                 if (!mbar_wait(&v_full[ps], pend_ph[s], cx, 4)) return false;
                 tc_fence_after();
-                const uint32_t vst = vbase + ps * C::TILE_BYTES;
+                const uint64_t vst = sdesc_advance(dV0, ps * C::TILE_BYTES);
 #pragma unroll
                 for (int kk = 0; kk < C::PV_KSTEPS; ++kk) {
-                    uint64_t bd;
-                    if constexpr (!TF32)
-                        bd = sdesc_sw128(vst + kk * 2048, 16384, 1024);
-                    else
-                        bd = sdesc_sw128(vst + (kk / 4) * (D * 128) + (kk % 4) * 32, 16, 1024);
-                    umma_ts<TF32>(tm + s * 256 + 128, tm + s * 256 + kk * 8, bd, C::ID_PV,
+                    const uint32_t off = TF32 ? (kk / 4) * (D * 128) + (kk % 4) * 32 : kk * 2048;
+                    umma_ts<TF32>(tm + s * 256 + 128, tm + s * 256 + kk * 8, sdesc_advance(vst, off), C::ID_PV,
                                   (nPV[s] > 0 || kk > 0) ? 1u : 0u);
                 }
                 ++nPV[s];
@@ -261,18 +263,18 @@ __global__ void __launch_bounds__(384, 1)
                 for (int s = 0; s < 2; ++s) {
                     if (!(nd & (1u << s))) continue;
                     if (pend_stage[s] >= 0 && !issue_pv(s)) { ok = false; break; }
-                    const uint32_t qs = qbase + s * C::SPLIT * C::TILE_BYTES;
-                    const uint32_t ks = kbase + stage * C::SPLIT * C::TILE_BYTES;
+                    const uint64_t qs = sdesc_advance(dQ0, s * C::SPLIT * C::TILE_BYTES);
+                    const uint64_t ks = sdesc_advance(dK0, stage * C::SPLIT * C::TILE_BYTES);
                     // bf16: one product; fp32: (Qh, Kh), (Qh, Kl), (Ql, Kh)
 #pragma unroll
                     for (int part = 0; part < (TF32 ? 3 : 1); ++part) {
-                        const uint32_t qa = qs + (part == 2 ? C::TILE_BYTES : 0);
-                        const uint32_t kb2 = ks + (part == 1 ? C::TILE_BYTES : 0);
+                        const uint64_t qa = sdesc_advance(qs, part == 2 ? C::TILE_BYTES : 0);
+                        const uint64_t kb2 = sdesc_advance(ks, part == 1 ? C::TILE_BYTES : 0);
 #pragma unroll
                         for (int kk = 0; kk < C::S_KSTEPS; ++kk) {
                             const uint32_t off = (kk / 4) * 16384 + (kk % 4) * 32;
-                            umma_ss<TF32>(tm + s * 256, sdesc_sw128(qa + off, 16, 1024),
-                                          sdesc_sw128(kb2 + off, 16, 1024), C::ID_S, (part > 0 || kk > 0) ? 1u : 0u);
+                            umma_ss<TF32>(tm + s * 256, sdesc_advance(qa, off), sdesc_advance(kb2, off), C::ID_S,
+                                          (part > 0 || kk > 0) ? 1u : 0u);
                         }
                     }
                     umma_commit(&s_full[s]);

@@ -31,8 +31,8 @@ struct BwdArgs {
     int causal;
     const uint8_t* blockmask;
     const int32_t* kv_len;
-    float* delta;     // [B,H,N] scratch: D = rowsum(dO * O)
-    float* lse2;      // [B,H,N] scratch: L in log2 units
+    float* delta;     // [B,H,N] scratch: -D = -rowsum(dO * O)
+    float* lse2;      // [B,H,N] scratch: -L in log2 units
     float* dq_accum;  // [B,H,N,d] fp32 scratch
     int* status;
     cudaEvent_t ev_begin, ev_end;  // optional, recorded around the main kernel
