@@ -330,7 +330,8 @@ __global__ void __launch_bounds__(384, 1)
 #pragma unroll
                 for (int c = 0; c < 4; ++c)
 #pragma unroll
-                    for (int i = 0; i < 32; ++i) mx = fmaxf(mx, __uint_as_float(sr[c][i]));
+                    for (int i = 0; i < 32; i += 2)
+                        mx = fmax3(mx, __uint_as_float(sr[c][i]), __uint_as_float(sr[c][i + 1]));
                 const float m_new = fmaxf(m_hat, mx * c2);
                 const bool resc = (m_new - m_hat) > kRescaleThreshold;
                 float alpha = 1.f;
@@ -342,17 +343,24 @@ __global__ void __launch_bounds__(384, 1)
                 }
                 const float mu = (m_hat == -CUDART_INF_F) ? 0.f : m_hat;
                 float rs = 0.f, rr = 0.f;
+                // two elements per f32x2 instruction: x = s * c2 - mu, the
+                // fp32 row sum and the sum of the bf16-rounded weights
+                const uint64_t c2c2 = f2_make(c2, c2), nmu2 = f2_make(-mu, -mu);
+                uint64_t rs2 = 0ull, rr2 = 0ull;
 #pragma unroll
                 for (int c = 0; c < 4; ++c) {
                     if constexpr (!TF32) {
                         uint32_t pk[16];
 #pragma unroll
                         for (int i = 0; i < 16; ++i) {
-                            const float p0 = ex2_approx(fmaf(__uint_as_float(sr[c][2 * i]), c2, -mu));
-                            const float p1 = ex2_approx(fmaf(__uint_as_float(sr[c][2 * i + 1]), c2, -mu));
+                            float x0, x1;
+                            f2_split(f2_fma(f2_make(__uint_as_float(sr[c][2 * i]), __uint_as_float(sr[c][2 * i + 1])),
+                                            c2c2, nmu2),
+                                     x0, x1);
+                            const float p0 = ex2_approx(x0), p1 = ex2_approx(x1);
                             pk[i] = pack_bf16x2(p0, p1);
-                            rs += p0 + p1;
-                            rr += __uint_as_float(pk[i] << 16) + __uint_as_float(pk[i] & 0xFFFF0000u);
+                            rs2 = f2_add(rs2, f2_make(p0, p1));
+                            rr2 = f2_add(rr2, f2_from_bf16x2(pk[i]));
                         }
                         tmem_st16(tl + c * 16, pk);
                     } else {
@@ -366,6 +374,13 @@ __global__ void __launch_bounds__(384, 1)
                         rr = rs;
                         tmem_st32(tl + c * 32, pk);
                     }
+                }
+                if constexpr (!TF32) {
+                    float a, b;
+                    f2_split(rs2, a, b);
+                    rs = a + b;
+                    f2_split(rr2, a, b);
+                    rr = a + b;
                 }
                 l += rs;
                 lw += rr;
