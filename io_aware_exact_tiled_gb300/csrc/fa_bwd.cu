@@ -87,7 +87,7 @@ template <int D>
 __global__ void __launch_bounds__(512, 1)
     fa_bwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                   const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmdO,
-                  const __grid_constant__ CUtensorMap tmdQacc, const BwdParams p) {
+                  const __grid_constant__ CUtensorMap tmdQacc, const __grid_constant__ BwdParams p) {
     using C = BwdCfg<D>;
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     // 1024-byte aligned base for the swizzled tiles; offsetting the shared
@@ -126,7 +126,9 @@ __global__ void __launch_bounds__(512, 1)
     const int bh = b * p.H + h;
     const int kvalid = keys_valid(p.mask, b, N);
     const int lo = p.mask.causal ? j : 0;
-    auto visible_i = [&](int i) -> bool { return tile_visible(p.mask, i, j, kvalid); };
+    // captured by value (a by-reference capture would move them to local memory)
+    const MaskArgs mk = p.mask;
+    auto visible_i = [=](int i) -> bool { return tile_visible(mk, i, j, kvalid); };
 
     if (tid == 0) {
         *abort_flag = 0;

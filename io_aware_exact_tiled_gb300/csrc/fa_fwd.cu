@@ -73,6 +73,42 @@ struct FwdParams {
     int* status;
 };
 
+// Issue state of the MMA thread, per Q tile s of the CTA.
+struct MmaState {
+    int pend_stage[2] = {-1, -1};  // K/V stage whose P V GEMM is still to be issued
+    uint32_t pend_ph[2] = {0, 0};  // V-full phase parity of that stage
+    int nP[2] = {0, 0};            // P-ready phases consumed
+    int nPV[2] = {0, 0};           // P V GEMMs issued
+    uint32_t rem = 0;              // 2 bits per stage: Q tiles still to read its V
+};
+
+// O_s += P_s V for Q tile s's pending K/V tile (waits for P_s and V).
+template <bool TF32, int D>
+__device__ __forceinline__ bool fwd_issue_pv(int s, MmaState& st, uint32_t tm, uint64_t dV0, uint64_t* p_full,
+                                             uint64_t* kv_empty, const WaitCtx& cx) {
+    using C = FwdCfg<TF32, D>;
+    const int ps = st.pend_stage[s];
+    if (!mbar_wait(&p_full[s], st.nP[s] & 1, cx, 3)) return false;
+    ++st.nP[s];
+    // V of this stage arrived with its K (one barrier per stage), which the
+    // MMA thread waited for before issuing S for this tile
+    tc_fence_after();
+    const uint64_t vst = sdesc_advance(dV0, ps * C::TILE_BYTES);
+#pragma unroll
+    for (int kk = 0; kk < C::PV_KSTEPS; ++kk) {
+        const uint32_t off = TF32 ? (kk / 4) * (D * 128) + (kk % 4) * 32 : kk * 2048;
+        umma_ts<TF32>(tm + s * 256 + 128, tm + s * 256 + kk * 8, sdesc_advance(vst, off), C::ID_PV,
+                      (st.nPV[s] > 0 || kk > 0) ? 1u : 0u);
+    }
+    ++st.nPV[s];
+    uint32_t r = (st.rem >> (2 * ps)) & 3u;
+    r -= 1;
+    st.rem = (st.rem & ~(3u << (2 * ps))) | (r << (2 * ps));
+    if (r == 0) umma_commit(&kv_empty[ps]);
+    st.pend_stage[s] = -1;
+    return true;
+}
+
 constexpr float kRescaleThreshold = 8.0f;  // log2 units
 constexpr float kLn2 = 0.69314718055994530942f;
 
@@ -80,7 +116,7 @@ template <bool TF32, int D>
 __global__ void __launch_bounds__(384, 1)
     fa_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                   const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmQlo,
-                  const __grid_constant__ CUtensorMap tmKlo, const FwdParams p) {
+                  const __grid_constant__ CUtensorMap tmKlo, const __grid_constant__ FwdParams p) {
     using C = FwdCfg<TF32, D>;
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     // 1024-byte aligned base for the swizzled tiles; offsetting the shared
@@ -89,9 +125,8 @@ __global__ void __launch_bounds__(384, 1)
     uint8_t* sm = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
     uint64_t* bars = reinterpret_cast<uint64_t*>(sm + C::BAR_OFF);
     uint64_t* bar_q = bars + 0;
-    uint64_t* k_full = bars + 1;
-    uint64_t* v_full = k_full + C::STAGES;
-    uint64_t* kv_empty = v_full + C::STAGES;
+    uint64_t* kv_full = bars + 1;             // K and V of a stage landed
+    uint64_t* kv_empty = kv_full + C::STAGES;
     uint64_t* s_full = kv_empty + C::STAGES;  // [2]
     uint64_t* p_full = s_full + 2;            // [2]
     uint64_t* o_done = p_full + 2;            // [2]
@@ -121,8 +156,7 @@ __global__ void __launch_bounds__(384, 1)
         *abort_flag = 0;
         mbar_init(bar_q, 1);
         for (int i = 0; i < C::STAGES; ++i) {
-            mbar_init(&k_full[i], 1);
-            mbar_init(&v_full[i], 1);
+            mbar_init(&kv_full[i], 1);
             mbar_init(&kv_empty[i], 1);
         }
         for (int i = 0; i < 2; ++i) {
@@ -152,9 +186,12 @@ __global__ void __launch_bounds__(384, 1)
     const uint32_t tm = *tmem_slot;
 
     // which Q tiles of this CTA need key tile t (bit s = Q tile s)
-    auto need_of = [&](int t) -> uint32_t {
-        uint32_t nd = tile_visible(p.mask, qb0, t, kvalid) ? 1u : 0u;
-        if (act1 && tile_visible(p.mask, qb1, t, kvalid)) nd |= 2u;
+    // (captured by value: a by-reference capture would give these variables
+    // addresses and move them to local memory)
+    const MaskArgs mk = p.mask;
+    auto need_of = [=](int t) -> uint32_t {
+        uint32_t nd = tile_visible(mk, qb0, t, kvalid) ? 1u : 0u;
+        if (act1 && tile_visible(mk, qb1, t, kvalid)) nd |= 2u;
         return nd;
     };
 
@@ -177,21 +214,20 @@ __global__ void __launch_bounds__(384, 1)
                 if (!mbar_wait(&kv_empty[stage], ph ^ 1, cx, 1)) break;
                 uint8_t* sk = sm + C::K_OFF + stage * C::SPLIT * C::TILE_BYTES;
                 uint8_t* sv = sm + C::V_OFF + stage * C::TILE_BYTES;
-                mbar_arrive_expect_tx(&k_full[stage], C::SPLIT * C::TILE_BYTES);
+                mbar_arrive_expect_tx(&kv_full[stage], (C::SPLIT + 1) * C::TILE_BYTES);
                 for (int r = 0; r < C::NREG; ++r) {
-                    tma_load_2d(sk + r * 16384, &tmK, r * C::BOXC, bh * N + t * kTile, &k_full[stage]);
+                    tma_load_2d(sk + r * 16384, &tmK, r * C::BOXC, bh * N + t * kTile, &kv_full[stage]);
                     if constexpr (TF32)
                         tma_load_2d(sk + C::TILE_BYTES + r * 16384, &tmKlo, r * C::BOXC, bh * N + t * kTile,
-                                    &k_full[stage]);
+                                    &kv_full[stage]);
                 }
-                mbar_arrive_expect_tx(&v_full[stage], C::TILE_BYTES);
                 if constexpr (!TF32) {
                     for (int r = 0; r < C::NREG; ++r)
-                        tma_load_2d(sv + r * 16384, &tmV, r * C::BOXC, bh * N + t * kTile, &v_full[stage]);
+                        tma_load_2d(sv + r * 16384, &tmV, r * C::BOXC, bh * N + t * kTile, &kv_full[stage]);
                 } else {
                     // V^T [d][keys]: four 32-key swizzle regions of [d][32]
                     for (int r = 0; r < 4; ++r)
-                        tma_load_2d(sv + r * D * 128, &tmV, t * kTile + r * 32, bh * D, &v_full[stage]);
+                        tma_load_2d(sv + r * D * 128, &tmV, t * kTile + r * 32, bh * D, &kv_full[stage]);
                 }
                 ++u;
             }
@@ -200,8 +236,7 @@ __global__ void __launch_bounds__(384, 1)
             for (int i = 0; i < C::STAGES && i < u; ++i) {
                 const int last = i + ((u - 1 - i) / C::STAGES) * C::STAGES;
                 const uint32_t ph = (last / C::STAGES) & 1;
-                mbar_wait_teardown(&k_full[i], ph, 200000000ull);
-                mbar_wait_teardown(&v_full[i], ph, 200000000ull);
+                mbar_wait_teardown(&kv_full[i], ph, 200000000ull);
             }
         }
     } else if (warp == 1) {
@@ -209,40 +244,17 @@ __global__ void __launch_bounds__(384, 1)
         if (lane == 0) {
             bool ok = mbar_wait(bar_q, 0, cx, 2);
             if (ok) tc_fence_after();
-            int pend_stage[2] = {-1, -1};
-            uint32_t pend_ph[2] = {0, 0};
-            int nP[2] = {0, 0};
-            int nPV[2] = {0, 0};
-            uint32_t rem = 0;  // 2 bits per stage: users still to finish
+            MmaState st;
             // descriptors are built once and advanced by constants per k-step
             const uint64_t dQ0 = sdesc_sw128(smem_u32(sm + C::Q_OFF), 16, 1024);
             const uint64_t dK0 = sdesc_sw128(smem_u32(sm + C::K_OFF), 16, 1024);
             // bf16: V MN-major (LBO = distance between 64-column regions);
             // tf32: V^T K-major
             const uint64_t dV0 = sdesc_sw128(smem_u32(sm + C::V_OFF), TF32 ? 16 : 16384, 1024);
-
-            auto issue_pv = [&](int s) -> bool {
-                const int ps = pend_stage[s];
-                if (!mbar_wait(&p_full[s], nP[s] & 1, cx, 3)) return false;
-                ++nP[s];
-                if (!mbar_wait(&v_full[ps], pend_ph[s], cx, 4)) return false;
-                tc_fence_after();
-                const uint64_t vst = sdesc_advance(dV0, ps * C::TILE_BYTES);
-#pragma unroll
-                for (int kk = 0; kk < C::PV_KSTEPS; ++kk) {
-                    const uint32_t off = TF32 ? (kk / 4) * (D * 128) + (kk % 4) * 32 : kk * 2048;
-                    umma_ts<TF32>(tm + s * 256 + 128, tm + s * 256 + kk * 8, sdesc_advance(vst, off), C::ID_PV,
-                                  (nPV[s] > 0 || kk > 0) ? 1u : 0u);
-                }
-                ++nPV[s];
-                umma_commit(&o_done[s]);
-                uint32_t r = (rem >> (2 * ps)) & 3u;
-                r -= 1;
-                rem = (rem & ~(3u << (2 * ps))) | (r << (2 * ps));
-                if (r == 0) umma_commit(&kv_empty[ps]);
-                pend_stage[s] = -1;
-                return true;
-            };
+#define issue_pv(S) fwd_issue_pv<TF32, D>((S), st, tm, dV0, p_full, kv_empty, cx)
+            int (&pend_stage)[2] = st.pend_stage;
+            uint32_t(&pend_ph)[2] = st.pend_ph;
+            uint32_t& rem = st.rem;
 
             int u = 0;
             for (int t = 0; ok && t < hi; ++t) {
@@ -256,7 +268,7 @@ __global__ void __launch_bounds__(384, 1)
                 for (int s = 0; s < 2; ++s)
                     if (ok && pend_stage[s] == stage && !issue_pv(s)) ok = false;
                 if (!ok) break;
-                if (!mbar_wait(&k_full[stage], ph, cx, 5)) { ok = false; break; }
+                if (!mbar_wait(&kv_full[stage], ph, cx, 5)) { ok = false; break; }
                 tc_fence_after();
                 rem = (rem & ~(3u << (2 * stage))) | ((uint32_t)__popc(nd) << (2 * stage));
 #pragma unroll
@@ -285,6 +297,12 @@ __global__ void __launch_bounds__(384, 1)
             }
             for (int s = 0; ok && s < 2; ++s)
                 if (pend_stage[s] >= 0 && !issue_pv(s)) ok = false;
+#undef issue_pv
+            // one commit per Q tile after its last P V: the epilogue waits on it
+            if (ok) {
+                umma_commit(&o_done[0]);
+                umma_commit(&o_done[1]);
+            }
             // wait for every MMA issued so far before TMEM can be released
             umma_commit(drain);
             mbar_wait_teardown(drain, 0, 200000000ull);
@@ -386,12 +404,10 @@ __global__ void __launch_bounds__(384, 1)
                 lw += rr;
                 tmem_st_wait();
                 if (__any_sync(0xffffffffu, resc) && n > 0) {
-                    // O holds the previous tiles' sum: wait for their last PV,
-                    // then bring it to the new reference maximum.
-                    ok = mbar_wait(&o_done[s], (n - 1) & 1, cx, 7);
-                    ok = __all_sync(0xffffffffu, ok);
-                    if (!ok) break;
-                    tc_fence_after();
+                    // O holds the previous tiles' sum; their last P V was issued
+                    // before this tile's S, and MMAs complete in issue order,
+                    // so S being complete means O is final: rescale it to the
+                    // new reference maximum.
 #pragma unroll
                     for (int c = 0; c < D / 32; ++c) {
                         uint32_t ov[32];
@@ -409,7 +425,7 @@ __global__ void __launch_bounds__(384, 1)
             }
             // ------------------------------------------------------------ epilogue
             if (ok && n > 0) {
-                ok = mbar_wait(&o_done[s], (n - 1) & 1, cx, 8);
+                ok = mbar_wait(&o_done[s], 0, cx, 8);
                 ok = __all_sync(0xffffffffu, ok);
                 if (ok) tc_fence_after();
             }
