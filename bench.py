@@ -43,6 +43,9 @@ def parse():
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--table", action="store_true",
+                    help="measure every workload (times, TFLOP/s, errors vs the oracle on sampled heads); "
+                         "prints one JSON object per workload instead of the benchmark line")
     return ap.parse_args()
 
 
@@ -231,9 +234,94 @@ def run_reference(args, rank, world):
     print(json.dumps(line), flush=True)
 
 
+# ------------------------------------------------------------------ per-workload table
+TABLE_HEADS = {"tiny": None, "bert": None, "gpt2": None, "long4k": [(0, 0), (0, 31)],
+               "long8k": [(0, 0), (0, 31)], "sparse16k": [(0, 0), (1, 15)]}
+
+
+def run_table(args):
+    import numpy as np
+    import torch
+
+    import io_aware_exact_tiled_gb300 as fa
+    import oracle
+    from io_aware_exact_tiled_gb300 import accounting as acc
+    from io_aware_exact_tiled_gb300 import workloads as W
+
+    dev = torch.device("cuda", 0)
+    peaks, _ = load_peaks()
+    peak = float(peaks["bf16_tflops"])
+    ev = lambda: torch.cuda.Event(enable_timing=True)
+    for name, w in W.WORKLOADS.items():
+        x = W.make_inputs(w, seed=0)
+        q, k, v, do = (t.to(dev) for t in (x.q, x.k, x.v, x.do))
+        bm = None if x.blockmask is None else x.blockmask.to(dev)
+        kl = None if x.kv_len is None else x.kv_len.to(dev)
+        kw = dict(scale=x.scale, causal=x.causal, blockmask=bm, kv_len=kl)
+        B, H, N, d = q.shape
+        fwd_flop, bwd_flop = acc.flops(B, H, N, d, x.causal, None if kl is None else x.kv_len.tolist(),
+                                       None if bm is None else x.blockmask.numpy())
+        o, lse = fa.forward(q, k, v, **kw)
+        ws_f = fa.workspace(fa.fwd_workspace_size(B, H, N, d), dev)
+        ws_b = fa.workspace(fa.bwd_workspace_size(B, H, N, d), dev) if w.backward else None
+        row = {"workload": describe(w)}
+
+        def timed(fn, reps=20):
+            """(mean ms per call, mean ms of the main kernel per call)."""
+            for _ in range(3):
+                fn()
+            pairs = [(ev(), ev()) for _ in range(reps)]
+            for a, b in pairs:  # materialise the event handles
+                a.record()
+                b.record()
+            c0, c1 = ev(), ev()
+            torch.cuda.synchronize()
+            c0.record()
+            for i in range(reps):
+                fa.set_timing_events(*pairs[i])
+                fn()
+            c1.record()
+            fa.set_timing_events(None, None)
+            torch.cuda.synchronize()
+            return c0.elapsed_time(c1) / reps, sum(a.elapsed_time(b) for a, b in pairs) / reps
+
+        fcall, fker = timed(lambda: fa.forward(q, k, v, out=o, lse=lse, ws=ws_f, **kw))
+        row["fwd"] = {"call_ms": fcall, "kernel_ms": fker, "tflops": fwd_flop / (fker * 1e-3) / 1e12,
+                      "pct_peak": 100 * fwd_flop / (fker * 1e-3) / 1e12 / peak}
+        g = {"o": o.float().cpu().numpy(), "lse": lse.cpu().numpy()}
+        if w.backward:
+            dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+            bcall, bker = timed(lambda: fa.backward(q, k, v, o, lse, do, dq=dq, dk=dk, dv=dv, ws=ws_b, **kw))
+            row["bwd"] = {"call_ms": bcall, "kernel_ms": bker, "tflops_call": bwd_flop / (bcall * 1e-3) / 1e12,
+                          "tflops_kernel": bwd_flop / (bker * 1e-3) / 1e12,
+                          "pct_peak_kernel": 100 * bwd_flop / (bker * 1e-3) / 1e12 / peak}
+            g.update(dq=dq.float().cpu().numpy(), dk=dk.float().cpu().numpy(), dv=dv.float().cpu().numpy())
+        heads = TABLE_HEADS.get(name)
+        okw = dict(causal=x.causal, kv_len=x.kv_len, blockmask=x.blockmask, heads=heads)
+        t0 = time.perf_counter()
+        O, L = oracle.forward(x.q, x.k, x.v, x.scale, **okw)
+        sel = (slice(None),) if heads is None else tuple(np.array(ix) for ix in zip(*heads))
+        err = {"o_maxabs": float(np.abs(g["o"][sel] - O[sel]).max()),
+               "lse_maxabs": float(np.nanmax(np.where(np.isneginf(L[sel]) & np.isneginf(g["lse"][sel]), 0.0,
+                                                      np.abs(g["lse"][sel] - L[sel]))))}
+        if w.backward:
+            dQ, dK, dV = oracle.backward(x.q, x.k, x.v, x.do, x.scale, **okw)
+            for n, ref in (("dq", dQ), ("dk", dK), ("dv", dV)):
+                err[n + "_rel"] = float(np.linalg.norm(g[n][sel] - ref[sel]) / np.linalg.norm(ref[sel]))
+        t_oracle = time.perf_counter() - t0
+        nheads = B * H if heads is None else len(heads)
+        row["errors"] = err
+        row["errors_on"] = "all heads" if heads is None else f"heads {heads}"
+        row["oracle_cpu_s_per_head"] = t_oracle / nheads
+        row["oracle_cores"] = os.cpu_count()
+        print(json.dumps(row), flush=True)
+
+
 # ------------------------------------------------------------------ our arm
 def main():
     args = parse()
+    if args.table:
+        return run_table(args)
     rank = int(os.environ.get("RANK", "0"))
     world = int(os.environ.get("WORLD_SIZE", "1"))
     local = int(os.environ.get("LOCAL_RANK", "0"))
