@@ -568,6 +568,9 @@ static cudaError_t launch_fwd_t(const FwdArgs& a, cudaStream_t stream, int* nlau
 }
 
 cudaError_t launch_fwd(const FwdArgs& a, cudaStream_t stream, int* nlaunch) {
+    // With a tile mask the two query tiles of a pair rarely share key tiles,
+    // which defeats the pairing: one query tile per CTA instead.
+    if (!a.fp32 && a.blockmask) return launch_fwd_bf16_q1(a, stream, nlaunch);
     if (a.fp32) {
         if (a.d == 64) return launch_fwd_t<true, 64>(a, stream, nlaunch);
         return cudaErrorInvalidValue;  // fp32 d=128 exceeds the shared-memory budget of this kernel
