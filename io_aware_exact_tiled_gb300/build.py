@@ -30,8 +30,8 @@ def nvcc() -> str:
     raise RuntimeError("nvcc not found: the CUDA toolkit is required to build libfa.so")
 
 
-def _compile(src: str, extra) -> str:
-    obj = os.path.join(BUILD_DIR, os.path.splitext(src)[0] + ".o")
+def _compile(src: str, extra, build_dir: str = BUILD_DIR) -> str:
+    obj = os.path.join(build_dir, os.path.splitext(src)[0] + ".o")
     cmd = [nvcc(), *ARCH, *FLAGS, *extra, "-c", os.path.join(CSRC, src), "-o", obj]
     r = subprocess.run(cmd, capture_output=True, text=True)
     if r.returncode != 0:
@@ -39,24 +39,35 @@ def _compile(src: str, extra) -> str:
     return obj
 
 
-def build(force: bool = False, extra_flags=()) -> str:
-    """Compile csrc/*.cu and link libfa.so; returns the library path."""
+def build(force: bool = False, extra_flags=(), lib: str = LIB, build_dir: str = BUILD_DIR) -> str:
+    """Compile csrc/*.cu and link the library (libfa.so unless `lib` says
+    otherwise, e.g. a debug variant built with extra flags); returns its path."""
     srcs = [os.path.join(CSRC, s) for s in SOURCES]
     deps = srcs + [os.path.join(CSRC, f) for f in os.listdir(CSRC)] + [os.path.join(INCLUDE, "fa.h")]
-    if not force and os.path.exists(LIB):
-        t = os.path.getmtime(LIB)
+    if not force and os.path.exists(lib):
+        t = os.path.getmtime(lib)
         if all(os.path.getmtime(d) <= t for d in deps):
-            return LIB
-    os.makedirs(BUILD_DIR, exist_ok=True)
+            return lib
+    os.makedirs(build_dir, exist_ok=True)
     with concurrent.futures.ThreadPoolExecutor(len(SOURCES)) as ex:
-        objs = list(ex.map(lambda s: _compile(s, list(extra_flags)), SOURCES))
-    tmp = LIB + ".tmp"
+        objs = list(ex.map(lambda s: _compile(s, list(extra_flags), build_dir), SOURCES))
+    tmp = lib + ".tmp"
     cmd = [nvcc(), *ARCH, "-shared", "-cudart", "static", "-o", tmp, *objs]
     r = subprocess.run(cmd, capture_output=True, text=True)
     if r.returncode != 0:
         raise RuntimeError(f"link failed:\n{r.stdout}\n{r.stderr}")
-    os.replace(tmp, LIB)
-    return LIB
+    os.replace(tmp, lib)
+    return lib
+
+
+DEBUG_LIB = os.path.join(PKG, "libfa_debug.so")
+
+
+def build_debug(force: bool = False) -> str:
+    """Debug variant for the give-up test: short (0.2 s) device wait limit and
+    one withheld "P ready" arrival per kernel (FA_DEBUG_DROP_ARRIVE)."""
+    return build(force, ("-DFA_DEBUG_DROP_ARRIVE", "-DFA_WAIT_LIMIT_NS=200000000ull"), DEBUG_LIB,
+                 os.path.join(PKG, "_build_debug"))
 
 
 if __name__ == "__main__":

@@ -323,7 +323,7 @@ __global__ void __launch_bounds__(512, 1)
             }
             tmem_st_wait();
             tc_fence_before();
-            mbar_arrive(p_ready);
+            if (!FA_DROP_THIS_ARRIVE(u == 0)) mbar_arrive(p_ready);
             // dS^T = P^T * (dP^T - D) (the scale is applied to dK and dQ at
             // the end), computed into registers before the shared buffer is
             // known to be free; P^T is read back from TMEM (bf16)

@@ -420,7 +420,7 @@ __global__ void __launch_bounds__(384, 1)
                     tmem_st_wait();
                 }
                 tc_fence_before();
-                mbar_arrive(&p_full[s]);
+                if (!FA_DROP_THIS_ARRIVE(n == 0)) mbar_arrive(&p_full[s]);
                 ++n;
             }
             // ------------------------------------------------------------ epilogue

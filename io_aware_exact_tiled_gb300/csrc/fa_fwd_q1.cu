@@ -302,7 +302,7 @@ __global__ void __launch_bounds__(384, 1)
                 tmem_st_wait();
             }
             tc_fence_before();
-            mbar_arrive(&p_full[u & 1]);
+            if (!FA_DROP_THIS_ARRIVE(u == 0)) mbar_arrive(&p_full[u & 1]);
             ++u;
         }
         // ------------------------------------------------------------ epilogue

@@ -133,6 +133,16 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
 #define FA_WAIT_LIMIT_NS 4000000000ull
 #endif
 
+// FA_DEBUG_DROP_ARRIVE (debug builds only): the first "P ready" arrival of
+// the first warp of each softmax / compute group is withheld, so that the
+// MMA thread's bounded wait runs out; used by a test to check that the
+// kernels give up cleanly and report FA_ERR_TIMEOUT instead of hanging.
+#ifdef FA_DEBUG_DROP_ARRIVE
+#define FA_DROP_THIS_ARRIVE(first_tile) ((first_tile) && (threadIdx.x & 127) < 32)
+#else
+#define FA_DROP_THIS_ARRIVE(first_tile) false
+#endif
+
 // Status codes written by the kernels into the status word.
 enum : int { FA_DEV_OK = 0, FA_DEV_TIMEOUT = 4 };
 
