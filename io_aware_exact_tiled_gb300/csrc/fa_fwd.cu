@@ -364,11 +364,11 @@ __global__ void __launch_bounds__(384, 1)
                 // two elements per f32x2 instruction: x = s * c2 - mu, the
                 // fp32 row sum and the sum of the bf16-rounded weights
                 const uint64_t c2c2 = f2_make(c2, c2), nmu2 = f2_make(-mu, -mu);
-                uint64_t rs2 = 0ull, rr2 = 0ull;
+                uint64_t rs2 = 0ull;
+                uint32_t pk[4][16];  // P as bf16 pairs; kept for the bf16-weight sum
 #pragma unroll
                 for (int c = 0; c < 4; ++c) {
                     if constexpr (!TF32) {
-                        uint32_t pk[16];
 #pragma unroll
                         for (int i = 0; i < 16; ++i) {
                             float x0, x1;
@@ -376,11 +376,10 @@ __global__ void __launch_bounds__(384, 1)
                                             c2c2, nmu2),
                                      x0, x1);
                             const float p0 = ex2_approx(x0), p1 = ex2_approx(x1);
-                            pk[i] = pack_bf16x2(p0, p1);
+                            pk[c][i] = pack_bf16x2(p0, p1);
                             rs2 = f2_add(rs2, f2_make(p0, p1));
-                            rr2 = f2_add(rr2, f2_from_bf16x2(pk[i]));
                         }
-                        tmem_st16(tl + c * 16, pk);
+                        tmem_st16(tl + c * 16, pk[c]);
                     } else {
                         uint32_t pk[32];
 #pragma unroll
@@ -393,17 +392,36 @@ __global__ void __launch_bounds__(384, 1)
                         tmem_st32(tl + c * 32, pk);
                     }
                 }
-                if constexpr (!TF32) {
-                    float a, b;
-                    f2_split(rs2, a, b);
-                    rs = a + b;
-                    f2_split(rr2, a, b);
-                    rr = a + b;
+                if constexpr (TF32) {
+                    l += rs;
+                    lw += rr;
                 }
-                l += rs;
-                lw += rr;
                 tmem_st_wait();
+                // Row sums of this tile: fp32 probabilities (for L) and their
+                // bf16 roundings, the weights P V uses (for O). They are not
+                // needed before the next tile, so in the usual case they are
+                // formed after P has been handed to the MMA thread.
+                if constexpr (!TF32) {
+                    float a_, b_;
+                    f2_split(rs2, a_, b_);
+                    l += a_ + b_;
+                }
+                // The sum of the bf16-rounded weights (what P V multiplies; it
+                // normalises O) is not needed before the next tile: in the usual
+                // case it is formed after P has been handed to the MMA thread.
+#define FA_ROW_SUMS()                                                                                     \
+    do {                                                                                                  \
+        if constexpr (!TF32) {                                                                            \
+            uint64_t rr2 = 0ull;                                                                          \
+            _Pragma("unroll") for (int c = 0; c < 4; ++c) _Pragma("unroll") for (int i = 0; i < 16; ++i)    \
+                rr2 = f2_add(rr2, f2_from_bf16x2(pk[c][i]));                                              \
+            float a_, b_;                                                                                 \
+            f2_split(rr2, a_, b_);                                                                        \
+            lw += a_ + b_;                                                                                \
+        }                                                                                                 \
+    } while (0)
                 if (__any_sync(0xffffffffu, resc) && n > 0) {
+                    FA_ROW_SUMS();
                     // O holds the previous tiles' sum; their last P V was issued
                     // before this tile's S, and MMAs complete in issue order,
                     // so S being complete means O is final: rescale it to the
@@ -418,9 +436,14 @@ __global__ void __launch_bounds__(384, 1)
                         tmem_st32(tl + 128 + c * 32, ov);
                     }
                     tmem_st_wait();
+                    tc_fence_before();
+                    if (!FA_DROP_THIS_ARRIVE(n == 0)) mbar_arrive(&p_full[s]);
+                } else {
+                    tc_fence_before();
+                    if (!FA_DROP_THIS_ARRIVE(n == 0)) mbar_arrive(&p_full[s]);
+                    FA_ROW_SUMS();
                 }
-                tc_fence_before();
-                if (!FA_DROP_THIS_ARRIVE(n == 0)) mbar_arrive(&p_full[s]);
+#undef FA_ROW_SUMS
                 ++n;
             }
             // ------------------------------------------------------------ epilogue
