@@ -199,7 +199,9 @@ __global__ void __launch_bounds__(512, 1)
         }
     } else if (warp == 1) {
         // ------------------------------------------------------------ MMA issuer
-        if (lane == 0) {
+        // the whole warp runs the loop; one elected lane issues
+        {
+            const uint32_t leader = elect_one_sync();
             // descriptors are built once and advanced by constants per k-step
             const uint64_t dK_k = sdesc_sw128(smem_u32(sm + C::K_OFF), 16, 1024);        // K_j, K-major
             const uint64_t dV_k = sdesc_sw128(smem_u32(sm + C::V_OFF), 16, 1024);        // V_j, K-major
@@ -211,11 +213,11 @@ __global__ void __launch_bounds__(512, 1)
             for (int i = lo; ok && i < T; ++i) {
                 if (!visible_i(i)) continue;
                 if (u == 0) {
-                    if (!(ok = mbar_wait(kv_full, 0, cx, 12))) break;
+                    if (!(ok = mbar_wait_warp(kv_full, 0, cx, 12))) break;
                 }
                 const int st = u % C::STAGES;
                 const uint32_t ph = (u / C::STAGES) & 1;
-                if (!(ok = mbar_wait(&qd_full[st], ph, cx, 13))) break;
+                if (!(ok = mbar_wait_warp(&qd_full[st], ph, cx, 13))) break;
                 tc_fence_after();
                 const uint32_t qb = smem_u32(sm + C::Q_OFF + st * C::TILE_BYTES);
                 const uint32_t dob = smem_u32(sm + C::DO_OFF + st * C::TILE_BYTES);
@@ -225,47 +227,47 @@ __global__ void __launch_bounds__(512, 1)
 #pragma unroll
                 for (int kk = 0; kk < D / 16; ++kk) {
                     const uint32_t off = (kk / 4) * 16384 + (kk % 4) * 32;
-                    umma_ss<false>(tm + C::COL_DP, sdesc_advance(dV_k, off), sdesc_advance(dO_k, off), C::ID_SQ,
+                    umma_ss<false>(leader, tm + C::COL_DP, sdesc_advance(dV_k, off), sdesc_advance(dO_k, off), C::ID_SQ,
                                    kk > 0);
                 }
-                umma_commit(dp_full);
+                umma_commit(leader, dp_full);
                 // S^T = K_j Q_i^T (these columns held dQ of the previous block)
-                if (u > 0 && !(ok = mbar_wait(dq_free, (u - 1) & 1, cx, 14))) break;
+                if (u > 0 && !(ok = mbar_wait_warp(dq_free, (u - 1) & 1, cx, 14))) break;
                 tc_fence_after();
 #pragma unroll
                 for (int kk = 0; kk < D / 16; ++kk) {
                     const uint32_t off = (kk / 4) * 16384 + (kk % 4) * 32;
-                    umma_ss<false>(tm + C::COL_S, sdesc_advance(dK_k, off), sdesc_advance(dQ_k, off), C::ID_SQ,
+                    umma_ss<false>(leader, tm + C::COL_S, sdesc_advance(dK_k, off), sdesc_advance(dQ_k, off), C::ID_SQ,
                                    kk > 0);
                 }
-                umma_commit(s_full);
+                umma_commit(leader, s_full);
                 // dV_j += P^T dO_i ; P^T of queries 0-63 sits in columns 0-31
                 // and that of queries 64-127 in columns 64-95
-                if (!(ok = mbar_wait(p_ready, u & 1, cx, 15))) break;
+                if (!(ok = mbar_wait_warp(p_ready, u & 1, cx, 15))) break;
                 tc_fence_after();
 #pragma unroll
                 for (int kk = 0; kk < 8; ++kk)
-                    umma_ts<false>(tm + C::COL_DV, tm + C::COL_S + (kk >> 2) * 64 + (kk & 3) * 8,
+                    umma_ts<false>(leader, tm + C::COL_DV, tm + C::COL_S + (kk >> 2) * 64 + (kk & 3) * 8,
                                    sdesc_advance(dO_mn, kk * 2048), C::ID_KN, (u > 0 || kk > 0) ? 1u : 0u);
                 // dK_j += dS^T Q_i ; dQ_i = dS K_j
-                if (!(ok = mbar_wait(ds_ready, u & 1, cx, 16))) break;
+                if (!(ok = mbar_wait_warp(ds_ready, u & 1, cx, 16))) break;
                 tc_fence_after();
 #pragma unroll
                 for (int kk = 0; kk < 8; ++kk) {
                     const uint32_t off = (kk / 4) * 16384 + (kk % 4) * 32;
-                    umma_ss<false>(tm + C::COL_DK, sdesc_advance(dS_k, off), sdesc_advance(dQ_mn, kk * 2048), C::ID_KN,
+                    umma_ss<false>(leader, tm + C::COL_DK, sdesc_advance(dS_k, off), sdesc_advance(dQ_mn, kk * 2048), C::ID_KN,
                                    (u > 0 || kk > 0) ? 1u : 0u);
                 }
 #pragma unroll
                 for (int kk = 0; kk < 8; ++kk)
-                    umma_ss<false>(tm + C::COL_DQ, sdesc_advance(dS_mn, kk * 2048), sdesc_advance(dK_mn, kk * 2048),
+                    umma_ss<false>(leader, tm + C::COL_DQ, sdesc_advance(dS_mn, kk * 2048), sdesc_advance(dK_mn, kk * 2048),
                                    C::ID_DQ, kk > 0 ? 1u : 0u);
-                umma_commit(dq_full);
-                umma_commit(&qd_empty[st]);
+                umma_commit(leader, dq_full);
+                umma_commit(leader, &qd_empty[st]);
                 ++u;
             }
-            if (ok && u > 0) umma_commit(dkv_done);
-            umma_commit(drain);
+            if (ok && u > 0) umma_commit(leader, dkv_done);
+            umma_commit(leader, drain);
             mbar_wait_teardown(drain, 0, 200000000ull);
         }
     } else if (warp >= 4 && warp < 12) {

@@ -62,6 +62,7 @@ struct FwdCfg {
     // tf32 operands must be K-major, so V arrives transposed ([d][keys]).
     static constexpr uint32_t ID_PV = idesc_make(128, D, TF32 ? kFmtTF32 : kFmtBF16, false, !TF32);
     static_assert(SMEM <= 232448, "shared memory budget");
+    static_assert((1 + 4 * STAGES + 7) * 8 + 8 <= 256, "barrier area");
 };
 
 struct FwdParams {
@@ -77,6 +78,7 @@ struct FwdParams {
 struct MmaState {
     int pend_stage[2] = {-1, -1};  // K/V stage whose P V GEMM is still to be issued
     uint32_t pend_ph[2] = {0, 0};  // V-full phase parity of that stage
+    int pend_u[2] = {0, 0};        // index (among loaded tiles) of that tile
     int nP[2] = {0, 0};            // P-ready phases consumed
     int nPV[2] = {0, 0};           // P V GEMMs issued
     uint32_t rem = 0;              // 2 bits per stage: Q tiles still to read its V
@@ -84,27 +86,28 @@ struct MmaState {
 
 // O_s += P_s V for Q tile s's pending K/V tile (waits for P_s and V).
 template <bool TF32, int D>
-__device__ __forceinline__ bool fwd_issue_pv(int s, MmaState& st, uint32_t tm, uint64_t dV0, uint64_t* p_full,
-                                             uint64_t* kv_empty, const WaitCtx& cx) {
+__device__ __forceinline__ bool fwd_issue_pv(uint32_t leader, int s, MmaState& st, uint32_t tm, uint64_t dV0,
+                                             uint64_t* p_full,
+                                             uint64_t* v_full, uint64_t* kv_empty, const WaitCtx& cx) {
     using C = FwdCfg<TF32, D>;
     const int ps = st.pend_stage[s];
-    if (!mbar_wait(&p_full[s], st.nP[s] & 1, cx, 3)) return false;
+    if (!mbar_wait_warp(&p_full[s], st.nP[s] & 1, cx, 3)) return false;
     ++st.nP[s];
-    // V of this stage arrived with its K (one barrier per stage), which the
-    // MMA thread waited for before issuing S for this tile
+    // V comes through its own ring and is normally resident long before P
+    if (!mbar_wait_warp(&v_full[ps], st.pend_ph[s], cx, 4)) return false;
     tc_fence_after();
     const uint64_t vst = sdesc_advance(dV0, ps * C::TILE_BYTES);
 #pragma unroll
     for (int kk = 0; kk < C::PV_KSTEPS; ++kk) {
         const uint32_t off = TF32 ? (kk / 4) * (D * 128) + (kk % 4) * 32 : kk * 2048;
-        umma_ts<TF32>(tm + s * 256 + 128, tm + s * 256 + kk * 8, sdesc_advance(vst, off), C::ID_PV,
+        umma_ts<TF32>(leader, tm + s * 256 + 128, tm + s * 256 + kk * 8, sdesc_advance(vst, off), C::ID_PV,
                       (st.nPV[s] > 0 || kk > 0) ? 1u : 0u);
     }
     ++st.nPV[s];
     uint32_t r = (st.rem >> (2 * ps)) & 3u;
     r -= 1;
     st.rem = (st.rem & ~(3u << (2 * ps))) | (r << (2 * ps));
-    if (r == 0) umma_commit(&kv_empty[ps]);
+    if (r == 0) umma_commit(leader, &kv_empty[ps]);
     st.pend_stage[s] = -1;
     return true;
 }
@@ -125,8 +128,14 @@ __global__ void __launch_bounds__(384, 1)
     uint8_t* sm = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
     uint64_t* bars = reinterpret_cast<uint64_t*>(sm + C::BAR_OFF);
     uint64_t* bar_q = bars + 0;
-    uint64_t* kv_full = bars + 1;             // K and V of a stage landed
-    uint64_t* kv_empty = kv_full + C::STAGES;
+    // K and V travel through separate rings with the same number of stages:
+    // a K stage is released once the S GEMMs that read it complete, a V stage
+    // once its P V GEMMs complete, so the next K tile loads during the
+    // current tile's softmax instead of waiting for its P V products.
+    uint64_t* k_full = bars + 1;              // K of a stage landed
+    uint64_t* v_full = k_full + C::STAGES;    // V of a stage landed
+    uint64_t* k_empty = v_full + C::STAGES;   // S GEMMs reading a K stage done
+    uint64_t* kv_empty = k_empty + C::STAGES; // P V GEMMs reading a V stage done
     uint64_t* s_full = kv_empty + C::STAGES;  // [2]
     uint64_t* p_full = s_full + 2;            // [2]
     uint64_t* o_done = p_full + 2;            // [2]
@@ -156,7 +165,9 @@ __global__ void __launch_bounds__(384, 1)
         *abort_flag = 0;
         mbar_init(bar_q, 1);
         for (int i = 0; i < C::STAGES; ++i) {
-            mbar_init(&kv_full[i], 1);
+            mbar_init(&k_full[i], 1);
+            mbar_init(&v_full[i], 1);
+            mbar_init(&k_empty[i], 1);
             mbar_init(&kv_empty[i], 1);
         }
         for (int i = 0; i < 2; ++i) {
@@ -206,43 +217,51 @@ __global__ void __launch_bounds__(384, 1)
                     tma_load_2d(dq, &tmQ, r * C::BOXC, qrow0 + s * kTile, bar_q);
                     if constexpr (TF32) tma_load_2d(dq + C::TILE_BYTES, &tmQlo, r * C::BOXC, qrow0 + s * kTile, bar_q);
                 }
-            int u = 0;
+            int nk = 0, nv = 0;  // K and V tiles whose loads were issued
             for (int t = 0; t < hi; ++t) {
                 if (!need_of(t)) continue;
-                const int stage = u % C::STAGES;
-                const uint32_t ph = (u / C::STAGES) & 1;
-                if (!mbar_wait(&kv_empty[stage], ph ^ 1, cx, 1)) break;
+                const int stage = nk % C::STAGES;
+                const uint32_t ph = (nk / C::STAGES) & 1;
+                if (!mbar_wait(&k_empty[stage], ph ^ 1, cx, 1)) break;
                 uint8_t* sk = sm + C::K_OFF + stage * C::SPLIT * C::TILE_BYTES;
                 uint8_t* sv = sm + C::V_OFF + stage * C::TILE_BYTES;
-                mbar_arrive_expect_tx(&kv_full[stage], (C::SPLIT + 1) * C::TILE_BYTES);
+                mbar_arrive_expect_tx(&k_full[stage], C::SPLIT * C::TILE_BYTES);
                 for (int r = 0; r < C::NREG; ++r) {
-                    tma_load_2d(sk + r * 16384, &tmK, r * C::BOXC, bh * N + t * kTile, &kv_full[stage]);
+                    tma_load_2d(sk + r * 16384, &tmK, r * C::BOXC, bh * N + t * kTile, &k_full[stage]);
                     if constexpr (TF32)
                         tma_load_2d(sk + C::TILE_BYTES + r * 16384, &tmKlo, r * C::BOXC, bh * N + t * kTile,
-                                    &kv_full[stage]);
+                                    &k_full[stage]);
                 }
+                ++nk;
+                if (!mbar_wait(&kv_empty[stage], ph ^ 1, cx, 9)) break;
+                mbar_arrive_expect_tx(&v_full[stage], C::TILE_BYTES);
                 if constexpr (!TF32) {
                     for (int r = 0; r < C::NREG; ++r)
-                        tma_load_2d(sv + r * 16384, &tmV, r * C::BOXC, bh * N + t * kTile, &kv_full[stage]);
+                        tma_load_2d(sv + r * 16384, &tmV, r * C::BOXC, bh * N + t * kTile, &v_full[stage]);
                 } else {
                     // V^T [d][keys]: four 32-key swizzle regions of [d][32]
                     for (int r = 0; r < 4; ++r)
-                        tma_load_2d(sv + r * D * 128, &tmV, t * kTile + r * 32, bh * D, &kv_full[stage]);
+                        tma_load_2d(sv + r * D * 128, &tmV, t * kTile + r * 32, bh * D, &v_full[stage]);
                 }
-                ++u;
+                ++nv;
             }
             // let every copy in flight land before the CTA can exit
             mbar_wait_teardown(bar_q, 0, 200000000ull);
-            for (int i = 0; i < C::STAGES && i < u; ++i) {
-                const int last = i + ((u - 1 - i) / C::STAGES) * C::STAGES;
-                const uint32_t ph = (last / C::STAGES) & 1;
-                mbar_wait_teardown(&kv_full[i], ph, 200000000ull);
+            for (int i = 0; i < C::STAGES && i < nk; ++i) {
+                const int last = i + ((nk - 1 - i) / C::STAGES) * C::STAGES;
+                mbar_wait_teardown(&k_full[i], (last / C::STAGES) & 1, 200000000ull);
+            }
+            for (int i = 0; i < C::STAGES && i < nv; ++i) {
+                const int last = i + ((nv - 1 - i) / C::STAGES) * C::STAGES;
+                mbar_wait_teardown(&v_full[i], (last / C::STAGES) & 1, 200000000ull);
             }
         }
     } else if (warp == 1) {
         // ------------------------------------------------------------ MMA issuer
-        if (lane == 0) {
-            bool ok = mbar_wait(bar_q, 0, cx, 2);
+        // the whole warp runs the loop; one elected lane issues
+        {
+            const uint32_t leader = elect_one_sync();
+            bool ok = mbar_wait_warp(bar_q, 0, cx, 2);
             if (ok) tc_fence_after();
             MmaState st;
             // descriptors are built once and advanced by constants per k-step
@@ -251,7 +270,7 @@ __global__ void __launch_bounds__(384, 1)
             // bf16: V MN-major (LBO = distance between 64-column regions);
             // tf32: V^T K-major
             const uint64_t dV0 = sdesc_sw128(smem_u32(sm + C::V_OFF), TF32 ? 16 : 16384, 1024);
-#define issue_pv(S) fwd_issue_pv<TF32, D>((S), st, tm, dV0, p_full, kv_empty, cx)
+#define issue_pv(S) fwd_issue_pv<TF32, D>(leader, (S), st, tm, dV0, p_full, v_full, kv_empty, cx)
             int (&pend_stage)[2] = st.pend_stage;
             uint32_t(&pend_ph)[2] = st.pend_ph;
             uint32_t& rem = st.rem;
@@ -262,13 +281,16 @@ __global__ void __launch_bounds__(384, 1)
                 if (!nd) continue;
                 const int stage = u % C::STAGES;
                 const uint32_t ph = (u / C::STAGES) & 1;
-                // The producer refills this stage only after every P V that
-                // reads its previous tile: issue those first.
+                // The producer issues K of tile u only after V of tile u - 1,
+                // which waits for every P V reading tile u - 1 - STAGES, and
+                // tile u reuses the V stage (and its reader count) of tile
+                // u - STAGES: a P V still pending for a tile that old (its Q
+                // tile skipped the tiles since) is issued first.
 #pragma unroll
                 for (int s = 0; s < 2; ++s)
-                    if (ok && pend_stage[s] == stage && !issue_pv(s)) ok = false;
+                    if (ok && pend_stage[s] >= 0 && st.pend_u[s] <= u - C::STAGES && !issue_pv(s)) ok = false;
                 if (!ok) break;
-                if (!mbar_wait(&kv_full[stage], ph, cx, 5)) { ok = false; break; }
+                if (!mbar_wait_warp(&k_full[stage], ph, cx, 5)) { ok = false; break; }
                 tc_fence_after();
                 rem = (rem & ~(3u << (2 * stage))) | ((uint32_t)__popc(nd) << (2 * stage));
 #pragma unroll
@@ -285,14 +307,17 @@ __global__ void __launch_bounds__(384, 1)
 #pragma unroll
                         for (int kk = 0; kk < C::S_KSTEPS; ++kk) {
                             const uint32_t off = (kk / 4) * 16384 + (kk % 4) * 32;
-                            umma_ss<TF32>(tm + s * 256, sdesc_advance(qa, off), sdesc_advance(kb2, off), C::ID_S,
+                            umma_ss<TF32>(leader, tm + s * 256, sdesc_advance(qa, off), sdesc_advance(kb2, off), C::ID_S,
                                           (part > 0 || kk > 0) ? 1u : 0u);
                         }
                     }
-                    umma_commit(&s_full[s]);
+                    umma_commit(leader, &s_full[s]);
                     pend_stage[s] = stage;
                     pend_ph[s] = ph;
+                    st.pend_u[s] = u;
                 }
+                if (!ok) break;
+                umma_commit(leader, &k_empty[stage]);  // S GEMMs reading this K stage are all issued
                 ++u;
             }
             for (int s = 0; ok && s < 2; ++s)
@@ -300,11 +325,11 @@ __global__ void __launch_bounds__(384, 1)
 #undef issue_pv
             // one commit per Q tile after its last P V: the epilogue waits on it
             if (ok) {
-                umma_commit(&o_done[0]);
-                umma_commit(&o_done[1]);
+                umma_commit(leader, &o_done[0]);
+                umma_commit(leader, &o_done[1]);
             }
             // wait for every MMA issued so far before TMEM can be released
-            umma_commit(drain);
+            umma_commit(leader, drain);
             mbar_wait_teardown(drain, 0, 200000000ull);
         }
     } else if (warp >= 4) {

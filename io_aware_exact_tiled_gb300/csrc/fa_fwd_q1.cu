@@ -164,44 +164,46 @@ __global__ void __launch_bounds__(384, 1)
         }
     } else if (warp == 1) {
         // ------------------------------------------------------------ MMA issuer
-        if (lane == 0 && ntiles > 0) {
-            bool ok = mbar_wait(bar_q, 0, cx, 32);
+        // the whole warp runs the loop; one elected lane issues
+        if (ntiles > 0) {
+            const uint32_t leader = elect_one_sync();
+            bool ok = mbar_wait_warp(bar_q, 0, cx, 32);
             const uint64_t dQ = sdesc_sw128(smem_u32(sm + C::Q_OFF), 16, 1024);
             const uint64_t dK0 = sdesc_sw128(smem_u32(sm + C::K_OFF), 16, 1024);
             const uint64_t dV0 = sdesc_sw128(smem_u32(sm + C::V_OFF), 16384, 1024);  // MN-major
             // S(j) = scale-free Q K_j^T into buffer j % 2
             auto issue_s = [=](int j) -> bool {
                 const int st = j % C::STAGES;
-                if (!mbar_wait(&kv_full[st], (j / C::STAGES) & 1, cx, 33)) return false;
+                if (!mbar_wait_warp(&kv_full[st], (j / C::STAGES) & 1, cx, 33)) return false;
                 tc_fence_after();
                 const uint64_t ks = sdesc_advance(dK0, st * C::TILE_BYTES);
                 const uint32_t sbuf = tm + (j & 1) * 128;
 #pragma unroll
                 for (int kk = 0; kk < D / 16; ++kk) {
                     const uint32_t off = (kk / 4) * 16384 + (kk % 4) * 32;
-                    umma_ss<false>(sbuf, sdesc_advance(dQ, off), sdesc_advance(ks, off), C::ID_S, kk > 0 ? 1u : 0u);
+                    umma_ss<false>(leader, sbuf, sdesc_advance(dQ, off), sdesc_advance(ks, off), C::ID_S, kk > 0 ? 1u : 0u);
                 }
-                umma_commit(&s_full[j & 1]);
+                umma_commit(leader, &s_full[j & 1]);
                 return true;
             };
             if (ok) tc_fence_after();
             for (int j = 0; ok && j < 2 && j < ntiles; ++j) ok = issue_s(j);
             for (int u = 0; ok && u < ntiles; ++u) {
                 // O += P(u) V(u); P of keys 0-63 in columns 0-31, keys 64-127 in 64-95
-                if (!(ok = mbar_wait(&p_full[u & 1], (u >> 1) & 1, cx, 34))) break;
+                if (!(ok = mbar_wait_warp(&p_full[u & 1], (u >> 1) & 1, cx, 34))) break;
                 tc_fence_after();
                 const int st = u % C::STAGES;
                 const uint64_t vs = sdesc_advance(dV0, st * C::TILE_BYTES);
                 const uint32_t pbuf = tm + (u & 1) * 128;
 #pragma unroll
                 for (int kk = 0; kk < 8; ++kk)
-                    umma_ts<false>(tm + C::COL_O, pbuf + (kk >> 2) * 64 + (kk & 3) * 8, sdesc_advance(vs, kk * 2048),
+                    umma_ts<false>(leader, tm + C::COL_O, pbuf + (kk >> 2) * 64 + (kk & 3) * 8, sdesc_advance(vs, kk * 2048),
                                    C::ID_PV, (u > 0 || kk > 0) ? 1u : 0u);
-                umma_commit(&kv_empty[st]);  // K and V of tile u consumed
+                umma_commit(leader, &kv_empty[st]);  // K and V of tile u consumed
                 if (u + 2 < ntiles) ok = issue_s(u + 2);
             }
-            if (ok) umma_commit(o_done);
-            umma_commit(drain);
+            if (ok) umma_commit(leader, o_done);
+            umma_commit(leader, drain);
             mbar_wait_teardown(drain, 0, 200000000ull);
         }
     } else if (warp >= 4) {

@@ -170,6 +170,12 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, const 
     }
 }
 
+// mbar_wait for a whole warp that runs in lock-step: every lane polls, and
+// the warp agrees on the outcome, so the lanes never part ways on a give-up.
+__device__ __forceinline__ bool mbar_wait_warp(uint64_t* bar, uint32_t parity, const WaitCtx& cx, int site) {
+    return __all_sync(0xffffffffu, mbar_wait(bar, parity, cx, site));
+}
+
 // Bounded wait that ignores the abort flag (used while tearing down, to let
 // copies already in flight land before the CTA exits).
 __device__ __forceinline__ bool mbar_wait_teardown(uint64_t* bar, uint32_t parity, uint64_t limit_ns) {
@@ -293,50 +299,66 @@ __host__ __device__ constexpr uint32_t idesc_make(int M, int N, uint32_t ab_form
 constexpr uint32_t kFmtBF16 = 1;
 constexpr uint32_t kFmtTF32 = 2;
 
+// MMA issue. The issuing loop runs in lock-step on all 32 lanes of one warp,
+// which compute the same (warp-uniform) operands, and one lane, `leader`
+// (from elect_one_sync), issues. Keeping the loop warp-uniform lets the
+// compiler hold descriptors and TMEM addresses in uniform registers; a loop
+// run by a single lane pays a move into the uniform datapath for every
+// operand of every MMA, which roughly triples the issue cost.
+__device__ __forceinline__ uint32_t elect_one_sync() {
+    uint32_t r;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\telect.sync _|p, 0xffffffff;\n\tselp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(r));
+    return r;
+}
+
 // D[tmem] (+)= A[smem] * B[smem]
 template <bool kTF32>
-__device__ __forceinline__ void umma_ss(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
-                                        uint32_t accumulate) {
+__device__ __forceinline__ void umma_ss(uint32_t leader, uint32_t d_tmem, uint64_t adesc, uint64_t bdesc,
+                                        uint32_t idesc, uint32_t accumulate) {
     if constexpr (kTF32) {
         asm volatile(
-            "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
-            "tcgen05.mma.cta_group::1.kind::tf32 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
-            "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+            "{\n\t.reg .pred p, e;\n\tsetp.ne.b32 p, %4, 0;\n\tsetp.ne.b32 e, %5, 0;\n\t"
+            "@e tcgen05.mma.cta_group::1.kind::tf32 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+            "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate), "r"(leader)
             : "memory");
     } else {
         asm volatile(
-            "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
-            "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
-            "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+            "{\n\t.reg .pred p, e;\n\tsetp.ne.b32 p, %4, 0;\n\tsetp.ne.b32 e, %5, 0;\n\t"
+            "@e tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+            "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate), "r"(leader)
             : "memory");
     }
 }
 
 // D[tmem] (+)= A[tmem] * B[smem]
 template <bool kTF32>
-__device__ __forceinline__ void umma_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t bdesc, uint32_t idesc,
-                                        uint32_t accumulate) {
+__device__ __forceinline__ void umma_ts(uint32_t leader, uint32_t d_tmem, uint32_t a_tmem, uint64_t bdesc,
+                                        uint32_t idesc, uint32_t accumulate) {
     if constexpr (kTF32) {
         asm volatile(
-            "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
-            "tcgen05.mma.cta_group::1.kind::tf32 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
-            "r"(a_tmem), "l"(bdesc), "r"(idesc), "r"(accumulate)
+            "{\n\t.reg .pred p, e;\n\tsetp.ne.b32 p, %4, 0;\n\tsetp.ne.b32 e, %5, 0;\n\t"
+            "@e tcgen05.mma.cta_group::1.kind::tf32 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
+            "r"(a_tmem), "l"(bdesc), "r"(idesc), "r"(accumulate), "r"(leader)
             : "memory");
     } else {
         asm volatile(
-            "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
-            "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
-            "r"(a_tmem), "l"(bdesc), "r"(idesc), "r"(accumulate)
+            "{\n\t.reg .pred p, e;\n\tsetp.ne.b32 p, %4, 0;\n\tsetp.ne.b32 e, %5, 0;\n\t"
+            "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
+            "r"(a_tmem), "l"(bdesc), "r"(idesc), "r"(accumulate), "r"(leader)
             : "memory");
     }
 }
 
-// Arrive once on `bar` when every tcgen05.mma issued so far by this thread
-// has completed.
-__device__ __forceinline__ void umma_commit(uint64_t* bar) {
-    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
-                     smem_u32(bar))
-                 : "memory");
+// Arrive once on `bar` when every tcgen05.mma issued so far by the leader
+// lane has completed.
+__device__ __forceinline__ void umma_commit(uint32_t leader, uint64_t* bar) {
+    asm volatile(
+        "{\n\t.reg .pred e;\n\tsetp.ne.b32 e, %1, 0;\n\t"
+        "@e tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];\n\t}" ::"r"(smem_u32(bar)),
+        "r"(leader)
+        : "memory");
 }
 
 // TMEM loads/stores, 32 lanes x 32 bits, 32 consecutive columns per thread.
