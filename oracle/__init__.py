@@ -19,3 +19,4 @@ from .attention import (  # noqa: F401
     tiled_forward,
     row_stat_D,
 )
+from .varlen import forward_varlen, backward_varlen  # noqa: F401
