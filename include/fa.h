@@ -102,6 +102,54 @@ fa_status fa_fwd(const void* q, const void* k, const void* v, void* o, float* ls
                  void* workspace, size_t ws_bytes, void* stream);
 
 /*
+ * Packed variable-length batches ("FlashAttention: making attention
+ * IO-aware", section "In practice": a packed kernel takes one flat batch of
+ * concatenated sequences plus their offsets, so padding costs nothing).
+ * Self-attention within each sequence: sequence b is tokens
+ * cu_seqlens[b] .. cu_seqlens[b+1]-1, it attends only to its own tokens, and
+ * the causal mask is aligned at the start of each sequence.
+ *   q, k, v     in,  device, token-major [total, H, d] bf16 (FA_BF16 only)
+ *   o           out, device, [total, H, d] bf16
+ *   lse         out, device, float32 [H, total] (natural log)
+ *   cu_seqlens  in,  device, int32 [B + 1]: 0 = cu_seqlens[0] <= ... <=
+ *               cu_seqlens[B] = total
+ *   max_seqlen  host, the longest cu_seqlens[b+1] - cu_seqlens[b] (sizes the
+ *               grid); 1 <= max_seqlen <= total
+ *   scale, causal, workspace as for fa_fwd (workspace of
+ *               fa_fwd_varlen_workspace_size bytes)
+ * Any sequence lengths are allowed (no multiple of 128 needed; empty
+ * sequences produce nothing). The offsets live in device memory, so they are
+ * checked on the device: values outside [0, total] are clamped, and a
+ * sequence longer than max_seqlen is cut to max_seqlen tokens and reported
+ * as FA_ERR_INVALID_ARG by fa_get_status (rows outside the cut are not
+ * written). Errors otherwise as for fa_fwd.
+ */
+size_t fa_fwd_varlen_workspace_size(int H, int total, int d);
+fa_status fa_fwd_varlen(const void* q, const void* k, const void* v, void* o, float* lse, const int32_t* cu_seqlens,
+                        int B, int H, int total, int max_seqlen, int d, float scale, int causal, fa_dtype dtype,
+                        void* workspace, size_t ws_bytes, void* stream);
+
+/*
+ * Backward pass of a packed variable-length batch: the gradients of
+ * <dO, O> for fa_fwd_varlen.
+ *   q, k, v, o, dout  in,  device, [total, H, d] bf16
+ *   lse               in,  device, float32 [H, total] from fa_fwd_varlen
+ *   dq, dk, dv        out, device, [total, H, d] bf16
+ *   cu_seqlens, B, max_seqlen, scale, causal as for fa_fwd_varlen
+ *   workspace         fa_bwd_varlen_workspace_size(B, H, total, d) bytes:
+ *                     the status word, the running tile counts of the
+ *                     sequences, -L and -D with every sequence starting on a
+ *                     128-row boundary, and the fp32 dQ accumulator
+ * Launches five kernels: the tile counts, D = rowsum(dO * O), the fused
+ * key-block kernel, and the dQ conversion (plus two memsets).
+ */
+size_t fa_bwd_varlen_workspace_size(int B, int H, int total, int d);
+fa_status fa_bwd_varlen(const void* q, const void* k, const void* v, const void* o, const float* lse,
+                        const void* dout, void* dq, void* dk, void* dv, const int32_t* cu_seqlens, int B, int H,
+                        int total, int max_seqlen, int d, float scale, int causal, fa_dtype dtype, void* workspace,
+                        size_t ws_bytes, void* stream);
+
+/*
  * Backward pass ("The backward pass: recompute, don't store"): given the
  * forward inputs, its outputs O and lse, and dO, writes dQ, dK, dV.
  *   q, k, v, o, dout  in,  device, [B,H,N,d] of `dtype` (FA_BF16 only)

@@ -8,6 +8,8 @@ from .binding import (  # noqa: F401
     FAError,
     forward,
     backward,
+    forward_varlen,
+    backward_varlen,
     fwd_workspace_size,
     bwd_workspace_size,
     get_status,

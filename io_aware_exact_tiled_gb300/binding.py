@@ -52,6 +52,14 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.fa_fwd.restype = i
     lib.fa_bwd.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, i, i, i, i, f, i, vp, vp, i, vp, sz, vp]
     lib.fa_bwd.restype = i
+    lib.fa_fwd_varlen_workspace_size.argtypes = [i, i, i]
+    lib.fa_fwd_varlen_workspace_size.restype = sz
+    lib.fa_fwd_varlen.argtypes = [vp, vp, vp, vp, vp, vp, i, i, i, i, i, f, i, i, vp, sz, vp]
+    lib.fa_fwd_varlen.restype = i
+    lib.fa_bwd_varlen_workspace_size.argtypes = [i, i, i, i]
+    lib.fa_bwd_varlen_workspace_size.restype = sz
+    lib.fa_bwd_varlen.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, i, i, i, i, i, f, i, i, vp, sz, vp]
+    lib.fa_bwd_varlen.restype = i
     lib.fa_get_status.argtypes = [vp, vp]
     lib.fa_get_status.restype = i
     lib.fa_status_string.argtypes = [i]
@@ -145,6 +153,69 @@ def forward(q, k, v, scale: Optional[float] = None, causal: bool = False, blockm
     if rc != FA_OK:
         raise FAError(rc, "fa_fwd")
     return o, L
+
+
+def _check_packed(cu_seqlens, *ts: torch.Tensor):
+    q = ts[0]
+    for t in ts:
+        if t.device.type != "cuda":
+            raise ValueError("tensors must be on a CUDA device")
+        if not t.is_contiguous() or t.dim() != 3:
+            raise ValueError("packed tensors must be contiguous [total, H, d]")
+        if t.shape != q.shape or t.dtype != q.dtype:
+            raise ValueError("packed q, k, v (and o, dO) must share shape and dtype")
+    if q.dtype != torch.bfloat16:
+        raise ValueError("packed variable-length batches are bfloat16 only")
+    if (cu_seqlens.dtype != torch.int32 or cu_seqlens.dim() != 1 or cu_seqlens.numel() < 2
+            or cu_seqlens.device != q.device or not cu_seqlens.is_contiguous()):
+        raise ValueError("cu_seqlens must be a contiguous int32 [B + 1] tensor on the same device")
+    return FA_BF16
+
+
+def forward_varlen(q, k, v, cu_seqlens, max_seqlen: int, scale: Optional[float] = None, causal: bool = False,
+                   out=None, lse=None, ws=None, stream=None):
+    """O, L = fa_fwd_varlen(...) on a packed batch. q, k, v: [total, H, d]
+    bf16; cu_seqlens: int32 [B + 1] offsets on the device; max_seqlen: the
+    longest sequence. Returns (o [total, H, d], lse fp32 [H, total])."""
+    lib = load()
+    dtype = _check_packed(cu_seqlens, q, k, v)
+    total, H, d = q.shape
+    B = cu_seqlens.numel() - 1
+    scale = 1.0 / math.sqrt(d) if scale is None else float(scale)
+    o = torch.empty_like(q) if out is None else out
+    L = torch.empty((H, total), dtype=torch.float32, device=q.device) if lse is None else lse
+    if ws is None:
+        ws = workspace(lib.fa_fwd_varlen_workspace_size(H, total, d), q.device)
+    rc = lib.fa_fwd_varlen(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(L), _ptr(cu_seqlens), B, H, total,
+                           int(max_seqlen), d, scale, int(bool(causal)), dtype, _ptr(ws), ws.numel(),
+                           _stream_handle(stream))
+    if rc != FA_OK:
+        raise FAError(rc, "fa_fwd_varlen")
+    return o, L
+
+
+def backward_varlen(q, k, v, o, lse, do, cu_seqlens, max_seqlen: int, scale: Optional[float] = None,
+                    causal: bool = False, dq=None, dk=None, dv=None, ws=None, stream=None):
+    """dQ, dK, dV = fa_bwd_varlen(...) on a packed batch ([total, H, d] bf16;
+    lse fp32 [H, total] from forward_varlen). Returns (dq, dk, dv)."""
+    lib = load()
+    dtype = _check_packed(cu_seqlens, q, k, v, o, do)
+    total, H, d = q.shape
+    B = cu_seqlens.numel() - 1
+    if lse.dtype != torch.float32 or lse.shape != (H, total) or not lse.is_contiguous():
+        raise ValueError("lse must be a contiguous float32 [H, total] tensor")
+    scale = 1.0 / math.sqrt(d) if scale is None else float(scale)
+    dq = torch.empty_like(q) if dq is None else dq
+    dk = torch.empty_like(k) if dk is None else dk
+    dv = torch.empty_like(v) if dv is None else dv
+    if ws is None:
+        ws = workspace(lib.fa_bwd_varlen_workspace_size(B, H, total, d), q.device)
+    rc = lib.fa_bwd_varlen(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), _ptr(do), _ptr(dq), _ptr(dk), _ptr(dv),
+                           _ptr(cu_seqlens), B, H, total, int(max_seqlen), d, scale, int(bool(causal)), dtype,
+                           _ptr(ws), ws.numel(), _stream_handle(stream))
+    if rc != FA_OK:
+        raise FAError(rc, "fa_bwd_varlen")
+    return dq, dk, dv
 
 
 def backward(q, k, v, o, lse, do, scale: Optional[float] = None, causal: bool = False, blockmask=None,

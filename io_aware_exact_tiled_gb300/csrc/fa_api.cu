@@ -30,6 +30,18 @@ fa_status check_shape(int B, int H, int N, int d, float scale) {
     return FA_OK;
 }
 
+// Shape checks of the packed variable-length entry points.
+fa_status check_varlen_shape(int B, int H, int total, int max_seqlen, int d, float scale) {
+    if (B <= 0 || H <= 0 || total <= 0 || max_seqlen <= 0 || d <= 0) return FA_ERR_INVALID_ARG;
+    if (max_seqlen > total) return FA_ERR_INVALID_ARG;
+    if (!(scale > 0.f) || !isfinite(scale)) return FA_ERR_INVALID_ARG;
+    if (d != 64 && d != 128) return FA_ERR_UNSUPPORTED;
+    if (static_cast<long long>(total) * H >= (1LL << 31) - 256) return FA_ERR_UNSUPPORTED;
+    const int tiles = (max_seqlen + 127) / 128;
+    if (B > 65535 || H > 65535 || (tiles + 1) / 2 > 65535) return FA_ERR_UNSUPPORTED;
+    return FA_OK;
+}
+
 fa_status map_cuda(cudaError_t e) { return e == cudaSuccess ? FA_OK : FA_ERR_CUDA; }
 
 }  // namespace
@@ -64,7 +76,7 @@ fa_status fa_fwd(const void* q, const void* k, const void* v, void* o, float* ls
     if (ws_bytes < need) return FA_ERR_INVALID_ARG;
 
     cudaStream_t s = static_cast<cudaStream_t>(stream);
-    fa::FwdArgs a;
+    fa::FwdArgs a{};
     a.q = q;
     a.k = k;
     a.v = v;
@@ -90,6 +102,120 @@ fa_status fa_fwd(const void* q, const void* k, const void* v, void* o, float* ls
     return st;
 }
 
+size_t fa_fwd_varlen_workspace_size(int H, int total, int d) {
+    if (H <= 0 || total <= 0 || d <= 0) return 0;
+    return kStatusBytes;
+}
+
+fa_status fa_fwd_varlen(const void* q, const void* k, const void* v, void* o, float* lse, const int32_t* cu_seqlens,
+                        int B, int H, int total, int max_seqlen, int d, float scale, int causal, fa_dtype dtype,
+                        void* workspace, size_t ws_bytes, void* stream) {
+    if (!q || !k || !v || !o || !lse || !cu_seqlens || !workspace) return FA_ERR_INVALID_ARG;
+    if (dtype != FA_BF16 && dtype != FA_FP32) return FA_ERR_INVALID_ARG;
+    if (causal != 0 && causal != 1) return FA_ERR_INVALID_ARG;
+    fa_status st = check_varlen_shape(B, H, total, max_seqlen, d, scale);
+    if (st != FA_OK) return st;
+    if (dtype != FA_BF16) return FA_ERR_UNSUPPORTED;
+    if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(o, 16) || !aligned(lse, 4) ||
+        !aligned(cu_seqlens, 4) || !aligned(workspace, 256))
+        return FA_ERR_INVALID_ARG;
+    if (ws_bytes < fa_fwd_varlen_workspace_size(H, total, d)) return FA_ERR_INVALID_ARG;
+
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    fa::FwdArgs a{};
+    a.q = q;
+    a.k = k;
+    a.v = v;
+    a.o = o;
+    a.lse = lse;
+    a.B = B;
+    a.H = H;
+    a.N = max_seqlen;
+    a.d = d;
+    a.scale = scale;
+    a.causal = causal;
+    a.cu_seqlens = cu_seqlens;
+    a.total = total;
+    a.status = static_cast<int*>(workspace);
+    a.ev_begin = g_ev_begin;
+    a.ev_end = g_ev_end;
+    if (cudaMemsetAsync(a.status, 0, sizeof(int) * 4, s) != cudaSuccess) return FA_ERR_CUDA;
+    int n = 0;
+    st = map_cuda(fa::launch_fwd(a, s, &n));
+    if (st == FA_OK) g_last_launches = n;
+    return st;
+}
+
+// Rows per head of the -L / -D blocks of a packed backward pass: every
+// sequence starts on a 128-row boundary, which costs at most 128 rows each.
+static long long varlen_lpad(int B, int total) {
+    return (static_cast<long long>(total) + 127) / 128 * 128 + 128LL * B;
+}
+
+size_t fa_bwd_varlen_workspace_size(int B, int H, int total, int d) {
+    if (B <= 0 || H <= 0 || total <= 0 || d <= 0) return 0;
+    const size_t lrows = static_cast<size_t>(H) * varlen_lpad(B, total);
+    return kStatusBytes + align256((static_cast<size_t>(B) + 1) * sizeof(int32_t)) +
+           2 * align256(lrows * sizeof(float)) + align256(static_cast<size_t>(total) * H * d * sizeof(float));
+}
+
+fa_status fa_bwd_varlen(const void* q, const void* k, const void* v, const void* o, const float* lse,
+                        const void* dout, void* dq, void* dk, void* dv, const int32_t* cu_seqlens, int B, int H,
+                        int total, int max_seqlen, int d, float scale, int causal, fa_dtype dtype, void* workspace,
+                        size_t ws_bytes, void* stream) {
+    if (!q || !k || !v || !o || !lse || !dout || !dq || !dk || !dv || !cu_seqlens || !workspace)
+        return FA_ERR_INVALID_ARG;
+    if (dtype != FA_BF16 && dtype != FA_FP32) return FA_ERR_INVALID_ARG;
+    if (causal != 0 && causal != 1) return FA_ERR_INVALID_ARG;
+    fa_status st = check_varlen_shape(B, H, total, max_seqlen, d, scale);
+    if (st != FA_OK) return st;
+    if (dtype != FA_BF16) return FA_ERR_UNSUPPORTED;
+    if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(o, 16) || !aligned(dout, 16) ||
+        !aligned(dq, 16) || !aligned(dk, 16) || !aligned(dv, 16) || !aligned(lse, 4) || !aligned(cu_seqlens, 4) ||
+        !aligned(workspace, 256))
+        return FA_ERR_INVALID_ARG;
+    if (ws_bytes < fa_bwd_varlen_workspace_size(B, H, total, d)) return FA_ERR_INVALID_ARG;
+
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    fa::BwdArgs a{};
+    a.q = q;
+    a.k = k;
+    a.v = v;
+    a.o = o;
+    a.dout = dout;
+    a.lse = lse;
+    a.dq = dq;
+    a.dk = dk;
+    a.dv = dv;
+    a.B = B;
+    a.H = H;
+    a.N = max_seqlen;
+    a.d = d;
+    a.scale = scale;
+    a.causal = causal;
+    a.cu_seqlens = cu_seqlens;
+    a.total = total;
+    a.lpad = varlen_lpad(B, total);
+    const size_t lrows = static_cast<size_t>(H) * a.lpad;
+    char* ws = static_cast<char*>(workspace);
+    size_t off = kStatusBytes;
+    a.status = reinterpret_cast<int*>(ws);
+    a.cu_tiles = reinterpret_cast<int32_t*>(ws + off);
+    off += align256((static_cast<size_t>(B) + 1) * sizeof(int32_t));
+    a.delta = reinterpret_cast<float*>(ws + off);
+    off += align256(lrows * sizeof(float));
+    a.lse2 = reinterpret_cast<float*>(ws + off);
+    off += align256(lrows * sizeof(float));
+    a.dq_accum = reinterpret_cast<float*>(ws + off);
+    a.ev_begin = g_ev_begin;
+    a.ev_end = g_ev_end;
+    if (cudaMemsetAsync(a.status, 0, sizeof(int) * 4, s) != cudaSuccess) return FA_ERR_CUDA;
+    int n = 0;
+    st = map_cuda(fa::launch_bwd(a, s, &n));
+    if (st == FA_OK) g_last_launches = n;
+    return st;
+}
+
 fa_status fa_bwd(const void* q, const void* k, const void* v, const void* o, const float* lse, const void* dout,
                  void* dq, void* dk, void* dv, int B, int H, int N, int d, float scale, int causal,
                  const uint8_t* blockmask, const int32_t* kv_len, fa_dtype dtype, void* workspace, size_t ws_bytes,
@@ -108,7 +234,7 @@ fa_status fa_bwd(const void* q, const void* k, const void* v, const void* o, con
 
     const size_t rows = static_cast<size_t>(B) * H * N;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
-    fa::BwdArgs a;
+    fa::BwdArgs a{};
     a.q = q;
     a.k = k;
     a.v = v;
@@ -148,7 +274,9 @@ fa_status fa_get_status(void* workspace, void* stream) {
     if (cudaMemcpy(&word, workspace, sizeof(int), cudaMemcpyDeviceToHost) != cudaSuccess) return FA_ERR_CUDA;
     if (word == 0) return FA_OK;
     if (cudaMemset(workspace, 0, sizeof(int)) != cudaSuccess) return FA_ERR_CUDA;
-    return (word & 0xFF) == FA_ERR_TIMEOUT ? FA_ERR_TIMEOUT : FA_ERR_CUDA;
+    if ((word & 0xFF) == FA_ERR_TIMEOUT) return FA_ERR_TIMEOUT;
+    if ((word & 0xFF) == FA_ERR_INVALID_ARG) return FA_ERR_INVALID_ARG;
+    return FA_ERR_CUDA;
 }
 
 const char* fa_status_string(fa_status s) {

@@ -68,6 +68,10 @@ struct BwdParams {
     void* dk;
     void* dv;
     int* status;
+    const int32_t* cu_seqlens;  // packed variable-length batch, else null
+    const int32_t* cu_tiles;    // [B + 1] running 128-row tile counts (packed)
+    int total;                  // tokens of the packed batch
+    long long lpad;             // rows per head of nlse2 / ndelta (packed)
 };
 
 constexpr float kLog2e = 1.4426950408889634f;
@@ -83,7 +87,9 @@ constexpr float kLog2e = 1.4426950408889634f;
 //   S^T  = K_j Q_i^T   (after the drain has read dQ_{i-1} out of these columns)
 //   dV  += P^T dO_i    (P^T from TMEM, written by the compute groups)
 //   dK  += dS^T Q_i, dQ_i = dS K_j  (dS^T from shared memory)
-template <int D>
+// VARLEN: packed variable-length batch; a separate instantiation so that the
+// [B, H, N, d] kernel carries none of its branches.
+template <int D, bool VARLEN>
 __global__ void __launch_bounds__(512, 1)
     fa_bwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                   const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmdO,
@@ -122,7 +128,22 @@ __global__ void __launch_bounds__(512, 1)
     // (j = 0, the longest causal column, first), so the CTAs running at any
     // time share the Q, dO and dQ-accumulator rows of a few heads in L2.
     const int j = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
-    const int N = p.N, T = p.mask.T;
+    // A packed variable-length batch puts sequence b at tokens seq0 ..
+    // seq0 + N - 1 of [total, H, d] tensors; its rows of -L and -D start at
+    // lrow0, a multiple of 128 (so that they can be bulk-copied). Key blocks
+    // past the end of a shorter sequence leave at once.
+    constexpr bool varlen = VARLEN;
+    int N = p.N, T = p.mask.T, seq0 = 0;
+    long long lrow0 = static_cast<long long>(b * p.H + h) * p.N;
+    if (varlen) {
+        const int s0 = min(max(p.cu_seqlens[b], 0), p.total);
+        const int s1 = min(max(p.cu_seqlens[b + 1], s0), p.total);
+        seq0 = s0;
+        N = min(s1 - s0, p.N);
+        T = (N + kTile - 1) / kTile;
+        lrow0 = static_cast<long long>(h) * p.lpad + static_cast<long long>(p.cu_tiles[b]) * kTile;
+    }
+    if (j >= T) return;  // uniform over the CTA, before any barrier or TMEM use
     const int bh = b * p.H + h;
     const int kvalid = keys_valid(p.mask, b, N);
     const int lo = p.mask.causal ? j : 0;
@@ -173,8 +194,13 @@ __global__ void __launch_bounds__(512, 1)
                 if (!kv_issued) {
                     mbar_arrive_expect_tx(kv_full, 2 * C::TILE_BYTES);
                     for (int r = 0; r < C::NREG; ++r) {
-                        tma_load_2d(sm + C::K_OFF + r * 16384, &tmK, r * 64, bh * N + j * kTile, kv_full);
-                        tma_load_2d(sm + C::V_OFF + r * 16384, &tmV, r * 64, bh * N + j * kTile, kv_full);
+                        if (varlen) {
+                            tma_load_3d(sm + C::K_OFF + r * 16384, &tmK, r * 64, h, seq0 + j * kTile, kv_full);
+                            tma_load_3d(sm + C::V_OFF + r * 16384, &tmV, r * 64, h, seq0 + j * kTile, kv_full);
+                        } else {
+                            tma_load_2d(sm + C::K_OFF + r * 16384, &tmK, r * 64, bh * N + j * kTile, kv_full);
+                            tma_load_2d(sm + C::V_OFF + r * 16384, &tmV, r * 64, bh * N + j * kTile, kv_full);
+                        }
                     }
                     kv_issued = true;
                 }
@@ -184,11 +210,19 @@ __global__ void __launch_bounds__(512, 1)
                 mbar_arrive_expect_tx(&qd_full[st], 2 * C::TILE_BYTES + 1024);
                 const int row = bh * N + i * kTile;
                 for (int r = 0; r < C::NREG; ++r) {
-                    tma_load_2d(sm + C::Q_OFF + st * C::TILE_BYTES + r * 16384, &tmQ, r * 64, row, &qd_full[st]);
-                    tma_load_2d(sm + C::DO_OFF + st * C::TILE_BYTES + r * 16384, &tmdO, r * 64, row, &qd_full[st]);
+                    uint8_t* dq_s = sm + C::Q_OFF + st * C::TILE_BYTES + r * 16384;
+                    uint8_t* ddo_s = sm + C::DO_OFF + st * C::TILE_BYTES + r * 16384;
+                    if (varlen) {
+                        tma_load_3d(dq_s, &tmQ, r * 64, h, seq0 + i * kTile, &qd_full[st]);
+                        tma_load_3d(ddo_s, &tmdO, r * 64, h, seq0 + i * kTile, &qd_full[st]);
+                    } else {
+                        tma_load_2d(dq_s, &tmQ, r * 64, row, &qd_full[st]);
+                        tma_load_2d(ddo_s, &tmdO, r * 64, row, &qd_full[st]);
+                    }
                 }
-                bulk_load(sm + C::LSE_OFF + st * 512, p.nlse2 + row, 512, &qd_full[st]);
-                bulk_load(sm + C::DEL_OFF + st * 512, p.ndelta + row, 512, &qd_full[st]);
+                const long long lrow = lrow0 + static_cast<long long>(i) * kTile;
+                bulk_load(sm + C::LSE_OFF + st * 512, p.nlse2 + lrow, 512, &qd_full[st]);
+                bulk_load(sm + C::DEL_OFF + st * 512, p.ndelta + lrow, 512, &qd_full[st]);
                 ++u;
             }
             if (kv_issued) mbar_wait_teardown(kv_full, 0, 200000000ull);
@@ -291,10 +325,12 @@ __global__ void __launch_bounds__(512, 1)
             ok = __all_sync(0xffffffffu, ok) && __all_sync(0xffffffffu, mbar_wait(s_full, u & 1, cx, 18));
             if (!ok) break;
             tc_fence_after();
-            // masking is needed only on the diagonal tile (causal) or for
-            // padded keys
+            // masking is needed only on the diagonal tile (causal), for
+            // padded keys, and for the query rows of a packed sequence's last
+            // block that lie past its end (they belong to the next sequence)
             const bool diag = p.mask.causal && i == j;
-            const bool masked = diag || !key_ok;
+            const int qlim = varlen ? N - i * kTile : kTile;
+            const bool masked = diag || !key_ok || qlim < kTile;
 #pragma unroll
             for (int c = 0; c < 2; ++c) {
                 uint32_t pk[16];  // P^T of 32 queries, bf16 pairs
@@ -313,10 +349,10 @@ __global__ void __launch_bounds__(512, 1)
                     float pv0 = ex2_approx(x0), pv1 = ex2_approx(x1), pv2 = ex2_approx(x2), pv3 = ex2_approx(x3);
                     if (masked) {
                         const int q = 64 * g + c * 32 + 4 * e;
-                        if (!key_ok || (diag && q + 0 < r)) pv0 = 0.f;
-                        if (!key_ok || (diag && q + 1 < r)) pv1 = 0.f;
-                        if (!key_ok || (diag && q + 2 < r)) pv2 = 0.f;
-                        if (!key_ok || (diag && q + 3 < r)) pv3 = 0.f;
+                        if (!key_ok || (diag && q + 0 < r) || q + 0 >= qlim) pv0 = 0.f;
+                        if (!key_ok || (diag && q + 1 < r) || q + 1 >= qlim) pv1 = 0.f;
+                        if (!key_ok || (diag && q + 2 < r) || q + 2 >= qlim) pv2 = 0.f;
+                        if (!key_ok || (diag && q + 3 < r) || q + 3 >= qlim) pv3 = 0.f;
                     }
                     pk[2 * e] = pack_bf16x2(pv0, pv1);
                     pk[2 * e + 1] = pack_bf16x2(pv2, pv3);
@@ -373,7 +409,11 @@ __global__ void __launch_bounds__(512, 1)
             if (ok) tc_fence_after();
         }
         if (ok) {
-            const size_t orow = (static_cast<size_t>(bh) * N + key) * D;
+            // packed keys past the end of the sequence: read (the TMEM loads
+            // are warp-wide) but not stored
+            const bool row_ok = !varlen || key < N;
+            const size_t orow = varlen ? (static_cast<size_t>(seq0 + key) * p.H + h) * D
+                                       : (static_cast<size_t>(bh) * N + key) * D;
             uint16_t* out = static_cast<uint16_t*>(g == 0 ? p.dv : p.dk) + orow;
             const uint32_t col = g == 0 ? C::COL_DV : C::COL_DK;
             const float mul = g == 0 ? 1.f : p.scale;
@@ -387,6 +427,7 @@ __global__ void __launch_bounds__(512, 1)
 #pragma unroll
                     for (int e = 0; e < 32; ++e) v[e] = 0u;
                 }
+                if (!row_ok) continue;
                 uint4* dst = reinterpret_cast<uint4*>(out + c * 32);
 #pragma unroll
                 for (int q = 0; q < 4; ++q)
@@ -437,8 +478,14 @@ __global__ void __launch_bounds__(512, 1)
                 fence_proxy_async_smem();
                 __syncwarp();
                 if (lane == 0) {
-                    tma_reduce_add_2d(&tmdQacc, half * 64, grow, stage_buf);
-                    tma_reduce_add_2d(&tmdQacc, half * 64 + 32, grow, stage_buf + 4096);
+                    if (varlen) {
+                        const int tok = seq0 + i * kTile + wq * 32;
+                        tma_reduce_add_3d(&tmdQacc, half * 64, h, tok, stage_buf);
+                        tma_reduce_add_3d(&tmdQacc, half * 64 + 32, h, tok, stage_buf + 4096);
+                    } else {
+                        tma_reduce_add_2d(&tmdQacc, half * 64, grow, stage_buf);
+                        tma_reduce_add_2d(&tmdQacc, half * 64 + 32, grow, stage_buf + 4096);
+                    }
                     bulk_commit_group();
                 }
             }
@@ -496,6 +543,102 @@ __global__ void __launch_bounds__(256) fa_bwd_pre_kernel(const uint16_t* __restr
     }
 }
 
+// Packed batches: cu_tiles[b] = number of 128-row tiles of the sequences
+// before b (each sequence clamped as the attention kernels clamp it), so that
+// sequence b's rows of -L and -D can start at the aligned row cu_tiles[b] *
+// 128 of a per-head block. One block; a scan over chunks of 1024 sequences.
+__global__ void __launch_bounds__(1024) fa_varlen_tiles_kernel(const int32_t* __restrict__ cu, int B, int total,
+                                                               int max_seqlen, int32_t* __restrict__ cu_tiles) {
+    __shared__ int warp_sums[32];
+    __shared__ int carry;
+    if (threadIdx.x == 0) carry = 0;
+    __syncthreads();
+    const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
+    for (int base = 0; base < B; base += 1024) {
+        const int bi = base + threadIdx.x;
+        int tiles = 0;
+        if (bi < B) {
+            const int s0 = min(max(cu[bi], 0), total);
+            const int s1 = min(max(cu[bi + 1], s0), total);
+            tiles = (min(s1 - s0, max_seqlen) + kTile - 1) / kTile;
+        }
+        int x = tiles;  // inclusive scan within the warp
+#pragma unroll
+        for (int off = 1; off < 32; off <<= 1) {
+            const int y = __shfl_up_sync(0xffffffffu, x, off);
+            if (lane >= off) x += y;
+        }
+        if (lane == 31) warp_sums[wid] = x;
+        __syncthreads();
+        if (wid == 0) {
+            int w = warp_sums[lane];
+#pragma unroll
+            for (int off = 1; off < 32; off <<= 1) {
+                const int y = __shfl_up_sync(0xffffffffu, w, off);
+                if (lane >= off) w += y;
+            }
+            warp_sums[lane] = w;  // inclusive over warps
+        }
+        __syncthreads();
+        const int before = carry + (wid > 0 ? warp_sums[wid - 1] : 0) + x - tiles;
+        if (bi < B) cu_tiles[bi] = before;
+        __syncthreads();
+        if (threadIdx.x == 1023) carry = before + tiles;
+        __syncthreads();
+    }
+    if (threadIdx.x == 0) cu_tiles[B] = carry;
+}
+
+// Packed-batch version of fa_bwd_pre_kernel: row = token * H + head of the
+// [total, H, d] tensors; -D and -L * log2 e go to the aligned per-sequence
+// rows of the scratch; tokens not covered by any (clamped) sequence only get
+// their dQ accumulator row zeroed.
+template <int D>
+__global__ void __launch_bounds__(256) fa_bwd_pre_varlen_kernel(
+    const uint16_t* __restrict__ o, const uint16_t* __restrict__ dout, const float* __restrict__ lse,
+    const int32_t* __restrict__ cu, const int32_t* __restrict__ cu_tiles, int B, int H, int total, int max_seqlen,
+    long long lpad, float* __restrict__ ndelta, float* __restrict__ nlse2, float* __restrict__ dq_accum) {
+    constexpr int TPR = D / 8;
+    const long long rows = static_cast<long long>(total) * H;
+    const long long row = (static_cast<long long>(blockIdx.x) * 256 + threadIdx.x) / TPR;
+    const int part = threadIdx.x % TPR;
+    float acc = 0.f;
+    if (row < rows) {
+        const uint4 a = *reinterpret_cast<const uint4*>(o + row * D + part * 8);
+        const uint4 g = *reinterpret_cast<const uint4*>(dout + row * D + part * 8);
+        const uint32_t av[4] = {a.x, a.y, a.z, a.w}, gv[4] = {g.x, g.y, g.z, g.w};
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+            acc = fmaf(__uint_as_float(av[e] << 16), __uint_as_float(gv[e] << 16), acc);
+            acc = fmaf(__uint_as_float(av[e] & 0xFFFF0000u), __uint_as_float(gv[e] & 0xFFFF0000u), acc);
+        }
+        float4* z = reinterpret_cast<float4*>(dq_accum + row * D + part * 8);
+        z[0] = make_float4(0.f, 0.f, 0.f, 0.f);
+        z[1] = make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+#pragma unroll
+    for (int off = TPR / 2; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
+    if (row < rows && part == 0) {
+        const int t = static_cast<int>(row / H), h = static_cast<int>(row % H);
+        // the sequence holding token t: the last b with cu[b] <= t
+        int lo = 0, hi = B - 1;
+        while (lo < hi) {
+            const int mid = (lo + hi + 1) >> 1;
+            if (min(max(cu[mid], 0), total) <= t) lo = mid; else hi = mid - 1;
+        }
+        const int s0 = min(max(cu[lo], 0), total);
+        const int s1 = min(max(cu[lo + 1], s0), total);
+        const int len = min(s1 - s0, max_seqlen);
+        const int local = t - s0;
+        if (local >= 0 && local < len) {
+            const long long dst = static_cast<long long>(h) * lpad + static_cast<long long>(cu_tiles[lo]) * kTile + local;
+            ndelta[dst] = -acc;
+            const float L = lse[static_cast<long long>(h) * total + t];
+            nlse2[dst] = L == -CUDART_INF_F ? -CUDART_INF_F : -L * kLog2e;
+        }
+    }
+}
+
 // dQ (bf16) <- scale * dQ_accum (fp32), 8 elements per thread.
 __global__ void __launch_bounds__(256) fa_bwd_dq_kernel(const float* __restrict__ acc, uint16_t* __restrict__ dq,
                                                         long long n8, float scale) {
@@ -513,24 +656,52 @@ __global__ void __launch_bounds__(256) fa_bwd_dq_kernel(const float* __restrict_
 template <int D>
 static cudaError_t launch_bwd_t(const BwdArgs& a, cudaStream_t stream, int* nlaunch) {
     using C = BwdCfg<D>;
-    const uint64_t rows = static_cast<uint64_t>(a.B) * a.H * a.N;
+    const bool varlen = a.cu_seqlens != nullptr;
+    // rows of the [rows, d] views: B * H * N, or total * H for a packed batch
+    const uint64_t rows = varlen ? static_cast<uint64_t>(a.total) * a.H : static_cast<uint64_t>(a.B) * a.H * a.N;
     CUtensorMap tq, tk, tv, tdo, tdq;
-    if (!make_tmap_2d_sw128(&tq, a.q, rows, D, 2, kTile, 64) || !make_tmap_2d_sw128(&tk, a.k, rows, D, 2, kTile, 64) ||
-        !make_tmap_2d_sw128(&tv, a.v, rows, D, 2, kTile, 64) ||
-        !make_tmap_2d_sw128(&tdo, a.dout, rows, D, 2, kTile, 64) ||
-        !make_tmap_2d_sw128(&tdq, a.dq_accum, rows, D, 4, 32, 32))
+    if (varlen) {
+        const uint64_t tot = static_cast<uint64_t>(a.total);
+        if (!make_tmap_packed_sw128(&tq, a.q, tot, a.H, D, 2, kTile, 64) ||
+            !make_tmap_packed_sw128(&tk, a.k, tot, a.H, D, 2, kTile, 64) ||
+            !make_tmap_packed_sw128(&tv, a.v, tot, a.H, D, 2, kTile, 64) ||
+            !make_tmap_packed_sw128(&tdo, a.dout, tot, a.H, D, 2, kTile, 64) ||
+            !make_tmap_packed_sw128(&tdq, a.dq_accum, tot, a.H, D, 4, 32, 32))
+            return cudaErrorInvalidValue;
+    } else if (!make_tmap_2d_sw128(&tq, a.q, rows, D, 2, kTile, 64) ||
+               !make_tmap_2d_sw128(&tk, a.k, rows, D, 2, kTile, 64) ||
+               !make_tmap_2d_sw128(&tv, a.v, rows, D, 2, kTile, 64) ||
+               !make_tmap_2d_sw128(&tdo, a.dout, rows, D, 2, kTile, 64) ||
+               !make_tmap_2d_sw128(&tdq, a.dq_accum, rows, D, 4, 32, 32))
         return cudaErrorInvalidValue;
     static bool attr_set = false;
     if (!attr_set) {
-        cudaError_t e = cudaFuncSetAttribute(fa_bwd_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
+        cudaError_t e = cudaFuncSetAttribute(fa_bwd_kernel<D, false>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
+        if (e == cudaSuccess)
+            e = cudaFuncSetAttribute(fa_bwd_kernel<D, true>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
         if (e != cudaSuccess) return e;
         attr_set = true;
     }
     const long long nrows = static_cast<long long>(rows);
     const long long pre_threads = nrows * (D / 8);
-    fa_bwd_pre_kernel<D><<<static_cast<unsigned>((pre_threads + 255) / 256), 256, 0, stream>>>(
-        static_cast<const uint16_t*>(a.o), static_cast<const uint16_t*>(a.dout), a.lse, a.delta, a.lse2, a.dq_accum,
-        nrows);
+    int launches = 0;
+    if (varlen) {
+        fa_varlen_tiles_kernel<<<1, 1024, 0, stream>>>(a.cu_seqlens, a.B, a.total, a.N, a.cu_tiles);
+        // rows of the -L / -D blocks that no token fills stay finite (zero)
+        const size_t lbytes = static_cast<size_t>(a.H) * a.lpad * sizeof(float);
+        cudaError_t e = cudaMemsetAsync(a.delta, 0, lbytes, stream);
+        if (e == cudaSuccess) e = cudaMemsetAsync(a.lse2, 0, lbytes, stream);
+        if (e != cudaSuccess) return e;
+        fa_bwd_pre_varlen_kernel<D><<<static_cast<unsigned>((pre_threads + 255) / 256), 256, 0, stream>>>(
+            static_cast<const uint16_t*>(a.o), static_cast<const uint16_t*>(a.dout), a.lse, a.cu_seqlens, a.cu_tiles,
+            a.B, a.H, a.total, a.N, a.lpad, a.delta, a.lse2, a.dq_accum);
+        launches += 2;
+    } else {
+        fa_bwd_pre_kernel<D><<<static_cast<unsigned>((pre_threads + 255) / 256), 256, 0, stream>>>(
+            static_cast<const uint16_t*>(a.o), static_cast<const uint16_t*>(a.dout), a.lse, a.delta, a.lse2,
+            a.dq_accum, nrows);
+        launches += 1;
+    }
     BwdParams p;
     p.B = a.B;
     p.H = a.H;
@@ -540,22 +711,29 @@ static cudaError_t launch_bwd_t(const BwdArgs& a, cudaStream_t stream, int* nlau
     p.mask.blockmask = a.blockmask;
     p.mask.kv_len = a.kv_len;
     p.mask.causal = a.causal;
-    p.mask.T = a.N / kTile;
+    p.mask.T = (a.N + kTile - 1) / kTile;
     p.nlse2 = a.lse2;
     p.ndelta = a.delta;
     p.dk = a.dk;
     p.dv = a.dv;
     p.status = a.status;
-    dim3 grid(a.N / kTile, a.H, a.B);
+    p.cu_seqlens = a.cu_seqlens;
+    p.cu_tiles = a.cu_tiles;
+    p.total = a.total;
+    p.lpad = a.lpad;
+    dim3 grid((a.N + kTile - 1) / kTile, a.H, a.B);
     if (a.ev_begin) cudaEventRecord(a.ev_begin, stream);
-    fa_bwd_kernel<D><<<grid, C::THREADS, C::SMEM, stream>>>(tq, tk, tv, tdo, tdq, p);
+    if (varlen)
+        fa_bwd_kernel<D, true><<<grid, C::THREADS, C::SMEM, stream>>>(tq, tk, tv, tdo, tdq, p);
+    else
+        fa_bwd_kernel<D, false><<<grid, C::THREADS, C::SMEM, stream>>>(tq, tk, tv, tdo, tdq, p);
     if (a.ev_end) cudaEventRecord(a.ev_end, stream);
     const long long n8 = nrows * D / 8;
     long long blocks = (n8 + 255) / 256;
     if (blocks > 152 * 16) blocks = 152 * 16;
     fa_bwd_dq_kernel<<<static_cast<unsigned>(blocks), 256, 0, stream>>>(a.dq_accum, static_cast<uint16_t*>(a.dq), n8,
                                                                         a.scale);
-    *nlaunch = 3;
+    *nlaunch = launches + 2;
     return cudaGetLastError();
 }
 

@@ -45,13 +45,16 @@ struct FwdCfg {
     // fp32 inputs: S is formed from tf32 high and low parts of Q and K
     // (Qh Kh^T + Qh Kl^T + Ql Kh^T), so Q and K tiles come in two copies.
     static constexpr int SPLIT = TF32 ? 2 : 1;
-    static constexpr int STAGES = TF32 ? 1 : (TILE_BYTES <= 16384 ? 4 : 2);
+    // K and V rings: a K stage frees as soon as the S GEMMs reading it
+    // complete, so extra K stages let the next K tiles load further ahead
+    static constexpr int KSTAGES = TF32 ? 1 : (TILE_BYTES <= 16384 ? 6 : 3);
+    static constexpr int VSTAGES = TF32 ? 1 : (TILE_BYTES <= 16384 ? 4 : 2);
     static constexpr int NQ = 2;                       // query tiles per CTA
     static constexpr int Q_OFF = 0;
     static constexpr int K_OFF = Q_OFF + NQ * SPLIT * TILE_BYTES;
-    static constexpr int V_OFF = K_OFF + STAGES * SPLIT * TILE_BYTES;
-    static constexpr int BAR_OFF = V_OFF + STAGES * TILE_BYTES;
-    static constexpr int SMEM = BAR_OFF + 256 + 1024;  // + barriers + alignment slack
+    static constexpr int V_OFF = K_OFF + KSTAGES * SPLIT * TILE_BYTES;
+    static constexpr int BAR_OFF = V_OFF + VSTAGES * TILE_BYTES;
+    static constexpr int SMEM = BAR_OFF + 512 + 1024;  // + barriers + alignment slack
     static constexpr int KSTEP = 32 / ELEM;            // K elements per MMA instruction
     static constexpr int S_KSTEPS = D / KSTEP;
     static constexpr int PV_KSTEPS = kTile / KSTEP;
@@ -62,7 +65,8 @@ struct FwdCfg {
     // tf32 operands must be K-major, so V arrives transposed ([d][keys]).
     static constexpr uint32_t ID_PV = idesc_make(128, D, TF32 ? kFmtTF32 : kFmtBF16, false, !TF32);
     static_assert(SMEM <= 232448, "shared memory budget");
-    static_assert((1 + 4 * STAGES + 7) * 8 + 8 <= 256, "barrier area");
+    static_assert((1 + 2 * KSTAGES + 2 * VSTAGES + 7) * 8 + 8 <= 512, "barrier area");
+    static_assert(VSTAGES <= 16, "two bits of reader count per V stage");
 };
 
 struct FwdParams {
@@ -72,11 +76,13 @@ struct FwdParams {
     void* o;
     float* lse;
     int* status;
+    const int32_t* cu_seqlens;  // packed variable-length batch (bf16), else null
+    int total;                  // tokens of the packed batch
 };
 
 // Issue state of the MMA thread, per Q tile s of the CTA.
 struct MmaState {
-    int pend_stage[2] = {-1, -1};  // K/V stage whose P V GEMM is still to be issued
+    int pend_stage[2] = {-1, -1};  // V stage whose P V GEMM is still to be issued
     uint32_t pend_ph[2] = {0, 0};  // V-full phase parity of that stage
     int pend_u[2] = {0, 0};        // index (among loaded tiles) of that tile
     int nP[2] = {0, 0};            // P-ready phases consumed
@@ -115,7 +121,9 @@ __device__ __forceinline__ bool fwd_issue_pv(uint32_t leader, int s, MmaState& s
 constexpr float kRescaleThreshold = 8.0f;  // log2 units
 constexpr float kLn2 = 0.69314718055994530942f;
 
-template <bool TF32, int D>
+// VARLEN: packed variable-length batch (bf16 only); a separate instantiation
+// so that the [B, H, N, d] kernels carry none of its branches.
+template <bool TF32, int D, bool VARLEN>
 __global__ void __launch_bounds__(384, 1)
     fa_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                   const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmQlo,
@@ -132,11 +140,11 @@ __global__ void __launch_bounds__(384, 1)
     // a K stage is released once the S GEMMs that read it complete, a V stage
     // once its P V GEMMs complete, so the next K tile loads during the
     // current tile's softmax instead of waiting for its P V products.
-    uint64_t* k_full = bars + 1;              // K of a stage landed
-    uint64_t* v_full = k_full + C::STAGES;    // V of a stage landed
-    uint64_t* k_empty = v_full + C::STAGES;   // S GEMMs reading a K stage done
-    uint64_t* kv_empty = k_empty + C::STAGES; // P V GEMMs reading a V stage done
-    uint64_t* s_full = kv_empty + C::STAGES;  // [2]
+    uint64_t* k_full = bars + 1;               // K of a stage landed
+    uint64_t* k_empty = k_full + C::KSTAGES;   // S GEMMs reading a K stage done
+    uint64_t* v_full = k_empty + C::KSTAGES;   // V of a stage landed
+    uint64_t* kv_empty = v_full + C::VSTAGES;  // P V GEMMs reading a V stage done
+    uint64_t* s_full = kv_empty + C::VSTAGES;  // [2]
     uint64_t* p_full = s_full + 2;            // [2]
     uint64_t* o_done = p_full + 2;            // [2]
     uint64_t* drain = o_done + 2;
@@ -149,12 +157,26 @@ __global__ void __launch_bounds__(384, 1)
     // slowest grid dimension): with causal masks the longest CTAs start first
     // and the short ones fill the tail.
     const int h = blockIdx.x, b = blockIdx.y;
-    const int T = p.mask.T;
+    // A packed variable-length batch puts sequence b at tokens seq0 ..
+    // seq0 + N - 1 of [total, H, d] tensors (the grid covers the longest
+    // sequence; CTAs past the end of a shorter one leave at once). Otherwise
+    // head (b, h) is rows bh * N .. of the [B * H * N, d] view.
+    constexpr bool varlen = VARLEN && !TF32;
+    int N = p.N, T = p.mask.T, seq0 = 0;
+    if (varlen) {
+        const int s0 = min(max(p.cu_seqlens[b], 0), p.total);
+        const int s1 = min(max(p.cu_seqlens[b + 1], s0), p.total);
+        if (s1 - s0 > p.N && tid == 0 && blockIdx.x == 0 && blockIdx.z == 0 && p.status)
+            atomicCAS(p.status, 0, FA_DEV_INVALID | (97 << 8));
+        seq0 = s0;
+        N = min(s1 - s0, p.N);
+        T = (N + kTile - 1) / kTile;
+    }
     const int npairs = (T + 1) >> 1;
     const int qp = npairs - 1 - static_cast<int>(blockIdx.z);
+    if (qp < 0) return;  // uniform over the CTA, before any barrier or TMEM use
     const int qb0 = 2 * qp, qb1 = 2 * qp + 1;
     const bool act1 = qb1 < T;
-    const int N = p.N;
     const int bh = b * p.H + h;
     const int kvalid = keys_valid(p.mask, b, N);
     int hi = T;
@@ -164,10 +186,12 @@ __global__ void __launch_bounds__(384, 1)
     if (tid == 0) {
         *abort_flag = 0;
         mbar_init(bar_q, 1);
-        for (int i = 0; i < C::STAGES; ++i) {
+        for (int i = 0; i < C::KSTAGES; ++i) {
             mbar_init(&k_full[i], 1);
-            mbar_init(&v_full[i], 1);
             mbar_init(&k_empty[i], 1);
+        }
+        for (int i = 0; i < C::VSTAGES; ++i) {
+            mbar_init(&v_full[i], 1);
             mbar_init(&kv_empty[i], 1);
         }
         for (int i = 0; i < 2; ++i) {
@@ -210,50 +234,57 @@ __global__ void __launch_bounds__(384, 1)
         // ------------------------------------------------------------ producer
         if (lane == 0) {
             const int qrow0 = bh * N + qb0 * kTile;
+            // rows row .. row + 127 of this head (packed: of this sequence)
+            auto load_rows = [&](void* dst, const CUtensorMap* m, int x, int row, uint64_t* bar) {
+                if (varlen)
+                    tma_load_3d(dst, m, x, h, seq0 + row, bar);
+                else
+                    tma_load_2d(dst, m, x, bh * N + row, bar);
+            };
             mbar_arrive_expect_tx(bar_q, (act1 ? 2 : 1) * C::SPLIT * C::TILE_BYTES);
             for (int s = 0; s < (act1 ? 2 : 1); ++s)
                 for (int r = 0; r < C::NREG; ++r) {
                     uint8_t* dq = sm + C::Q_OFF + s * C::SPLIT * C::TILE_BYTES + r * 16384;
-                    tma_load_2d(dq, &tmQ, r * C::BOXC, qrow0 + s * kTile, bar_q);
+                    load_rows(dq, &tmQ, r * C::BOXC, (qb0 + s) * kTile, bar_q);
                     if constexpr (TF32) tma_load_2d(dq + C::TILE_BYTES, &tmQlo, r * C::BOXC, qrow0 + s * kTile, bar_q);
                 }
             int nk = 0, nv = 0;  // K and V tiles whose loads were issued
             for (int t = 0; t < hi; ++t) {
                 if (!need_of(t)) continue;
-                const int stage = nk % C::STAGES;
-                const uint32_t ph = (nk / C::STAGES) & 1;
-                if (!mbar_wait(&k_empty[stage], ph ^ 1, cx, 1)) break;
-                uint8_t* sk = sm + C::K_OFF + stage * C::SPLIT * C::TILE_BYTES;
-                uint8_t* sv = sm + C::V_OFF + stage * C::TILE_BYTES;
-                mbar_arrive_expect_tx(&k_full[stage], C::SPLIT * C::TILE_BYTES);
+                const int kst = nk % C::KSTAGES;
+                if (!mbar_wait(&k_empty[kst], ((nk / C::KSTAGES) & 1) ^ 1, cx, 1)) break;
+                uint8_t* sk = sm + C::K_OFF + kst * C::SPLIT * C::TILE_BYTES;
+                mbar_arrive_expect_tx(&k_full[kst], C::SPLIT * C::TILE_BYTES);
                 for (int r = 0; r < C::NREG; ++r) {
-                    tma_load_2d(sk + r * 16384, &tmK, r * C::BOXC, bh * N + t * kTile, &k_full[stage]);
+                    load_rows(sk + r * 16384, &tmK, r * C::BOXC, t * kTile, &k_full[kst]);
                     if constexpr (TF32)
                         tma_load_2d(sk + C::TILE_BYTES + r * 16384, &tmKlo, r * C::BOXC, bh * N + t * kTile,
-                                    &k_full[stage]);
+                                    &k_full[kst]);
                 }
                 ++nk;
-                if (!mbar_wait(&kv_empty[stage], ph ^ 1, cx, 9)) break;
-                mbar_arrive_expect_tx(&v_full[stage], C::TILE_BYTES);
+                const int vst = nv % C::VSTAGES;
+                if (!mbar_wait(&kv_empty[vst], ((nv / C::VSTAGES) & 1) ^ 1, cx, 9)) break;
+                uint8_t* sv = sm + C::V_OFF + vst * C::TILE_BYTES;
+                mbar_arrive_expect_tx(&v_full[vst], C::TILE_BYTES);
                 if constexpr (!TF32) {
                     for (int r = 0; r < C::NREG; ++r)
-                        tma_load_2d(sv + r * 16384, &tmV, r * C::BOXC, bh * N + t * kTile, &v_full[stage]);
+                        load_rows(sv + r * 16384, &tmV, r * C::BOXC, t * kTile, &v_full[vst]);
                 } else {
                     // V^T [d][keys]: four 32-key swizzle regions of [d][32]
                     for (int r = 0; r < 4; ++r)
-                        tma_load_2d(sv + r * D * 128, &tmV, t * kTile + r * 32, bh * D, &v_full[stage]);
+                        tma_load_2d(sv + r * D * 128, &tmV, t * kTile + r * 32, bh * D, &v_full[vst]);
                 }
                 ++nv;
             }
             // let every copy in flight land before the CTA can exit
             mbar_wait_teardown(bar_q, 0, 200000000ull);
-            for (int i = 0; i < C::STAGES && i < nk; ++i) {
-                const int last = i + ((nk - 1 - i) / C::STAGES) * C::STAGES;
-                mbar_wait_teardown(&k_full[i], (last / C::STAGES) & 1, 200000000ull);
+            for (int i = 0; i < C::KSTAGES && i < nk; ++i) {
+                const int last = i + ((nk - 1 - i) / C::KSTAGES) * C::KSTAGES;
+                mbar_wait_teardown(&k_full[i], (last / C::KSTAGES) & 1, 200000000ull);
             }
-            for (int i = 0; i < C::STAGES && i < nv; ++i) {
-                const int last = i + ((nv - 1 - i) / C::STAGES) * C::STAGES;
-                mbar_wait_teardown(&v_full[i], (last / C::STAGES) & 1, 200000000ull);
+            for (int i = 0; i < C::VSTAGES && i < nv; ++i) {
+                const int last = i + ((nv - 1 - i) / C::VSTAGES) * C::VSTAGES;
+                mbar_wait_teardown(&v_full[i], (last / C::VSTAGES) & 1, 200000000ull);
             }
         }
     } else if (warp == 1) {
@@ -279,26 +310,27 @@ __global__ void __launch_bounds__(384, 1)
             for (int t = 0; ok && t < hi; ++t) {
                 const uint32_t nd = need_of(t);
                 if (!nd) continue;
-                const int stage = u % C::STAGES;
-                const uint32_t ph = (u / C::STAGES) & 1;
+                const int kst = u % C::KSTAGES;
+                const int vst = u % C::VSTAGES;
+                const uint32_t vph = (u / C::VSTAGES) & 1;
                 // The producer issues K of tile u only after V of tile u - 1,
-                // which waits for every P V reading tile u - 1 - STAGES, and
+                // which waits for every P V reading tile u - 1 - VSTAGES, and
                 // tile u reuses the V stage (and its reader count) of tile
-                // u - STAGES: a P V still pending for a tile that old (its Q
+                // u - VSTAGES: a P V still pending for a tile that old (its Q
                 // tile skipped the tiles since) is issued first.
 #pragma unroll
                 for (int s = 0; s < 2; ++s)
-                    if (ok && pend_stage[s] >= 0 && st.pend_u[s] <= u - C::STAGES && !issue_pv(s)) ok = false;
+                    if (ok && pend_stage[s] >= 0 && st.pend_u[s] <= u - C::VSTAGES && !issue_pv(s)) ok = false;
                 if (!ok) break;
-                if (!mbar_wait_warp(&k_full[stage], ph, cx, 5)) { ok = false; break; }
+                if (!mbar_wait_warp(&k_full[kst], (u / C::KSTAGES) & 1, cx, 5)) { ok = false; break; }
                 tc_fence_after();
-                rem = (rem & ~(3u << (2 * stage))) | ((uint32_t)__popc(nd) << (2 * stage));
+                rem = (rem & ~(3u << (2 * vst))) | ((uint32_t)__popc(nd) << (2 * vst));
 #pragma unroll
                 for (int s = 0; s < 2; ++s) {
                     if (!(nd & (1u << s))) continue;
                     if (pend_stage[s] >= 0 && !issue_pv(s)) { ok = false; break; }
                     const uint64_t qs = sdesc_advance(dQ0, s * C::SPLIT * C::TILE_BYTES);
-                    const uint64_t ks = sdesc_advance(dK0, stage * C::SPLIT * C::TILE_BYTES);
+                    const uint64_t ks = sdesc_advance(dK0, kst * C::SPLIT * C::TILE_BYTES);
                     // bf16: one product; fp32: (Qh, Kh), (Qh, Kl), (Ql, Kh)
 #pragma unroll
                     for (int part = 0; part < (TF32 ? 3 : 1); ++part) {
@@ -312,12 +344,12 @@ __global__ void __launch_bounds__(384, 1)
                         }
                     }
                     umma_commit(leader, &s_full[s]);
-                    pend_stage[s] = stage;
-                    pend_ph[s] = ph;
+                    pend_stage[s] = vst;
+                    pend_ph[s] = vph;
                     st.pend_u[s] = u;
                 }
                 if (!ok) break;
-                umma_commit(leader, &k_empty[stage]);  // S GEMMs reading this K stage are all issued
+                umma_commit(leader, &k_empty[kst]);  // S GEMMs reading this K stage are all issued
                 ++u;
             }
             for (int s = 0; ok && s < 2; ++s)
@@ -479,7 +511,13 @@ __global__ void __launch_bounds__(384, 1)
             }
             if (ok) {
                 const float inv = lw > 0.f ? 1.f / lw : 0.f;
-                const size_t orow = (static_cast<size_t>(bh) * N + grow) * D;
+                // packed rows past the end of the sequence belong to the next
+                // one: computed (the TMEM loads are warp-wide) but not stored
+                const bool row_ok = !varlen || grow < N;
+                const size_t orow = varlen ? (static_cast<size_t>(seq0 + grow) * p.H + h) * D
+                                           : (static_cast<size_t>(bh) * N + grow) * D;
+                const size_t lrow = varlen ? static_cast<size_t>(h) * p.total + seq0 + grow
+                                           : static_cast<size_t>(bh) * N + grow;
 #pragma unroll
                 for (int c = 0; c < D / 32; ++c) {
                     uint32_t ov[32];
@@ -490,6 +528,7 @@ __global__ void __launch_bounds__(384, 1)
 #pragma unroll
                         for (int i = 0; i < 32; ++i) ov[i] = 0u;
                     }
+                    if (!row_ok) continue;
                     if constexpr (!TF32) {
                         uint4* dst = reinterpret_cast<uint4*>(static_cast<uint16_t*>(p.o) + orow + c * 32);
 #pragma unroll
@@ -510,7 +549,7 @@ __global__ void __launch_bounds__(384, 1)
                                                  __uint_as_float(ov[4 * j + 3]) * inv);
                     }
                 }
-                p.lse[static_cast<size_t>(bh) * N + grow] = l > 0.f ? (m_hat + log2f(l)) * kLn2 : -CUDART_INF_F;
+                if (row_ok) p.lse[lrow] = l > 0.f ? (m_hat + log2f(l)) * kLn2 : -CUDART_INF_F;
             }
         }
     }
@@ -580,16 +619,26 @@ static cudaError_t launch_fwd_t(const FwdArgs& a, cudaStream_t stream, int* nlau
             !make_tmap_2d_sw128(&tkl, kl, rows, D, elem, kTile, C::BOXC))
             return cudaErrorInvalidValue;
     } else {
-        if (!make_tmap_2d_sw128(&tq, a.q, rows, D, elem, kTile, C::BOXC) ||
-            !make_tmap_2d_sw128(&tk, a.k, rows, D, elem, kTile, C::BOXC) ||
-            !make_tmap_2d_sw128(&tv, a.v, rows, D, elem, kTile, C::BOXC))
+        if (a.cu_seqlens) {
+            const uint64_t tot = static_cast<uint64_t>(a.total);
+            if (!make_tmap_packed_sw128(&tq, a.q, tot, a.H, D, elem, kTile, C::BOXC) ||
+                !make_tmap_packed_sw128(&tk, a.k, tot, a.H, D, elem, kTile, C::BOXC) ||
+                !make_tmap_packed_sw128(&tv, a.v, tot, a.H, D, elem, kTile, C::BOXC))
+                return cudaErrorInvalidValue;
+        } else if (!make_tmap_2d_sw128(&tq, a.q, rows, D, elem, kTile, C::BOXC) ||
+                   !make_tmap_2d_sw128(&tk, a.k, rows, D, elem, kTile, C::BOXC) ||
+                   !make_tmap_2d_sw128(&tv, a.v, rows, D, elem, kTile, C::BOXC))
             return cudaErrorInvalidValue;
         tql = tq;
         tkl = tk;
     }
     static bool attr_set = false;
     if (!attr_set) {
-        cudaError_t e = cudaFuncSetAttribute(fa_fwd_kernel<TF32, D>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
+        cudaError_t e = cudaFuncSetAttribute(fa_fwd_kernel<TF32, D, false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             C::SMEM);
+        if (e == cudaSuccess && !TF32)
+            e = cudaFuncSetAttribute(fa_fwd_kernel<TF32, D, !TF32>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                     C::SMEM);
         if (e != cudaSuccess) return e;
         attr_set = true;
     }
@@ -601,14 +650,19 @@ static cudaError_t launch_fwd_t(const FwdArgs& a, cudaStream_t stream, int* nlau
     p.mask.blockmask = a.blockmask;
     p.mask.kv_len = a.kv_len;
     p.mask.causal = a.causal;
-    p.mask.T = a.N / kTile;
+    p.mask.T = (a.N + kTile - 1) / kTile;
     p.o = a.o;
     p.lse = a.lse;
     p.status = a.status;
-    const int T = a.N / kTile;
+    p.cu_seqlens = TF32 ? nullptr : a.cu_seqlens;
+    p.total = a.total;
+    const int T = (a.N + kTile - 1) / kTile;
     dim3 grid(a.H, a.B, (T + 1) / 2);
     if (a.ev_begin) cudaEventRecord(a.ev_begin, stream);
-    fa_fwd_kernel<TF32, D><<<grid, C::THREADS, C::SMEM, stream>>>(tq, tk, tv, tql, tkl, p);
+    if (p.cu_seqlens)
+        fa_fwd_kernel<TF32, D, !TF32><<<grid, C::THREADS, C::SMEM, stream>>>(tq, tk, tv, tql, tkl, p);
+    else
+        fa_fwd_kernel<TF32, D, false><<<grid, C::THREADS, C::SMEM, stream>>>(tq, tk, tv, tql, tkl, p);
     if (a.ev_end) cudaEventRecord(a.ev_end, stream);
     ++launches;
     *nlaunch = launches;

@@ -20,6 +20,11 @@ struct FwdArgs {
     void* fp32_scratch;  // fp32 only: V^T [B,H,d,N], then Qh, Ql, Kh, Kl [B,H,N,d]
     int* status;
     cudaEvent_t ev_begin, ev_end;  // optional, recorded around the main kernel
+    // Packed variable-length batch (bf16 only): q, k, v, o are [total, H, d],
+    // lse is [H, total], sequence b is tokens cu_seqlens[b] .. cu_seqlens[b+1]-1
+    // and N is the longest sequence. Null for the [B, H, N, d] layout.
+    const int32_t* cu_seqlens;
+    int total;
 };
 
 struct BwdArgs {
@@ -36,6 +41,15 @@ struct BwdArgs {
     float* dq_accum;  // [B,H,N,d] fp32 scratch
     int* status;
     cudaEvent_t ev_begin, ev_end;  // optional, recorded around the main kernel
+    // Packed variable-length batch (see FwdArgs): q, k, v, o, dout, dq, dk,
+    // dv and dq_accum are [total, H, d], lse is [H, total]; delta and lse2
+    // are [H][lpad] with each sequence starting at a multiple of 128 rows
+    // (cu_tiles[b] * 128, cu_tiles being the running count of 128-row tiles,
+    // computed on the device into the workspace). Null for [B, H, N, d].
+    const int32_t* cu_seqlens;
+    int32_t* cu_tiles;  // [B + 1] scratch
+    int total;
+    long long lpad;     // rows per head of delta / lse2: align128(total) + 128 * B
 };
 
 cudaError_t launch_fwd(const FwdArgs& a, cudaStream_t stream, int* nlaunch);

@@ -144,7 +144,7 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
 #endif
 
 // Status codes written by the kernels into the status word.
-enum : int { FA_DEV_OK = 0, FA_DEV_TIMEOUT = 4 };
+enum : int { FA_DEV_OK = 0, FA_DEV_INVALID = 1, FA_DEV_TIMEOUT = 4 };
 
 struct WaitCtx {
     volatile int* abort_flag;  // shared memory, one per CTA
@@ -202,6 +202,15 @@ __device__ __forceinline__ void tma_load_2d(void* smem_dst, const CUtensorMap* m
         : "memory");
 }
 
+// 3D tiled load (x = column, y = head, z = token) of a packed tensor map.
+__device__ __forceinline__ void tma_load_3d(void* smem_dst, const CUtensorMap* map, int x, int y, int z,
+                                            uint64_t* bar) {
+    asm volatile(
+        "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3, %4}], [%5];"
+        ::"r"(smem_u32(smem_dst)), "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(z), "r"(smem_u32(bar))
+        : "memory");
+}
+
 // Same with an L2 eviction-priority hint (a createpolicy value).
 __device__ __forceinline__ void tma_load_2d_hint(void* smem_dst, const CUtensorMap* map, int x, int y, uint64_t* bar,
                                                  uint64_t policy) {
@@ -227,6 +236,13 @@ __device__ __forceinline__ void tma_reduce_add_2d(const CUtensorMap* map, int x,
     asm volatile(
         "cp.reduce.async.bulk.tensor.2d.global.shared::cta.add.tile.bulk_group [%0, {%1, %2}], [%3];"
         ::"l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(smem_u32(smem_src))
+        : "memory");
+}
+// Same for a packed 3D tensor map (x = column, y = head, z = token).
+__device__ __forceinline__ void tma_reduce_add_3d(const CUtensorMap* map, int x, int y, int z, const void* smem_src) {
+    asm volatile(
+        "cp.reduce.async.bulk.tensor.3d.global.shared::cta.add.tile.bulk_group [%0, {%1, %2, %3}], [%4];"
+        ::"l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(z), "r"(smem_u32(smem_src))
         : "memory");
 }
 __device__ __forceinline__ void bulk_commit_group() {

@@ -45,4 +45,25 @@ inline bool make_tmap_2d_sw128(CUtensorMap* map, const void* base, uint64_t rows
     return r == CUDA_SUCCESS;
 }
 
+// Packed token-major tensor [tokens][heads][cols] (variable-length batches),
+// read in boxes of box_rows consecutive tokens of one head and box_cols
+// columns, with the 128-byte swizzle. A box of one head is laid out in shared
+// memory exactly like the [box_rows, box_cols] box of make_tmap_2d_sw128.
+// Rows past `tokens` read as zero.
+inline bool make_tmap_packed_sw128(CUtensorMap* map, const void* base, uint64_t tokens, uint64_t heads,
+                                   uint64_t cols, int elem_bytes, uint32_t box_rows, uint32_t box_cols) {
+    EncodeTiledFn fn = encode_tiled_fn();
+    if (!fn) return false;
+    CUtensorMapDataType dt =
+        elem_bytes == 2 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT32;
+    cuuint64_t gdim[3] = {cols, heads, tokens};
+    cuuint64_t gstride[2] = {cols * static_cast<uint64_t>(elem_bytes), heads * cols * static_cast<uint64_t>(elem_bytes)};
+    cuuint32_t box[3] = {box_cols, 1, box_rows};
+    cuuint32_t estride[3] = {1, 1, 1};
+    CUresult r = fn(map, dt, 3, const_cast<void*>(base), gdim, gstride, box, estride, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                    CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
 }  // namespace fa

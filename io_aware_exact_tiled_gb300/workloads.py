@@ -122,3 +122,77 @@ def make_inputs(w: Workload, seed: int = 0, device: str = "cpu") -> Inputs:
         blockmask = make_blockmask(w.N // TILE, w.block_density, cpu_gen)
     dt = w.torch_dtype
     return Inputs(q.to(dt), k.to(dt), v.to(dt), do.to(dt), kv_len, blockmask, w.scale, w.causal)
+
+
+# --------------------------------------------------------------------------
+# Packed variable-length batches (sequences concatenated along one token axis)
+# --------------------------------------------------------------------------
+
+@dataclasses.dataclass(frozen=True)
+class PackedWorkload:
+    """A packed batch: B sequences with lengths drawn uniformly from the
+    inclusive range ``len_range``, H heads of size d, bf16."""
+    name: str
+    B: int
+    H: int
+    d: int
+    len_range: tuple
+    causal: bool = False
+
+    @property
+    def scale(self) -> float:
+        return 1.0 / math.sqrt(self.d)
+
+
+# bert_packed: the key-padding batch of the "bert" workload without its
+#   padding: 8 sequences, lengths ~ U{256..512}, 16 heads, d = 64.
+# mix8k_packed: a long-context mix, 16 sequences, lengths ~ U{512..8192},
+#   32 heads, d = 128, causal.
+PACKED_WORKLOADS = {
+    "bert_packed": PackedWorkload("bert_packed", 8, 16, 64, (256, 512)),
+    "mix8k_packed": PackedWorkload("mix8k_packed", 16, 32, 128, (512, 8192), causal=True),
+}
+
+
+@dataclasses.dataclass
+class PackedInputs:
+    q: torch.Tensor           # [total, H, d]
+    k: torch.Tensor
+    v: torch.Tensor
+    do: torch.Tensor
+    cu_seqlens: torch.Tensor  # int32 [B + 1], on the CPU
+    lens: list
+    scale: float
+    causal: bool
+
+    @property
+    def max_seqlen(self) -> int:
+        return max(self.lens) if self.lens else 0
+
+
+def make_packed(lens, H: int, d: int, causal: bool = False, seed: int = 0, device: str = "cpu",
+                k_scale: float = 1.0) -> PackedInputs:
+    """Seeded packed inputs for the given sequence lengths: standard normal
+    fp32 Q, K, V, dO of shape [sum(lens), H, d] drawn in that order, K times
+    ``k_scale``, rounded to bf16."""
+    lens = [int(x) for x in lens]
+    total = sum(lens)
+    gen = torch.Generator(device=device)
+    gen.manual_seed(seed)
+    shape = (total, H, d)
+    q, k, v, do = (torch.randn(shape, generator=gen, device=device, dtype=torch.float32) for _ in range(4))
+    if k_scale != 1.0:
+        k.mul_(k_scale)
+    cu = torch.zeros(len(lens) + 1, dtype=torch.int32)
+    cu[1:] = torch.cumsum(torch.tensor(lens, dtype=torch.int64), 0).to(torch.int32)
+    bf = torch.bfloat16
+    return PackedInputs(q.to(bf), k.to(bf), v.to(bf), do.to(bf), cu, lens, 1.0 / math.sqrt(d), causal)
+
+
+def make_packed_workload(w: PackedWorkload, seed: int = 0, device: str = "cpu") -> PackedInputs:
+    """Lengths ~ U{len_range} from a CPU generator seeded with ``seed``, then
+    the tensors as in make_packed."""
+    g = torch.Generator().manual_seed(seed)
+    lo, hi = w.len_range
+    lens = torch.randint(lo, hi + 1, (w.B,), generator=g).tolist()
+    return make_packed(lens, w.H, w.d, w.causal, seed, device)
