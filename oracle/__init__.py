@@ -20,3 +20,4 @@ from .attention import (  # noqa: F401
     row_stat_D,
 )
 from .varlen import forward_varlen, backward_varlen  # noqa: F401
+from .decode import decode_forward, split_decode  # noqa: F401
