@@ -317,6 +317,193 @@ def run_table(args):
         print(json.dumps(row), flush=True)
 
 
+# ------------------------------------------------------------------ decoding and packed batches
+def _timed_loop(fn, K, ev, fa):
+    """Run fn K times with the library's main-kernel events; returns
+    (total ms, mean main-kernel ms, launches)."""
+    import torch
+    pairs = [(ev(), ev()) for _ in range(K)]
+    for a, b in pairs:
+        a.record()
+        b.record()
+    t0, t1 = ev(), ev()
+    torch.cuda.synchronize()
+    n = 0
+    t0.record()
+    for i in range(K):
+        fa.set_timing_events(*pairs[i])
+        n += fn()
+    t1.record()
+    fa.set_timing_events(None, None)
+    torch.cuda.synchronize()
+    return t0.elapsed_time(t1), sum(a.elapsed_time(b) for a, b in pairs) / K, n
+
+
+def run_decode(args, rank, world):
+    """Split-key decoding: one step = fa_decode (split kernel + merge) for
+    every (request, head) of the workload; value = cache bytes read per
+    second (K and V of the valid entries; q, o and lse are added to the
+    algorithmic bytes of the roofline)."""
+    import torch
+
+    import io_aware_exact_tiled_gb300 as fa
+    from io_aware_exact_tiled_gb300 import workloads as W
+    w = W.DECODE_WORKLOADS[args.workload]
+    dev = torch.device("cuda", int(os.environ.get("LOCAL_RANK", "0")))
+    torch.cuda.set_device(dev)
+    fa.load()
+    x = W.make_decode_workload(w, seed=rank, device="cuda")
+    q, k, v = (t.to(dev) for t in (x.q, x.k, x.v))
+    cl = x.cache_len.to(dev)
+    B, H, Nq, d = q.shape
+    o = torch.empty_like(q)
+    lse = torch.empty((B, H, Nq), dtype=torch.float32, device=dev)
+    ws = fa.workspace(fa.load().fa_decode_workspace_size(B, H, Nq, w.Nk, d, 0), dev)
+    valid = int(x.cache_len.sum())
+    cache_bytes = 2 * valid * H * d * 2
+    io_bytes = 2 * q.numel() * q.element_size() + lse.numel() * 4
+    ev = lambda: torch.cuda.Event(enable_timing=True)
+
+    def step():
+        fa.decode(q, k, v, cache_len=cl, scale=x.scale, out=o, lse=lse, ws=ws)
+        return fa.last_launch_count()
+
+    for _ in range(max(3, args.warmup)):
+        step()
+    torch.cuda.synchronize()
+    sampler = ClockSampler()
+    sampler.start()
+    wall0 = time.time()
+    ms, ker_ms, launches = _timed_loop(step, args.steps, ev, fa)
+    wall1 = time.time()
+    sampler.stop()
+    if fa.get_status(ws) != 0:
+        raise RuntimeError("device status word reports a timed-out wait")
+    ms_step = ms / args.steps
+    value = cache_bytes / (ms_step * 1e-3) / 1e9
+    peaks, src = load_peaks()
+    hbm = float(peaks["hbm_gbs"])
+    achieved = (cache_bytes + io_bytes) / (ker_ms * 1e-3) / 1e9
+    e2e = None
+    if not args.no_e2e:
+        hq = x.q.pin_memory()
+        ho = torch.empty_like(hq).pin_memory()
+        hl = torch.empty((B, H, Nq), dtype=torch.float32).pin_memory()
+        qd = torch.empty_like(q)
+
+        def e2e_step():
+            qd.copy_(hq, non_blocking=True)
+            fa.decode(qd, k, v, cache_len=cl, scale=x.scale, out=o, lse=lse, ws=ws)
+            ho.copy_(o, non_blocking=True)
+            hl.copy_(lse, non_blocking=True)
+            return 0
+
+        for _ in range(3):
+            e2e_step()
+        e_ms, _, _ = _timed_loop(e2e_step, max(3, min(args.steps, 50)), ev, fa)
+        e_step = e_ms / max(3, min(args.steps, 50))
+        e2e = {"value": cache_bytes / (e_step * 1e-3) / 1e9, "unit": "GB/s",
+               "h2d_bytes_per_step": hq.numel() * 2, "d2h_bytes_per_step": ho.numel() * 2 + hl.numel() * 4,
+               "ms_per_step": e_step, "note": "the cache stays resident in HBM; q in, o and lse out per step"}
+    cpu = None
+    if not args.no_cpu_baseline:
+        from oracle import decode as DEC
+        xs = W.make_decode_workload(w, seed=0)
+        t_used, nb, byt = 0.0, 0, 0
+        for b in range(B):
+            t0 = time.perf_counter()
+            DEC.decode_forward(xs.q[b:b + 1], xs.k[b:b + 1], xs.v[b:b + 1], xs.scale, xs.cache_len[b:b + 1])
+            t_used += time.perf_counter() - t0
+            nb += 1
+            byt += 2 * int(xs.cache_len[b]) * H * d * 2
+            if t_used > 10.0:
+                break
+        cpu = {"value": byt / t_used / 1e9, "unit": "GB/s", "cores": os.cpu_count(), "kind": "oracle",
+               "sample": f"fp64 NumPy decode of {nb} request(s) (all {H} heads) of the workload ({t_used:.1f} s)"}
+    line = {
+        "metric": "decode: KV-cache bytes read per second (split-key decoding)", "value": value, "unit": "GB/s",
+        "n_gpus": 1, "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic (seeded N(0,1) q and cache)",
+        "config": {"workload": f"{w.name}: decode, B={B} H={H} Nq={Nq} Nk={w.Nk} d={d}, cache_len "
+                               f"U{{{w.len_range[0]}..{w.len_range[1]}}}",
+                   "l2": "cache larger than L2 (%d MiB of K+V allocated)" % (2 * k.numel() * 2 >> 20)},
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": hbm, "unit": "GB/s", "frac": achieved / hbm,
+                     "traffic": None, "kernel": "fa_decode_split_kernel",
+                     "peak_source": f"{src} HBM copy bandwidth (MEASURED_PEAKS.json hbm_gbs)"},
+        "split_kernel_ms": ker_ms, "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": launches,
+        "clocks": sampler.summary(wall0, wall1),
+    }
+    print(json.dumps(line), flush=True)
+
+
+def run_packed(args, rank, world):
+    """Packed variable-length batch: one step = fa_fwd_varlen + fa_bwd_varlen."""
+    import torch
+
+    import io_aware_exact_tiled_gb300 as fa
+    from io_aware_exact_tiled_gb300 import binding as fb
+    from io_aware_exact_tiled_gb300 import workloads as W
+    w = W.PACKED_WORKLOADS[args.workload]
+    dev = torch.device("cuda", int(os.environ.get("LOCAL_RANK", "0")))
+    torch.cuda.set_device(dev)
+    fa.load()
+    x = W.make_packed_workload(w, seed=rank, device="cuda")
+    q, k, v, do = (t.to(dev) for t in (x.q, x.k, x.v, x.do))
+    cu = x.cu_seqlens.to(dev)
+    total, H, d = q.shape
+    B = len(x.lens)
+    o = torch.empty_like(q)
+    lse = torch.empty((H, total), dtype=torch.float32, device=dev)
+    dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+    ws_f = fa.workspace(256, dev)
+    ws_b = fa.workspace(fb.load().fa_bwd_varlen_workspace_size(B, H, total, d), dev)
+    pairs = sum((n * n / 2 if w.causal else n * n) for n in x.lens) * H
+    fwd_flop, bwd_flop = 4.0 * d * pairs, 10.0 * d * pairs
+    ev = lambda: torch.cuda.Event(enable_timing=True)
+    kw = dict(scale=x.scale, causal=w.causal)
+
+    def fwd():
+        fa.forward_varlen(q, k, v, cu, x.max_seqlen, out=o, lse=lse, ws=ws_f, **kw)
+        return fa.last_launch_count()
+
+    def bwd():
+        fa.backward_varlen(q, k, v, o, lse, do, cu, x.max_seqlen, dq=dq, dk=dk, dv=dv, ws=ws_b, **kw)
+        return fa.last_launch_count()
+
+    for _ in range(max(3, args.warmup)):
+        fwd()
+        bwd()
+    torch.cuda.synchronize()
+    sampler = ClockSampler()
+    sampler.start()
+    wall0 = time.time()
+    f_ms, f_ker, nf = _timed_loop(fwd, args.steps, ev, fa)
+    b_ms, b_ker, nb = _timed_loop(bwd, args.steps, ev, fa)
+    wall1 = time.time()
+    sampler.stop()
+    if fa.get_status(ws_f) != 0 or fa.get_status(ws_b) != 0:
+        raise RuntimeError("device status word reports an error")
+    ms_step = (f_ms + b_ms) / args.steps
+    value = (fwd_flop + bwd_flop) / (ms_step * 1e-3) / 1e12
+    peaks, src = load_peaks()
+    peak = float(peaks["bf16_tflops"])
+    fwd_tf, bwd_tf = fwd_flop / (f_ker * 1e-3) / 1e12, bwd_flop / (b_ker * 1e-3) / 1e12
+    line = {
+        "metric": "packed variable-length attention fwd+bwd TFLOP/s", "value": value, "unit": "TFLOP/s",
+        "n_gpus": 1, "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic (seeded N(0,1), packed)",
+        "config": {"workload": f"{w.name}: B={B} sequences, lengths U{{{w.len_range[0]}..{w.len_range[1]}}} "
+                               f"(total {total} tokens), H={H} d={d}, causal={w.causal}"},
+        "fwd": {"kernel_ms": f_ker, "tflops": fwd_tf, "pct_peak": 100 * fwd_tf / peak},
+        "bwd": {"kernel_ms": b_ker, "tflops": bwd_tf, "pct_peak": 100 * bwd_tf / peak},
+        "roofline": {"bound": "tensor", "achieved": bwd_tf, "peak": peak, "unit": "TFLOP/s", "frac": bwd_tf / peak,
+                     "traffic": None, "kernel": "fa_bwd_kernel (packed)",
+                     "peak_source": f"{src} bf16 dense burst"},
+        "cpu_baseline": None, "e2e": None, "gpu_launches": nf + nb, "clocks": sampler.summary(wall0, wall1),
+    }
+    print(json.dumps(line), flush=True)
+
+
 # ------------------------------------------------------------------ our arm
 def main():
     args = parse()
@@ -327,6 +514,11 @@ def main():
     local = int(os.environ.get("LOCAL_RANK", "0"))
     if args.impl == "reference":
         return run_reference(args, rank, world)
+    from io_aware_exact_tiled_gb300 import workloads as W_
+    if args.workload in W_.DECODE_WORKLOADS:
+        return run_decode(args, rank, world)
+    if args.workload in W_.PACKED_WORKLOADS:
+        return run_packed(args, rank, world)
 
     import torch
     import torch.distributed as dist

@@ -130,6 +130,31 @@ fa_status fa_fwd_varlen(const void* q, const void* k, const void* v, void* o, fl
                         void* workspace, size_t ws_bytes, void* stream);
 
 /*
+ * Decoding: a few new query rows against a long key/value cache
+ * ("FlashAttention: making attention IO-aware", section "In practice": with
+ * one query row there is no query block to parallelise over, so
+ * Flash-Decoding splits the keys across thread blocks and merges the partial
+ * results with logsumexp rescaling). Every query row of batch element b sees
+ * the first cache_len[b] cache entries.
+ *   q           in,  device, [B, H, Nq, d] bf16, 1 <= Nq <= 8
+ *   k, v        in,  device, the cache, [B, H, Nk, d] bf16 (any Nk >= 1)
+ *   o           out, device, [B, H, Nq, d] bf16
+ *   lse         out, device, float32 [B, H, Nq] (natural log; -inf for a row
+ *               with no valid key, whose o row is 0)
+ *   cache_len   NULL (all Nk entries valid) or device int32 [B]; values are
+ *               clamped to [0, Nk] on the device
+ *   num_splits  key splits per (b, h): 0 picks a count from the sizes;
+ *               otherwise at most one split per 64 keys is used
+ *   workspace   fa_decode_workspace_size(B, H, Nq, Nk, d, num_splits) bytes
+ *               (partial maxima, sums and outputs of the splits)
+ * Runs two kernels (the splits, then the merge). FA_BF16 only; d in {64, 128}.
+ */
+size_t fa_decode_workspace_size(int B, int H, int Nq, int Nk, int d, int num_splits);
+fa_status fa_decode(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int Nq, int Nk,
+                    int d, float scale, const int32_t* cache_len, int num_splits, fa_dtype dtype, void* workspace,
+                    size_t ws_bytes, void* stream);
+
+/*
  * Backward pass of a packed variable-length batch: the gradients of
  * <dO, O> for fa_fwd_varlen.
  *   q, k, v, o, dout  in,  device, [total, H, d] bf16

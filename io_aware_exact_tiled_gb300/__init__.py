@@ -10,6 +10,7 @@ from .binding import (  # noqa: F401
     backward,
     forward_varlen,
     backward_varlen,
+    decode,
     fwd_workspace_size,
     bwd_workspace_size,
     get_status,

@@ -60,6 +60,10 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.fa_bwd_varlen_workspace_size.restype = sz
     lib.fa_bwd_varlen.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, i, i, i, i, i, f, i, i, vp, sz, vp]
     lib.fa_bwd_varlen.restype = i
+    lib.fa_decode_workspace_size.argtypes = [i, i, i, i, i, i]
+    lib.fa_decode_workspace_size.restype = sz
+    lib.fa_decode.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, f, vp, i, i, vp, sz, vp]
+    lib.fa_decode.restype = i
     lib.fa_get_status.argtypes = [vp, vp]
     lib.fa_get_status.restype = i
     lib.fa_status_string.argtypes = [i]
@@ -216,6 +220,34 @@ def backward_varlen(q, k, v, o, lse, do, cu_seqlens, max_seqlen: int, scale: Opt
     if rc != FA_OK:
         raise FAError(rc, "fa_bwd_varlen")
     return dq, dk, dv
+
+
+def decode(q, k_cache, v_cache, cache_len=None, scale: Optional[float] = None, num_splits: int = 0, out=None,
+           lse=None, ws=None, stream=None):
+    """O, L = fa_decode(...): Nq (1..8) query rows per (b, h) against a
+    [B, H, Nk, d] bf16 cache, keys split across CTAs and merged. Returns
+    (o [B, H, Nq, d], lse fp32 [B, H, Nq])."""
+    lib = load()
+    for t in (q, k_cache, v_cache):
+        if t.device.type != "cuda" or not t.is_contiguous() or t.dim() != 4 or t.dtype != torch.bfloat16:
+            raise ValueError("q and the cache must be contiguous bf16 [B, H, N, d] CUDA tensors")
+    B, H, Nq, d = q.shape
+    if k_cache.shape != v_cache.shape or k_cache.shape[:2] != (B, H) or k_cache.shape[3] != d:
+        raise ValueError("the cache must be [B, H, Nk, d] with q's B, H and d")
+    Nk = k_cache.shape[2]
+    if cache_len is not None and (cache_len.dtype != torch.int32 or cache_len.shape != (B,)
+                                  or cache_len.device != q.device):
+        raise ValueError("cache_len must be an int32 [B] tensor on the same device")
+    scale = 1.0 / math.sqrt(d) if scale is None else float(scale)
+    o = torch.empty_like(q) if out is None else out
+    L = torch.empty((B, H, Nq), dtype=torch.float32, device=q.device) if lse is None else lse
+    if ws is None:
+        ws = workspace(lib.fa_decode_workspace_size(B, H, Nq, Nk, d, num_splits), q.device)
+    rc = lib.fa_decode(_ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(o), _ptr(L), B, H, Nq, Nk, d, scale,
+                       _ptr(cache_len), int(num_splits), FA_BF16, _ptr(ws), ws.numel(), _stream_handle(stream))
+    if rc != FA_OK:
+        raise FAError(rc, "fa_decode")
+    return o, L
 
 
 def backward(q, k, v, o, lse, do, scale: Optional[float] = None, causal: bool = False, blockmask=None,

@@ -6,6 +6,7 @@
 #include <string.h>
 
 #include "fa.h"
+#include "fa_decode.h"
 #include "fa_launch.h"
 
 namespace {
@@ -212,6 +213,81 @@ fa_status fa_bwd_varlen(const void* q, const void* k, const void* v, const void*
     if (cudaMemsetAsync(a.status, 0, sizeof(int) * 4, s) != cudaSuccess) return FA_ERR_CUDA;
     int n = 0;
     st = map_cuda(fa::launch_bwd(a, s, &n));
+    if (st == FA_OK) g_last_launches = n;
+    return st;
+}
+
+// Splits per head of a decode call: num_splits if given (at most one per 64
+// keys), else enough CTAs for a few waves of two per SM while keeping at
+// least 512 keys per split; then the keys per split, a multiple of 64.
+static void decode_splits(int B, int H, int Nk, int num_splits, int* splits, int* split_keys) {
+    const int max_s = (Nk + 63) / 64;
+    int s = num_splits;
+    if (s <= 0) {
+        const long long heads = static_cast<long long>(B) * H;
+        const long long want = (152LL * 2 * 3 + heads - 1) / heads;
+        s = static_cast<int>(want < 1 ? 1 : want);
+        const int by_len = (Nk + 511) / 512;
+        if (s > by_len) s = by_len;
+    }
+    if (s > max_s) s = max_s;
+    if (s < 1) s = 1;
+    int keys = (Nk + s - 1) / s;
+    keys = (keys + 63) / 64 * 64;
+    *split_keys = keys;
+    *splits = (Nk + keys - 1) / keys;
+}
+
+size_t fa_decode_workspace_size(int B, int H, int Nq, int Nk, int d, int num_splits) {
+    if (B <= 0 || H <= 0 || Nq <= 0 || Nk <= 0 || d <= 0) return 0;
+    int S = 1, keys = 64;
+    decode_splits(B, H, Nk, num_splits, &S, &keys);
+    const size_t parts = static_cast<size_t>(B) * H * Nq * S;
+    return kStatusBytes + 2 * align256(parts * sizeof(float)) + align256(parts * d * sizeof(float));
+}
+
+fa_status fa_decode(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int Nq, int Nk,
+                    int d, float scale, const int32_t* cache_len, int num_splits, fa_dtype dtype, void* workspace,
+                    size_t ws_bytes, void* stream) {
+    if (!q || !k || !v || !o || !lse || !workspace) return FA_ERR_INVALID_ARG;
+    if (dtype != FA_BF16 && dtype != FA_FP32) return FA_ERR_INVALID_ARG;
+    if (B <= 0 || H <= 0 || Nq <= 0 || Nk <= 0 || d <= 0 || num_splits < 0) return FA_ERR_INVALID_ARG;
+    if (!(scale > 0.f) || !isfinite(scale)) return FA_ERR_INVALID_ARG;
+    if (dtype != FA_BF16) return FA_ERR_UNSUPPORTED;
+    if (d != 64 && d != 128) return FA_ERR_UNSUPPORTED;
+    if (Nq > 8) return FA_ERR_UNSUPPORTED;
+    if (static_cast<long long>(B) * H * Nk >= (1LL << 31) || B > 65535 || H > 65535) return FA_ERR_UNSUPPORTED;
+    if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(o, 16) || !aligned(lse, 4) ||
+        (cache_len && !aligned(cache_len, 4)) || !aligned(workspace, 256))
+        return FA_ERR_INVALID_ARG;
+    if (ws_bytes < fa_decode_workspace_size(B, H, Nq, Nk, d, num_splits)) return FA_ERR_INVALID_ARG;
+
+    fa::DecodeArgs a{};
+    a.q = q;
+    a.k = k;
+    a.v = v;
+    a.o = o;
+    a.lse = lse;
+    a.cache_len = cache_len;
+    a.B = B;
+    a.H = H;
+    a.Nq = Nq;
+    a.Nk = Nk;
+    a.d = d;
+    a.scale = scale;
+    decode_splits(B, H, Nk, num_splits, &a.splits, &a.split_keys);
+    const size_t parts = static_cast<size_t>(B) * H * Nq * a.splits;
+    char* ws = static_cast<char*>(workspace);
+    a.status = reinterpret_cast<int*>(ws);
+    a.pm = reinterpret_cast<float*>(ws + kStatusBytes);
+    a.pl = reinterpret_cast<float*>(ws + kStatusBytes + align256(parts * sizeof(float)));
+    a.po = reinterpret_cast<float*>(ws + kStatusBytes + 2 * align256(parts * sizeof(float)));
+    a.ev_begin = g_ev_begin;
+    a.ev_end = g_ev_end;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (cudaMemsetAsync(a.status, 0, sizeof(int) * 4, s) != cudaSuccess) return FA_ERR_CUDA;
+    int n = 0;
+    fa_status st = map_cuda(fa::launch_decode(a, s, &n));
     if (st == FA_OK) g_last_launches = n;
     return st;
 }

@@ -196,3 +196,61 @@ def make_packed_workload(w: PackedWorkload, seed: int = 0, device: str = "cpu") 
     lo, hi = w.len_range
     lens = torch.randint(lo, hi + 1, (w.B,), generator=g).tolist()
     return make_packed(lens, w.H, w.d, w.causal, seed, device)
+
+
+# --------------------------------------------------------------------------
+# Decoding: a few query rows against a key/value cache
+# --------------------------------------------------------------------------
+
+@dataclasses.dataclass(frozen=True)
+class DecodeWorkload:
+    """Nq new query rows per (b, h) against a [B, H, Nk, d] bf16 cache whose
+    valid length per batch element is drawn uniformly from the inclusive
+    range ``len_range``."""
+    name: str
+    B: int
+    H: int
+    Nq: int
+    Nk: int
+    d: int
+    len_range: tuple
+
+    @property
+    def scale(self) -> float:
+        return 1.0 / math.sqrt(self.d)
+
+
+# decode16k: one new token for 16 requests of 32 heads, d = 128, caches of
+#   8K..16K valid entries in a 16K-entry allocation.
+DECODE_WORKLOADS = {
+    "decode16k": DecodeWorkload("decode16k", 16, 32, 1, 16384, 128, (8192, 16384)),
+}
+
+
+@dataclasses.dataclass
+class DecodeInputs:
+    q: torch.Tensor          # [B, H, Nq, d]
+    k: torch.Tensor          # [B, H, Nk, d]
+    v: torch.Tensor
+    cache_len: torch.Tensor  # int32 [B], on the CPU
+    scale: float
+
+
+def make_decode(B: int, H: int, Nq: int, Nk: int, d: int, len_range, seed: int = 0,
+                device: str = "cpu") -> DecodeInputs:
+    """Seeded decode inputs: standard normal fp32 q, then the K and V caches,
+    rounded to bf16; cache lengths ~ U{len_range} from a CPU generator seeded
+    with ``seed + 1``."""
+    gen = torch.Generator(device=device)
+    gen.manual_seed(seed)
+    q = torch.randn((B, H, Nq, d), generator=gen, device=device, dtype=torch.float32)
+    k = torch.randn((B, H, Nk, d), generator=gen, device=device, dtype=torch.float32)
+    v = torch.randn((B, H, Nk, d), generator=gen, device=device, dtype=torch.float32)
+    lo, hi = len_range
+    cl = torch.randint(lo, hi + 1, (B,), generator=torch.Generator().manual_seed(seed + 1)).to(torch.int32)
+    bf = torch.bfloat16
+    return DecodeInputs(q.to(bf), k.to(bf), v.to(bf), cl, 1.0 / math.sqrt(d))
+
+
+def make_decode_workload(w: DecodeWorkload, seed: int = 0, device: str = "cpu") -> DecodeInputs:
+    return make_decode(w.B, w.H, w.Nq, w.Nk, w.d, w.len_range, seed, device)
