@@ -132,10 +132,22 @@ class ClockSampler:
 
 
 # ------------------------------------------------------------------ helpers
-def kernel_source_sha():
+# source files each profiled kernel is compiled from (its .cu plus the shared
+# headers); a recorded DRAM-traffic figure stays valid while they are unchanged
+KERNEL_SOURCES = {
+    "fa_fwd_kernel": ["fa_fwd.cu"],
+    "fa_bwd_kernel": ["fa_bwd.cu"],
+    "fa_fwd_q1_kernel": ["fa_fwd_q1.cu"],
+    "fa_decode_split_kernel": ["fa_decode.cu", "fa_decode.h"],
+}
+SHARED_HEADERS = ["fa_common.cuh", "fa_launch.h", "sm103_ptx.cuh", "tmap.h"]
+
+
+def kernel_source_sha(kernel: str):
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "io_aware_exact_tiled_gb300", "csrc")
-    for f in sorted(os.listdir(csrc)):
+    for f in sorted(KERNEL_SOURCES.get(kernel, []) + SHARED_HEADERS):
+        h.update(f.encode())
         h.update(open(os.path.join(csrc, f), "rb").read())
     return h.hexdigest()[:16]
 
@@ -149,7 +161,7 @@ def recorded_traffic(kernel: str, workload: str):
     try:
         d = json.load(open(p))
         e = d.get(kernel, {}).get(workload)
-        if e and e.get("source_sha") == kernel_source_sha():
+        if e and e.get("source_sha") == kernel_source_sha(kernel):
             return e["dram_bytes_per_launch"]
     except (ValueError, KeyError, TypeError):
         return None
@@ -386,7 +398,7 @@ def run_decode(args, rank, world):
     achieved = (cache_bytes + io_bytes) / (ker_ms * 1e-3) / 1e9
     e2e = None
     if not args.no_e2e:
-        hq = x.q.pin_memory()
+        hq = x.q.cpu().pin_memory()
         ho = torch.empty_like(hq).pin_memory()
         hl = torch.empty((B, H, Nq), dtype=torch.float32).pin_memory()
         qd = torch.empty_like(q)
@@ -408,18 +420,20 @@ def run_decode(args, rank, world):
     cpu = None
     if not args.no_cpu_baseline:
         from oracle import decode as DEC
-        xs = W.make_decode_workload(w, seed=0)
+        # two requests of the workload's shape and length range, decoded
+        # repeatedly until about 10 s of CPU time is spent
+        xs = W.make_decode(2, H, Nq, w.Nk, d, w.len_range, seed=0)
         t_used, nb, byt = 0.0, 0, 0
-        for b in range(B):
+        while t_used < 10.0 and nb < 400:
+            b = nb % 2
             t0 = time.perf_counter()
             DEC.decode_forward(xs.q[b:b + 1], xs.k[b:b + 1], xs.v[b:b + 1], xs.scale, xs.cache_len[b:b + 1])
             t_used += time.perf_counter() - t0
             nb += 1
             byt += 2 * int(xs.cache_len[b]) * H * d * 2
-            if t_used > 10.0:
-                break
         cpu = {"value": byt / t_used / 1e9, "unit": "GB/s", "cores": os.cpu_count(), "kind": "oracle",
-               "sample": f"fp64 NumPy decode of {nb} request(s) (all {H} heads) of the workload ({t_used:.1f} s)"}
+               "sample": f"fp64 NumPy decode of {nb} request-steps (all {H} heads, Nk={w.Nk}, cache_len "
+                         f"U{{{w.len_range[0]}..{w.len_range[1]}}}) ({t_used:.1f} s)"}
     line = {
         "metric": "decode: KV-cache bytes read per second (split-key decoding)", "value": value, "unit": "GB/s",
         "n_gpus": 1, "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True,
@@ -428,7 +442,8 @@ def run_decode(args, rank, world):
                                f"U{{{w.len_range[0]}..{w.len_range[1]}}}",
                    "l2": "cache larger than L2 (%d MiB of K+V allocated)" % (2 * k.numel() * 2 >> 20)},
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": hbm, "unit": "GB/s", "frac": achieved / hbm,
-                     "traffic": None, "kernel": "fa_decode_split_kernel",
+                     "traffic": recorded_traffic("fa_decode_split_kernel", w.name),
+                     "algorithmic_bytes": cache_bytes + io_bytes, "kernel": "fa_decode_split_kernel",
                      "peak_source": f"{src} HBM copy bandwidth (MEASURED_PEAKS.json hbm_gbs)"},
         "split_kernel_ms": ker_ms, "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": launches,
         "clocks": sampler.summary(wall0, wall1),

@@ -58,11 +58,11 @@ def decode_forward(q, k, v, scale: float, cache_len=None):
         n = int(cl[b])
         if n == 0:
             continue
-        s = scale * np.einsum("hqd,hkd->hqk", q[b], k[b, :, :n])
+        s = scale * (q[b] @ k[b, :, :n].transpose(0, 2, 1))   # [H, Nq, n]
         m = s.max(axis=-1, keepdims=True)
         e = np.exp(s - m)
         lsum = e.sum(axis=-1, keepdims=True)
-        O[b] = np.einsum("hqk,hkd->hqd", e / lsum, v[b, :, :n])
+        O[b] = (e / lsum) @ v[b, :, :n]
         L[b] = (m + np.log(lsum))[..., 0]
     return O, L
 
@@ -85,12 +85,12 @@ def split_partials(q, k, v, scale: float, split: int, cache_len=None):
             j0, j1 = c * split, min(Nk, (c + 1) * split, int(cl[b]))
             if j1 <= j0:
                 continue
-            s = scale * np.einsum("hqd,hkd->hqk", q[b], k[b, :, j0:j1])
+            s = scale * (q[b] @ k[b, :, j0:j1].transpose(0, 2, 1))
             mc = s.max(axis=-1)
             e = np.exp(s - mc[..., None])
             m[b, :, :, c] = mc
             lsum[b, :, :, c] = e.sum(axis=-1)
-            o[b, :, :, c] = np.einsum("hqk,hkd->hqd", e, v[b, :, j0:j1])
+            o[b, :, :, c] = e @ v[b, :, j0:j1]
     return m, lsum, o
 
 
