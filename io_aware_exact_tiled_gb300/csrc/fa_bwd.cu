@@ -22,8 +22,9 @@
 //                       TMA bulk reduce-adds staged through shared memory
 //   fa_bwd_dq_kernel    fp32 dQ accumulator -> dQ in bf16
 //
-// TMEM columns of fa_bwd_kernel: [0,128) S^T, then P^T (bf16), then dQ_i;
-// [128,256) dP^T; [256, 256+d) dV_j; [256+d, 256+2d) dK_j. The softmax
+// TMEM columns of fa_bwd_kernel: two 128-column buffers in [0, 256) that
+// alternate between query blocks (one holds S^T, then P^T (bf16), then dQ_i;
+// the other dP^T); [256, 256+d) dV_j; [256+d, 256+2d) dK_j. The softmax
 // scale is applied once, to dK_j in the epilogue and to dQ in the conversion
 // kernel, instead of to every element of dS.
 #include <math_constants.h>
@@ -54,8 +55,12 @@ struct BwdCfg {
     static constexpr uint32_t ID_SQ = idesc_make(128, 128, kFmtBF16, false, false);  // S^T, dP^T
     static constexpr uint32_t ID_KN = idesc_make(128, D, kFmtBF16, false, true);     // dV, dK
     static constexpr uint32_t ID_DQ = idesc_make(128, D, kFmtBF16, true, true);      // dQ
-    // dQ_i reuses the S^T / P^T columns once dV_i has read P^T
-    static constexpr int COL_S = 0, COL_DQ = 0, COL_DP = 128, COL_DV = 256, COL_DK = 256 + D;
+    // Columns [0, 256) are two 128-column buffers that trade roles every
+    // query block u: S^T (then P^T, then dQ_u) goes to buffer u % 2 and dP^T
+    // to the other one (col_s / col_dp below). S^T of block u + 1 can then be
+    // issued right after dQ_u, without waiting for the drain to read dQ_u;
+    // the wait moves to dP^T of block u + 1, which is needed only later.
+    static constexpr int COL_DV = 256, COL_DK = 256 + D;
 };
 
 struct BwdParams {
@@ -83,8 +88,8 @@ constexpr float kLog2e = 1.4426950408889634f;
 //   warps 8-11    compute group 1: key r, queries 64-127
 //   warps 12-15   dQ drain: thread r owns query r of block i
 // Per query block i the MMA thread issues, in this order:
-//   dP^T = V_j dO_i^T  (its columns were last read by the compute groups)
-//   S^T  = K_j Q_i^T   (after the drain has read dQ_{i-1} out of these columns)
+//   S^T  = K_j Q_i^T   (into the buffer that held dP^T of the previous block)
+//   dP^T = V_j dO_i^T  (after the drain has read dQ_{i-1} out of its buffer)
 //   dV  += P^T dO_i    (P^T from TMEM, written by the compute groups)
 //   dK  += dS^T Q_i, dQ_i = dS K_j  (dS^T from shared memory)
 // VARLEN: packed variable-length batch; a separate instantiation so that the
@@ -117,8 +122,7 @@ __global__ void __launch_bounds__(512, 1)
     uint64_t* ds_ready = p_ready + 1;
     uint64_t* dq_full = ds_ready + 1;
     uint64_t* dq_free = dq_full + 1;
-    uint64_t* ds_free = dq_free + 1;   // dS^T buffer free again (drain done reading it)
-    uint64_t* dkv_done = ds_free + 1;
+    uint64_t* dkv_done = dq_free + 1;
     uint64_t* drain = dkv_done + 1;
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
@@ -156,7 +160,7 @@ __global__ void __launch_bounds__(512, 1)
         mbar_init(kv_full, 1);
         for (int s = 0; s < C::STAGES; ++s) {
             mbar_init(&qd_full[s], 1);
-            mbar_init(&qd_empty[s], 1);
+            mbar_init(&qd_empty[s], 4);  // the four dQ drain warps, done staging through it
         }
         mbar_init(s_full, 1);
         mbar_init(dp_full, 1);
@@ -164,7 +168,6 @@ __global__ void __launch_bounds__(512, 1)
         mbar_init(ds_ready, 256);
         mbar_init(dq_full, 1);
         mbar_init(dq_free, 128);
-        mbar_init(ds_free, 4);
         mbar_init(dkv_done, 1);
         mbar_init(drain, 1);
         fence_barrier_init();
@@ -257,31 +260,34 @@ __global__ void __launch_bounds__(512, 1)
                 const uint32_t dob = smem_u32(sm + C::DO_OFF + st * C::TILE_BYTES);
                 const uint64_t dQ_k = sdesc_sw128(qb, 16, 1024), dQ_mn = sdesc_sw128(qb, 16384, 1024);
                 const uint64_t dO_k = sdesc_sw128(dob, 16, 1024), dO_mn = sdesc_sw128(dob, 16384, 1024);
-                // dP^T = V_j dO_i^T
+                const uint32_t col_s = (u & 1) ? 128u : 0u, col_dp = col_s ^ 128u;
+                // S^T = K_j Q_i^T (its buffer last held dP^T of the previous
+                // block, read by the compute groups before they signalled
+                // dS^T of that block, which the previous dK / dQ waited for)
 #pragma unroll
                 for (int kk = 0; kk < D / 16; ++kk) {
                     const uint32_t off = (kk / 4) * 16384 + (kk % 4) * 32;
-                    umma_ss<false>(leader, tm + C::COL_DP, sdesc_advance(dV_k, off), sdesc_advance(dO_k, off), C::ID_SQ,
+                    umma_ss<false>(leader, tm + col_s, sdesc_advance(dK_k, off), sdesc_advance(dQ_k, off), C::ID_SQ,
                                    kk > 0);
                 }
-                umma_commit(leader, dp_full);
-                // S^T = K_j Q_i^T (these columns held dQ of the previous block)
+                umma_commit(leader, s_full);
+                // dP^T = V_j dO_i^T (its buffer held dQ of the previous block)
                 if (u > 0 && !(ok = mbar_wait_warp(dq_free, (u - 1) & 1, cx, 14))) break;
                 tc_fence_after();
 #pragma unroll
                 for (int kk = 0; kk < D / 16; ++kk) {
                     const uint32_t off = (kk / 4) * 16384 + (kk % 4) * 32;
-                    umma_ss<false>(leader, tm + C::COL_S, sdesc_advance(dK_k, off), sdesc_advance(dQ_k, off), C::ID_SQ,
+                    umma_ss<false>(leader, tm + col_dp, sdesc_advance(dV_k, off), sdesc_advance(dO_k, off), C::ID_SQ,
                                    kk > 0);
                 }
-                umma_commit(leader, s_full);
-                // dV_j += P^T dO_i ; P^T of queries 0-63 sits in columns 0-31
-                // and that of queries 64-127 in columns 64-95
+                umma_commit(leader, dp_full);
+                // dV_j += P^T dO_i ; P^T of queries 0-63 sits in the buffer's
+                // columns 0-31 and that of queries 64-127 in columns 64-95
                 if (!(ok = mbar_wait_warp(p_ready, u & 1, cx, 15))) break;
                 tc_fence_after();
 #pragma unroll
                 for (int kk = 0; kk < 8; ++kk)
-                    umma_ts<false>(leader, tm + C::COL_DV, tm + C::COL_S + (kk >> 2) * 64 + (kk & 3) * 8,
+                    umma_ts<false>(leader, tm + C::COL_DV, tm + col_s + (kk >> 2) * 64 + (kk & 3) * 8,
                                    sdesc_advance(dO_mn, kk * 2048), C::ID_KN, (u > 0 || kk > 0) ? 1u : 0u);
                 // dK_j += dS^T Q_i ; dQ_i = dS K_j
                 if (!(ok = mbar_wait_warp(ds_ready, u & 1, cx, 16))) break;
@@ -294,10 +300,9 @@ __global__ void __launch_bounds__(512, 1)
                 }
 #pragma unroll
                 for (int kk = 0; kk < 8; ++kk)
-                    umma_ss<false>(leader, tm + C::COL_DQ, sdesc_advance(dS_mn, kk * 2048), sdesc_advance(dK_mn, kk * 2048),
+                    umma_ss<false>(leader, tm + col_s, sdesc_advance(dS_mn, kk * 2048), sdesc_advance(dK_mn, kk * 2048),
                                    C::ID_DQ, kk > 0 ? 1u : 0u);
                 umma_commit(leader, dq_full);
-                umma_commit(leader, &qd_empty[st]);
                 ++u;
             }
             if (ok && u > 0) umma_commit(leader, dkv_done);
@@ -325,6 +330,7 @@ __global__ void __launch_bounds__(512, 1)
             ok = __all_sync(0xffffffffu, ok) && __all_sync(0xffffffffu, mbar_wait(s_full, u & 1, cx, 18));
             if (!ok) break;
             tc_fence_after();
+            const uint32_t col_s = (u & 1) ? 128u : 0u, col_dp = col_s ^ 128u;
             // masking is needed only on the diagonal tile (causal), for
             // padded keys, and for the query rows of a packed sequence's last
             // block that lie past its end (they belong to the next sequence)
@@ -335,7 +341,7 @@ __global__ void __launch_bounds__(512, 1)
             for (int c = 0; c < 2; ++c) {
                 uint32_t pk[16];  // P^T of 32 queries, bf16 pairs
                 uint32_t sr[32];
-                tmem_ld32(tl + C::COL_S + 64 * g + c * 32, sr);
+                tmem_ld32(tl + col_s + 64 * g + c * 32, sr);
                 tmem_ld_wait(sr);
 #pragma unroll
                 for (int e = 0; e < 8; ++e) {
@@ -357,7 +363,7 @@ __global__ void __launch_bounds__(512, 1)
                     pk[2 * e] = pack_bf16x2(pv0, pv1);
                     pk[2 * e + 1] = pack_bf16x2(pv2, pv3);
                 }
-                tmem_st16(tl + C::COL_S + 64 * g + c * 16, pk);
+                tmem_st16(tl + col_s + 64 * g + c * 16, pk);
             }
             tmem_st_wait();
             tc_fence_before();
@@ -372,8 +378,8 @@ __global__ void __launch_bounds__(512, 1)
 #pragma unroll
             for (int c = 0; c < 2; ++c) {
                 uint32_t dr[32], pk[16];
-                tmem_ld32(tl + C::COL_DP + 64 * g + c * 32, dr);
-                tmem_ld16(tl + C::COL_S + 64 * g + c * 16, pk);
+                tmem_ld32(tl + col_dp + 64 * g + c * 32, dr);
+                tmem_ld16(tl + col_s + 64 * g + c * 16, pk);
                 tmem_ld_wait(dr);
                 tmem_ld_wait(pk);
 #pragma unroll
@@ -389,8 +395,8 @@ __global__ void __launch_bounds__(512, 1)
             }
             if (u > 0) {
                 // the previous dS^T must have been consumed by its dK / dQ
-                // GEMMs and the buffer released by the dQ drain
-                ok = __all_sync(0xffffffffu, mbar_wait(ds_free, (u - 1) & 1, cx, 20));
+                // GEMMs (their completion is what releases dQ to the drain)
+                ok = __all_sync(0xffffffffu, mbar_wait(dq_full, (u - 1) & 1, cx, 20));
                 if (!ok) break;
             }
 #pragma unroll
@@ -440,9 +446,15 @@ __global__ void __launch_bounds__(512, 1)
         }
     } else if (warp >= 12) {
         // ------------------------------------------------------------ dQ drain (thread = query)
+        // dQ_i is staged through the Q_i and dO_i stage of its own block:
+        // its GEMMs are complete once dQ_i is, and the producer reloads the
+        // stage only after the four drain warps release it. Warp wq's rows
+        // form D / 32 boxes of [32 x 32] fp32 (4 KiB); box k sits in the Q
+        // tile for the first half of the boxes and in the dO tile for the
+        // rest, so every reduce-add of the block is issued before any wait.
+        constexpr int NB = D / 32, NBH = NB / 2;
         const int wq = warp & 3;
         const uint32_t tl = tm + (static_cast<uint32_t>(wq * 32) << 16);
-        uint8_t* stage_buf = sm + C::DS_OFF + wq * 8192;  // two [32 x 32] fp32 boxes of 4 KiB
         int u = 0;
         for (int i = lo; i < T; ++i) {
             if (!visible_i(i)) continue;
@@ -451,12 +463,15 @@ __global__ void __launch_bounds__(512, 1)
             if (!ok) break;
             tc_fence_after();
             const int grow = bh * N + i * kTile + wq * 32;  // first accumulator row of this warp
-            const uint32_t sb = smem_u32(stage_buf);
+            const int st = u % C::STAGES;
+            uint8_t* box_q = sm + C::Q_OFF + st * C::TILE_BYTES + wq * (NBH * 4096);
+            uint8_t* box_do = sm + C::DO_OFF + st * C::TILE_BYTES + wq * (NBH * 4096);
 #pragma unroll
             for (int half = 0; half < D / 64; ++half) {
                 uint32_t v[2][32];
-                tmem_ld32(tl + C::COL_DQ + half * 64, v[0]);
-                tmem_ld32(tl + C::COL_DQ + half * 64 + 32, v[1]);
+                const uint32_t col_q = (u & 1) ? 128u : 0u;  // dQ_u shares the buffer of S^T_u
+                tmem_ld32(tl + col_q + half * 64, v[0]);
+                tmem_ld32(tl + col_q + half * 64 + 32, v[1]);
                 tmem_ld_wait(v[0]);
                 tmem_ld_wait(v[1]);
                 if (half == D / 64 - 1) {
@@ -464,34 +479,36 @@ __global__ void __launch_bounds__(512, 1)
                     tc_fence_before();
                     mbar_arrive(dq_free);
                 }
-                if (half > 0) {
-                    if (lane == 0) bulk_wait_group_read0();
-                    __syncwarp();
-                }
 #pragma unroll
-                for (int bx = 0; bx < 2; ++bx)
+                for (int bx = 0; bx < 2; ++bx) {
+                    const int k = half * 2 + bx;
+                    uint8_t* box = k < NBH ? box_q + k * 4096 : box_do + (k - NBH) * 4096;
+                    const uint32_t sb = smem_u32(box);
 #pragma unroll
                     for (int c = 0; c < 8; ++c) {
                         const uint32_t* w = &v[bx][4 * c];
-                        sts128(sb + bx * 4096 + lane * 128 + ((c ^ (lane & 7)) * 16), w[0], w[1], w[2], w[3]);
+                        sts128(sb + lane * 128 + ((c ^ (lane & 7)) * 16), w[0], w[1], w[2], w[3]);
                     }
+                }
                 fence_proxy_async_smem();
                 __syncwarp();
                 if (lane == 0) {
-                    if (varlen) {
-                        const int tok = seq0 + i * kTile + wq * 32;
-                        tma_reduce_add_3d(&tmdQacc, half * 64, h, tok, stage_buf);
-                        tma_reduce_add_3d(&tmdQacc, half * 64 + 32, h, tok, stage_buf + 4096);
-                    } else {
-                        tma_reduce_add_2d(&tmdQacc, half * 64, grow, stage_buf);
-                        tma_reduce_add_2d(&tmdQacc, half * 64 + 32, grow, stage_buf + 4096);
+#pragma unroll
+                    for (int bx = 0; bx < 2; ++bx) {
+                        const int k = half * 2 + bx;
+                        const uint8_t* box = k < NBH ? box_q + k * 4096 : box_do + (k - NBH) * 4096;
+                        if (varlen)
+                            tma_reduce_add_3d(&tmdQacc, k * 32, h, seq0 + i * kTile + wq * 32, box);
+                        else
+                            tma_reduce_add_2d(&tmdQacc, k * 32, grow, box);
                     }
                     bulk_commit_group();
                 }
             }
             if (lane == 0) {
+                // the stage may be refilled once the reduce-adds have read it
                 bulk_wait_group_read0();
-                mbar_arrive(ds_free);
+                mbar_arrive(&qd_empty[st]);
             }
             __syncwarp();
             ++u;
