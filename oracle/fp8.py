@@ -1,0 +1,134 @@
+"""fp64 oracle for the FP8 forward pass with block scales and a Hadamard
+rotation of Q and K.
+
+Test infrastructure only: imported by ``tests/``, by ``__graft_entry__.smoke``
+and by the benchmark's CPU-baseline leg. The product path never uses it.
+
+Source: "FlashAttention: making attention IO-aware", section
+"FlashAttention-3", the bullet on FP8 with incoherent processing: FP8 doubles
+throughput again but is fragile with outliers, so FA3 quantises per block and
+first multiplies Q and K by a random orthogonal (Hadamard) matrix, which
+spreads outliers across dimensions.
+
+This is an approximation of attention, not an exact method, so the oracle
+states the algorithm's steps in order (each in plain fp64 arithmetic on the
+values the FP8 format can hold), with these readings where the page is
+silent:
+
+1. Rotation. R = diag(s) H_d / sqrt(d), with H_d the Sylvester Hadamard
+   matrix (H_1 = [1], H_2n = [[H_n, H_n], [H_n, -H_n]]) and s a vector of
+   random signs drawn once and passed in. R is orthogonal, so
+   (Q R)(K R)^T = Q K^T: the rotation changes only the quantisation error.
+2. Format. OCP FP8 E4M3: 1 sign, 4 exponent bits (bias 7), 3 mantissa bits;
+   normal values 2^(e-7) (1 + m/8), subnormals 2^-6 m/8, largest finite 448,
+   no infinities. Conversion rounds to nearest, ties to even, and saturates
+   at +-448.
+3. Block scales. Each block of 128 rows of one head of Q R and of K R gets
+   one scale, and V one scale per head (its P V product sums over every key
+   block in one accumulator, so a per-block V scale cannot be applied). A
+   scale is the power of two 2^ceil(log2(amax / 448)) (1 for an all-zero
+   block), so that x / scale fits the format and every rescaling is exact.
+4. Scores. S = scale_attn * deq(Q8) deq(K8)^T with deq(x8) = x8 * scale,
+   masked as in the dense oracle.
+5. Probabilities. With x = S log2(e) and M = floor(max_j x_j) per row,
+   p_j = 2^(x_j - M) in (0, 2) is rounded to E4M3 (p8_j). Quantising relative
+   to an integer exponent makes p8 independent of which power of two the
+   running maximum of an online (tiled) evaluation happens to use.
+6. Output. O = sum_j p8_j deq(V8_j) / sum_j p8_j (a convex combination of
+   the dequantised values), and L = logsumexp_j S_j (natural log) from the
+   unquantised probabilities.
+"""
+
+from __future__ import annotations
+
+import numpy as np
+
+from .attention import _f64, visible
+
+E4M3_MAX = 448.0
+BLOCK = 128
+
+
+def e4m3_round(x) -> np.ndarray:
+    """Round to the nearest E4M3 value (ties to even), saturating at +-448."""
+    x = np.asarray(x, dtype=np.float64)
+    a = np.abs(x)
+    # binade exponent, floored at the subnormal range (spacing 2^-9 below 2^-6)
+    e = np.floor(np.log2(np.where(a > 0, a, 1.0)))
+    e = np.maximum(e, -6.0)
+    step = np.exp2(e - 3.0)
+    r = np.round(a / step) * step  # numpy rounds halves to even
+    r = np.minimum(r, E4M3_MAX)
+    return np.copysign(r, x)
+
+
+def hadamard(d: int) -> np.ndarray:
+    """Sylvester Hadamard matrix of order d (a power of two), entries +-1."""
+    if d < 1 or d & (d - 1):
+        raise ValueError("d must be a power of two")
+    h = np.ones((1, 1))
+    while h.shape[0] < d:
+        h = np.block([[h, h], [h, -h]])
+    return h
+
+
+def rotation(signs) -> np.ndarray:
+    """R = diag(signs) H_d / sqrt(d)."""
+    s = np.asarray(signs, dtype=np.float64)
+    d = s.size
+    return (s[:, None] * hadamard(d)) / np.sqrt(d)
+
+
+def pow2_scale(amax: float) -> float:
+    """Smallest power of two 2^k with amax / 2^k <= 448 (1 for amax = 0)."""
+    if amax <= 0:
+        return 1.0
+    return float(np.exp2(np.ceil(np.log2(amax / E4M3_MAX))))
+
+
+def quantize_rows(x, rows: int = BLOCK):
+    """Block quantisation of a [N, d] matrix: blocks of `rows` rows.
+
+    Returns (x8 [N, d] on the E4M3 grid, scales [ceil(N / rows)])."""
+    x = np.asarray(x, dtype=np.float64)
+    N = x.shape[0]
+    nb = -(-N // rows)
+    x8 = np.zeros_like(x)
+    sc = np.ones(nb)
+    for b in range(nb):
+        blk = x[b * rows:(b + 1) * rows]
+        sc[b] = pow2_scale(float(np.abs(blk).max()) if blk.size else 0.0)
+        x8[b * rows:(b + 1) * rows] = e4m3_round(blk / sc[b])
+    return x8, sc
+
+
+def dequantize_rows(x8, sc, rows: int = BLOCK):
+    return x8 * np.repeat(sc, rows)[: x8.shape[0], None]
+
+
+def fp8_forward(q, k, v, scale: float, signs, causal: bool = False, rotate: bool = True, rows: int = BLOCK):
+    """FP8 forward of [B, H, N, d] inputs. Returns (O, L) in fp64.
+
+    ``rotate=False`` skips step 1 (plain block-quantised FP8), for comparing
+    the error with and without the rotation."""
+    q, k, v = _f64(q), _f64(k), _f64(v)
+    B, H, N, d = q.shape
+    R = rotation(signs) if rotate else np.eye(d)
+    O = np.zeros((B, H, N, d))
+    L = np.zeros((B, H, N))
+    vis = visible(N, causal)
+    for b in range(B):
+        for h in range(H):
+            q8, sq = quantize_rows(q[b, h] @ R, rows)
+            k8, sk = quantize_rows(k[b, h] @ R, rows)
+            sv = pow2_scale(float(np.abs(v[b, h]).max()))
+            v8 = e4m3_round(v[b, h] / sv)
+            s = scale * (dequantize_rows(q8, sq, rows) @ dequantize_rows(k8, sk, rows).T)
+            s = np.where(vis, s, -np.inf)
+            x = s * np.log2(np.e)
+            xm = x.max(axis=1, keepdims=True)
+            M = np.floor(xm)
+            p8 = e4m3_round(np.exp2(x - M))
+            O[b, h] = (p8 @ (v8 * sv)) / p8.sum(axis=1, keepdims=True)
+            L[b, h] = (xm[:, 0] + np.log2(np.exp2(x - xm).sum(axis=1))) * np.log(2.0)
+    return O, L
