@@ -19,17 +19,21 @@ silent:
    matrix (H_1 = [1], H_2n = [[H_n, H_n], [H_n, -H_n]]) and s a vector of
    random signs drawn once and passed in. R is orthogonal, so
    (Q R)(K R)^T = Q K^T: the rotation changes only the quantisation error.
+   The values quantised are Q diag(s) H_d = sqrt(d) Q R (and the same for K),
+   with the factor 1/d folded into the score scale: a Hadamard transform of
+   bf16 inputs is exact in fp32, so both sides quantise the same numbers.
 2. Format. OCP FP8 E4M3: 1 sign, 4 exponent bits (bias 7), 3 mantissa bits;
    normal values 2^(e-7) (1 + m/8), subnormals 2^-6 m/8, largest finite 448,
    no infinities. Conversion rounds to nearest, ties to even, and saturates
    at +-448.
-3. Block scales. Each block of 128 rows of one head of Q R and of K R gets
-   one scale, and V one scale per head (its P V product sums over every key
+3. Block scales. Each block of 128 rows of one head of the rotated Q and K
+   of step 1 gets one scale, and V one scale per head (its P V product sums over every key
    block in one accumulator, so a per-block V scale cannot be applied). A
    scale is the power of two 2^ceil(log2(amax / 448)) (1 for an all-zero
    block), so that x / scale fits the format and every rescaling is exact.
-4. Scores. S = scale_attn * deq(Q8) deq(K8)^T with deq(x8) = x8 * scale,
-   masked as in the dense oracle.
+4. Scores. S = (scale_attn / d) * deq(Q8) deq(K8)^T with
+   deq(x8) = x8 * scale (1/d undoes the sqrt(d) of step 1 on both sides;
+   without the rotation it is 1), masked as in the dense oracle.
 5. Probabilities. With x = S log2(e) and M = floor(max_j x_j) per row,
    p_j = 2^(x_j - M) in (0, 2) is rounded to E4M3 (p8_j). Quantising relative
    to an integer exponent makes p8 independent of which power of two the
@@ -106,29 +110,53 @@ def dequantize_rows(x8, sc, rows: int = BLOCK):
     return x8 * np.repeat(sc, rows)[: x8.shape[0], None]
 
 
-def fp8_forward(q, k, v, scale: float, signs, causal: bool = False, rotate: bool = True, rows: int = BLOCK):
+def quantized_inputs(q, k, v, signs, rows: int = BLOCK):
+    """Steps 1-3 for one head ([N, d] arrays): (q8, q scales, k8, k scales,
+    v8, v scale), the values on the E4M3 grid as fp64."""
+    q, k, v = _f64(q), _f64(k), _f64(v)
+    d = q.shape[-1]
+    T = rotation(signs) * np.sqrt(d)
+    q8, sq = quantize_rows(q @ T, rows)
+    k8, sk = quantize_rows(k @ T, rows)
+    sv = pow2_scale(float(np.abs(v).max()))
+    return q8, sq, k8, sk, e4m3_round(v / sv), sv
+
+
+def fp8_forward(q, k, v, scale: float, signs, causal: bool = False, rotate: bool = True, rows: int = BLOCK,
+                kv_len=None):
     """FP8 forward of [B, H, N, d] inputs. Returns (O, L) in fp64.
+
+    ``kv_len`` (optional, [B]) masks keys j >= kv_len[b] as in the dense
+    oracle; the quantisation of steps 1-3 still covers every row.
 
     ``rotate=False`` skips step 1 (plain block-quantised FP8), for comparing
     the error with and without the rotation."""
     q, k, v = _f64(q), _f64(k), _f64(v)
     B, H, N, d = q.shape
-    R = rotation(signs) if rotate else np.eye(d)
+    # sqrt(d) R = diag(s) H_d: the transform the GPU applies exactly in fp32
+    T = rotation(signs) * np.sqrt(d) if rotate else np.eye(d)
+    s_fold = scale / d if rotate else scale
     O = np.zeros((B, H, N, d))
     L = np.zeros((B, H, N))
-    vis = visible(N, causal)
+    kl = None if kv_len is None else np.asarray(kv_len.cpu() if hasattr(kv_len, "cpu") else kv_len)
     for b in range(B):
+        vis = visible(N, causal, None if kl is None else int(kl[b]))
         for h in range(H):
-            q8, sq = quantize_rows(q[b, h] @ R, rows)
-            k8, sk = quantize_rows(k[b, h] @ R, rows)
+            q8, sq = quantize_rows(q[b, h] @ T, rows)
+            k8, sk = quantize_rows(k[b, h] @ T, rows)
             sv = pow2_scale(float(np.abs(v[b, h]).max()))
             v8 = e4m3_round(v[b, h] / sv)
-            s = scale * (dequantize_rows(q8, sq, rows) @ dequantize_rows(k8, sk, rows).T)
+            s = s_fold * (dequantize_rows(q8, sq, rows) @ dequantize_rows(k8, sk, rows).T)
             s = np.where(vis, s, -np.inf)
             x = s * np.log2(np.e)
             xm = x.max(axis=1, keepdims=True)
             M = np.floor(xm)
+            seen = np.isfinite(xm[:, 0])
+            M = np.where(np.isfinite(M), M, 0.0)
+            xs = np.where(np.isfinite(xm), xm, 0.0)
             p8 = e4m3_round(np.exp2(x - M))
-            O[b, h] = (p8 @ (v8 * sv)) / p8.sum(axis=1, keepdims=True)
-            L[b, h] = (xm[:, 0] + np.log2(np.exp2(x - xm).sum(axis=1))) * np.log(2.0)
+            l8 = p8.sum(axis=1, keepdims=True)
+            O[b, h] = np.where(seen[:, None], (p8 @ (v8 * sv)) / np.where(l8 > 0, l8, 1.0), 0.0)
+            with np.errstate(divide="ignore"):
+                L[b, h] = np.where(seen, (xs[:, 0] + np.log2(np.exp2(x - xs).sum(axis=1))) * np.log(2.0), -np.inf)
     return O, L

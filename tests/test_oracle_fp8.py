@@ -122,3 +122,15 @@ def test_rotation_lowers_error_with_outlier_channels():
         e_plain = np.linalg.norm(F8.fp8_forward(q, k, v, scale, signs, rotate=False)[0] - O)
         ratios.append(e_plain / e_rot)
     assert np.median(ratios) > 1.5, ratios
+
+
+def test_key_padding_rows_and_empty_rows():
+    rng = np.random.default_rng(6)
+    B, H, N, d = 2, 1, 130, 16
+    q, k, v = (rng.standard_normal((B, H, N, d)) for _ in range(3))
+    signs = np.ones(d)
+    O, L = F8.fp8_forward(q, k, v, 0.25, signs, kv_len=np.array([1, 0]))
+    # one valid key: every row is that key's (quantised) value row
+    _, _, _, _, v8, sv = F8.quantized_inputs(q[0, 0], k[0, 0], v[0, 0], signs)
+    np.testing.assert_allclose(O[0, 0], np.broadcast_to(v8[0] * sv, O[0, 0].shape), atol=1e-14)
+    assert np.all(O[1] == 0) and np.all(np.isneginf(L[1]))
