@@ -34,13 +34,20 @@ silent:
 4. Scores. S = (scale_attn / d) * deq(Q8) deq(K8)^T with
    deq(x8) = x8 * scale (1/d undoes the sqrt(d) of step 1 on both sides;
    without the rotation it is 1), masked as in the dense oracle.
-5. Probabilities. With x = S log2(e) and M = floor(max_j x_j) per row,
-   p_j = 2^(x_j - M) in (0, 2) is rounded to E4M3 (p8_j). Quantising relative
-   to an integer exponent makes p8 independent of which power of two the
-   running maximum of an online (tiled) evaluation happens to use.
+5. Probabilities, online. With x = S log2(e), the keys are taken in tiles
+   of 128 in order (the tiling of "Online softmax"). Each row keeps an
+   integer reference exponent m: on the first tile with a visible key, and
+   whenever a tile's maximum exceeds m by more than 7, m becomes
+   floor(tile maximum) and the sums so far are multiplied by 2^(m_old - m)
+   (exact). The weights of a tile are p_j = 2^(x_j - m) (at most 2^8, inside
+   E4M3) rounded to E4M3 (p8_j). Because m is an integer, rounding
+   2^(x_j - m) is the same as rounding relative to any other integer
+   exponent, except for weights in E4M3's subnormal range (below 2^-6 of the
+   reference): there the result depends on m, which is why the procedure,
+   and not only the final maximum, is part of the definition.
 6. Output. O = sum_j p8_j deq(V8_j) / sum_j p8_j (a convex combination of
    the dequantised values), and L = logsumexp_j S_j (natural log) from the
-   unquantised probabilities.
+   unrounded weights.
 """
 
 from __future__ import annotations
@@ -50,7 +57,9 @@ import numpy as np
 from .attention import _f64, visible
 
 E4M3_MAX = 448.0
-BLOCK = 128
+BLOCK = 128           # rows per quantisation block of Q and K
+TILE_KEYS = 128       # keys per tile of the online softmax
+RESCALE_LOG2 = 7.0    # move the reference when a tile exceeds it by more than this
 
 
 def e4m3_round(x) -> np.ndarray:
@@ -149,14 +158,33 @@ def fp8_forward(q, k, v, scale: float, signs, causal: bool = False, rotate: bool
             s = s_fold * (dequantize_rows(q8, sq, rows) @ dequantize_rows(k8, sk, rows).T)
             s = np.where(vis, s, -np.inf)
             x = s * np.log2(np.e)
-            xm = x.max(axis=1, keepdims=True)
-            M = np.floor(xm)
-            seen = np.isfinite(xm[:, 0])
-            M = np.where(np.isfinite(M), M, 0.0)
-            xs = np.where(np.isfinite(xm), xm, 0.0)
-            p8 = e4m3_round(np.exp2(x - M))
-            l8 = p8.sum(axis=1, keepdims=True)
-            O[b, h] = np.where(seen[:, None], (p8 @ (v8 * sv)) / np.where(l8 > 0, l8, 1.0), 0.0)
+            vd = v8 * sv
+            m = np.full(N, -np.inf)    # integer reference exponent per row
+            l8 = np.zeros(N)           # sum of the rounded weights
+            lx = np.zeros(N)           # sum of the unrounded weights
+            o = np.zeros((N, d))
+            err = np.seterr(invalid="ignore")  # -inf - (-inf) on rows that have seen no key yet
+            for j0 in range(0, N, TILE_KEYS):
+                xt = x[:, j0:j0 + TILE_KEYS]
+                tmax = xt.max(axis=1)
+                first = np.isneginf(m)
+                upd = np.isfinite(tmax) & (first | (tmax - m > RESCALE_LOG2))
+                m_new = np.where(upd, np.floor(np.where(np.isfinite(tmax), tmax, 0.0)), m)
+                alpha = np.where(upd & ~first, np.exp2(np.where(upd & ~first, m - m_new, 0.0)), 1.0)
+                m = m_new
+                l8 *= alpha
+                lx *= alpha
+                o *= alpha[:, None]
+                mu = np.where(np.isfinite(m), m, 0.0)
+                pt = np.exp2(xt - mu[:, None])   # masked keys give 0
+                p8 = e4m3_round(pt)
+                l8 += p8.sum(axis=1)
+                lx += pt.sum(axis=1)
+                o += p8 @ vd[j0:j0 + TILE_KEYS]
+            np.seterr(**err)
+            seen = l8 > 0
+            O[b, h] = np.where(seen[:, None], o / np.where(seen, l8, 1.0)[:, None], 0.0)
             with np.errstate(divide="ignore"):
-                L[b, h] = np.where(seen, (xs[:, 0] + np.log2(np.exp2(x - xs).sum(axis=1))) * np.log(2.0), -np.inf)
+                L[b, h] = np.where(lx > 0, (np.where(np.isfinite(m), m, 0.0) + np.log2(np.where(lx > 0, lx, 1.0)))
+                                   * np.log(2.0), -np.inf)
     return O, L

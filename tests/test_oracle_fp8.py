@@ -134,3 +134,24 @@ def test_key_padding_rows_and_empty_rows():
     _, _, _, _, v8, sv = F8.quantized_inputs(q[0, 0], k[0, 0], v[0, 0], signs)
     np.testing.assert_allclose(O[0, 0], np.broadcast_to(v8[0] * sv, O[0, 0].shape), atol=1e-14)
     assert np.all(O[1] == 0) and np.all(np.isneginf(L[1]))
+
+
+def test_online_reference_matches_global_maximum_away_from_subnormals():
+    """Reading 5: with every weight far from E4M3's subnormal range (scores
+    spread by less than 5 in log2 units and no tile raising the maximum past
+    the threshold) the online rounding equals rounding relative to the
+    integer part of the row maximum."""
+    rng = np.random.default_rng(7)
+    B, H, N, d = 1, 1, 384, 16
+    q, k, v = (rng.standard_normal((B, H, N, d)) for _ in range(3))
+    scale = 0.05
+    O, L = F8.fp8_forward(q, k, v, scale, np.ones(d), rotate=False)
+    q8, sq = F8.quantize_rows(q[0, 0])
+    k8, sk = F8.quantize_rows(k[0, 0])
+    sv = F8.pow2_scale(float(np.abs(v[0, 0]).max()))
+    vd = F8.e4m3_round(v[0, 0] / sv) * sv
+    x = scale * (F8.dequantize_rows(q8, sq) @ F8.dequantize_rows(k8, sk).T) * np.log2(np.e)
+    assert (x.max(axis=1) - x.min(axis=1)).max() < 5.0
+    p8 = F8.e4m3_round(np.exp2(x - np.floor(x.max(axis=1, keepdims=True))))
+    np.testing.assert_allclose(O[0, 0], (p8 @ vd) / p8.sum(axis=1, keepdims=True), atol=1e-13)
+    np.testing.assert_allclose(L[0, 0], np.log(np.exp(x / np.log2(np.e)).sum(axis=1)), atol=1e-12)
