@@ -136,6 +136,7 @@ class ClockSampler:
 # headers); a recorded DRAM-traffic figure stays valid while they are unchanged
 KERNEL_SOURCES = {
     "fa_fwd_kernel": ["fa_fwd.cu"],
+    "fa_fwd_fp8_kernel": ["fa_fwd_fp8.cu", "fa_fp8.h"],
     "fa_bwd_kernel": ["fa_bwd.cu"],
     "fa_fwd_q1_kernel": ["fa_fwd_q1.cu"],
     "fa_decode_split_kernel": ["fa_decode.cu", "fa_decode.h"],
@@ -519,6 +520,65 @@ def run_packed(args, rank, world):
     print(json.dumps(line), flush=True)
 
 
+def run_fp8(args, rank, world):
+    """FP8 forward (rotation + block quantisation + attention) on a dense
+    workload's shape: one step = one fa_fwd_fp8 call (all five kernels)."""
+    import torch
+
+    import io_aware_exact_tiled_gb300 as fa
+    from io_aware_exact_tiled_gb300 import accounting as acc
+    from io_aware_exact_tiled_gb300 import workloads as W
+    base = args.workload[: -len("_fp8")]
+    w = W.WORKLOADS[base]
+    dev = torch.device("cuda", int(os.environ.get("LOCAL_RANK", "0")))
+    torch.cuda.set_device(dev)
+    fa.load()
+    x = W.make_inputs(w, seed=rank, device="cuda")
+    q, k, v = (t.to(dev) for t in (x.q, x.k, x.v))
+    signs = W.make_signs(w.d, seed=rank).to(dev)
+    B, H, N, d = q.shape
+    kl = None if x.kv_len is None else x.kv_len.to(dev)
+    o = torch.empty_like(q)
+    lse = torch.empty((B, H, N), dtype=torch.float32, device=dev)
+    ws = fa.workspace(fa.load().fa_fwd_fp8_workspace_size(B, H, N, d), dev)
+    fwd_flop, _ = acc.flops(B, H, N, d, x.causal, None if kl is None else x.kv_len.tolist(), None)
+    ev = lambda: torch.cuda.Event(enable_timing=True)
+
+    def step():
+        fa.forward_fp8(q, k, v, signs, scale=x.scale, causal=x.causal, kv_len=kl, out=o, lse=lse, ws=ws)
+        return fa.last_launch_count()
+
+    for _ in range(max(3, args.warmup)):
+        step()
+    torch.cuda.synchronize()
+    sampler = ClockSampler()
+    sampler.start()
+    wall0 = time.time()
+    ms, ker_ms, launches = _timed_loop(step, args.steps, ev, fa)
+    wall1 = time.time()
+    sampler.stop()
+    if fa.get_status(ws) != 0:
+        raise RuntimeError("device status word reports an error")
+    ms_step = ms / args.steps
+    peaks, src = load_peaks()
+    peak8 = 2.0 * float(peaks["bf16_tflops"])
+    ker_tf = fwd_flop / (ker_ms * 1e-3) / 1e12
+    line = {
+        "metric": "FP8 attention forward TFLOP/s (Hadamard rotation + block-quantised E4M3)",
+        "value": fwd_flop / (ms_step * 1e-3) / 1e12, "unit": "TFLOP/s", "n_gpus": 1, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "e4m3 (fp32 accumulate; bf16 in and out)", "data": "synthetic (seeded N(0,1))",
+        "config": {"workload": describe(w) + ", FP8 forward only"},
+        "attention_kernel": {"ms": ker_ms, "tflops": ker_tf},
+        "quantisation_ms": ms_step - ker_ms,
+        "roofline": {"bound": "tensor", "achieved": ker_tf, "peak": peak8, "unit": "TFLOP/s", "frac": ker_tf / peak8,
+                     "traffic": recorded_traffic("fa_fwd_fp8_kernel", args.workload), "kernel": "fa_fwd_fp8_kernel",
+                     "peak_source": f"{src} bf16 dense burst x 2 (nominal FP8 / BF16 ratio 4.5 / 2.25)"},
+        "cpu_baseline": None, "e2e": None, "gpu_launches": launches, "clocks": sampler.summary(wall0, wall1),
+    }
+    print(json.dumps(line), flush=True)
+
+
 # ------------------------------------------------------------------ our arm
 def main():
     args = parse()
@@ -534,6 +594,8 @@ def main():
         return run_decode(args, rank, world)
     if args.workload in W_.PACKED_WORKLOADS:
         return run_packed(args, rank, world)
+    if args.workload.endswith("_fp8") and args.workload[:-4] in W_.WORKLOADS:
+        return run_fp8(args, rank, world)
 
     import torch
     import torch.distributed as dist

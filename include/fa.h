@@ -155,6 +155,35 @@ fa_status fa_decode(const void* q, const void* k, const void* v, void* o, float*
                     size_t ws_bytes, void* stream);
 
 /*
+ * FP8 forward pass ("FlashAttention: making attention IO-aware", section
+ * "FlashAttention-3": FP8 doubles the tensor rate but is fragile with
+ * outliers, so Q and K are multiplied by a random orthogonal Hadamard matrix
+ * first and quantised per block). An approximation of attention:
+ *   1. Q' = Q diag(signs) H_128 and K' = K diag(signs) H_128 (Sylvester
+ *      Hadamard matrix; the 1/128 left in Q' K'^T joins the score scale);
+ *   2. each 128-row block of Q' and of K', and V (one block per head), is
+ *      divided by the power of two 2^ceil(log2(amax / 448)) and rounded to
+ *      E4M3 (nearest even, saturating);
+ *   3. S and O = softmax(S) V on the FP8 tensor cores; the weights are
+ *      rounded to E4M3 relative to an integer exponent, O is normalised by
+ *      the sum of the rounded weights and L comes from the unrounded ones.
+ *   q, k, v   in,  device, [B, H, N, 128] bf16
+ *   o         out, device, [B, H, N, 128] bf16
+ *   lse       out, device, float32 [B, H, N]
+ *   signs     in,  device, float32 [128], each +1 or -1 (drawn by the caller)
+ *   causal, kv_len  masks as for fa_fwd (no tile mask)
+ *   workspace fa_fwd_fp8_workspace_size(B, H, N, d) bytes: the quantised
+ *             Q, K and V^T and their scale exponents
+ * d = 128 and N a multiple of 128 only (FA_ERR_UNSUPPORTED otherwise). Runs
+ * five kernels: quantisation of Q, of K, V's maximum, V's quantisation, and
+ * the attention kernel.
+ */
+size_t fa_fwd_fp8_workspace_size(int B, int H, int N, int d);
+fa_status fa_fwd_fp8(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int N, int d,
+                     float scale, int causal, const int32_t* kv_len, const float* signs, void* workspace,
+                     size_t ws_bytes, void* stream);
+
+/*
  * Backward pass of a packed variable-length batch: the gradients of
  * <dO, O> for fa_fwd_varlen.
  *   q, k, v, o, dout  in,  device, [total, H, d] bf16

@@ -11,6 +11,7 @@ from .binding import (  # noqa: F401
     forward_varlen,
     backward_varlen,
     decode,
+    forward_fp8,
     fwd_workspace_size,
     bwd_workspace_size,
     get_status,

@@ -64,6 +64,10 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.fa_decode_workspace_size.restype = sz
     lib.fa_decode.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, f, vp, i, i, vp, sz, vp]
     lib.fa_decode.restype = i
+    lib.fa_fwd_fp8_workspace_size.argtypes = [i, i, i, i]
+    lib.fa_fwd_fp8_workspace_size.restype = sz
+    lib.fa_fwd_fp8.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, f, i, vp, vp, vp, sz, vp]
+    lib.fa_fwd_fp8.restype = i
     lib.fa_get_status.argtypes = [vp, vp]
     lib.fa_get_status.restype = i
     lib.fa_status_string.argtypes = [i]
@@ -220,6 +224,31 @@ def backward_varlen(q, k, v, o, lse, do, cu_seqlens, max_seqlen: int, scale: Opt
     if rc != FA_OK:
         raise FAError(rc, "fa_bwd_varlen")
     return dq, dk, dv
+
+
+def forward_fp8(q, k, v, signs, scale: Optional[float] = None, causal: bool = False, kv_len=None, out=None,
+                lse=None, ws=None, stream=None):
+    """O, L = fa_fwd_fp8(...): the FP8 forward pass with a Hadamard rotation
+    (signs: float32 [128] of +-1 on the device) and per-block scales. q, k, v:
+    [B, H, N, 128] bf16. Returns (o bf16, lse fp32 [B, H, N])."""
+    lib = load()
+    dtype = _check_qkv(q, k, v)
+    if dtype != FA_BF16:
+        raise ValueError("the FP8 path takes bfloat16 inputs")
+    B, H, N, d = q.shape
+    if signs.dtype != torch.float32 or signs.shape != (d,) or signs.device != q.device:
+        raise ValueError("signs must be a float32 [d] tensor on the same device")
+    scale = 1.0 / math.sqrt(d) if scale is None else float(scale)
+    o = torch.empty_like(q) if out is None else out
+    L = torch.empty((B, H, N), dtype=torch.float32, device=q.device) if lse is None else lse
+    if ws is None:
+        ws = workspace(lib.fa_fwd_fp8_workspace_size(B, H, N, d), q.device)
+    _, kl = _mask_ptrs(None, kv_len, q)
+    rc = lib.fa_fwd_fp8(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(L), B, H, N, d, scale, int(bool(causal)), kl,
+                        _ptr(signs), _ptr(ws), ws.numel(), _stream_handle(stream))
+    if rc != FA_OK:
+        raise FAError(rc, "fa_fwd_fp8")
+    return o, L
 
 
 def decode(q, k_cache, v_cache, cache_len=None, scale: Optional[float] = None, num_splits: int = 0, out=None,

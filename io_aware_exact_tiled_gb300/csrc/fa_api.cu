@@ -7,6 +7,7 @@
 
 #include "fa.h"
 #include "fa_decode.h"
+#include "fa_fp8.h"
 #include "fa_launch.h"
 
 namespace {
@@ -288,6 +289,67 @@ fa_status fa_decode(const void* q, const void* k, const void* v, void* o, float*
     if (cudaMemsetAsync(a.status, 0, sizeof(int) * 4, s) != cudaSuccess) return FA_ERR_CUDA;
     int n = 0;
     fa_status st = map_cuda(fa::launch_decode(a, s, &n));
+    if (st == FA_OK) g_last_launches = n;
+    return st;
+}
+
+size_t fa_fwd_fp8_workspace_size(int B, int H, int N, int d) {
+    if (B <= 0 || H <= 0 || N <= 0 || d <= 0) return 0;
+    const size_t bhn = static_cast<size_t>(B) * H * N, bh = static_cast<size_t>(B) * H;
+    const size_t tiles = bh * ((N + 127) / 128);
+    return kStatusBytes + 3 * align256(bhn * d) + 2 * align256(tiles * sizeof(int)) + 2 * align256(bh * sizeof(int));
+}
+
+fa_status fa_fwd_fp8(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int N, int d,
+                     float scale, int causal, const int32_t* kv_len, const float* signs, void* workspace,
+                     size_t ws_bytes, void* stream) {
+    if (!q || !k || !v || !o || !lse || !signs || !workspace) return FA_ERR_INVALID_ARG;
+    if (causal != 0 && causal != 1) return FA_ERR_INVALID_ARG;
+    fa_status st = check_shape(B, H, N, d, scale);
+    if (st != FA_OK) return st;
+    if (d != 128) return FA_ERR_UNSUPPORTED;
+    if (N / 128 > 65535) return FA_ERR_UNSUPPORTED;
+    if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(o, 16) || !aligned(lse, 4) ||
+        !aligned(signs, 4) || !aligned(workspace, 256) || (kv_len && !aligned(kv_len, 4)))
+        return FA_ERR_INVALID_ARG;
+    if (ws_bytes < fa_fwd_fp8_workspace_size(B, H, N, d)) return FA_ERR_INVALID_ARG;
+    const size_t bhn = static_cast<size_t>(B) * H * N, bh = static_cast<size_t>(B) * H;
+    const size_t tiles = bh * (N / 128);
+    char* ws = static_cast<char*>(workspace);
+    size_t off = kStatusBytes;
+    fa::Fp8Args a{};
+    a.q = q;
+    a.k = k;
+    a.v = v;
+    a.o = o;
+    a.lse = lse;
+    a.B = B;
+    a.H = H;
+    a.N = N;
+    a.scale = scale;
+    a.causal = causal;
+    a.kv_len = kv_len;
+    a.signs = signs;
+    a.status = reinterpret_cast<int*>(ws);
+    a.q8 = reinterpret_cast<uint8_t*>(ws + off);
+    off += align256(bhn * d);
+    a.k8 = reinterpret_cast<uint8_t*>(ws + off);
+    off += align256(bhn * d);
+    a.vt8 = reinterpret_cast<uint8_t*>(ws + off);
+    off += align256(bhn * d);
+    a.qexp = reinterpret_cast<int*>(ws + off);
+    off += align256(tiles * sizeof(int));
+    a.kexp = reinterpret_cast<int*>(ws + off);
+    off += align256(tiles * sizeof(int));
+    a.vexp = reinterpret_cast<int*>(ws + off);
+    off += align256(bh * sizeof(int));
+    a.vmax_bits = reinterpret_cast<int*>(ws + off);
+    a.ev_begin = g_ev_begin;
+    a.ev_end = g_ev_end;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (cudaMemsetAsync(a.status, 0, sizeof(int) * 4, s) != cudaSuccess) return FA_ERR_CUDA;
+    int n = 0;
+    st = map_cuda(fa::launch_fwd_fp8(a, s, &n));
     if (st == FA_OK) g_last_launches = n;
     return st;
 }

@@ -1,0 +1,591 @@
+// FP8 forward pass with block scales and a Hadamard rotation of Q and K.
+//
+// What it computes ("FlashAttention: making attention IO-aware", section
+// "FlashAttention-3", FP8 with incoherent processing: FP8 doubles the tensor
+// rate but is fragile with outliers, so Q and K are multiplied by a random
+// orthogonal Hadamard matrix first and every block is quantised with its own
+// scale):
+//   1. Q' = Q diag(s) H_d and K' = K diag(s) H_d (s random signs, H_d the
+//      Sylvester Hadamard matrix; diag(s) H_d / sqrt(d) is orthogonal, and
+//      the 1/d this leaves in Q' K'^T is folded into the score scale);
+//   2. every 128-row block of Q' and K' is divided by its own power-of-two
+//      scale 2^ceil(log2(amax / 448)) and rounded to E4M3 (nearest even,
+//      saturating), V likewise with one scale per head, stored transposed;
+//   3. S = scale / d * 2^(e_q + e_k) * (Q8 K8^T) on the tensor cores
+//      (kind::f8f6f4, fp32 accumulator in TMEM);
+//   4. online softmax with an integer reference exponent m: the weights
+//      p = 2^(x - m) (x = S log2 e) are rounded to E4M3 and stored four per
+//      TMEM column as the A operand of O += P8 V8; the row sum l of the fp32
+//      weights gives L = ln 2 (m + log2 l), the sum lw of the rounded weights
+//      normalises O = 2^e_v o / lw.
+// Because m is an integer and every scale a power of two, the rounded weights
+// do not depend on when the running maximum was last moved: rounding to E4M3
+// commutes with multiplication by powers of two (away from the subnormals).
+//
+// Kernels: fa_fp8_qk_kernel (rotate + quantise Q and K, one CTA per 128-row
+// block), fa_fp8_vmax_kernel and fa_fp8_v_kernel (per-head amax of V, then
+// quantise and transpose it), fa_fwd_fp8_kernel (attention; two 128-row query
+// tiles per CTA, warp 0 TMA, warp 1 MMA, two softmax warpgroups, as in the
+// bf16 kernel). d = 128.
+#include <math_constants.h>
+
+#include "fa_common.cuh"
+#include "fa_fp8.h"
+#include "tmap.h"
+
+namespace fa {
+
+constexpr int kD8 = 128;               // head dimension of the FP8 path
+constexpr float kE4M3Max = 448.0f;
+
+// Exponent e of the smallest power of two with amax / 2^e <= 448 (0 for 0).
+__device__ __forceinline__ int pow2_scale_exp(float amax) {
+    if (!(amax > 0.f)) return 0;
+    const float r = amax / kE4M3Max;
+    const int bits = __float_as_int(r);
+    int e = ((bits >> 23) & 0xFF) - 127;       // floor(log2 r) for normal r
+    if ((bits & 0x7FFFFF) != 0) e += 1;        // not a power of two: round up
+    if (((bits >> 23) & 0xFF) == 0) e = -126;  // subnormal ratio
+    return max(-126, min(127, e));
+}
+
+// ---------------------------------------------------------------------------
+// Q and K: one CTA per (128-row block, head). Each warp rotates 16 rows:
+// lane l holds columns 4l .. 4l+3; the Walsh-Hadamard butterflies with
+// strides 1 and 2 stay in the lane, strides 4 .. 64 use shuffles. The
+// butterflies only add and subtract bf16 values, which fp32 holds exactly.
+// ---------------------------------------------------------------------------
+__global__ void __launch_bounds__(256) fa_fp8_qk_kernel(const uint16_t* __restrict__ x, const float* __restrict__ signs,
+                                                        uint8_t* __restrict__ x8, int* __restrict__ exps, int N) {
+    constexpr int RPW = kTile / 8;  // rows per warp, kept in registers until the block scale is known
+    __shared__ float wmax[8];
+    __shared__ int e_sh;
+    const int blk = blockIdx.x, bh = blockIdx.y;
+    const int T = N / kTile;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const size_t row0 = static_cast<size_t>(bh) * N + static_cast<size_t>(blk) * kTile;
+    float sg[4];
+#pragma unroll
+    for (int t = 0; t < 4; ++t) sg[t] = signs[lane * 4 + t];
+    float amax = 0.f;
+    float y[RPW][4];
+#pragma unroll
+    for (int j = 0; j < RPW; ++j) {
+        const int rr = warp + 8 * j;
+        const uint2 w = *reinterpret_cast<const uint2*>(x + (row0 + rr) * kD8 + lane * 4);
+        float a[4] = {__uint_as_float(w.x << 16) * sg[0], __uint_as_float(w.x & 0xFFFF0000u) * sg[1],
+                      __uint_as_float(w.y << 16) * sg[2], __uint_as_float(w.y & 0xFFFF0000u) * sg[3]};
+        // in-lane strides 1 and 2
+        float b0 = a[0] + a[1], b1 = a[0] - a[1], b2 = a[2] + a[3], b3 = a[2] - a[3];
+        a[0] = b0 + b2;
+        a[1] = b1 + b3;
+        a[2] = b0 - b2;
+        a[3] = b1 - b3;
+        // strides 4 .. 64: partner lane l ^ (stride / 4)
+#pragma unroll
+        for (int m = 1; m < 32; m <<= 1) {
+            const bool upper = (lane & m) != 0;
+#pragma unroll
+            for (int t = 0; t < 4; ++t) {
+                const float o = __shfl_xor_sync(0xffffffffu, a[t], m);
+                a[t] = upper ? o - a[t] : a[t] + o;
+            }
+        }
+#pragma unroll
+        for (int t = 0; t < 4; ++t) {
+            y[j][t] = a[t];
+            amax = fmaxf(amax, fabsf(a[t]));
+        }
+    }
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, off));
+    if (lane == 0) wmax[warp] = amax;
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        float m = 0.f;
+        for (int w = 0; w < 8; ++w) m = fmaxf(m, wmax[w]);
+        const int e = pow2_scale_exp(m);
+        e_sh = e;
+        exps[static_cast<size_t>(bh) * T + blk] = e;
+    }
+    __syncthreads();
+    const float inv = exp2i(-e_sh);
+#pragma unroll
+    for (int j = 0; j < RPW; ++j) {
+        const int rr = warp + 8 * j;
+        const uint32_t lo = pack_e4m3x2(y[j][0] * inv, y[j][1] * inv), hi = pack_e4m3x2(y[j][2] * inv, y[j][3] * inv);
+        *reinterpret_cast<uint32_t*>(x8 + (row0 + rr) * kD8 + lane * 4) = lo | (hi << 16);
+    }
+}
+
+// Per-head max |v| (as float bits; nonnegative floats order like integers).
+__global__ void __launch_bounds__(256) fa_fp8_vmax_kernel(const uint16_t* __restrict__ v, int* __restrict__ vmax_bits,
+                                                          long long per_head) {
+    const int bh = blockIdx.y;
+    const uint4* src = reinterpret_cast<const uint4*>(v + static_cast<size_t>(bh) * per_head);
+    const long long n8 = per_head / 8;
+    float m = 0.f;
+    for (long long i = static_cast<long long>(blockIdx.x) * 256 + threadIdx.x; i < n8;
+         i += static_cast<long long>(gridDim.x) * 256) {
+        const uint4 w = src[i];
+        const uint32_t u[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+        for (int e = 0; e < 4; ++e)
+            m = fmaxf(m, fmaxf(fabsf(__uint_as_float(u[e] << 16)), fabsf(__uint_as_float(u[e] & 0xFFFF0000u))));
+    }
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, off));
+    if ((threadIdx.x & 31) == 0) atomicMax(vmax_bits + bh, __float_as_int(m));
+}
+
+// V -> E4M3 with the head's scale, transposed to [d][keys] (the P V product
+// needs K-major operands): one CTA per (128-key block, head).
+__global__ void __launch_bounds__(256) fa_fp8_v_kernel(const uint16_t* __restrict__ v,
+                                                       const int* __restrict__ vmax_bits, uint8_t* __restrict__ vt8,
+                                                       int* __restrict__ vexp, int N) {
+    __shared__ uint8_t t8[kD8][kTile + 16];
+    const int blk = blockIdx.x, bh = blockIdx.y;
+    const int e = pow2_scale_exp(__int_as_float(vmax_bits[bh]));
+    if (blk == 0 && threadIdx.x == 0) vexp[bh] = e;
+    const float inv = exp2i(-e);
+    const size_t row0 = static_cast<size_t>(bh) * N + static_cast<size_t>(blk) * kTile;
+    // thread: key kk = threadIdx.x / 2, 64 columns starting at 64 * (threadIdx.x & 1)
+    const int kk = threadIdx.x >> 1, c0 = (threadIdx.x & 1) * 64;
+    const uint16_t* src = v + (row0 + kk) * kD8 + c0;
+#pragma unroll
+    for (int c = 0; c < 64; c += 8) {
+        const uint4 w = *reinterpret_cast<const uint4*>(src + c);
+        const uint32_t u[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+        for (int e2 = 0; e2 < 4; ++e2) {
+            const uint32_t b = pack_e4m3x2(__uint_as_float(u[e2] << 16) * inv, __uint_as_float(u[e2] & 0xFFFF0000u) * inv);
+            t8[c0 + c + 2 * e2][kk] = static_cast<uint8_t>(b & 0xFF);
+            t8[c0 + c + 2 * e2 + 1][kk] = static_cast<uint8_t>(b >> 8);
+        }
+    }
+    __syncthreads();
+    // rows of V^T: [bh * d + dd][blk * 128 .. + 127]
+    for (int i = threadIdx.x; i < kD8 * 8; i += 256) {
+        const int dd = i >> 3, part = i & 7;
+        const uint32_t* s4 = reinterpret_cast<const uint32_t*>(&t8[dd][part * 16]);
+        uint4 w = make_uint4(s4[0], s4[1], s4[2], s4[3]);
+        *reinterpret_cast<uint4*>(vt8 + (static_cast<size_t>(bh) * kD8 + dd) * N + static_cast<size_t>(blk) * kTile +
+                                  part * 16) = w;
+    }
+}
+
+// ---------------------------------------------------------------------------
+// Attention kernel
+// ---------------------------------------------------------------------------
+struct Fp8Cfg {
+    static constexpr int TILE_BYTES = kTile * kD8;   // 128 rows x 128 bytes
+    static constexpr int KSTAGES = 5, VSTAGES = 4;
+    static constexpr int Q_OFF = 0;
+    static constexpr int K_OFF = Q_OFF + 2 * TILE_BYTES;
+    static constexpr int V_OFF = K_OFF + KSTAGES * TILE_BYTES;
+    static constexpr int BAR_OFF = V_OFF + VSTAGES * TILE_BYTES;
+    static constexpr int SMEM = BAR_OFF + 512 + 1024;
+    static constexpr int THREADS = 384;
+    static constexpr uint32_t ID_S = idesc_make(128, 128, kFmtE4M3, false, false);
+    static constexpr uint32_t ID_PV = idesc_make(128, kD8, kFmtE4M3, false, false);
+    static_assert((1 + 2 * KSTAGES + 2 * VSTAGES + 7) * 8 + 8 <= 512, "barrier area");
+    static_assert(SMEM <= 232448, "shared memory budget");
+};
+
+struct Fp8Params {
+    int B, H, N;
+    float c2;  // scale * log2(e) / d
+    MaskArgs mask;
+    const int* qexp;  // [B*H*T] block scale exponents of Q
+    const int* kexp;  // [B*H*T]
+    const int* vexp;  // [B*H]
+    void* o;
+    float* lse;
+    int* status;
+};
+
+constexpr float kFp8Rescale = 7.0f;  // log2 units: keeps every weight <= 2^7, inside E4M3
+
+struct Fp8Mma {
+    int pend_stage[2] = {-1, -1};
+    uint32_t pend_ph[2] = {0, 0};
+    int pend_u[2] = {0, 0};
+    int nP[2] = {0, 0};
+    int nPV[2] = {0, 0};
+    uint32_t rem = 0;
+};
+
+__device__ __forceinline__ bool fp8_issue_pv(uint32_t leader, int s, Fp8Mma& st, uint32_t tm, uint64_t dV0,
+                                             uint64_t* p_full, uint64_t* v_full, uint64_t* kv_empty,
+                                             const WaitCtx& cx) {
+    using C = Fp8Cfg;
+    const int ps = st.pend_stage[s];
+    if (!mbar_wait_warp(&p_full[s], st.nP[s] & 1, cx, 3)) return false;
+    ++st.nP[s];
+    if (!mbar_wait_warp(&v_full[ps], st.pend_ph[s], cx, 4)) return false;
+    tc_fence_after();
+    const uint64_t vst = sdesc_advance(dV0, ps * C::TILE_BYTES);
+#pragma unroll
+    for (int kk = 0; kk < 4; ++kk)  // 32 keys (8 TMEM columns of P8) per instruction
+        umma_ts_f8(leader, tm + s * 256 + 128, tm + s * 256 + kk * 8, sdesc_advance(vst, kk * 32), C::ID_PV,
+                   (st.nPV[s] > 0 || kk > 0) ? 1u : 0u);
+    ++st.nPV[s];
+    uint32_t r = (st.rem >> (2 * ps)) & 3u;
+    r -= 1;
+    st.rem = (st.rem & ~(3u << (2 * ps))) | (r << (2 * ps));
+    if (r == 0) umma_commit(leader, &kv_empty[ps]);
+    st.pend_stage[s] = -1;
+    return true;
+}
+
+__global__ void __launch_bounds__(384, 1)
+    fa_fwd_fp8_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
+                      const __grid_constant__ CUtensorMap tmVt, const __grid_constant__ Fp8Params p) {
+    using C = Fp8Cfg;
+    extern __shared__ __align__(1024) uint8_t smem_raw[];
+    uint8_t* sm = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
+    uint64_t* bars = reinterpret_cast<uint64_t*>(sm + C::BAR_OFF);
+    uint64_t* bar_q = bars + 0;
+    uint64_t* k_full = bars + 1;
+    uint64_t* k_empty = k_full + C::KSTAGES;
+    uint64_t* v_full = k_empty + C::KSTAGES;
+    uint64_t* kv_empty = v_full + C::VSTAGES;
+    uint64_t* s_full = kv_empty + C::VSTAGES;  // [2]
+    uint64_t* p_full = s_full + 2;             // [2]
+    uint64_t* o_done = p_full + 2;             // [2]
+    uint64_t* drain = o_done + 2;
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+    const WaitCtx cx{abort_flag, p.status};
+
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int h = blockIdx.x, b = blockIdx.y;
+    const int T = p.mask.T;
+    const int npairs = (T + 1) >> 1;
+    const int qp = npairs - 1 - static_cast<int>(blockIdx.z);
+    const int qb0 = 2 * qp, qb1 = 2 * qp + 1;
+    const bool act1 = qb1 < T;
+    const int N = p.N;
+    const int bh = b * p.H + h;
+    const int kvalid = keys_valid(p.mask, b, N);
+    int hi = T;
+    if (p.mask.causal) hi = min(hi, (act1 ? qb1 : qb0) + 1);
+    hi = min(hi, (kvalid + kTile - 1) / kTile);
+
+    if (tid == 0) {
+        *abort_flag = 0;
+        mbar_init(bar_q, 1);
+        for (int i = 0; i < C::KSTAGES; ++i) {
+            mbar_init(&k_full[i], 1);
+            mbar_init(&k_empty[i], 1);
+        }
+        for (int i = 0; i < C::VSTAGES; ++i) {
+            mbar_init(&v_full[i], 1);
+            mbar_init(&kv_empty[i], 1);
+        }
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(&s_full[i], 1);
+            mbar_init(&p_full[i], 128);
+            mbar_init(&o_done[i], 1);
+        }
+        mbar_init(drain, 1);
+        fence_barrier_init();
+    }
+    if (warp == 0 && lane == 0) {
+        tma_prefetch_desc(&tmQ);
+        tma_prefetch_desc(&tmK);
+        tma_prefetch_desc(&tmVt);
+    }
+    if (warp == 1) {
+        tmem_alloc(tmem_slot, 512);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tm = *tmem_slot;
+    const MaskArgs mk = p.mask;
+    auto need_of = [=](int t) -> uint32_t {
+        uint32_t nd = tile_visible(mk, qb0, t, kvalid) ? 1u : 0u;
+        if (act1 && tile_visible(mk, qb1, t, kvalid)) nd |= 2u;
+        return nd;
+    };
+
+    if (warp == 0) {
+        // ------------------------------------------------------------ producer
+        if (lane == 0) {
+            mbar_arrive_expect_tx(bar_q, (act1 ? 2 : 1) * C::TILE_BYTES);
+            for (int s = 0; s < (act1 ? 2 : 1); ++s)
+                tma_load_2d(sm + C::Q_OFF + s * C::TILE_BYTES, &tmQ, 0, bh * N + (qb0 + s) * kTile, bar_q);
+            int nk = 0, nv = 0;
+            for (int t = 0; t < hi; ++t) {
+                if (!need_of(t)) continue;
+                const int kst = nk % C::KSTAGES;
+                if (!mbar_wait(&k_empty[kst], ((nk / C::KSTAGES) & 1) ^ 1, cx, 1)) break;
+                mbar_arrive_expect_tx(&k_full[kst], C::TILE_BYTES);
+                tma_load_2d(sm + C::K_OFF + kst * C::TILE_BYTES, &tmK, 0, bh * N + t * kTile, &k_full[kst]);
+                ++nk;
+                const int vst = nv % C::VSTAGES;
+                if (!mbar_wait(&kv_empty[vst], ((nv / C::VSTAGES) & 1) ^ 1, cx, 9)) break;
+                mbar_arrive_expect_tx(&v_full[vst], C::TILE_BYTES);
+                // V^T [d][keys]: 128 rows of d, 128 keys of this tile
+                tma_load_2d(sm + C::V_OFF + vst * C::TILE_BYTES, &tmVt, t * kTile, bh * kD8, &v_full[vst]);
+                ++nv;
+            }
+            mbar_wait_teardown(bar_q, 0, 200000000ull);
+            for (int i = 0; i < C::KSTAGES && i < nk; ++i) {
+                const int last = i + ((nk - 1 - i) / C::KSTAGES) * C::KSTAGES;
+                mbar_wait_teardown(&k_full[i], (last / C::KSTAGES) & 1, 200000000ull);
+            }
+            for (int i = 0; i < C::VSTAGES && i < nv; ++i) {
+                const int last = i + ((nv - 1 - i) / C::VSTAGES) * C::VSTAGES;
+                mbar_wait_teardown(&v_full[i], (last / C::VSTAGES) & 1, 200000000ull);
+            }
+        }
+    } else if (warp == 1) {
+        // ------------------------------------------------------------ MMA issuer (whole warp, one lane issues)
+        const uint32_t leader = elect_one_sync();
+        bool ok = mbar_wait_warp(bar_q, 0, cx, 2);
+        if (ok) tc_fence_after();
+        Fp8Mma st;
+        const uint64_t dQ0 = sdesc_sw128(smem_u32(sm + C::Q_OFF), 16, 1024);
+        const uint64_t dK0 = sdesc_sw128(smem_u32(sm + C::K_OFF), 16, 1024);
+        const uint64_t dV0 = sdesc_sw128(smem_u32(sm + C::V_OFF), 16, 1024);
+#define issue_pv8(S) fp8_issue_pv(leader, (S), st, tm, dV0, p_full, v_full, kv_empty, cx)
+        int u = 0;
+        for (int t = 0; ok && t < hi; ++t) {
+            const uint32_t nd = need_of(t);
+            if (!nd) continue;
+            const int kst = u % C::KSTAGES;
+            const int vst = u % C::VSTAGES;
+            const uint32_t vph = (u / C::VSTAGES) & 1;
+            // a P V still pending for a tile as old as u - VSTAGES holds the V
+            // stage (and its reader count) that tile u reuses: issue it first
+#pragma unroll
+            for (int s = 0; s < 2; ++s)
+                if (ok && st.pend_stage[s] >= 0 && st.pend_u[s] <= u - C::VSTAGES && !issue_pv8(s)) ok = false;
+            if (!ok) break;
+            if (!mbar_wait_warp(&k_full[kst], (u / C::KSTAGES) & 1, cx, 5)) { ok = false; break; }
+            tc_fence_after();
+            st.rem = (st.rem & ~(3u << (2 * vst))) | ((uint32_t)__popc(nd) << (2 * vst));
+#pragma unroll
+            for (int s = 0; s < 2; ++s) {
+                if (!(nd & (1u << s))) continue;
+                if (st.pend_stage[s] >= 0 && !issue_pv8(s)) { ok = false; break; }
+                const uint64_t qs = sdesc_advance(dQ0, s * C::TILE_BYTES);
+                const uint64_t ks = sdesc_advance(dK0, kst * C::TILE_BYTES);
+#pragma unroll
+                for (int kk = 0; kk < kD8 / 32; ++kk)  // 32 bytes of K per instruction
+                    umma_ss_f8(leader, tm + s * 256, sdesc_advance(qs, kk * 32), sdesc_advance(ks, kk * 32), C::ID_S,
+                               kk > 0 ? 1u : 0u);
+                umma_commit(leader, &s_full[s]);
+                st.pend_stage[s] = vst;
+                st.pend_ph[s] = vph;
+                st.pend_u[s] = u;
+            }
+            if (!ok) break;
+            umma_commit(leader, &k_empty[kst]);
+            ++u;
+        }
+        for (int s = 0; ok && s < 2; ++s)
+            if (st.pend_stage[s] >= 0 && !issue_pv8(s)) ok = false;
+#undef issue_pv8
+        if (ok) {
+            umma_commit(leader, &o_done[0]);
+            umma_commit(leader, &o_done[1]);
+        }
+        umma_commit(leader, drain);
+        mbar_wait_teardown(drain, 0, 200000000ull);
+    } else if (warp >= 4) {
+        // ------------------------------------------------------------ softmax (thread = query row)
+        const int s = (warp - 4) >> 2;
+        const int wq = warp & 3;
+        const int r = wq * 32 + lane;
+        const bool active = (s == 0) || act1;
+        const int qb = s == 0 ? qb0 : qb1;
+        const int grow = qb * kTile + r;
+        const uint32_t tl = tm + (static_cast<uint32_t>(wq * 32) << 16) + s * 256;
+        const int T_ = p.mask.T;
+        const int eq = p.qexp[static_cast<size_t>(bh) * T_ + min(qb, T_ - 1)];
+        // m: integer reference exponent (log2 units); l: fp32 weights; lw: E4M3 weights
+        float m_hat = -CUDART_INF_F, l = 0.f, lw = 0.f;
+        int n = 0;
+        bool ok = true;
+        if (active) {
+            for (int t = 0; t < hi; ++t) {
+                const uint32_t nd = need_of(t);
+                if (!(nd & (1u << s))) continue;
+                const float c2t = p.c2 * exp2i(eq + p.kexp[static_cast<size_t>(bh) * T_ + t]);
+                ok = mbar_wait(&s_full[s], n & 1, cx, 6);
+                ok = __all_sync(0xffffffffu, ok);
+                if (!ok) break;
+                tc_fence_after();
+                uint32_t sr[4][32];
+#pragma unroll
+                for (int c = 0; c < 4; ++c) tmem_ld32(tl + c * 32, sr[c]);
+#pragma unroll
+                for (int c = 0; c < 4; ++c) tmem_ld_wait(sr[c]);
+                if (tile_partial(p.mask, qb, t, kvalid)) {
+                    const int lim = min(kvalid - t * kTile, p.mask.causal && t == qb ? r + 1 : kTile);
+#pragma unroll
+                    for (int c = 0; c < 4; ++c)
+#pragma unroll
+                        for (int i = 0; i < 32; ++i)
+                            if (c * 32 + i >= lim) sr[c][i] = __float_as_uint(-CUDART_INF_F);
+                }
+                float mx = -CUDART_INF_F;
+#pragma unroll
+                for (int c = 0; c < 4; ++c)
+#pragma unroll
+                    for (int i = 0; i < 32; i += 2)
+                        mx = fmax3(mx, __uint_as_float(sr[c][i]), __uint_as_float(sr[c][i + 1]));
+                const float xmax = mx * c2t;
+                float alpha = 1.f;
+                bool resc = false;
+                if (xmax > -CUDART_INF_F && (m_hat == -CUDART_INF_F || xmax - m_hat > kFp8Rescale)) {
+                    const float m_new = floorf(xmax);
+                    const float dm = m_hat - m_new;  // an integer <= 0
+                    alpha = (m_hat == -CUDART_INF_F || dm < -126.f) ? 0.f : exp2i(static_cast<int>(dm));
+                    m_hat = m_new;
+                    l *= alpha;
+                    lw *= alpha;
+                    resc = true;
+                }
+                const float mu = (m_hat == -CUDART_INF_F) ? 0.f : m_hat;
+                const uint64_t cc = f2_make(c2t, c2t), nmu2 = f2_make(-mu, -mu);
+                uint64_t rs2 = 0ull, rr2 = 0ull;
+                uint32_t pk[32];  // 128 keys, four E4M3 weights per word
+#pragma unroll
+                for (int c = 0; c < 4; ++c)
+#pragma unroll
+                    for (int i = 0; i < 8; ++i) {
+                        float x0, x1, x2, x3;
+                        f2_split(f2_fma(f2_make(__uint_as_float(sr[c][4 * i]), __uint_as_float(sr[c][4 * i + 1])), cc,
+                                        nmu2), x0, x1);
+                        f2_split(f2_fma(f2_make(__uint_as_float(sr[c][4 * i + 2]), __uint_as_float(sr[c][4 * i + 3])),
+                                        cc, nmu2), x2, x3);
+                        const float p0 = ex2_approx(x0), p1 = ex2_approx(x1), p2 = ex2_approx(x2), p3 = ex2_approx(x3);
+                        rs2 = f2_add(rs2, f2_add(f2_make(p0, p1), f2_make(p2, p3)));
+                        const uint32_t lo = pack_e4m3x2(p0, p1), hi2 = pack_e4m3x2(p2, p3);
+                        pk[c * 8 + i] = lo | (hi2 << 16);
+                        rr2 = f2_add(rr2, f2_add(f2_from_e4m3x2(lo), f2_from_e4m3x2(hi2)));
+                    }
+                tmem_st32(tl, pk);
+                {
+                    float a_, b_;
+                    f2_split(rs2, a_, b_);
+                    l += a_ + b_;
+                    f2_split(rr2, a_, b_);
+                    lw += a_ + b_;
+                }
+                tmem_st_wait();
+                if (__any_sync(0xffffffffu, resc) && n > 0) {
+                    // O holds the previous tiles' sum (their P V was issued
+                    // before this tile's S): bring it to the new reference
+#pragma unroll
+                    for (int c = 0; c < kD8 / 32; ++c) {
+                        uint32_t ov[32];
+                        tmem_ld32(tl + 128 + c * 32, ov);
+                        tmem_ld_wait(ov);
+#pragma unroll
+                        for (int i = 0; i < 32; ++i) ov[i] = __float_as_uint(__uint_as_float(ov[i]) * alpha);
+                        tmem_st32(tl + 128 + c * 32, ov);
+                    }
+                    tmem_st_wait();
+                }
+                tc_fence_before();
+                if (!FA_DROP_THIS_ARRIVE(n == 0)) mbar_arrive(&p_full[s]);
+                ++n;
+            }
+            // ------------------------------------------------------------ epilogue
+            if (ok && n > 0) {
+                ok = __all_sync(0xffffffffu, mbar_wait(&o_done[s], 0, cx, 8));
+                if (ok) tc_fence_after();
+            }
+            if (ok) {
+                const float inv = lw > 0.f ? exp2i(p.vexp[bh]) / lw : 0.f;
+                const size_t orow = (static_cast<size_t>(bh) * N + grow) * kD8;
+#pragma unroll
+                for (int c = 0; c < kD8 / 32; ++c) {
+                    uint32_t ov[32];
+                    if (n > 0) {
+                        tmem_ld32(tl + 128 + c * 32, ov);
+                        tmem_ld_wait(ov);
+                    } else {
+#pragma unroll
+                        for (int i = 0; i < 32; ++i) ov[i] = 0u;
+                    }
+                    uint4* dst = reinterpret_cast<uint4*>(static_cast<uint16_t*>(p.o) + orow + c * 32);
+#pragma unroll
+                    for (int j = 0; j < 4; ++j) {
+                        uint4 w;
+                        w.x = pack_bf16x2(__uint_as_float(ov[8 * j + 0]) * inv, __uint_as_float(ov[8 * j + 1]) * inv);
+                        w.y = pack_bf16x2(__uint_as_float(ov[8 * j + 2]) * inv, __uint_as_float(ov[8 * j + 3]) * inv);
+                        w.z = pack_bf16x2(__uint_as_float(ov[8 * j + 4]) * inv, __uint_as_float(ov[8 * j + 5]) * inv);
+                        w.w = pack_bf16x2(__uint_as_float(ov[8 * j + 6]) * inv, __uint_as_float(ov[8 * j + 7]) * inv);
+                        dst[j] = w;
+                    }
+                }
+                p.lse[static_cast<size_t>(bh) * N + grow] =
+                    l > 0.f ? (m_hat + log2f(l)) * 0.69314718055994530942f : -CUDART_INF_F;
+            }
+        }
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        tc_fence_after();
+        tmem_dealloc(tm, 512);
+    }
+}
+
+cudaError_t launch_fwd_fp8(const Fp8Args& a, cudaStream_t stream, int* nlaunch) {
+    using C = Fp8Cfg;
+    const int T = a.N / kTile;
+    const int BH = a.B * a.H;
+    const uint64_t rows = static_cast<uint64_t>(BH) * a.N;
+    // quantisation
+    fa_fp8_qk_kernel<<<dim3(T, BH), 256, 0, stream>>>(static_cast<const uint16_t*>(a.q), a.signs, a.q8, a.qexp, a.N);
+    fa_fp8_qk_kernel<<<dim3(T, BH), 256, 0, stream>>>(static_cast<const uint16_t*>(a.k), a.signs, a.k8, a.kexp, a.N);
+    cudaError_t e = cudaMemsetAsync(a.vmax_bits, 0, sizeof(int) * BH, stream);
+    if (e != cudaSuccess) return e;
+    const long long per_head = static_cast<long long>(a.N) * kD8;
+    const int chunks = static_cast<int>(min(64LL, (per_head / 8 + 255) / 256));
+    fa_fp8_vmax_kernel<<<dim3(chunks, BH), 256, 0, stream>>>(static_cast<const uint16_t*>(a.v), a.vmax_bits, per_head);
+    fa_fp8_v_kernel<<<dim3(T, BH), 256, 0, stream>>>(static_cast<const uint16_t*>(a.v), a.vmax_bits, a.vt8, a.vexp,
+                                                      a.N);
+    CUtensorMap tq, tk, tv;
+    if (!make_tmap_2d_sw128(&tq, a.q8, rows, kD8, 1, kTile, 128) ||
+        !make_tmap_2d_sw128(&tk, a.k8, rows, kD8, 1, kTile, 128) ||
+        !make_tmap_2d_sw128(&tv, a.vt8, static_cast<uint64_t>(BH) * kD8, a.N, 1, kD8, 128))
+        return cudaErrorInvalidValue;
+    static bool attr_set = false;
+    if (!attr_set) {
+        e = cudaFuncSetAttribute(fa_fwd_fp8_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
+        if (e != cudaSuccess) return e;
+        attr_set = true;
+    }
+    Fp8Params p;
+    p.B = a.B;
+    p.H = a.H;
+    p.N = a.N;
+    p.c2 = a.scale * 1.4426950408889634f / static_cast<float>(kD8);
+    p.mask.blockmask = nullptr;
+    p.mask.kv_len = a.kv_len;
+    p.mask.causal = a.causal;
+    p.mask.T = T;
+    p.qexp = a.qexp;
+    p.kexp = a.kexp;
+    p.vexp = a.vexp;
+    p.o = a.o;
+    p.lse = a.lse;
+    p.status = a.status;
+    dim3 grid(a.H, a.B, (T + 1) / 2);
+    if (a.ev_begin) cudaEventRecord(a.ev_begin, stream);
+    fa_fwd_fp8_kernel<<<grid, C::THREADS, C::SMEM, stream>>>(tq, tk, tv, p);
+    if (a.ev_end) cudaEventRecord(a.ev_end, stream);
+    *nlaunch = 5;
+    return cudaGetLastError();
+}
+
+}  // namespace fa

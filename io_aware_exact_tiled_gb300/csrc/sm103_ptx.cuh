@@ -372,6 +372,51 @@ __device__ __forceinline__ void umma_ts(uint32_t leader, uint32_t d_tmem, uint32
     }
 }
 
+// FP8 (kind::f8f6f4) products, E4M3 operands, fp32 accumulator.
+// D[tmem] (+)= A[smem] * B[smem]
+__device__ __forceinline__ void umma_ss_f8(uint32_t leader, uint32_t d_tmem, uint64_t adesc, uint64_t bdesc,
+                                           uint32_t idesc, uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p, e;\n\tsetp.ne.b32 p, %4, 0;\n\tsetp.ne.b32 e, %5, 0;\n\t"
+        "@e tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate), "r"(leader)
+        : "memory");
+}
+// D[tmem] (+)= A[tmem] * B[smem]; A holds four E4M3 values per 32-bit column
+__device__ __forceinline__ void umma_ts_f8(uint32_t leader, uint32_t d_tmem, uint32_t a_tmem, uint64_t bdesc,
+                                           uint32_t idesc, uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p, e;\n\tsetp.ne.b32 p, %4, 0;\n\tsetp.ne.b32 e, %5, 0;\n\t"
+        "@e tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "r"(a_tmem), "l"(bdesc), "r"(idesc), "r"(accumulate), "r"(leader)
+        : "memory");
+}
+constexpr uint32_t kFmtE4M3 = 0;  // kind::f8f6f4 operand format code
+
+// Two fp32 values to E4M3 (round to nearest even, saturating at +-448):
+// lo in the low byte, hi in the high byte.
+__device__ __forceinline__ uint32_t pack_e4m3x2(float lo, float hi) {
+    uint16_t r;
+    asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(r) : "f"(hi), "f"(lo));
+    return r;
+}
+// Two E4M3 values (low byte first) back to an fp32 pair (exact).
+__device__ __forceinline__ uint64_t f2_from_e4m3x2(uint32_t x) {
+    uint64_t r;
+    asm("{\n\t.reg .b32 t;\n\t.reg .b16 h0, h1, x16;\n\t.reg .f32 f0, f1;\n\t"
+        "cvt.u16.u32 x16, %1;\n\t"
+        "cvt.rn.f16x2.e4m3x2 t, x16;\n\t"
+        "mov.b32 {h0, h1}, t;\n\t"
+        "cvt.f32.f16 f0, h0;\n\t"
+        "cvt.f32.f16 f1, h1;\n\t"
+        "mov.b64 %0, {f0, f1};\n\t}"
+        : "=l"(r)
+        : "r"(x));
+    return r;
+}
+// 2^n for an integer n in [-126, 127], exactly.
+__device__ __forceinline__ float exp2i(int n) { return __int_as_float((127 + n) << 23); }
+
 // Arrive once on `bar` when every tcgen05.mma issued so far by the leader
 // lane has completed.
 __device__ __forceinline__ void umma_commit(uint32_t leader, uint64_t* bar) {

@@ -33,8 +33,9 @@ inline bool make_tmap_2d_sw128(CUtensorMap* map, const void* base, uint64_t rows
                                uint32_t box_rows, uint32_t box_cols) {
     EncodeTiledFn fn = encode_tiled_fn();
     if (!fn) return false;
-    CUtensorMapDataType dt =
-        elem_bytes == 2 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT32;
+    CUtensorMapDataType dt = elem_bytes == 1   ? CU_TENSOR_MAP_DATA_TYPE_UINT8
+                             : elem_bytes == 2 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16
+                                               : CU_TENSOR_MAP_DATA_TYPE_FLOAT32;
     cuuint64_t gdim[2] = {cols, rows};
     cuuint64_t gstride[1] = {cols * static_cast<uint64_t>(elem_bytes)};
     cuuint32_t box[2] = {box_cols, box_rows};

@@ -254,3 +254,10 @@ def make_decode(B: int, H: int, Nq: int, Nk: int, d: int, len_range, seed: int =
 
 def make_decode_workload(w: DecodeWorkload, seed: int = 0, device: str = "cpu") -> DecodeInputs:
     return make_decode(w.B, w.H, w.Nq, w.Nk, w.d, w.len_range, seed, device)
+
+
+def make_signs(d: int, seed: int = 0) -> torch.Tensor:
+    """Random signs (float32 +-1, [d]) for the FP8 path's Hadamard rotation,
+    from a CPU generator seeded with ``seed + 7``."""
+    g = torch.Generator().manual_seed(seed + 7)
+    return torch.where(torch.rand(d, generator=g) < 0.5, -1.0, 1.0).to(torch.float32)
