@@ -22,3 +22,4 @@ from .attention import (  # noqa: F401
 from .varlen import forward_varlen, backward_varlen  # noqa: F401
 from .decode import decode_forward, split_decode  # noqa: F401
 from .fp8 import fp8_forward, e4m3_round  # noqa: F401
+from . import dropout  # noqa: F401

@@ -1,0 +1,107 @@
+"""Pins for the dropout oracle (no GPU).
+
+The generator is pinned to the published Philox-4x32-10 known-answer
+vectors (Salmon et al., SC 2011), the element-to-bits mapping to a scalar
+restatement in plain Python integers, the keep rate to its binomial
+expectation, p = 0 to the dense oracle, and the backward to central finite
+differences of <dO, O> and to the D = rowsum(P * dP) identity.
+"""
+
+import numpy as np
+import pytest
+
+from oracle import attention as A
+from oracle import dropout as DR
+
+KAT = [((0, 0, 0, 0), (0, 0), (0x6627E8D5, 0xE169C58D, 0xBC57AC4C, 0x9B00DBD8)),
+       ((0xFFFFFFFF,) * 4, (0xFFFFFFFF, 0xFFFFFFFF), (0x408F276D, 0x41C83B0E, 0xA20BC7C6, 0x6D5451FD)),
+       ((0x243F6A88, 0x85A308D3, 0x13198A2E, 0x03707344), (0xA4093822, 0x299F31D0),
+        (0xD16CFE09, 0x94FDCCEB, 0x5001E420, 0x24126EA1))]
+
+
+@pytest.mark.parametrize("ctr,key,expect", KAT)
+def test_philox_known_answers(ctr, key, expect):
+    out = DR.philox4x32_10(*ctr, *key)
+    assert tuple(int(x) for x in out) == expect
+
+
+def _scalar_philox(c, k):
+    c0, c1, c2, c3 = c
+    k0, k1 = k
+    for _ in range(10):
+        p0, p1 = 0xD2511F53 * c0, 0xCD9E8D57 * c2
+        c0, c1, c2, c3 = ((p1 >> 32) ^ c1 ^ k0) & 0xFFFFFFFF, p1 & 0xFFFFFFFF, ((p0 >> 32) ^ c3 ^ k1) & 0xFFFFFFFF, \
+            p0 & 0xFFFFFFFF
+        k0, k1 = (k0 + 0x9E3779B9) & 0xFFFFFFFF, (k1 + 0xBB67AE85) & 0xFFFFFFFF
+    return c0, c1, c2, c3
+
+
+def test_mask_layout_matches_scalar_restatement():
+    seed, p = 0x0123456789ABCDEF, 0.3
+    b, h, N = 2, 5, 40
+    Z = DR.keep_mask(b, h, np.arange(N), N, seed, p)
+    t = DR.threshold(p)
+    for i, j in [(0, 0), (3, 7), (5, 2), (17, 33), (39, 39), (12, 0)]:
+        words = _scalar_philox((i // 4, j // 4, h, b), (seed & 0xFFFFFFFF, seed >> 32))
+        byte = (words[i % 4] >> (8 * (j % 4))) & 0xFF
+        assert Z[i, j] == (byte >= t)
+
+
+def test_keep_rate_is_binomial():
+    p = 0.1
+    Z = DR.keep_mask(0, 0, np.arange(512), 512, 7, p)
+    keep = 1.0 - DR.threshold(p) / 256.0
+    n = Z.size
+    assert abs(Z.mean() - keep) < 4 * np.sqrt(keep * (1 - keep) / n)
+    # heads draw different masks
+    assert (DR.keep_mask(0, 1, np.arange(64), 64, 7, p) != DR.keep_mask(0, 0, np.arange(64), 64, 7, p)).any()
+
+
+def test_zero_rate_is_the_dense_definition():
+    rng = np.random.default_rng(0)
+    q, k, v, do = (rng.standard_normal((1, 2, 40, 8)) for _ in range(4))
+    O, L = DR.forward(q, k, v, 0.4, 0.0, 11, causal=True)
+    Od, Ld = A.forward(q, k, v, 0.4, causal=True)
+    np.testing.assert_allclose(O, Od, atol=1e-13)
+    np.testing.assert_allclose(L, Ld, atol=1e-13)
+    g = DR.backward(q, k, v, do, 0.4, 0.0, 11, causal=True)
+    gd = A.backward(q, k, v, do, 0.4, causal=True)
+    for a, b in zip(g, gd):
+        np.testing.assert_allclose(a, b, atol=1e-12)
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_finite_differences(causal):
+    rng = np.random.default_rng(1)
+    B, H, N, d = 1, 2, 9, 3
+    q, k, v, do = (rng.standard_normal((B, H, N, d)) for _ in range(4))
+    args = dict(scale=0.7, p=0.25, seed=99, causal=causal, kv_len=np.array([7]))
+
+    def loss(q_, k_, v_):
+        return float((DR.forward(q_, k_, v_, **args)[0] * do).sum())
+
+    g = DR.backward(q, k, v, do, **args)
+    h = 1e-6
+    for idx, x in enumerate((q, k, v)):
+        num = np.zeros_like(x)
+        for pos in np.ndindex(x.shape):
+            xp, xm = x.copy(), x.copy()
+            xp[pos] += h
+            xm[pos] -= h
+            a = [q, k, v]
+            a[idx] = xp
+            fp = loss(*a)
+            a[idx] = xm
+            num[pos] = (fp - loss(*a)) / (2 * h)
+        assert np.linalg.norm(num - g[idx]) / np.linalg.norm(g[idx]) < 1e-6
+
+
+def test_D_identity_with_dropout():
+    rng = np.random.default_rng(2)
+    q, k, v, do = (rng.standard_normal((1, 1, 33, 6)) for _ in range(4))
+    O, _ = DR.forward(q, k, v, 0.5, 0.2, 5)
+    vis = A.visible(33)
+    P, _, _ = A.probabilities(A.scores(q[0, 0], k[0, 0], 0.5, vis))
+    Zs = DR.keep_mask(0, 0, np.arange(33), 33, 5, 0.2) / (1 - DR.threshold(0.2) / 256)
+    dP = (do[0, 0] @ v[0, 0].T) * Zs
+    np.testing.assert_allclose((do[0, 0] * O[0, 0]).sum(axis=1), (P * dP).sum(axis=1), atol=1e-12)
