@@ -579,6 +579,72 @@ def run_fp8(args, rank, world):
     print(json.dumps(line), flush=True)
 
 
+def run_dropout(args, rank, world, p_drop: float = 0.1):
+    """Attention fwd + bwd with fused dropout (rate 0.1) on a dense workload's
+    shape: one step = fa_fwd_dropout + fa_bwd_dropout."""
+    import torch
+
+    import io_aware_exact_tiled_gb300 as fa
+    from io_aware_exact_tiled_gb300 import accounting as acc
+    from io_aware_exact_tiled_gb300 import workloads as W
+    w = W.WORKLOADS[args.workload[: -len("_dropout")]]
+    dev = torch.device("cuda", int(os.environ.get("LOCAL_RANK", "0")))
+    torch.cuda.set_device(dev)
+    fa.load()
+    x = W.make_inputs(w, seed=rank, device="cuda")
+    q, k, v, do = (t.to(dev) for t in (x.q, x.k, x.v, x.do))
+    kl = None if x.kv_len is None else x.kv_len.to(dev)
+    B, H, N, d = q.shape
+    o = torch.empty_like(q)
+    lse = torch.empty((B, H, N), dtype=torch.float32, device=dev)
+    dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+    ws_f = fa.workspace(256, dev)
+    ws_b = fa.workspace(fa.bwd_workspace_size(B, H, N, d), dev)
+    fwd_flop, bwd_flop = acc.flops(B, H, N, d, x.causal, None if kl is None else x.kv_len.tolist(), None)
+    ev = lambda: torch.cuda.Event(enable_timing=True)
+    kw = dict(scale=x.scale, causal=x.causal, kv_len=kl)
+    seed = 1234 + rank
+
+    def fwd():
+        fa.forward_dropout(q, k, v, p_drop, seed, out=o, lse=lse, ws=ws_f, **kw)
+        return fa.last_launch_count()
+
+    def bwd():
+        fa.backward_dropout(q, k, v, o, lse, do, p_drop, seed, dq=dq, dk=dk, dv=dv, ws=ws_b, **kw)
+        return fa.last_launch_count()
+
+    for _ in range(max(3, args.warmup)):
+        fwd()
+        bwd()
+    torch.cuda.synchronize()
+    sampler = ClockSampler()
+    sampler.start()
+    wall0 = time.time()
+    f_ms, f_ker, nf = _timed_loop(fwd, args.steps, ev, fa)
+    b_ms, b_ker, nb = _timed_loop(bwd, args.steps, ev, fa)
+    wall1 = time.time()
+    sampler.stop()
+    if fa.get_status(ws_f) != 0 or fa.get_status(ws_b) != 0:
+        raise RuntimeError("device status word reports an error")
+    ms_step = (f_ms + b_ms) / args.steps
+    peaks, src = load_peaks()
+    peak = float(peaks["bf16_tflops"])
+    fwd_tf, bwd_tf = fwd_flop / (f_ker * 1e-3) / 1e12, bwd_flop / (b_ker * 1e-3) / 1e12
+    line = {
+        "metric": f"attention fwd+bwd with fused dropout (p = {p_drop}) TFLOP/s", "unit": "TFLOP/s",
+        "value": (fwd_flop + bwd_flop) / (ms_step * 1e-3) / 1e12, "n_gpus": 1, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16", "data": "synthetic (seeded N(0,1))",
+        "config": {"workload": describe(w) + f", dropout p = {p_drop} (Philox-4x32-10 masks)"},
+        "fwd": {"kernel_ms": f_ker, "tflops": fwd_tf, "pct_peak": 100 * fwd_tf / peak},
+        "bwd": {"kernel_ms": b_ker, "tflops": bwd_tf, "pct_peak": 100 * bwd_tf / peak},
+        "roofline": {"bound": "tensor", "achieved": bwd_tf, "peak": peak, "unit": "TFLOP/s", "frac": bwd_tf / peak,
+                     "traffic": None, "kernel": "fa_bwd_kernel (dropout)", "peak_source": f"{src} bf16 dense burst"},
+        "cpu_baseline": None, "e2e": None, "gpu_launches": nf + nb, "clocks": sampler.summary(wall0, wall1),
+    }
+    print(json.dumps(line), flush=True)
+
+
 # ------------------------------------------------------------------ our arm
 def main():
     args = parse()
@@ -596,6 +662,8 @@ def main():
         return run_packed(args, rank, world)
     if args.workload.endswith("_fp8") and args.workload[:-4] in W_.WORKLOADS:
         return run_fp8(args, rank, world)
+    if args.workload.endswith("_dropout") and args.workload[: -len("_dropout")] in W_.WORKLOADS:
+        return run_dropout(args, rank, world)
 
     import torch
     import torch.distributed as dist

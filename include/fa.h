@@ -184,6 +184,27 @@ fa_status fa_fwd_fp8(const void* q, const void* k, const void* v, void* o, float
                      size_t ws_bytes, void* stream);
 
 /*
+ * Attention with dropout on the probabilities, fused into the kernels ("Why
+ * is FlashAttention faster?", "Kernel fusion removes stage boundaries":
+ * masking, softmax and dropout become stages of one kernel). The forward
+ * computes O = (softmax(S) * Z / (1 - p)) V and L = logsumexp(S); the
+ * backward regenerates the same keep mask Z instead of storing it.
+ * Z for (b, h, query i, key j): byte (j mod 4) of word (i mod 4) of
+ * Philox-4x32-10 (Salmon et al., SC 2011) with counter (i/4, j/4, h, b) and
+ * key (seed mod 2^32, seed / 2^32); kept iff the byte >= t = round(256 p),
+ * so the effective rate is t / 256 (0 <= p < 1, t capped at 255).
+ * Arguments as for fa_fwd / fa_bwd with FA_BF16 tensors and no tile mask,
+ * plus dropout_p and seed; the backward must get the forward's p and seed.
+ */
+fa_status fa_fwd_dropout(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int N, int d,
+                         float scale, int causal, const int32_t* kv_len, float dropout_p, unsigned long long seed,
+                         void* workspace, size_t ws_bytes, void* stream);
+fa_status fa_bwd_dropout(const void* q, const void* k, const void* v, const void* o, const float* lse,
+                         const void* dout, void* dq, void* dk, void* dv, int B, int H, int N, int d, float scale,
+                         int causal, const int32_t* kv_len, float dropout_p, unsigned long long seed, void* workspace,
+                         size_t ws_bytes, void* stream);
+
+/*
  * Backward pass of a packed variable-length batch: the gradients of
  * <dO, O> for fa_fwd_varlen.
  *   q, k, v, o, dout  in,  device, [total, H, d] bf16

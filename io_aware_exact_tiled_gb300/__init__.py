@@ -12,6 +12,8 @@ from .binding import (  # noqa: F401
     backward_varlen,
     decode,
     forward_fp8,
+    forward_dropout,
+    backward_dropout,
     fwd_workspace_size,
     bwd_workspace_size,
     get_status,

@@ -68,6 +68,11 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.fa_fwd_fp8_workspace_size.restype = sz
     lib.fa_fwd_fp8.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, f, i, vp, vp, vp, sz, vp]
     lib.fa_fwd_fp8.restype = i
+    u64 = ctypes.c_ulonglong
+    lib.fa_fwd_dropout.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, f, i, vp, f, u64, vp, sz, vp]
+    lib.fa_fwd_dropout.restype = i
+    lib.fa_bwd_dropout.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, i, i, i, i, f, i, vp, f, u64, vp, sz, vp]
+    lib.fa_bwd_dropout.restype = i
     lib.fa_get_status.argtypes = [vp, vp]
     lib.fa_get_status.restype = i
     lib.fa_status_string.argtypes = [i]
@@ -249,6 +254,50 @@ def forward_fp8(q, k, v, signs, scale: Optional[float] = None, causal: bool = Fa
     if rc != FA_OK:
         raise FAError(rc, "fa_fwd_fp8")
     return o, L
+
+
+def forward_dropout(q, k, v, dropout_p: float, seed: int, scale: Optional[float] = None, causal: bool = False,
+                    kv_len=None, out=None, lse=None, ws=None, stream=None):
+    """O, L = fa_fwd_dropout(...): attention with dropout on the
+    probabilities (bf16 [B, H, N, d]). Returns (o, lse)."""
+    lib = load()
+    if _check_qkv(q, k, v) != FA_BF16:
+        raise ValueError("dropout takes bfloat16 inputs")
+    B, H, N, d = q.shape
+    scale = 1.0 / math.sqrt(d) if scale is None else float(scale)
+    o = torch.empty_like(q) if out is None else out
+    L = torch.empty((B, H, N), dtype=torch.float32, device=q.device) if lse is None else lse
+    if ws is None:
+        ws = workspace(256, q.device)
+    _, kl = _mask_ptrs(None, kv_len, q)
+    rc = lib.fa_fwd_dropout(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(L), B, H, N, d, scale, int(bool(causal)), kl,
+                            float(dropout_p), int(seed) & 0xFFFFFFFFFFFFFFFF, _ptr(ws), ws.numel(),
+                            _stream_handle(stream))
+    if rc != FA_OK:
+        raise FAError(rc, "fa_fwd_dropout")
+    return o, L
+
+
+def backward_dropout(q, k, v, o, lse, do, dropout_p: float, seed: int, scale: Optional[float] = None,
+                     causal: bool = False, kv_len=None, dq=None, dk=None, dv=None, ws=None, stream=None):
+    """dQ, dK, dV = fa_bwd_dropout(...) for forward_dropout's outputs."""
+    lib = load()
+    if _check_qkv(q, k, v, o, do) != FA_BF16:
+        raise ValueError("dropout takes bfloat16 inputs")
+    B, H, N, d = q.shape
+    scale = 1.0 / math.sqrt(d) if scale is None else float(scale)
+    dq = torch.empty_like(q) if dq is None else dq
+    dk = torch.empty_like(k) if dk is None else dk
+    dv = torch.empty_like(v) if dv is None else dv
+    if ws is None:
+        ws = workspace(lib.fa_bwd_workspace_size(B, H, N, d), q.device)
+    _, kl = _mask_ptrs(None, kv_len, q)
+    rc = lib.fa_bwd_dropout(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), _ptr(do), _ptr(dq), _ptr(dk), _ptr(dv),
+                            B, H, N, d, scale, int(bool(causal)), kl, float(dropout_p),
+                            int(seed) & 0xFFFFFFFFFFFFFFFF, _ptr(ws), ws.numel(), _stream_handle(stream))
+    if rc != FA_OK:
+        raise FAError(rc, "fa_bwd_dropout")
+    return dq, dk, dv
 
 
 def decode(q, k_cache, v_cache, cache_len=None, scale: Optional[float] = None, num_splits: int = 0, out=None,

@@ -354,6 +354,103 @@ fa_status fa_fwd_fp8(const void* q, const void* k, const void* v, void* o, float
     return st;
 }
 
+// Dropout parameters: byte threshold t = round(256 p) (<= 255), its keep rate.
+static bool make_dropout(float p, unsigned long long seed, fa::DropoutArgs* d) {
+    if (!(p >= 0.f) || !(p < 1.f)) return false;
+    int t = static_cast<int>(lrintf(256.f * p));
+    if (t > 255) t = 255;
+    d->seed_lo = static_cast<uint32_t>(seed & 0xFFFFFFFFull);
+    d->seed_hi = static_cast<uint32_t>(seed >> 32);
+    d->t4 = static_cast<uint32_t>(t) * 0x01010101u;
+    d->inv_keep = 256.f / static_cast<float>(256 - t);
+    return true;
+}
+
+fa_status fa_fwd_dropout(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int N, int d,
+                         float scale, int causal, const int32_t* kv_len, float dropout_p, unsigned long long seed,
+                         void* workspace, size_t ws_bytes, void* stream) {
+    if (!q || !k || !v || !o || !lse || !workspace) return FA_ERR_INVALID_ARG;
+    if (causal != 0 && causal != 1) return FA_ERR_INVALID_ARG;
+    fa_status st = check_shape(B, H, N, d, scale);
+    if (st != FA_OK) return st;
+    fa::FwdArgs a{};
+    if (!make_dropout(dropout_p, seed, &a.drop)) return FA_ERR_INVALID_ARG;
+    if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(o, 16) || !aligned(lse, 4) ||
+        !aligned(workspace, 256) || (kv_len && !aligned(kv_len, 4)))
+        return FA_ERR_INVALID_ARG;
+    if (ws_bytes < kStatusBytes) return FA_ERR_INVALID_ARG;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    a.q = q;
+    a.k = k;
+    a.v = v;
+    a.o = o;
+    a.lse = lse;
+    a.B = B;
+    a.H = H;
+    a.N = N;
+    a.d = d;
+    a.scale = scale;
+    a.causal = causal;
+    a.kv_len = kv_len;
+    a.dropout = 1;
+    a.status = static_cast<int*>(workspace);
+    a.ev_begin = g_ev_begin;
+    a.ev_end = g_ev_end;
+    if (cudaMemsetAsync(a.status, 0, sizeof(int) * 4, s) != cudaSuccess) return FA_ERR_CUDA;
+    int n = 0;
+    st = map_cuda(fa::launch_fwd(a, s, &n));
+    if (st == FA_OK) g_last_launches = n;
+    return st;
+}
+
+fa_status fa_bwd_dropout(const void* q, const void* k, const void* v, const void* o, const float* lse,
+                         const void* dout, void* dq, void* dk, void* dv, int B, int H, int N, int d, float scale,
+                         int causal, const int32_t* kv_len, float dropout_p, unsigned long long seed, void* workspace,
+                         size_t ws_bytes, void* stream) {
+    if (!q || !k || !v || !o || !lse || !dout || !dq || !dk || !dv || !workspace) return FA_ERR_INVALID_ARG;
+    if (causal != 0 && causal != 1) return FA_ERR_INVALID_ARG;
+    fa_status st = check_shape(B, H, N, d, scale);
+    if (st != FA_OK) return st;
+    fa::BwdArgs a{};
+    if (!make_dropout(dropout_p, seed, &a.drop)) return FA_ERR_INVALID_ARG;
+    if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(o, 16) || !aligned(dout, 16) ||
+        !aligned(dq, 16) || !aligned(dk, 16) || !aligned(dv, 16) || !aligned(lse, 16) ||
+        !aligned(workspace, 256) || (kv_len && !aligned(kv_len, 4)))
+        return FA_ERR_INVALID_ARG;
+    if (ws_bytes < fa_bwd_workspace_size(B, H, N, d)) return FA_ERR_INVALID_ARG;
+    const size_t rows = static_cast<size_t>(B) * H * N;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    a.q = q;
+    a.k = k;
+    a.v = v;
+    a.o = o;
+    a.dout = dout;
+    a.lse = lse;
+    a.dq = dq;
+    a.dk = dk;
+    a.dv = dv;
+    a.B = B;
+    a.H = H;
+    a.N = N;
+    a.d = d;
+    a.scale = scale;
+    a.causal = causal;
+    a.kv_len = kv_len;
+    a.dropout = 1;
+    char* ws = static_cast<char*>(workspace);
+    a.status = reinterpret_cast<int*>(ws);
+    a.delta = reinterpret_cast<float*>(ws + kStatusBytes);
+    a.lse2 = reinterpret_cast<float*>(ws + kStatusBytes + align256(rows * sizeof(float)));
+    a.dq_accum = reinterpret_cast<float*>(ws + kStatusBytes + 2 * align256(rows * sizeof(float)));
+    a.ev_begin = g_ev_begin;
+    a.ev_end = g_ev_end;
+    if (cudaMemsetAsync(a.status, 0, sizeof(int) * 4, s) != cudaSuccess) return FA_ERR_CUDA;
+    int n = 0;
+    st = map_cuda(fa::launch_bwd(a, s, &n));
+    if (st == FA_OK) g_last_launches = n;
+    return st;
+}
+
 fa_status fa_bwd(const void* q, const void* k, const void* v, const void* o, const float* lse, const void* dout,
                  void* dq, void* dk, void* dv, int B, int H, int N, int d, float scale, int causal,
                  const uint8_t* blockmask, const int32_t* kv_len, fa_dtype dtype, void* workspace, size_t ws_bytes,

@@ -30,6 +30,7 @@
 #include <math_constants.h>
 
 #include "fa_common.cuh"
+#include "fa_philox.cuh"
 #include "fa_launch.h"
 #include "tmap.h"
 
@@ -77,6 +78,7 @@ struct BwdParams {
     const int32_t* cu_tiles;    // [B + 1] running 128-row tile counts (packed)
     int total;                  // tokens of the packed batch
     long long lpad;             // rows per head of nlse2 / ndelta (packed)
+    DropoutArgs drop;           // dropout on the probabilities (DROPOUT kernel)
 };
 
 constexpr float kLog2e = 1.4426950408889634f;
@@ -94,7 +96,10 @@ constexpr float kLog2e = 1.4426950408889634f;
 //   dK  += dS^T Q_i, dQ_i = dS K_j  (dS^T from shared memory)
 // VARLEN: packed variable-length batch; a separate instantiation so that the
 // [B, H, N, d] kernel carries none of its branches.
-template <int D, bool VARLEN>
+// DROPOUT: the keep mask of the forward pass is regenerated (fa_philox.cuh);
+// P^T masked by it feeds dV, the unmasked P^T (kept in the free half of the
+// buffer's columns) feeds dS.
+template <int D, bool VARLEN, bool DROPOUT = false>
 __global__ void __launch_bounds__(512, 1)
     fa_bwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                   const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmdO,
@@ -337,12 +342,31 @@ __global__ void __launch_bounds__(512, 1)
             const bool diag = p.mask.causal && i == j;
             const int qlim = varlen ? N - i * kTile : kTile;
             const bool masked = diag || !key_ok || qlim < kTile;
+            uint32_t pu0[DROPOUT ? 16 : 1];  // dropout: unmasked P^T of the first 32 queries
 #pragma unroll
             for (int c = 0; c < 2; ++c) {
                 uint32_t pk[16];  // P^T of 32 queries, bf16 pairs
                 uint32_t sr[32];
                 tmem_ld32(tl + col_s + 64 * g + c * 32, sr);
                 tmem_ld_wait(sr);
+                uint32_t kw[DROPOUT ? 8 : 1];  // keep bytes of this key for the chunk's 32 queries
+                if constexpr (DROPOUT) {
+                    const int s4 = lane & 3;
+#pragma unroll
+                    for (int m4 = 0; m4 < 2; ++m4) {
+                        // this lane's call: query block m4 * 4 + s4 of the chunk
+                        const uint32_t qblk = static_cast<uint32_t>((i * kTile + 64 * g + c * 32) >> 2) + m4 * 4 + s4;
+                        const uint4 w = quad_transpose(
+                            byte_transpose(philox4x32_10(make_uint4(qblk, static_cast<uint32_t>(key) >> 2,
+                                                                    static_cast<uint32_t>(h), static_cast<uint32_t>(b)),
+                                                         p.drop.seed_lo, p.drop.seed_hi)),
+                            s4);
+                        kw[m4 * 4 + 0] = w.x;
+                        kw[m4 * 4 + 1] = w.y;
+                        kw[m4 * 4 + 2] = w.z;
+                        kw[m4 * 4 + 3] = w.w;
+                    }
+                }
 #pragma unroll
                 for (int e = 0; e < 8; ++e) {
                     // x = S * scale * log2(e) - L * log2(e), two queries per instruction
@@ -363,7 +387,28 @@ __global__ void __launch_bounds__(512, 1)
                     pk[2 * e] = pack_bf16x2(pv0, pv1);
                     pk[2 * e + 1] = pack_bf16x2(pv2, pv3);
                 }
-                tmem_st16(tl + col_s + 64 * g + c * 16, pk);
+                if constexpr (DROPOUT) {
+                    uint32_t pz[16];
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) {
+                        uint32_t lo, hi;
+                        keep_masks16(kw[e], p.drop.t4, lo, hi);
+                        pz[2 * e] = pk[2 * e] & lo;
+                        pz[2 * e + 1] = pk[2 * e + 1] & hi;
+                    }
+                    tmem_st16(tl + col_s + 64 * g + c * 16, pz);
+                    // the unmasked P^T goes to columns 32-63 of the group,
+                    // which hold the second chunk's scores until it is read
+                    if (c == 0) {
+#pragma unroll
+                        for (int e = 0; e < 16; ++e) pu0[e] = pk[e];
+                    } else {
+                        tmem_st16(tl + col_s + 64 * g + 32, pu0);
+                        tmem_st16(tl + col_s + 64 * g + 48, pk);
+                    }
+                } else {
+                    tmem_st16(tl + col_s + 64 * g + c * 16, pk);
+                }
             }
             tmem_st_wait();
             tc_fence_before();
@@ -377,11 +422,26 @@ __global__ void __launch_bounds__(512, 1)
             uint32_t dsw[32];
 #pragma unroll
             for (int c = 0; c < 2; ++c) {
-                uint32_t dr[32], pk[16];
+                uint32_t dr[32], pk[16], pz[DROPOUT ? 16 : 1];
                 tmem_ld32(tl + col_dp + 64 * g + c * 32, dr);
-                tmem_ld16(tl + col_s + 64 * g + c * 16, pk);
+                if constexpr (DROPOUT) {
+                    tmem_ld16(tl + col_s + 64 * g + 32 + c * 16, pk);  // unmasked P^T
+                    tmem_ld16(tl + col_s + 64 * g + c * 16, pz);       // masked P^T (zero where dropped)
+                    tmem_ld_wait(pz);
+                } else {
+                    tmem_ld16(tl + col_s + 64 * g + c * 16, pk);
+                }
                 tmem_ld_wait(dr);
                 tmem_ld_wait(pk);
+                if constexpr (DROPOUT) {
+                    // dP of a dropped element is 0; a kept one is divided by the keep rate
+                    const float ik = p.drop.inv_keep;
+#pragma unroll
+                    for (int e = 0; e < 16; ++e) {
+                        dr[2 * e] = __float_as_uint(__uint_as_float(dr[2 * e]) * ((pz[e] & 0xFFFFu) ? ik : 0.f));
+                        dr[2 * e + 1] = __float_as_uint(__uint_as_float(dr[2 * e + 1]) * ((pz[e] >> 16) ? ik : 0.f));
+                    }
+                }
 #pragma unroll
                 for (int e = 0; e < 8; ++e) {  // 4 queries
                     const float4 nD = lds128(ndel_s + (c * 8 + e) * 16);
@@ -422,7 +482,7 @@ __global__ void __launch_bounds__(512, 1)
                                        : (static_cast<size_t>(bh) * N + key) * D;
             uint16_t* out = static_cast<uint16_t*>(g == 0 ? p.dv : p.dk) + orow;
             const uint32_t col = g == 0 ? C::COL_DV : C::COL_DK;
-            const float mul = g == 0 ? 1.f : p.scale;
+            const float mul = g == 0 ? (DROPOUT ? p.drop.inv_keep : 1.f) : p.scale;
 #pragma unroll
             for (int c = 0; c < D / 32; ++c) {
                 uint32_t v[32];
@@ -696,6 +756,9 @@ static cudaError_t launch_bwd_t(const BwdArgs& a, cudaStream_t stream, int* nlau
         cudaError_t e = cudaFuncSetAttribute(fa_bwd_kernel<D, false>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
         if (e == cudaSuccess)
             e = cudaFuncSetAttribute(fa_bwd_kernel<D, true>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
+        if (e == cudaSuccess)
+            e = cudaFuncSetAttribute(fa_bwd_kernel<D, false, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                     C::SMEM);
         if (e != cudaSuccess) return e;
         attr_set = true;
     }
@@ -740,8 +803,11 @@ static cudaError_t launch_bwd_t(const BwdArgs& a, cudaStream_t stream, int* nlau
     p.lpad = a.lpad;
     dim3 grid((a.N + kTile - 1) / kTile, a.H, a.B);
     if (a.ev_begin) cudaEventRecord(a.ev_begin, stream);
+    p.drop = a.drop;
     if (varlen)
         fa_bwd_kernel<D, true><<<grid, C::THREADS, C::SMEM, stream>>>(tq, tk, tv, tdo, tdq, p);
+    else if (a.dropout)
+        fa_bwd_kernel<D, false, true><<<grid, C::THREADS, C::SMEM, stream>>>(tq, tk, tv, tdo, tdq, p);
     else
         fa_bwd_kernel<D, false><<<grid, C::THREADS, C::SMEM, stream>>>(tq, tk, tv, tdo, tdq, p);
     if (a.ev_end) cudaEventRecord(a.ev_end, stream);

@@ -31,6 +31,7 @@
 #include <math_constants.h>
 
 #include "fa_common.cuh"
+#include "fa_philox.cuh"
 #include "fa_launch.h"
 #include "tmap.h"
 
@@ -78,6 +79,7 @@ struct FwdParams {
     int* status;
     const int32_t* cu_seqlens;  // packed variable-length batch (bf16), else null
     int total;                  // tokens of the packed batch
+    DropoutArgs drop;           // dropout on the probabilities (DROPOUT kernels)
 };
 
 // Issue state of the MMA thread, per Q tile s of the CTA.
@@ -123,7 +125,9 @@ constexpr float kLn2 = 0.69314718055994530942f;
 
 // VARLEN: packed variable-length batch (bf16 only); a separate instantiation
 // so that the [B, H, N, d] kernels carry none of its branches.
-template <bool TF32, int D, bool VARLEN>
+// DROPOUT: dropout on the probabilities, with the keep mask regenerated from
+// Philox (fa_philox.cuh); a separate instantiation as well.
+template <bool TF32, int D, bool VARLEN, bool DROPOUT = false>
 __global__ void __launch_bounds__(384, 1)
     fa_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                   const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmQlo,
@@ -422,6 +426,7 @@ __global__ void __launch_bounds__(384, 1)
                 // fp32 row sum and the sum of the bf16-rounded weights
                 const uint64_t c2c2 = f2_make(c2, c2), nmu2 = f2_make(-mu, -mu);
                 uint64_t rs2 = 0ull;
+                uint64_t rr2d = 0ull;  // dropout: bf16-weight sum, formed before the weights are masked
                 uint32_t pk[4][16];  // P as bf16 pairs; kept for the bf16-weight sum
 #pragma unroll
                 for (int c = 0; c < 4; ++c) {
@@ -435,6 +440,31 @@ __global__ void __launch_bounds__(384, 1)
                             const float p0 = ex2_approx(x0), p1 = ex2_approx(x1);
                             pk[c][i] = pack_bf16x2(p0, p1);
                             rs2 = f2_add(rs2, f2_make(p0, p1));
+                        }
+                        if constexpr (DROPOUT) {
+                            // the normaliser sums every weight; dropout then
+                            // zeroes the dropped ones before the P V product
+#pragma unroll
+                            for (int i = 0; i < 16; ++i) rr2d = f2_add(rr2d, f2_from_bf16x2(pk[c][i]));
+                            const int s4 = lane & 3;
+#pragma unroll
+                            for (int g4 = 0; g4 < 2; ++g4) {
+                                // this lane's call: key block g4 * 4 + s4 of the chunk
+                                const uint32_t kb = static_cast<uint32_t>((t * kTile + c * 32) >> 2) + g4 * 4 + s4;
+                                const uint4 w = quad_transpose(
+                                    philox4x32_10(make_uint4(static_cast<uint32_t>(grow) >> 2, kb,
+                                                             static_cast<uint32_t>(h), static_cast<uint32_t>(b)),
+                                                  p.drop.seed_lo, p.drop.seed_hi),
+                                    s4);
+                                const uint32_t kw[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+                                for (int n4 = 0; n4 < 4; ++n4) {
+                                    uint32_t lo, hi;
+                                    keep_masks16(kw[n4], p.drop.t4, lo, hi);
+                                    pk[c][2 * (g4 * 4 + n4)] &= lo;
+                                    pk[c][2 * (g4 * 4 + n4) + 1] &= hi;
+                                }
+                            }
                         }
                         tmem_st16(tl + c * 16, pk[c]);
                     } else {
@@ -468,7 +498,11 @@ __global__ void __launch_bounds__(384, 1)
                 // case it is formed after P has been handed to the MMA thread.
 #define FA_ROW_SUMS()                                                                                     \
     do {                                                                                                  \
-        if constexpr (!TF32) {                                                                            \
+        if constexpr (DROPOUT) {                                                                          \
+            float a_, b_;                                                                                 \
+            f2_split(rr2d, a_, b_);                                                                       \
+            lw += a_ + b_;                                                                                \
+        } else if constexpr (!TF32) {                                                                     \
             uint64_t rr2 = 0ull;                                                                          \
             _Pragma("unroll") for (int c = 0; c < 4; ++c) _Pragma("unroll") for (int i = 0; i < 16; ++i)    \
                 rr2 = f2_add(rr2, f2_from_bf16x2(pk[c][i]));                                              \
@@ -510,7 +544,8 @@ __global__ void __launch_bounds__(384, 1)
                 if (ok) tc_fence_after();
             }
             if (ok) {
-                const float inv = lw > 0.f ? 1.f / lw : 0.f;
+                float inv = lw > 0.f ? 1.f / lw : 0.f;
+                if constexpr (DROPOUT) inv *= p.drop.inv_keep;
                 // packed rows past the end of the sequence belong to the next
                 // one: computed (the TMEM loads are warp-wide) but not stored
                 const bool row_ok = !varlen || grow < N;
@@ -639,6 +674,9 @@ static cudaError_t launch_fwd_t(const FwdArgs& a, cudaStream_t stream, int* nlau
         if (e == cudaSuccess && !TF32)
             e = cudaFuncSetAttribute(fa_fwd_kernel<TF32, D, !TF32>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                      C::SMEM);
+        if (e == cudaSuccess && !TF32)
+            e = cudaFuncSetAttribute(fa_fwd_kernel<TF32, D, false, !TF32>,
+                                     cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
         if (e != cudaSuccess) return e;
         attr_set = true;
     }
@@ -659,8 +697,11 @@ static cudaError_t launch_fwd_t(const FwdArgs& a, cudaStream_t stream, int* nlau
     const int T = (a.N + kTile - 1) / kTile;
     dim3 grid(a.H, a.B, (T + 1) / 2);
     if (a.ev_begin) cudaEventRecord(a.ev_begin, stream);
+    p.drop = a.drop;
     if (p.cu_seqlens)
         fa_fwd_kernel<TF32, D, !TF32><<<grid, C::THREADS, C::SMEM, stream>>>(tq, tk, tv, tql, tkl, p);
+    else if (a.dropout && !TF32)
+        fa_fwd_kernel<TF32, D, false, !TF32><<<grid, C::THREADS, C::SMEM, stream>>>(tq, tk, tv, tql, tkl, p);
     else
         fa_fwd_kernel<TF32, D, false><<<grid, C::THREADS, C::SMEM, stream>>>(tq, tk, tv, tql, tkl, p);
     if (a.ev_end) cudaEventRecord(a.ev_end, stream);

@@ -5,6 +5,8 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include "fa_philox.cuh"
+
 namespace fa {
 
 struct FwdArgs {
@@ -25,6 +27,9 @@ struct FwdArgs {
     // and N is the longest sequence. Null for the [B, H, N, d] layout.
     const int32_t* cu_seqlens;
     int total;
+    // dropout on the probabilities (bf16, no tile mask, no packed batch)
+    int dropout;
+    DropoutArgs drop;
 };
 
 struct BwdArgs {
@@ -50,6 +55,8 @@ struct BwdArgs {
     int32_t* cu_tiles;  // [B + 1] scratch
     int total;
     long long lpad;     // rows per head of delta / lse2: align128(total) + 128 * B
+    int dropout;
+    DropoutArgs drop;
 };
 
 cudaError_t launch_fwd(const FwdArgs& a, cudaStream_t stream, int* nlaunch);
