@@ -329,8 +329,10 @@ __global__ void __launch_bounds__(512, 1)
             if (!visible_i(i)) continue;
             const int st = u % C::STAGES;
             const uint32_t ph = (u / C::STAGES) & 1;
-            const uint32_t nlse_s = smem_u32(sm + C::LSE_OFF + st * 512) + 256 * g;
-            const uint32_t ndel_s = smem_u32(sm + C::DEL_OFF + st * 512) + 256 * g;
+            // -L log2 e and -D of this group's 64 queries (shared memory; plain
+            // loads, so that the compiler may schedule them early)
+            const float4* nlse_s = reinterpret_cast<const float4*>(sm + C::LSE_OFF + st * 512 + 256 * g);
+            const float4* ndel_s = reinterpret_cast<const float4*>(sm + C::DEL_OFF + st * 512 + 256 * g);
             ok = mbar_wait(&qd_full[st], ph, cx, 17);
             ok = __all_sync(0xffffffffu, ok) && __all_sync(0xffffffffu, mbar_wait(s_full, u & 1, cx, 18));
             if (!ok) break;
@@ -343,12 +345,16 @@ __global__ void __launch_bounds__(512, 1)
             const int qlim = varlen ? N - i * kTile : kTile;
             const bool masked = diag || !key_ok || qlim < kTile;
             uint32_t pu0[DROPOUT ? 16 : 1];  // dropout: unmasked P^T of the first 32 queries
+            // both halves of S^T are requested before either is waited for
+            uint32_t srs[2][32];
+            tmem_ld32(tl + col_s + 64 * g, srs[0]);
+            tmem_ld32(tl + col_s + 64 * g + 32, srs[1]);
+            tmem_ld_wait(srs[0]);
+            tmem_ld_wait(srs[1]);
 #pragma unroll
             for (int c = 0; c < 2; ++c) {
                 uint32_t pk[16];  // P^T of 32 queries, bf16 pairs
-                uint32_t sr[32];
-                tmem_ld32(tl + col_s + 64 * g + c * 32, sr);
-                tmem_ld_wait(sr);
+                uint32_t(&sr)[32] = srs[c];
                 uint32_t kw[DROPOUT ? 8 : 1];  // keep bytes of this key for the chunk's 32 queries
                 if constexpr (DROPOUT) {
                     const int s4 = lane & 3;
@@ -370,7 +376,7 @@ __global__ void __launch_bounds__(512, 1)
 #pragma unroll
                 for (int e = 0; e < 8; ++e) {
                     // x = S * scale * log2(e) - L * log2(e), two queries per instruction
-                    const float4 nL = lds128(nlse_s + (c * 8 + e) * 16);
+                    const float4 nL = nlse_s[c * 8 + e];
                     float x0, x1, x2, x3;
                     f2_split(f2_fma(f2_make(__uint_as_float(sr[4 * e]), __uint_as_float(sr[4 * e + 1])), c2c2,
                                     f2_make(nL.x, nL.y)), x0, x1);
@@ -414,12 +420,14 @@ __global__ void __launch_bounds__(512, 1)
             tc_fence_before();
             if (!FA_DROP_THIS_ARRIVE(u == 0)) mbar_arrive(p_ready);
             // dS^T = P^T * (dP^T - D) (the scale is applied to dK and dQ at
-            // the end), computed into registers before the shared buffer is
-            // known to be free; P^T is read back from TMEM (bf16)
+            // the end); P^T is read back from TMEM (bf16). The previous dS^T
+            // must have been consumed by its dK / dQ GEMMs before this one is
+            // written (long done by now: their completion released dQ_{i-1}
+            // to the drain), so each half is stored as soon as it is formed.
             ok = __all_sync(0xffffffffu, mbar_wait(dp_full, u & 1, cx, 19));
+            if (ok && u > 0) ok = __all_sync(0xffffffffu, mbar_wait(dq_full, (u - 1) & 1, cx, 20));
             if (!ok) break;
             tc_fence_after();
-            uint32_t dsw[32];
 #pragma unroll
             for (int c = 0; c < 2; ++c) {
                 uint32_t dr[32], pk[16], pz[DROPOUT ? 16 : 1];
@@ -442,27 +450,22 @@ __global__ void __launch_bounds__(512, 1)
                         dr[2 * e + 1] = __float_as_uint(__uint_as_float(dr[2 * e + 1]) * ((pz[e] >> 16) ? ik : 0.f));
                     }
                 }
+                uint32_t dsw[16];
 #pragma unroll
                 for (int e = 0; e < 8; ++e) {  // 4 queries
-                    const float4 nD = lds128(ndel_s + (c * 8 + e) * 16);
+                    const float4 nD = ndel_s[c * 8 + e];
                     const uint64_t t01 = f2_add(f2_make(__uint_as_float(dr[4 * e]), __uint_as_float(dr[4 * e + 1])),
                                                 f2_make(nD.x, nD.y));
                     const uint64_t t23 = f2_add(f2_make(__uint_as_float(dr[4 * e + 2]), __uint_as_float(dr[4 * e + 3])),
                                                 f2_make(nD.z, nD.w));
-                    dsw[c * 16 + 2 * e] = bf16x2_from_f2(f2_mul(t01, f2_from_bf16x2(pk[2 * e])));
-                    dsw[c * 16 + 2 * e + 1] = bf16x2_from_f2(f2_mul(t23, f2_from_bf16x2(pk[2 * e + 1])));
+                    dsw[2 * e] = bf16x2_from_f2(f2_mul(t01, f2_from_bf16x2(pk[2 * e])));
+                    dsw[2 * e + 1] = bf16x2_from_f2(f2_mul(t23, f2_from_bf16x2(pk[2 * e + 1])));
                 }
-            }
-            if (u > 0) {
-                // the previous dS^T must have been consumed by its dK / dQ
-                // GEMMs (their completion is what releases dQ to the drain)
-                ok = __all_sync(0xffffffffu, mbar_wait(dq_full, (u - 1) & 1, cx, 20));
-                if (!ok) break;
-            }
 #pragma unroll
-            for (int chunk = 0; chunk < 8; ++chunk)  // 8 queries per 16-byte chunk
-                sts128(ds_row + ((chunk ^ (r & 7)) * 16), dsw[4 * chunk], dsw[4 * chunk + 1], dsw[4 * chunk + 2],
-                       dsw[4 * chunk + 3]);
+                for (int chunk = 0; chunk < 4; ++chunk)  // 8 queries per 16-byte chunk
+                    sts128(ds_row + (((c * 4 + chunk) ^ (r & 7)) * 16), dsw[4 * chunk], dsw[4 * chunk + 1],
+                           dsw[4 * chunk + 2], dsw[4 * chunk + 3]);
+            }
             fence_proxy_async_smem();
             tc_fence_before();
             mbar_arrive(ds_ready);
