@@ -80,6 +80,7 @@ struct FwdParams {
     const int32_t* cu_seqlens;  // packed variable-length batch (bf16), else null
     int total;                  // tokens of the packed batch
     DropoutArgs drop;           // dropout on the probabilities (DROPOUT kernels)
+    int head_major;             // grid (pairs, H, B) instead of (H, B, pairs)
 };
 
 // Issue state of the MMA thread, per Q tile s of the CTA.
@@ -160,7 +161,11 @@ __global__ void __launch_bounds__(384, 1)
     // Longest-first order across all heads (the query-tile pair index is the
     // slowest grid dimension): with causal masks the longest CTAs start first
     // and the short ones fill the tail.
-    const int h = blockIdx.x, b = blockIdx.y;
+    // Without causal masking every pair of a head costs about the same, and
+    // a tile mask makes the pairs share few key tiles, so the grid is then
+    // head-major instead: the CTAs running together read one head's K and V,
+    // which stays in L2.
+    const int h = p.head_major ? blockIdx.y : blockIdx.x, b = p.head_major ? blockIdx.z : blockIdx.y;
     // A packed variable-length batch puts sequence b at tokens seq0 ..
     // seq0 + N - 1 of [total, H, d] tensors (the grid covers the longest
     // sequence; CTAs past the end of a shorter one leave at once). Otherwise
@@ -177,7 +182,7 @@ __global__ void __launch_bounds__(384, 1)
         T = (N + kTile - 1) / kTile;
     }
     const int npairs = (T + 1) >> 1;
-    const int qp = npairs - 1 - static_cast<int>(blockIdx.z);
+    const int qp = npairs - 1 - static_cast<int>(p.head_major ? blockIdx.x : blockIdx.z);
     if (qp < 0) return;  // uniform over the CTA, before any barrier or TMEM use
     const int qb0 = 2 * qp, qb1 = 2 * qp + 1;
     const bool act1 = qb1 < T;
@@ -695,7 +700,8 @@ static cudaError_t launch_fwd_t(const FwdArgs& a, cudaStream_t stream, int* nlau
     p.cu_seqlens = TF32 ? nullptr : a.cu_seqlens;
     p.total = a.total;
     const int T = (a.N + kTile - 1) / kTile;
-    dim3 grid(a.H, a.B, (T + 1) / 2);
+    p.head_major = (a.blockmask && !a.causal && !p.cu_seqlens) ? 1 : 0;
+    const dim3 grid = p.head_major ? dim3((T + 1) / 2, a.H, a.B) : dim3(a.H, a.B, (T + 1) / 2);
     if (a.ev_begin) cudaEventRecord(a.ev_begin, stream);
     p.drop = a.drop;
     if (p.cu_seqlens)
@@ -711,9 +717,7 @@ static cudaError_t launch_fwd_t(const FwdArgs& a, cudaStream_t stream, int* nlau
 }
 
 cudaError_t launch_fwd(const FwdArgs& a, cudaStream_t stream, int* nlaunch) {
-    // With a tile mask the two query tiles of a pair rarely share key tiles,
-    // which defeats the pairing: one query tile per CTA instead.
-    if (!a.fp32 && a.blockmask) return launch_fwd_bf16_q1(a, stream, nlaunch);
+    if (!a.fp32 && a.blockmask && a.causal) return launch_fwd_bf16_q1(a, stream, nlaunch);
     if (a.fp32) {
         if (a.d == 64) return launch_fwd_t<true, 64>(a, stream, nlaunch);
         return cudaErrorInvalidValue;  // fp32 d=128 exceeds the shared-memory budget of this kernel
