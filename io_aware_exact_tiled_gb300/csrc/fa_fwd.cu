@@ -37,6 +37,11 @@
 
 namespace fa {
 
+// Key tiles per sequence up to which a tile-masked CTA keeps its visible
+// tiles as bitmaps in shared memory (N <= 524,288); longer sequences read the
+// tile mask in global memory tile by tile.
+constexpr int kVisMaxTiles = 4096;
+
 template <bool TF32, int D>
 struct FwdCfg {
     static constexpr int ELEM = TF32 ? 4 : 2;
@@ -55,7 +60,10 @@ struct FwdCfg {
     static constexpr int K_OFF = Q_OFF + NQ * SPLIT * TILE_BYTES;
     static constexpr int V_OFF = K_OFF + KSTAGES * SPLIT * TILE_BYTES;
     static constexpr int BAR_OFF = V_OFF + VSTAGES * TILE_BYTES;
-    static constexpr int SMEM = BAR_OFF + 512 + 1024;  // + barriers + alignment slack
+    // visible-tile bitmaps of the two Q tiles (tile-masked calls)
+    static constexpr int VIS_OFF = BAR_OFF + 512;
+    static constexpr int VIS_WORDS = kVisMaxTiles / 32;
+    static constexpr int SMEM = VIS_OFF + 2 * VIS_WORDS * 4 + 1024;  // + alignment slack
     static constexpr int KSTEP = 32 / ELEM;            // K elements per MMA instruction
     static constexpr int S_KSTEPS = D / KSTEP;
     static constexpr int PV_KSTEPS = kTile / KSTEP;
@@ -128,7 +136,9 @@ constexpr float kLn2 = 0.69314718055994530942f;
 // so that the [B, H, N, d] kernels carry none of its branches.
 // DROPOUT: dropout on the probabilities, with the keep mask regenerated from
 // Philox (fa_philox.cuh); a separate instantiation as well.
-template <bool TF32, int D, bool VARLEN, bool DROPOUT = false>
+// TMASK: calls with a tile mask (bf16, [B, H, N, d]); the visible-tile
+// bitmaps and the jumps over masked tiles live only in this instantiation.
+template <bool TF32, int D, bool VARLEN, bool DROPOUT = false, bool TMASK = false>
 __global__ void __launch_bounds__(384, 1)
     fa_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                   const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmQlo,
@@ -224,6 +234,27 @@ __global__ void __launch_bounds__(384, 1)
         tmem_alloc(tmem_slot, 512);
         tmem_relinquish();
     }
+    // With a tile mask, finding the next visible tile by reading the mask in
+    // global memory one tile at a time costs a dependent load per skipped
+    // tile on the issue paths; warps 2 and 3 (otherwise idle) first turn the
+    // two Q tiles' mask rows into bitmaps (bit t of Q tile s: tile t visible),
+    // and every role then jumps to the next visible tile with a find-first-set.
+    const MaskArgs mk = p.mask;
+    constexpr bool kVis = TMASK && !TF32 && !VARLEN && !DROPOUT;
+    const bool use_vis = kVis && mk.blockmask != nullptr && hi <= kVisMaxTiles;
+    uint32_t* vis = reinterpret_cast<uint32_t*>(sm + C::VIS_OFF);  // [2][VIS_WORDS]
+    if (use_vis && (warp == 2 || warp == 3)) {
+        const int s = warp - 2;
+        const int qb = s == 0 ? qb0 : qb1;
+        const bool on = s == 0 || act1;
+        const int nw = (hi + 31) >> 5;
+#pragma unroll 4
+        for (int w = 0; w < nw; ++w) {
+            const int t = w * 32 + lane;
+            const uint32_t word = __ballot_sync(0xffffffffu, on && t < hi && tile_visible(mk, qb, t, kvalid));
+            if (lane == 0) vis[s * C::VIS_WORDS + w] = word;
+        }
+    }
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
@@ -232,11 +263,32 @@ __global__ void __launch_bounds__(384, 1)
     // which Q tiles of this CTA need key tile t (bit s = Q tile s)
     // (captured by value: a by-reference capture would give these variables
     // addresses and move them to local memory)
-    const MaskArgs mk = p.mask;
     auto need_of = [=](int t) -> uint32_t {
+        if (kVis && use_vis)
+            return ((vis[t >> 5] >> (t & 31)) & 1u) | (((vis[C::VIS_WORDS + (t >> 5)] >> (t & 31)) & 1u) << 1);
         uint32_t nd = tile_visible(mk, qb0, t, kvalid) ? 1u : 0u;
         if (act1 && tile_visible(mk, qb1, t, kvalid)) nd |= 2u;
         return nd;
+    };
+    // The roles walk the tiles as "for t from next_tile(0) on, skipping tiles
+    // whose need bits are clear": next_tile(t, sides) is t itself except in
+    // the tile-masked kernel, where it jumps to the first tile >= t that a Q
+    // tile in sides (bit s = Q tile s) needs, or to hi.
+    auto next_tile = [=](int t, uint32_t sides) -> int {
+        if constexpr (kVis) {
+            if (use_vis) {
+                while (t < hi) {
+                    uint32_t w = 0;
+                    if (sides & 1u) w |= vis[t >> 5];
+                    if (sides & 2u) w |= vis[C::VIS_WORDS + (t >> 5)];
+                    w >>= (t & 31);
+                    if (w) return t + __ffs(w) - 1;
+                    t = (t | 31) + 1;
+                }
+                return hi;
+            }
+        }
+        return t;
     };
 
     if (warp == 0) {
@@ -258,7 +310,7 @@ __global__ void __launch_bounds__(384, 1)
                     if constexpr (TF32) tma_load_2d(dq + C::TILE_BYTES, &tmQlo, r * C::BOXC, qrow0 + s * kTile, bar_q);
                 }
             int nk = 0, nv = 0;  // K and V tiles whose loads were issued
-            for (int t = 0; t < hi; ++t) {
+            for (int t = next_tile(0, 3u); t < hi; t = next_tile(t + 1, 3u)) {
                 if (!need_of(t)) continue;
                 const int kst = nk % C::KSTAGES;
                 if (!mbar_wait(&k_empty[kst], ((nk / C::KSTAGES) & 1) ^ 1, cx, 1)) break;
@@ -316,7 +368,7 @@ __global__ void __launch_bounds__(384, 1)
             uint32_t& rem = st.rem;
 
             int u = 0;
-            for (int t = 0; ok && t < hi; ++t) {
+            for (int t = next_tile(0, 3u); ok && t < hi; t = next_tile(t + 1, 3u)) {
                 const uint32_t nd = need_of(t);
                 if (!nd) continue;
                 const int kst = u % C::KSTAGES;
@@ -390,7 +442,7 @@ __global__ void __launch_bounds__(384, 1)
         int n = 0;
         bool ok = true;
         if (active) {
-            for (int t = 0; t < hi; ++t) {
+            for (int t = next_tile(0, 1u << s); t < hi; t = next_tile(t + 1, 1u << s)) {
                 const uint32_t nd = need_of(t);
                 if (!(nd & (1u << s))) continue;
                 ok = mbar_wait(&s_full[s], n & 1, cx, 6);
@@ -682,6 +734,9 @@ static cudaError_t launch_fwd_t(const FwdArgs& a, cudaStream_t stream, int* nlau
         if (e == cudaSuccess && !TF32)
             e = cudaFuncSetAttribute(fa_fwd_kernel<TF32, D, false, !TF32>,
                                      cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
+        if (e == cudaSuccess && !TF32)
+            e = cudaFuncSetAttribute(fa_fwd_kernel<TF32, D, false, false, !TF32>,
+                                     cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
         if (e != cudaSuccess) return e;
         attr_set = true;
     }
@@ -708,6 +763,8 @@ static cudaError_t launch_fwd_t(const FwdArgs& a, cudaStream_t stream, int* nlau
         fa_fwd_kernel<TF32, D, !TF32><<<grid, C::THREADS, C::SMEM, stream>>>(tq, tk, tv, tql, tkl, p);
     else if (a.dropout && !TF32)
         fa_fwd_kernel<TF32, D, false, !TF32><<<grid, C::THREADS, C::SMEM, stream>>>(tq, tk, tv, tql, tkl, p);
+    else if (a.blockmask && !TF32)
+        fa_fwd_kernel<TF32, D, false, false, !TF32><<<grid, C::THREADS, C::SMEM, stream>>>(tq, tk, tv, tql, tkl, p);
     else
         fa_fwd_kernel<TF32, D, false><<<grid, C::THREADS, C::SMEM, stream>>>(tq, tk, tv, tql, tkl, p);
     if (a.ev_end) cudaEventRecord(a.ev_end, stream);

@@ -9,7 +9,8 @@ import torch
 import io_aware_exact_tiled_gb300 as fa
 from io_aware_exact_tiled_gb300 import workloads as W
 
-from parity import check, errors, run_gpu
+import oracle
+from parity import TOL_L, TOL_O, check, errors, run_gpu
 
 pytestmark = pytest.mark.gpu
 
@@ -109,3 +110,22 @@ def test_status_word_clear_after_calls(cuda_device):
     fa.backward(q, k, v, o, lse, do, causal=True, ws=ws)
     assert fa.get_status(ws) == 0
     assert fa.last_launch_count() == 3
+
+
+def test_tile_mask_longer_than_the_forward_bitmaps(cuda_device):
+    """4,097 key tiles, one more than the tile-masked forward keeps as
+    shared-memory bitmaps: it then reads the tile mask in global memory tile
+    by tile. Sampled query tiles (first, middle, last) against the oracle."""
+    T = 4097
+    N = T * 128
+    w = W.Workload("sparse-long", 1, 1, N, 64, backward=False)
+    x = W.make_inputs(w, seed=7)
+    g = torch.Generator().manual_seed(8)
+    bm = (torch.rand(T, T, generator=g) < 0.002).to(torch.uint8)
+    bm.fill_diagonal_(1)
+    x.blockmask = bm
+    out = run_gpu(x, cuda_device, backward=False)
+    for r0 in (0, 2048 * 128, N - 128):
+        O, L = oracle.forward(x.q, x.k, x.v, x.scale, blockmask=bm, rows=(r0, r0 + 128))
+        assert np.abs(out["o"][0, 0, r0:r0 + 128] - O[0, 0, r0:r0 + 128]).max() <= TOL_O
+        assert np.abs(out["lse"][0, 0, r0:r0 + 128] - L[0, 0, r0:r0 + 128]).max() <= TOL_L
