@@ -36,6 +36,11 @@
 
 namespace fa {
 
+// Query tiles per sequence up to which a tile-masked CTA keeps the visible
+// query tiles of its key tile as a bitmap in shared memory (N <= 262,144);
+// longer sequences read the tile mask in global memory tile by tile.
+constexpr int kBwdVisMaxTiles = 2048;
+
 template <int D>
 struct BwdCfg {
     static constexpr int ROWB = D * 2;
@@ -50,7 +55,9 @@ struct BwdCfg {
     static constexpr int LSE_OFF = DS_OFF + 32768;                    // [STAGES][128] fp32
     static constexpr int DEL_OFF = LSE_OFF + STAGES * 512;            // [STAGES][128] fp32
     static constexpr int BAR_OFF = DEL_OFF + STAGES * 512;
-    static constexpr int USED = BAR_OFF + 256;
+    static constexpr int VIS_OFF = BAR_OFF + 256;                     // visible query tiles (tile mask)
+    static constexpr int VIS_WORDS = kBwdVisMaxTiles / 32;
+    static constexpr int USED = VIS_OFF + VIS_WORDS * 4;
     static constexpr int SMEM = USED + 1024 <= 232448 ? USED + 1024 : 232448;
     static constexpr int THREADS = 512;
     static constexpr uint32_t ID_SQ = idesc_make(128, 128, kFmtBF16, false, false);  // S^T, dP^T
@@ -99,7 +106,9 @@ constexpr float kLog2e = 1.4426950408889634f;
 // DROPOUT: the keep mask of the forward pass is regenerated (fa_philox.cuh);
 // P^T masked by it feeds dV, the unmasked P^T (kept in the free half of the
 // buffer's columns) feeds dS.
-template <int D, bool VARLEN, bool DROPOUT = false>
+// TMASK: calls with a tile mask; the visible-tile bitmap and the jumps over
+// masked query tiles live only in this instantiation.
+template <int D, bool VARLEN, bool DROPOUT = false, bool TMASK = false>
 __global__ void __launch_bounds__(512, 1)
     fa_bwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                   const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmdO,
@@ -158,7 +167,33 @@ __global__ void __launch_bounds__(512, 1)
     const int lo = p.mask.causal ? j : 0;
     // captured by value (a by-reference capture would move them to local memory)
     const MaskArgs mk = p.mask;
-    auto visible_i = [=](int i) -> bool { return tile_visible(mk, i, j, kvalid); };
+    // With a tile mask every role would otherwise find the next visible query
+    // tile by reading a column of the mask in global memory, a dependent load
+    // (and a new cache line) per skipped tile; warps 2 and 3 (otherwise idle)
+    // first gather the column into a bitmap (bit i: query tile i visible), and
+    // the roles jump to the next visible tile with a find-first-set.
+    constexpr bool kVis = TMASK && !VARLEN && !DROPOUT;
+    const bool use_vis = kVis && mk.blockmask != nullptr && T <= kBwdVisMaxTiles;
+    uint32_t* vis = reinterpret_cast<uint32_t*>(sm + C::VIS_OFF);
+    auto visible_i = [=](int i) -> bool {
+        if (kVis && use_vis) return (vis[i >> 5] >> (i & 31)) & 1u;
+        return tile_visible(mk, i, j, kvalid);
+    };
+    // first query tile >= i that the walk visits: i itself except in the
+    // tile-masked kernel, which jumps to the next visible one (or T)
+    auto next_i = [=](int i) -> int {
+        if constexpr (kVis) {
+            if (use_vis) {
+                while (i < T) {
+                    const uint32_t w = vis[i >> 5] >> (i & 31);
+                    if (w) return i + __ffs(w) - 1;
+                    i = (i | 31) + 1;
+                }
+                return T;
+            }
+        }
+        return i;
+    };
 
     if (tid == 0) {
         *abort_flag = 0;
@@ -188,6 +223,15 @@ __global__ void __launch_bounds__(512, 1)
         tmem_alloc(tmem_slot, 512);
         tmem_relinquish();
     }
+    if (use_vis && (warp == 2 || warp == 3)) {
+        const int nw = (T + 31) >> 5;
+#pragma unroll 4
+        for (int w = warp - 2; w < nw; w += 2) {
+            const int i = w * 32 + lane;
+            const uint32_t word = __ballot_sync(0xffffffffu, i >= lo && i < T && tile_visible(mk, i, j, kvalid));
+            if (lane == 0) vis[w] = word;
+        }
+    }
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
@@ -197,7 +241,7 @@ __global__ void __launch_bounds__(512, 1)
         if (lane == 0) {
             int u = 0;
             bool kv_issued = false;
-            for (int i = lo; i < T; ++i) {
+            for (int i = next_i(lo); i < T; i = next_i(i + 1)) {
                 if (!visible_i(i)) continue;
                 if (!kv_issued) {
                     mbar_arrive_expect_tx(kv_full, 2 * C::TILE_BYTES);
@@ -252,7 +296,7 @@ __global__ void __launch_bounds__(512, 1)
             const uint64_t dS_mn = sdesc_sw128(smem_u32(sm + C::DS_OFF), 16384, 1024);   // dS, MN-major
             bool ok = true;
             int u = 0;
-            for (int i = lo; ok && i < T; ++i) {
+            for (int i = next_i(lo); ok && i < T; i = next_i(i + 1)) {
                 if (!visible_i(i)) continue;
                 if (u == 0) {
                     if (!(ok = mbar_wait_warp(kv_full, 0, cx, 12))) break;
@@ -325,7 +369,7 @@ __global__ void __launch_bounds__(512, 1)
         const uint32_t ds_row = smem_u32(sm + C::DS_OFF + g * 16384 + r * 128);
         bool ok = true;
         int u = 0;
-        for (int i = lo; i < T; ++i) {
+        for (int i = next_i(lo); i < T; i = next_i(i + 1)) {
             if (!visible_i(i)) continue;
             const int st = u % C::STAGES;
             const uint32_t ph = (u / C::STAGES) & 1;
@@ -519,7 +563,7 @@ __global__ void __launch_bounds__(512, 1)
         const int wq = warp & 3;
         const uint32_t tl = tm + (static_cast<uint32_t>(wq * 32) << 16);
         int u = 0;
-        for (int i = lo; i < T; ++i) {
+        for (int i = next_i(lo); i < T; i = next_i(i + 1)) {
             if (!visible_i(i)) continue;
             bool ok = mbar_wait(dq_full, u & 1, cx, 22);
             ok = __all_sync(0xffffffffu, ok);
@@ -762,6 +806,9 @@ static cudaError_t launch_bwd_t(const BwdArgs& a, cudaStream_t stream, int* nlau
         if (e == cudaSuccess)
             e = cudaFuncSetAttribute(fa_bwd_kernel<D, false, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                      C::SMEM);
+        if (e == cudaSuccess)
+            e = cudaFuncSetAttribute(fa_bwd_kernel<D, false, false, true>,
+                                     cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
         if (e != cudaSuccess) return e;
         attr_set = true;
     }
@@ -811,6 +858,8 @@ static cudaError_t launch_bwd_t(const BwdArgs& a, cudaStream_t stream, int* nlau
         fa_bwd_kernel<D, true><<<grid, C::THREADS, C::SMEM, stream>>>(tq, tk, tv, tdo, tdq, p);
     else if (a.dropout)
         fa_bwd_kernel<D, false, true><<<grid, C::THREADS, C::SMEM, stream>>>(tq, tk, tv, tdo, tdq, p);
+    else if (a.blockmask)
+        fa_bwd_kernel<D, false, false, true><<<grid, C::THREADS, C::SMEM, stream>>>(tq, tk, tv, tdo, tdq, p);
     else
         fa_bwd_kernel<D, false><<<grid, C::THREADS, C::SMEM, stream>>>(tq, tk, tv, tdo, tdq, p);
     if (a.ev_end) cudaEventRecord(a.ev_end, stream);

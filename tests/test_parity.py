@@ -10,7 +10,7 @@ import io_aware_exact_tiled_gb300 as fa
 from io_aware_exact_tiled_gb300 import workloads as W
 
 import oracle
-from parity import TOL_L, TOL_O, check, errors, run_gpu
+from parity import TOL_G, TOL_L, TOL_O, check, errors, run_gpu
 
 pytestmark = pytest.mark.gpu
 
@@ -129,3 +129,31 @@ def test_tile_mask_longer_than_the_forward_bitmaps(cuda_device):
         O, L = oracle.forward(x.q, x.k, x.v, x.scale, blockmask=bm, rows=(r0, r0 + 128))
         assert np.abs(out["o"][0, 0, r0:r0 + 128] - O[0, 0, r0:r0 + 128]).max() <= TOL_O
         assert np.abs(out["lse"][0, 0, r0:r0 + 128] - L[0, 0, r0:r0 + 128]).max() <= TOL_L
+
+
+def test_tile_mask_longer_than_the_backward_bitmaps(cuda_device):
+    """2,049 query tiles, one more than the tile-masked backward keeps as a
+    shared-memory bitmap. Sampled query tiles r whose key-tile column holds
+    only the diagonal: dQ of their rows and dK, dV of key tile r then depend
+    on those 128 rows alone, which the oracle computes one by one."""
+    T = 2049
+    N = T * 128
+    w = W.Workload("sparse-long-bwd", 1, 1, N, 64)
+    x = W.make_inputs(w, seed=9)
+    g = torch.Generator().manual_seed(10)
+    bm = (torch.rand(T, T, generator=g) < 0.002).to(torch.uint8)
+    sampled = (0, 1024, T - 1)
+    for r in sampled:
+        bm[:, r] = 0
+    bm.fill_diagonal_(1)
+    x.blockmask = bm
+    out = run_gpu(x, cuda_device)
+    for r in sampled:
+        rows = (r * 128, r * 128 + 128)
+        sl = slice(*rows)
+        O, L = oracle.forward(x.q, x.k, x.v, x.scale, blockmask=bm, rows=rows)
+        assert np.abs(out["o"][0, 0, sl] - O[0, 0, sl]).max() <= TOL_O
+        dq, dk, dv = oracle.backward(x.q, x.k, x.v, x.do, x.scale, blockmask=bm, rows=rows)
+        for name, ref in (("dq", dq), ("dk", dk), ("dv", dv)):
+            a, b = out[name][0, 0, sl], ref[0, 0, sl]
+            assert np.linalg.norm(a - b) / np.linalg.norm(b) <= TOL_G, name
