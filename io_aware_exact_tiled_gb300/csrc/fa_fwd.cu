@@ -142,7 +142,8 @@ template <bool TF32, int D, bool VARLEN, bool DROPOUT = false, bool TMASK = fals
 __global__ void __launch_bounds__(384, 1)
     fa_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                   const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmQlo,
-                  const __grid_constant__ CUtensorMap tmKlo, const __grid_constant__ FwdParams p) {
+                  const __grid_constant__ CUtensorMap tmKlo, const __grid_constant__ CUtensorMap tmO,
+                  const __grid_constant__ FwdParams p) {
     using C = FwdCfg<TF32, D>;
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     // 1024-byte aligned base for the swizzled tiles; offsetting the shared
@@ -610,6 +611,17 @@ __global__ void __launch_bounds__(384, 1)
                                            : (static_cast<size_t>(bh) * N + grow) * D;
                 const size_t lrow = varlen ? static_cast<size_t>(h) * p.total + seq0 + grow
                                            : static_cast<size_t>(bh) * N + grow;
+                // bf16: a warp whose 32 rows all lie in the sequence stages them
+                // in its Q tile's buffer (every S GEMM is complete once o_done
+                // is), in the 128-byte swizzled layout of [32 x 64] boxes, and
+                // stores them with one bulk tensor copy per box; a store per
+                // thread and row would touch 32 rows (cache lines) per
+                // instruction. Other warps store their valid rows directly, and
+                // so does a Q tile that saw no key tile (n == 0: nothing waited
+                // for its Q load, which may still be landing in the buffer).
+                const int wrow0 = qb * kTile + wq * 32;
+                const bool tma_rows = !TF32 && n > 0 && wrow0 + 32 <= N;
+                uint8_t* ob = sm + C::Q_OFF + s * C::SPLIT * C::TILE_BYTES + wq * (C::NREG * 4096);
 #pragma unroll
                 for (int c = 0; c < D / 32; ++c) {
                     uint32_t ov[32];
@@ -620,7 +632,6 @@ __global__ void __launch_bounds__(384, 1)
 #pragma unroll
                         for (int i = 0; i < 32; ++i) ov[i] = 0u;
                     }
-                    if (!row_ok) continue;
                     if constexpr (!TF32) {
                         uint4* dst = reinterpret_cast<uint4*>(static_cast<uint16_t*>(p.o) + orow + c * 32);
 #pragma unroll
@@ -630,15 +641,38 @@ __global__ void __launch_bounds__(384, 1)
                             w.y = pack_bf16x2(__uint_as_float(ov[8 * j + 2]) * inv, __uint_as_float(ov[8 * j + 3]) * inv);
                             w.z = pack_bf16x2(__uint_as_float(ov[8 * j + 4]) * inv, __uint_as_float(ov[8 * j + 5]) * inv);
                             w.w = pack_bf16x2(__uint_as_float(ov[8 * j + 6]) * inv, __uint_as_float(ov[8 * j + 7]) * inv);
-                            dst[j] = w;
+                            if (tma_rows) {
+                                const int ch = ((c & 1) << 2) + j;  // 16-byte chunk within the 128-byte row
+                                sts128(smem_u32(ob + (c >> 1) * 4096 + lane * 128 + ((ch ^ (lane & 7)) << 4)), w.x, w.y,
+                                       w.z, w.w);
+                            } else if (row_ok) {
+                                dst[j] = w;
+                            }
                         }
                     } else {
+                        if (!row_ok) continue;
                         float4* dst = reinterpret_cast<float4*>(static_cast<float*>(p.o) + orow + c * 32);
 #pragma unroll
                         for (int j = 0; j < 8; ++j)
                             dst[j] = make_float4(__uint_as_float(ov[4 * j]) * inv, __uint_as_float(ov[4 * j + 1]) * inv,
                                                  __uint_as_float(ov[4 * j + 2]) * inv,
                                                  __uint_as_float(ov[4 * j + 3]) * inv);
+                    }
+                }
+                if (tma_rows) {
+                    fence_proxy_async_smem();
+                    __syncwarp();
+                    if (lane == 0) {
+#pragma unroll
+                        for (int rg = 0; rg < C::NREG; ++rg) {
+                            if (varlen)
+                                tma_store_3d(&tmO, rg * C::BOXC, h, seq0 + wrow0, ob + rg * 4096);
+                            else
+                                tma_store_2d(&tmO, rg * C::BOXC, bh * N + wrow0, ob + rg * 4096);
+                        }
+                        bulk_commit_group();
+                        // the shared buffer must be read out before the CTA exits
+                        bulk_wait_group_read0();
                     }
                 }
                 if (row_ok) p.lse[lrow] = l > 0.f ? (m_hat + log2f(l)) * kLn2 : -CUDART_INF_F;
@@ -688,7 +722,7 @@ static cudaError_t launch_fwd_t(const FwdArgs& a, cudaStream_t stream, int* nlau
     using C = FwdCfg<TF32, D>;
     const int elem = TF32 ? 4 : 2;
     const uint64_t rows = static_cast<uint64_t>(a.B) * a.H * a.N;
-    CUtensorMap tq, tk, tv, tql, tkl;
+    CUtensorMap tq, tk, tv, tql, tkl, to;
     int launches = 0;
     if constexpr (TF32) {
         // scratch: V^T, Qh, Ql, Kh, Kl (each [B,H,N,d] fp32)
@@ -711,19 +745,23 @@ static cudaError_t launch_fwd_t(const FwdArgs& a, cudaStream_t stream, int* nlau
             !make_tmap_2d_sw128(&tkl, kl, rows, D, elem, kTile, C::BOXC))
             return cudaErrorInvalidValue;
     } else {
+        // O is stored in [32 rows x 64 columns] boxes, one per warp and region
         if (a.cu_seqlens) {
             const uint64_t tot = static_cast<uint64_t>(a.total);
             if (!make_tmap_packed_sw128(&tq, a.q, tot, a.H, D, elem, kTile, C::BOXC) ||
                 !make_tmap_packed_sw128(&tk, a.k, tot, a.H, D, elem, kTile, C::BOXC) ||
-                !make_tmap_packed_sw128(&tv, a.v, tot, a.H, D, elem, kTile, C::BOXC))
+                !make_tmap_packed_sw128(&tv, a.v, tot, a.H, D, elem, kTile, C::BOXC) ||
+                !make_tmap_packed_sw128(&to, a.o, tot, a.H, D, elem, 32, C::BOXC))
                 return cudaErrorInvalidValue;
         } else if (!make_tmap_2d_sw128(&tq, a.q, rows, D, elem, kTile, C::BOXC) ||
                    !make_tmap_2d_sw128(&tk, a.k, rows, D, elem, kTile, C::BOXC) ||
-                   !make_tmap_2d_sw128(&tv, a.v, rows, D, elem, kTile, C::BOXC))
+                   !make_tmap_2d_sw128(&tv, a.v, rows, D, elem, kTile, C::BOXC) ||
+                   !make_tmap_2d_sw128(&to, a.o, rows, D, elem, 32, C::BOXC))
             return cudaErrorInvalidValue;
         tql = tq;
         tkl = tk;
     }
+    if constexpr (TF32) to = tq;  // unused: fp32 O is stored directly
     static bool attr_set = false;
     if (!attr_set) {
         cudaError_t e = cudaFuncSetAttribute(fa_fwd_kernel<TF32, D, false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -760,13 +798,13 @@ static cudaError_t launch_fwd_t(const FwdArgs& a, cudaStream_t stream, int* nlau
     if (a.ev_begin) cudaEventRecord(a.ev_begin, stream);
     p.drop = a.drop;
     if (p.cu_seqlens)
-        fa_fwd_kernel<TF32, D, !TF32><<<grid, C::THREADS, C::SMEM, stream>>>(tq, tk, tv, tql, tkl, p);
+        fa_fwd_kernel<TF32, D, !TF32><<<grid, C::THREADS, C::SMEM, stream>>>(tq, tk, tv, tql, tkl, to, p);
     else if (a.dropout && !TF32)
-        fa_fwd_kernel<TF32, D, false, !TF32><<<grid, C::THREADS, C::SMEM, stream>>>(tq, tk, tv, tql, tkl, p);
+        fa_fwd_kernel<TF32, D, false, !TF32><<<grid, C::THREADS, C::SMEM, stream>>>(tq, tk, tv, tql, tkl, to, p);
     else if (a.blockmask && !TF32)
-        fa_fwd_kernel<TF32, D, false, false, !TF32><<<grid, C::THREADS, C::SMEM, stream>>>(tq, tk, tv, tql, tkl, p);
+        fa_fwd_kernel<TF32, D, false, false, !TF32><<<grid, C::THREADS, C::SMEM, stream>>>(tq, tk, tv, tql, tkl, to, p);
     else
-        fa_fwd_kernel<TF32, D, false><<<grid, C::THREADS, C::SMEM, stream>>>(tq, tk, tv, tql, tkl, p);
+        fa_fwd_kernel<TF32, D, false><<<grid, C::THREADS, C::SMEM, stream>>>(tq, tk, tv, tql, tkl, to, p);
     if (a.ev_end) cudaEventRecord(a.ev_end, stream);
     ++launches;
     *nlaunch = launches;
