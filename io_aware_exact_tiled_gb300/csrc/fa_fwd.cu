@@ -221,6 +221,20 @@ __global__ void __launch_bounds__(384, 1)
         }
         mbar_init(drain, 1);
         fence_barrier_init();
+        // Both Q tiles are requested at once, by the thread that set up the
+        // barriers (the producer), before TMEM allocation and the CTA-wide
+        // barrier: the Q and first K loads are the CTA's start-up latency.
+        mbar_arrive_expect_tx(bar_q, (act1 ? 2 : 1) * C::SPLIT * C::TILE_BYTES);
+        for (int s = 0; s < (act1 ? 2 : 1); ++s)
+            for (int r = 0; r < C::NREG; ++r) {
+                uint8_t* dq = sm + C::Q_OFF + s * C::SPLIT * C::TILE_BYTES + r * 16384;
+                if (varlen)
+                    tma_load_3d(dq, &tmQ, r * C::BOXC, h, seq0 + (qb0 + s) * kTile, bar_q);
+                else
+                    tma_load_2d(dq, &tmQ, r * C::BOXC, bh * N + (qb0 + s) * kTile, bar_q);
+                if constexpr (TF32)
+                    tma_load_2d(dq + C::TILE_BYTES, &tmQlo, r * C::BOXC, bh * N + (qb0 + s) * kTile, bar_q);
+            }
     }
     if (warp == 0 && lane == 0) {
         tma_prefetch_desc(&tmQ);
@@ -295,7 +309,6 @@ __global__ void __launch_bounds__(384, 1)
     if (warp == 0) {
         // ------------------------------------------------------------ producer
         if (lane == 0) {
-            const int qrow0 = bh * N + qb0 * kTile;
             // rows row .. row + 127 of this head (packed: of this sequence)
             auto load_rows = [&](void* dst, const CUtensorMap* m, int x, int row, uint64_t* bar) {
                 if (varlen)
@@ -303,13 +316,6 @@ __global__ void __launch_bounds__(384, 1)
                 else
                     tma_load_2d(dst, m, x, bh * N + row, bar);
             };
-            mbar_arrive_expect_tx(bar_q, (act1 ? 2 : 1) * C::SPLIT * C::TILE_BYTES);
-            for (int s = 0; s < (act1 ? 2 : 1); ++s)
-                for (int r = 0; r < C::NREG; ++r) {
-                    uint8_t* dq = sm + C::Q_OFF + s * C::SPLIT * C::TILE_BYTES + r * 16384;
-                    load_rows(dq, &tmQ, r * C::BOXC, (qb0 + s) * kTile, bar_q);
-                    if constexpr (TF32) tma_load_2d(dq + C::TILE_BYTES, &tmQlo, r * C::BOXC, qrow0 + s * kTile, bar_q);
-                }
             int nk = 0, nv = 0;  // K and V tiles whose loads were issued
             for (int t = next_tile(0, 3u); t < hi; t = next_tile(t + 1, 3u)) {
                 if (!need_of(t)) continue;
@@ -414,14 +420,15 @@ __global__ void __launch_bounds__(384, 1)
                 umma_commit(leader, &k_empty[kst]);  // S GEMMs reading this K stage are all issued
                 ++u;
             }
-            for (int s = 0; ok && s < 2; ++s)
+            // one commit per Q tile after its last P V: the epilogue waits on
+            // it. Q tile 0 usually finishes a tile earlier (with a causal
+            // mask Q tile 1 alone sees the last key tile), so its commit goes
+            // out before Q tile 1's last P V waits for its probabilities.
+            for (int s = 0; ok && s < 2; ++s) {
                 if (pend_stage[s] >= 0 && !issue_pv(s)) ok = false;
-#undef issue_pv
-            // one commit per Q tile after its last P V: the epilogue waits on it
-            if (ok) {
-                umma_commit(leader, &o_done[0]);
-                umma_commit(leader, &o_done[1]);
+                if (ok) umma_commit(leader, &o_done[s]);
             }
+#undef issue_pv
             // wait for every MMA issued so far before TMEM can be released
             umma_commit(leader, drain);
             mbar_wait_teardown(drain, 0, 200000000ull);
@@ -622,16 +629,22 @@ __global__ void __launch_bounds__(384, 1)
                 const int wrow0 = qb * kTile + wq * 32;
                 const bool tma_rows = !TF32 && n > 0 && wrow0 + 32 <= N;
                 uint8_t* ob = sm + C::Q_OFF + s * C::SPLIT * C::TILE_BYTES + wq * (C::NREG * 4096);
+                // all of O's TMEM loads in flight before the first wait
+                uint32_t oa[D / 32][32];
+                if (n > 0) {
+#pragma unroll
+                    for (int c = 0; c < D / 32; ++c) tmem_ld32(tl + 128 + c * 32, oa[c]);
+#pragma unroll
+                    for (int c = 0; c < D / 32; ++c) tmem_ld_wait(oa[c]);
+                } else {
+#pragma unroll
+                    for (int c = 0; c < D / 32; ++c)
+#pragma unroll
+                        for (int i = 0; i < 32; ++i) oa[c][i] = 0u;
+                }
 #pragma unroll
                 for (int c = 0; c < D / 32; ++c) {
-                    uint32_t ov[32];
-                    if (n > 0) {
-                        tmem_ld32(tl + 128 + c * 32, ov);
-                        tmem_ld_wait(ov);
-                    } else {
-#pragma unroll
-                        for (int i = 0; i < 32; ++i) ov[i] = 0u;
-                    }
+                    const uint32_t* ov = oa[c];
                     if constexpr (!TF32) {
                         uint4* dst = reinterpret_cast<uint4*>(static_cast<uint16_t*>(p.o) + orow + c * 32);
 #pragma unroll
