@@ -112,7 +112,8 @@ template <int D, bool VARLEN, bool DROPOUT = false, bool TMASK = false>
 __global__ void __launch_bounds__(512, 1)
     fa_bwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                   const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmdO,
-                  const __grid_constant__ CUtensorMap tmdQacc, const __grid_constant__ BwdParams p) {
+                  const __grid_constant__ CUtensorMap tmdQacc, const __grid_constant__ CUtensorMap tmdK,
+                  const __grid_constant__ CUtensorMap tmdV, const __grid_constant__ BwdParams p) {
     using C = BwdCfg<D>;
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     // 1024-byte aligned base for the swizzled tiles; offsetting the shared
@@ -530,25 +531,66 @@ __global__ void __launch_bounds__(512, 1)
             uint16_t* out = static_cast<uint16_t*>(g == 0 ? p.dv : p.dk) + orow;
             const uint32_t col = g == 0 ? C::COL_DV : C::COL_DK;
             const float mul = g == 0 ? (DROPOUT ? p.drop.inv_keep : 1.f) : p.scale;
+            // A warp whose 32 keys all lie in the sequence stages its rows in
+            // the V (dV) or K (dK) tile buffer, free once every GEMM is
+            // complete, as [32 x 64] swizzled boxes, and writes them with one
+            // bulk tensor store per box; other warps (and a key tile that saw
+            // no query tile) store their valid rows directly.
+            const int wkey0 = j * kTile + (warp & 3) * 32;
+            const bool tma_rows = u > 0 && wkey0 + 32 <= N;
+            uint8_t* ob = sm + (g == 0 ? C::V_OFF : C::K_OFF) + (warp & 3) * (C::NREG * 4096);
+            // two 32-column TMEM loads in flight at a time (128 registers a
+            // thread at 512 threads leave no room for all of them)
 #pragma unroll
-            for (int c = 0; c < D / 32; ++c) {
-                uint32_t v[32];
+            for (int c2 = 0; c2 < D / 64; ++c2) {
+                uint32_t va[2][32];
                 if (u > 0) {
-                    tmem_ld32(tl + col + c * 32, v);
-                    tmem_ld_wait(v);
+                    tmem_ld32(tl + col + c2 * 64, va[0]);
+                    tmem_ld32(tl + col + c2 * 64 + 32, va[1]);
+                    tmem_ld_wait(va[0]);
+                    tmem_ld_wait(va[1]);
                 } else {
 #pragma unroll
-                    for (int e = 0; e < 32; ++e) v[e] = 0u;
+                    for (int e = 0; e < 32; ++e) va[0][e] = va[1][e] = 0u;
                 }
-                if (!row_ok) continue;
-                uint4* dst = reinterpret_cast<uint4*>(out + c * 32);
 #pragma unroll
-                for (int q = 0; q < 4; ++q)
-                    dst[q] = make_uint4(
-                        pack_bf16x2(__uint_as_float(v[8 * q]) * mul, __uint_as_float(v[8 * q + 1]) * mul),
-                        pack_bf16x2(__uint_as_float(v[8 * q + 2]) * mul, __uint_as_float(v[8 * q + 3]) * mul),
-                        pack_bf16x2(__uint_as_float(v[8 * q + 4]) * mul, __uint_as_float(v[8 * q + 5]) * mul),
-                        pack_bf16x2(__uint_as_float(v[8 * q + 6]) * mul, __uint_as_float(v[8 * q + 7]) * mul));
+                for (int half = 0; half < 2; ++half) {
+                    const int c = 2 * c2 + half;
+                    const uint32_t* v = va[half];
+                    uint4* dst = reinterpret_cast<uint4*>(out + c * 32);
+#pragma unroll
+                    for (int q = 0; q < 4; ++q) {
+                        const uint4 w = make_uint4(
+                            pack_bf16x2(__uint_as_float(v[8 * q]) * mul, __uint_as_float(v[8 * q + 1]) * mul),
+                            pack_bf16x2(__uint_as_float(v[8 * q + 2]) * mul, __uint_as_float(v[8 * q + 3]) * mul),
+                            pack_bf16x2(__uint_as_float(v[8 * q + 4]) * mul, __uint_as_float(v[8 * q + 5]) * mul),
+                            pack_bf16x2(__uint_as_float(v[8 * q + 6]) * mul, __uint_as_float(v[8 * q + 7]) * mul));
+                        if (tma_rows) {
+                            const int ch = (half << 2) + q;  // 16-byte chunk within the 128-byte row
+                            sts128(smem_u32(ob + c2 * 4096 + lane * 128 + ((ch ^ (lane & 7)) << 4)), w.x, w.y, w.z,
+                                   w.w);
+                        } else if (row_ok) {
+                            dst[q] = w;
+                        }
+                    }
+                }
+            }
+            if (tma_rows) {
+                fence_proxy_async_smem();
+                __syncwarp();
+                if (lane == 0) {
+                    const CUtensorMap* m = g == 0 ? &tmdV : &tmdK;
+#pragma unroll
+                    for (int rg = 0; rg < C::NREG; ++rg) {
+                        if (varlen)
+                            tma_store_3d(m, rg * 64, h, seq0 + wkey0, ob + rg * 4096);
+                        else
+                            tma_store_2d(m, rg * 64, bh * N + wkey0, ob + rg * 4096);
+                    }
+                    bulk_commit_group();
+                    // the shared buffer must be read out before the CTA exits
+                    bulk_wait_group_read0();
+                }
             }
         }
     } else if (warp >= 12) {
@@ -783,20 +825,24 @@ static cudaError_t launch_bwd_t(const BwdArgs& a, cudaStream_t stream, int* nlau
     const bool varlen = a.cu_seqlens != nullptr;
     // rows of the [rows, d] views: B * H * N, or total * H for a packed batch
     const uint64_t rows = varlen ? static_cast<uint64_t>(a.total) * a.H : static_cast<uint64_t>(a.B) * a.H * a.N;
-    CUtensorMap tq, tk, tv, tdo, tdq;
+    CUtensorMap tq, tk, tv, tdo, tdq, tdk, tdv;
     if (varlen) {
         const uint64_t tot = static_cast<uint64_t>(a.total);
         if (!make_tmap_packed_sw128(&tq, a.q, tot, a.H, D, 2, kTile, 64) ||
             !make_tmap_packed_sw128(&tk, a.k, tot, a.H, D, 2, kTile, 64) ||
             !make_tmap_packed_sw128(&tv, a.v, tot, a.H, D, 2, kTile, 64) ||
             !make_tmap_packed_sw128(&tdo, a.dout, tot, a.H, D, 2, kTile, 64) ||
-            !make_tmap_packed_sw128(&tdq, a.dq_accum, tot, a.H, D, 4, 32, 32))
+            !make_tmap_packed_sw128(&tdq, a.dq_accum, tot, a.H, D, 4, 32, 32) ||
+            !make_tmap_packed_sw128(&tdk, a.dk, tot, a.H, D, 2, 32, 64) ||
+            !make_tmap_packed_sw128(&tdv, a.dv, tot, a.H, D, 2, 32, 64))
             return cudaErrorInvalidValue;
     } else if (!make_tmap_2d_sw128(&tq, a.q, rows, D, 2, kTile, 64) ||
                !make_tmap_2d_sw128(&tk, a.k, rows, D, 2, kTile, 64) ||
                !make_tmap_2d_sw128(&tv, a.v, rows, D, 2, kTile, 64) ||
                !make_tmap_2d_sw128(&tdo, a.dout, rows, D, 2, kTile, 64) ||
-               !make_tmap_2d_sw128(&tdq, a.dq_accum, rows, D, 4, 32, 32))
+               !make_tmap_2d_sw128(&tdq, a.dq_accum, rows, D, 4, 32, 32) ||
+               !make_tmap_2d_sw128(&tdk, a.dk, rows, D, 2, 32, 64) ||
+               !make_tmap_2d_sw128(&tdv, a.dv, rows, D, 2, 32, 64))
         return cudaErrorInvalidValue;
     static bool attr_set = false;
     if (!attr_set) {
@@ -855,13 +901,13 @@ static cudaError_t launch_bwd_t(const BwdArgs& a, cudaStream_t stream, int* nlau
     if (a.ev_begin) cudaEventRecord(a.ev_begin, stream);
     p.drop = a.drop;
     if (varlen)
-        fa_bwd_kernel<D, true><<<grid, C::THREADS, C::SMEM, stream>>>(tq, tk, tv, tdo, tdq, p);
+        fa_bwd_kernel<D, true><<<grid, C::THREADS, C::SMEM, stream>>>(tq, tk, tv, tdo, tdq, tdk, tdv, p);
     else if (a.dropout)
-        fa_bwd_kernel<D, false, true><<<grid, C::THREADS, C::SMEM, stream>>>(tq, tk, tv, tdo, tdq, p);
+        fa_bwd_kernel<D, false, true><<<grid, C::THREADS, C::SMEM, stream>>>(tq, tk, tv, tdo, tdq, tdk, tdv, p);
     else if (a.blockmask)
-        fa_bwd_kernel<D, false, false, true><<<grid, C::THREADS, C::SMEM, stream>>>(tq, tk, tv, tdo, tdq, p);
+        fa_bwd_kernel<D, false, false, true><<<grid, C::THREADS, C::SMEM, stream>>>(tq, tk, tv, tdo, tdq, tdk, tdv, p);
     else
-        fa_bwd_kernel<D, false><<<grid, C::THREADS, C::SMEM, stream>>>(tq, tk, tv, tdo, tdq, p);
+        fa_bwd_kernel<D, false><<<grid, C::THREADS, C::SMEM, stream>>>(tq, tk, tv, tdo, tdq, tdk, tdv, p);
     if (a.ev_end) cudaEventRecord(a.ev_end, stream);
     const long long n8 = nrows * D / 8;
     long long blocks = (n8 + 255) / 256;
