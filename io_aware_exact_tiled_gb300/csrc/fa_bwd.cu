@@ -86,6 +86,7 @@ struct BwdParams {
     int total;                  // tokens of the packed batch
     long long lpad;             // rows per head of nlse2 / ndelta (packed)
     DropoutArgs drop;           // dropout on the probabilities (DROPOUT kernel)
+    int group;                  // > 0: causal head-group order on a 1D grid (heads per group)
 };
 
 constexpr float kLog2e = 1.4426950408889634f;
@@ -146,7 +147,21 @@ __global__ void __launch_bounds__(512, 1)
     // Head-major order: the key blocks of one head are adjacent in the grid
     // (j = 0, the longest causal column, first), so the CTAs running at any
     // time share the Q, dO and dQ-accumulator rows of a few heads in L2.
-    const int j = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
+    // With a causal mask that order ends on the long columns of the last
+    // heads; there the grid is 1D and runs groups of p.group heads in turn,
+    // longest column first across the heads of a group (sized so that a
+    // group's rows still fit in L2), so that the kernel ends on short CTAs.
+    int j = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
+    if (p.group > 0) {
+        const int Tg = p.mask.T, nb = p.B * p.H;
+        const int L = static_cast<int>(blockIdx.x);
+        const int gi = L / (p.group * Tg), r = L - gi * p.group * Tg;
+        const int g0 = gi * p.group, gsz = min(p.group, nb - g0);
+        j = r / gsz;
+        const int bhx = g0 + (r - j * gsz);
+        b = bhx / p.H;
+        h = bhx - b * p.H;
+    }
     // A packed variable-length batch puts sequence b at tokens seq0 ..
     // seq0 + N - 1 of [total, H, d] tensors; its rows of -L and -D start at
     // lrow0, a multiple of 128 (so that they can be bulk-copied). Key blocks
@@ -897,7 +912,17 @@ static cudaError_t launch_bwd_t(const BwdArgs& a, cudaStream_t stream, int* nlau
     p.cu_tiles = a.cu_tiles;
     p.total = a.total;
     p.lpad = a.lpad;
-    dim3 grid((a.N + kTile - 1) / kTile, a.H, a.B);
+    // causal [B, H, N, d] calls: head groups whose Q, dO (bf16) and dQ
+    // accumulator (fp32) rows take at most 64 MiB of L2
+    const int Tn = (a.N + kTile - 1) / kTile;
+    p.group = 0;
+    if (a.causal && !varlen) {
+        const long long per_head = 8LL * a.N * D;
+        long long g = (64LL << 20) / per_head;
+        g = g < 1 ? 1 : g;
+        p.group = static_cast<int>(g < a.B * a.H ? g : a.B * a.H);
+    }
+    const dim3 grid = p.group > 0 ? dim3(static_cast<unsigned>(Tn) * a.H * a.B) : dim3(Tn, a.H, a.B);
     if (a.ev_begin) cudaEventRecord(a.ev_begin, stream);
     p.drop = a.drop;
     if (varlen)
