@@ -89,6 +89,7 @@ struct FwdParams {
     int total;                  // tokens of the packed batch
     DropoutArgs drop;           // dropout on the probabilities (DROPOUT kernels)
     int head_major;             // grid (pairs, H, B) instead of (H, B, pairs)
+    int group;                  // > 0: 1D grid of head groups (heads per group), longest pair first in each
 };
 
 // Issue state of the MMA thread, per Q tile s of the CTA.
@@ -169,14 +170,28 @@ __global__ void __launch_bounds__(384, 1)
     const WaitCtx cx{abort_flag, p.status};
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    // Longest-first order across all heads (the query-tile pair index is the
-    // slowest grid dimension): with causal masks the longest CTAs start first
-    // and the short ones fill the tail.
+    // Longest-first order (the query-tile pair index is the slowest grid
+    // dimension): with causal masks the longest CTAs start first and the
+    // short ones fill the tail. Causal [B, H, N, d] calls run it within
+    // groups of p.group heads in turn on a 1D grid, the group sized so that
+    // its K and V stay in L2 (across all heads the resident CTAs' K and V
+    // tiles would span every head and part of them would be read again).
     // Without causal masking every pair of a head costs about the same, and
     // a tile mask makes the pairs share few key tiles, so the grid is then
     // head-major instead: the CTAs running together read one head's K and V,
     // which stays in L2.
-    const int h = p.head_major ? blockIdx.y : blockIdx.x, b = p.head_major ? blockIdx.z : blockIdx.y;
+    int h = p.head_major ? blockIdx.y : blockIdx.x, b = p.head_major ? blockIdx.z : blockIdx.y;
+    int zq = static_cast<int>(p.head_major ? blockIdx.x : blockIdx.z);  // pair rank, longest first
+    if (!VARLEN && p.group > 0) {
+        const int np = (p.mask.T + 1) >> 1, nb = p.B * p.H;
+        const int L = static_cast<int>(blockIdx.x);
+        const int gi = L / (p.group * np), r = L - gi * p.group * np;
+        const int g0 = gi * p.group, gsz = min(p.group, nb - g0);
+        zq = r / gsz;
+        const int bhx = g0 + (r - zq * gsz);
+        b = bhx / p.H;
+        h = bhx - b * p.H;
+    }
     // A packed variable-length batch puts sequence b at tokens seq0 ..
     // seq0 + N - 1 of [total, H, d] tensors (the grid covers the longest
     // sequence; CTAs past the end of a shorter one leave at once). Otherwise
@@ -193,7 +208,7 @@ __global__ void __launch_bounds__(384, 1)
         T = (N + kTile - 1) / kTile;
     }
     const int npairs = (T + 1) >> 1;
-    const int qp = npairs - 1 - static_cast<int>(p.head_major ? blockIdx.x : blockIdx.z);
+    const int qp = npairs - 1 - zq;
     if (qp < 0) return;  // uniform over the CTA, before any barrier or TMEM use
     const int qb0 = 2 * qp, qb1 = 2 * qp + 1;
     const bool act1 = qb1 < T;
@@ -807,7 +822,17 @@ static cudaError_t launch_fwd_t(const FwdArgs& a, cudaStream_t stream, int* nlau
     p.total = a.total;
     const int T = (a.N + kTile - 1) / kTile;
     p.head_major = (a.blockmask && !a.causal && !p.cu_seqlens) ? 1 : 0;
-    const dim3 grid = p.head_major ? dim3((T + 1) / 2, a.H, a.B) : dim3(a.H, a.B, (T + 1) / 2);
+    // causal [B, H, N, d] calls: head groups whose K and V take at most 64 MiB
+    p.group = 0;
+    if (a.causal && !p.cu_seqlens) {
+        const long long per_head = 2LL * a.N * D * elem;
+        long long g = (64LL << 20) / per_head;
+        g = g < 1 ? 1 : g;
+        p.group = static_cast<int>(g < a.B * a.H ? g : a.B * a.H);
+    }
+    const dim3 grid = p.group > 0     ? dim3(static_cast<unsigned>((T + 1) / 2) * a.H * a.B)
+                      : p.head_major ? dim3((T + 1) / 2, a.H, a.B)
+                                     : dim3(a.H, a.B, (T + 1) / 2);
     if (a.ev_begin) cudaEventRecord(a.ev_begin, stream);
     p.drop = a.drop;
     if (p.cu_seqlens)
