@@ -50,52 +50,87 @@ __device__ __forceinline__ int pow2_scale_exp(float amax) {
 }
 
 // ---------------------------------------------------------------------------
-// Q and K: one CTA per (128-row block, head). Each warp rotates 16 rows:
-// lane l holds columns 4l .. 4l+3; the Walsh-Hadamard butterflies with
-// strides 1 and 2 stay in the lane, strides 4 .. 64 use shuffles. The
-// butterflies only add and subtract bf16 values, which fp32 holds exactly.
+// Q and K: one CTA per (128-row block, head); four lanes per row, eight rows
+// per warp at a time, two passes. Lane t of a row's quad holds columns
+// 32 k + 8 t + e (k, e = 0..3, 0..7), read as four 16-byte pieces (a quad
+// reads 64 contiguous bytes per instruction). The Walsh-Hadamard butterflies
+// over column bits 0-2 (e) and 5-6 (k) stay in the lane; bits 3-4 (t) use
+// two shuffle stages. The stages commute (the Sylvester matrix is the
+// Kronecker power of H_2), so their order is free.
 // ---------------------------------------------------------------------------
+__device__ __forceinline__ void fwht8_inlane(float (&a)[8]) {
+#pragma unroll
+    for (int m = 1; m < 8; m <<= 1)
+#pragma unroll
+        for (int e = 0; e < 8; ++e)
+            if (!(e & m)) {
+                const float x = a[e], y = a[e + m];
+                a[e] = x + y;
+                a[e + m] = x - y;
+            }
+}
+
 __global__ void __launch_bounds__(256) fa_fp8_qk_kernel(const uint16_t* __restrict__ x, const float* __restrict__ signs,
                                                         uint8_t* __restrict__ x8, int* __restrict__ exps, int N) {
-    constexpr int RPW = kTile / 8;  // rows per warp, kept in registers until the block scale is known
     __shared__ float wmax[8];
     __shared__ int e_sh;
+    __shared__ float sg_sh[kD8];
     const int blk = blockIdx.x, bh = blockIdx.y;
     const int T = N / kTile;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int t = lane & 3, rq = lane >> 2;  // column quarter, row within the warp's 8
     const size_t row0 = static_cast<size_t>(bh) * N + static_cast<size_t>(blk) * kTile;
-    float sg[4];
+    if (threadIdx.x < kD8) sg_sh[threadIdx.x] = signs[threadIdx.x];
+    // both passes' rows are requested before any arithmetic
+    uint4 raw[2][4];
 #pragma unroll
-    for (int t = 0; t < 4; ++t) sg[t] = signs[lane * 4 + t];
+    for (int ps = 0; ps < 2; ++ps) {
+        const uint16_t* src = x + (row0 + warp * 16 + ps * 8 + rq) * kD8;
+#pragma unroll
+        for (int k = 0; k < 4; ++k) raw[ps][k] = *reinterpret_cast<const uint4*>(src + 32 * k + 8 * t);
+    }
+    __syncthreads();
+    float y[2][4][8];
     float amax = 0.f;
-    float y[RPW][4];
 #pragma unroll
-    for (int j = 0; j < RPW; ++j) {
-        const int rr = warp + 8 * j;
-        const uint2 w = *reinterpret_cast<const uint2*>(x + (row0 + rr) * kD8 + lane * 4);
-        float a[4] = {__uint_as_float(w.x << 16) * sg[0], __uint_as_float(w.x & 0xFFFF0000u) * sg[1],
-                      __uint_as_float(w.y << 16) * sg[2], __uint_as_float(w.y & 0xFFFF0000u) * sg[3]};
-        // in-lane strides 1 and 2
-        float b0 = a[0] + a[1], b1 = a[0] - a[1], b2 = a[2] + a[3], b3 = a[2] - a[3];
-        a[0] = b0 + b2;
-        a[1] = b1 + b3;
-        a[2] = b0 - b2;
-        a[3] = b1 - b3;
-        // strides 4 .. 64: partner lane l ^ (stride / 4)
+    for (int ps = 0; ps < 2; ++ps) {
 #pragma unroll
-        for (int m = 1; m < 32; m <<= 1) {
-            const bool upper = (lane & m) != 0;
+        for (int k = 0; k < 4; ++k) {
+            const uint32_t u[4] = {raw[ps][k].x, raw[ps][k].y, raw[ps][k].z, raw[ps][k].w};
 #pragma unroll
-            for (int t = 0; t < 4; ++t) {
-                const float o = __shfl_xor_sync(0xffffffffu, a[t], m);
-                a[t] = upper ? o - a[t] : a[t] + o;
+            for (int h = 0; h < 4; ++h) {
+                const int c = 32 * k + 8 * t + 2 * h;
+                y[ps][k][2 * h] = __uint_as_float(u[h] << 16) * sg_sh[c];
+                y[ps][k][2 * h + 1] = __uint_as_float(u[h] & 0xFFFF0000u) * sg_sh[c + 1];
             }
+            fwht8_inlane(y[ps][k]);  // column bits 0-2
+        }
+        // column bits 5-6: butterflies across k
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+            float b0 = y[ps][0][e] + y[ps][1][e], b1 = y[ps][0][e] - y[ps][1][e];
+            float b2 = y[ps][2][e] + y[ps][3][e], b3 = y[ps][2][e] - y[ps][3][e];
+            y[ps][0][e] = b0 + b2;
+            y[ps][1][e] = b1 + b3;
+            y[ps][2][e] = b0 - b2;
+            y[ps][3][e] = b1 - b3;
+        }
+        // column bits 3-4: partner lanes t ^ 1, t ^ 2
+#pragma unroll
+        for (int m = 1; m < 4; m <<= 1) {
+            const bool upper = (t & m) != 0;
+#pragma unroll
+            for (int k = 0; k < 4; ++k)
+#pragma unroll
+                for (int e = 0; e < 8; ++e) {
+                    const float o = __shfl_xor_sync(0xffffffffu, y[ps][k][e], m);
+                    y[ps][k][e] = upper ? o - y[ps][k][e] : y[ps][k][e] + o;
+                }
         }
 #pragma unroll
-        for (int t = 0; t < 4; ++t) {
-            y[j][t] = a[t];
-            amax = fmaxf(amax, fabsf(a[t]));
-        }
+        for (int k = 0; k < 4; ++k)
+#pragma unroll
+            for (int e = 0; e < 8; ++e) amax = fmaxf(amax, fabsf(y[ps][k][e]));
     }
 #pragma unroll
     for (int off = 16; off > 0; off >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, off));
@@ -111,27 +146,41 @@ __global__ void __launch_bounds__(256) fa_fp8_qk_kernel(const uint16_t* __restri
     __syncthreads();
     const float inv = exp2i(-e_sh);
 #pragma unroll
-    for (int j = 0; j < RPW; ++j) {
-        const int rr = warp + 8 * j;
-        const uint32_t lo = pack_e4m3x2(y[j][0] * inv, y[j][1] * inv), hi = pack_e4m3x2(y[j][2] * inv, y[j][3] * inv);
-        *reinterpret_cast<uint32_t*>(x8 + (row0 + rr) * kD8 + lane * 4) = lo | (hi << 16);
+    for (int ps = 0; ps < 2; ++ps) {
+        uint8_t* dst = x8 + (row0 + warp * 16 + ps * 8 + rq) * kD8;
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+            uint2 w;
+            w.x = pack_e4m3x2(y[ps][k][0] * inv, y[ps][k][1] * inv) | (pack_e4m3x2(y[ps][k][2] * inv, y[ps][k][3] * inv) << 16);
+            w.y = pack_e4m3x2(y[ps][k][4] * inv, y[ps][k][5] * inv) | (pack_e4m3x2(y[ps][k][6] * inv, y[ps][k][7] * inv) << 16);
+            *reinterpret_cast<uint2*>(dst + 32 * k + 8 * t) = w;
+        }
     }
 }
 
-// Per-head max |v| (as float bits; nonnegative floats order like integers).
+// Per-head max |v| (as float bits; nonnegative floats order like integers);
+// four independent 16-byte loads in flight per thread.
 __global__ void __launch_bounds__(256) fa_fp8_vmax_kernel(const uint16_t* __restrict__ v, int* __restrict__ vmax_bits,
                                                           long long per_head) {
     const int bh = blockIdx.y;
     const uint4* src = reinterpret_cast<const uint4*>(v + static_cast<size_t>(bh) * per_head);
     const long long n8 = per_head / 8;
+    const long long stride = static_cast<long long>(gridDim.x) * 256;
     float m = 0.f;
-    for (long long i = static_cast<long long>(blockIdx.x) * 256 + threadIdx.x; i < n8;
-         i += static_cast<long long>(gridDim.x) * 256) {
-        const uint4 w = src[i];
-        const uint32_t u[4] = {w.x, w.y, w.z, w.w};
+    for (long long i0 = static_cast<long long>(blockIdx.x) * 256 + threadIdx.x; i0 < n8; i0 += 4 * stride) {
+        uint4 w[4];
 #pragma unroll
-        for (int e = 0; e < 4; ++e)
-            m = fmaxf(m, fmaxf(fabsf(__uint_as_float(u[e] << 16)), fabsf(__uint_as_float(u[e] & 0xFFFF0000u))));
+        for (int q = 0; q < 4; ++q) {
+            const long long i = i0 + q * stride;
+            w[q] = i < n8 ? src[i] : make_uint4(0u, 0u, 0u, 0u);
+        }
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+            const uint32_t u[4] = {w[q].x, w[q].y, w[q].z, w[q].w};
+#pragma unroll
+            for (int e = 0; e < 4; ++e)
+                m = fmaxf(m, fmaxf(fabsf(__uint_as_float(u[e] << 16)), fabsf(__uint_as_float(u[e] & 0xFFFF0000u))));
+        }
     }
 #pragma unroll
     for (int off = 16; off > 0; off >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, off));
@@ -139,38 +188,57 @@ __global__ void __launch_bounds__(256) fa_fp8_vmax_kernel(const uint16_t* __rest
 }
 
 // V -> E4M3 with the head's scale, transposed to [d][keys] (the P V product
-// needs K-major operands): one CTA per (128-key block, head).
+// needs K-major operands): one CTA per (128-key block, head). Thread (lane,
+// warp) converts keys 4 lane .. 4 lane + 3 of columns 16 warp .. 16 warp + 15,
+// so each column's four key bytes form one 32-bit word of the transposed
+// tile (a warp writes 128 contiguous bytes of a row of it).
 __global__ void __launch_bounds__(256) fa_fp8_v_kernel(const uint16_t* __restrict__ v,
                                                        const int* __restrict__ vmax_bits, uint8_t* __restrict__ vt8,
                                                        int* __restrict__ vexp, int N) {
-    __shared__ uint8_t t8[kD8][kTile + 16];
+    __shared__ __align__(16) uint32_t t8w[kD8][kTile / 4 + 4];  // [column][key quad]; +4 words keep rows 16-byte aligned
     const int blk = blockIdx.x, bh = blockIdx.y;
     const int e = pow2_scale_exp(__int_as_float(vmax_bits[bh]));
     if (blk == 0 && threadIdx.x == 0) vexp[bh] = e;
     const float inv = exp2i(-e);
     const size_t row0 = static_cast<size_t>(bh) * N + static_cast<size_t>(blk) * kTile;
-    // thread: key kk = threadIdx.x / 2, 64 columns starting at 64 * (threadIdx.x & 1)
-    const int kk = threadIdx.x >> 1, c0 = (threadIdx.x & 1) * 64;
-    const uint16_t* src = v + (row0 + kk) * kD8 + c0;
+    const int kq = threadIdx.x & 31, cg = threadIdx.x >> 5;
+    uint4 w[4][2];
 #pragma unroll
-    for (int c = 0; c < 64; c += 8) {
-        const uint4 w = *reinterpret_cast<const uint4*>(src + c);
-        const uint32_t u[4] = {w.x, w.y, w.z, w.w};
+    for (int r = 0; r < 4; ++r) {
+        const uint4* src = reinterpret_cast<const uint4*>(v + (row0 + 4 * kq + r) * kD8 + 16 * cg);
+        w[r][0] = src[0];
+        w[r][1] = src[1];
+    }
 #pragma unroll
-        for (int e2 = 0; e2 < 4; ++e2) {
-            const uint32_t b = pack_e4m3x2(__uint_as_float(u[e2] << 16) * inv, __uint_as_float(u[e2] & 0xFFFF0000u) * inv);
-            t8[c0 + c + 2 * e2][kk] = static_cast<uint8_t>(b & 0xFF);
-            t8[c0 + c + 2 * e2 + 1][kk] = static_cast<uint8_t>(b >> 8);
+    for (int h = 0; h < 2; ++h) {
+        uint32_t u[4][4];
+#pragma unroll
+        for (int r = 0; r < 4; ++r) {
+            u[r][0] = w[r][h].x;
+            u[r][1] = w[r][h].y;
+            u[r][2] = w[r][h].z;
+            u[r][3] = w[r][h].w;
+        }
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+#pragma unroll
+            for (int half = 0; half < 2; ++half) {
+                // column 16 cg + 8 h + 2 q + half of keys 4 kq .. 4 kq + 3
+                float x[4];
+#pragma unroll
+                for (int r = 0; r < 4; ++r)
+                    x[r] = __uint_as_float(half ? (u[r][q] & 0xFFFF0000u) : (u[r][q] << 16)) * inv;
+                t8w[16 * cg + 8 * h + 2 * q + half][kq] = pack_e4m3x2(x[0], x[1]) | (pack_e4m3x2(x[2], x[3]) << 16);
+            }
         }
     }
     __syncthreads();
-    // rows of V^T: [bh * d + dd][blk * 128 .. + 127]
+    // rows of V^T: [bh * d + dd][blk * 128 .. + 127], 16 bytes per thread and step
     for (int i = threadIdx.x; i < kD8 * 8; i += 256) {
         const int dd = i >> 3, part = i & 7;
-        const uint32_t* s4 = reinterpret_cast<const uint32_t*>(&t8[dd][part * 16]);
-        uint4 w = make_uint4(s4[0], s4[1], s4[2], s4[3]);
+        const uint4 o = *reinterpret_cast<const uint4*>(&t8w[dd][part * 4]);
         *reinterpret_cast<uint4*>(vt8 + (static_cast<size_t>(bh) * kD8 + dd) * N + static_cast<size_t>(blk) * kTile +
-                                  part * 16) = w;
+                                  part * 16) = o;
     }
 }
 
