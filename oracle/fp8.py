@@ -20,8 +20,11 @@ silent:
    random signs drawn once and passed in. R is orthogonal, so
    (Q R)(K R)^T = Q K^T: the rotation changes only the quantisation error.
    The values quantised are Q diag(s) H_d = sqrt(d) Q R (and the same for K),
-   with the factor 1/d folded into the score scale: a Hadamard transform of
-   bf16 inputs is exact in fp32, so both sides quantise the same numbers.
+   with the factor 1/d folded into the score scale. Each output is a signed
+   sum of bf16 inputs, which fp32 holds exactly unless their exponents span
+   more than about 16 binades; a rounding there (2^-24 relative) can change
+   an E4M3 code only for a value that close to a rounding boundary, so the
+   CUDA side's fp32 transform quantises to the same codes in practice.
 2. Format. OCP FP8 E4M3: 1 sign, 4 exponent bits (bias 7), 3 mantissa bits;
    normal values 2^(e-7) (1 + m/8), subnormals 2^-6 m/8, largest finite 448,
    no infinities. Conversion rounds to nearest, ties to even, and saturates
@@ -142,7 +145,7 @@ def fp8_forward(q, k, v, scale: float, signs, causal: bool = False, rotate: bool
     the error with and without the rotation."""
     q, k, v = _f64(q), _f64(k), _f64(v)
     B, H, N, d = q.shape
-    # sqrt(d) R = diag(s) H_d: the transform the GPU applies exactly in fp32
+    # sqrt(d) R = diag(s) H_d: the transform the GPU applies in fp32
     T = rotation(signs) * np.sqrt(d) if rotate else np.eye(d)
     s_fold = scale / d if rotate else scale
     O = np.zeros((B, H, N, d))

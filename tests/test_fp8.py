@@ -1,7 +1,7 @@
 """GPU parity of the FP8 forward pass (fa_fwd_fp8) against the FP8 oracle.
 
 The quantised operands are compared bit for bit with the oracle's (the
-Hadamard transform of bf16 inputs is exact in fp32 on both sides), the
+Hadamard transform of these bf16 inputs needs no rounding in fp32), the
 outputs element by element, with the tolerances derived in the design notes
 for FP8 weights: O max-abs <= 2e-2 and relative Frobenius <= 5e-3, L max-abs
 <= 1e-3. A last test checks the FP8 result against exact attention.
