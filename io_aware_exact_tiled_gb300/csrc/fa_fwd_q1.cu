@@ -40,7 +40,11 @@ struct Q1Cfg {
     static constexpr int V_OFF = K_OFF + STAGES * TILE_BYTES;
     static constexpr int X_OFF = V_OFF + STAGES * TILE_BYTES;  // [2 parities][2 groups][128] fp32
     static constexpr int BAR_OFF = X_OFF + 2048;
-    static constexpr int USED = BAR_OFF + 256;
+    // visible key tiles of the query tile as a bitmap (tile-masked calls);
+    // longer rows than it holds read the mask tile by tile
+    static constexpr int VIS_OFF = BAR_OFF + 256;
+    static constexpr int VIS_WORDS = (D == 64 ? 4096 : 1024) / 32;
+    static constexpr int USED = VIS_OFF + VIS_WORDS * 4;
     static constexpr int SMEM = USED + 1024 <= 232448 ? USED + 1024 : 232448;
     static constexpr int COL_O = 256;
     static constexpr uint32_t ID_S = idesc_make(128, 128, kFmtBF16, false, false);
@@ -99,9 +103,33 @@ __global__ void __launch_bounds__(384, 1)
     const int kvalid = keys_valid(mk, b, N);
     int hi = mk.causal ? min(T, qb + 1) : T;
     hi = min(hi, (kvalid + kTile - 1) / kTile);
-    // number of key tiles this query tile visits (same enumeration in every role)
-    int ntiles = 0;
-    for (int t = 0; t < hi; ++t) ntiles += tile_visible(mk, qb, t, kvalid) ? 1 : 0;
+    // With a tile mask, warps 2 and 3 (otherwise idle) first turn the mask
+    // row into a bitmap in shared memory: counting the visible tiles and
+    // finding the next one then take a popcount and a find-first-set instead
+    // of a dependent load of the mask per tile in every role.
+    const bool use_vis = mk.blockmask != nullptr && hi <= C::VIS_WORDS * 32;
+    uint32_t* vis = reinterpret_cast<uint32_t*>(sm + C::VIS_OFF);
+    if (use_vis && (warp == 2 || warp == 3)) {
+        const int nw = (hi + 31) >> 5;
+        for (int w = warp - 2; w < nw; w += 2) {
+            const int t = w * 32 + lane;
+            const uint32_t word = __ballot_sync(0xffffffffu, t < hi && tile_visible(mk, qb, t, kvalid));
+            if (lane == 0) vis[w] = word;
+        }
+    }
+    // first visible key tile >= t, or hi (the same enumeration in every role)
+    auto next_vis = [=](int t) -> int {
+        if (use_vis) {
+            while (t < hi) {
+                const uint32_t w = vis[t >> 5] >> (t & 31);
+                if (w) return t + __ffs(w) - 1;
+                t = (t | 31) + 1;
+            }
+            return hi;
+        }
+        while (t < hi && !tile_visible(mk, qb, t, kvalid)) ++t;
+        return t;
+    };
 
     if (tid == 0) {
         *abort_flag = 0;
@@ -119,6 +147,12 @@ __global__ void __launch_bounds__(384, 1)
         mbar_init(o_done, 1);
         mbar_init(drain, 1);
         fence_barrier_init();
+        // the Q tile is requested before TMEM allocation and the CTA-wide
+        // barrier (a query tile with no visible key tile never waits for it,
+        // and the producer lets it land before the CTA exits)
+        mbar_arrive_expect_tx(bar_q, C::TILE_BYTES);
+        for (int r = 0; r < C::NREG; ++r)
+            tma_load_2d(sm + C::Q_OFF + r * 16384, &tmQ, r * 64, bh * N + qb * kTile, bar_q);
     }
     if (warp == 0 && lane == 0) {
         tma_prefetch_desc(&tmQ);
@@ -133,16 +167,19 @@ __global__ void __launch_bounds__(384, 1)
     __syncthreads();
     tc_fence_after();
     const uint32_t tm = *tmem_slot;
+    // number of key tiles this query tile visits
+    int ntiles = 0;
+    if (use_vis) {
+        for (int w = 0; w < ((hi + 31) >> 5); ++w) ntiles += __popc(vis[w]);
+    } else {
+        for (int t = 0; t < hi; ++t) ntiles += tile_visible(mk, qb, t, kvalid) ? 1 : 0;
+    }
 
     if (warp == 0) {
         // ------------------------------------------------------------ producer
-        if (lane == 0 && ntiles > 0) {
-            mbar_arrive_expect_tx(bar_q, C::TILE_BYTES);
-            for (int r = 0; r < C::NREG; ++r)
-                tma_load_2d(sm + C::Q_OFF + r * 16384, &tmQ, r * 64, bh * N + qb * kTile, bar_q);
+        if (lane == 0) {
             int u = 0;
-            for (int t = 0; t < hi; ++t) {
-                if (!tile_visible(mk, qb, t, kvalid)) continue;
+            for (int t = next_vis(0); t < hi; t = next_vis(t + 1)) {
                 const int st = u % C::STAGES;
                 const uint32_t ph = (u / C::STAGES) & 1;
                 if (!mbar_wait(&kv_empty[st], ph ^ 1, cx, 31)) break;
@@ -218,8 +255,7 @@ __global__ void __launch_bounds__(384, 1)
         float m_hat = -CUDART_INF_F, l = 0.f, lw = 0.f;  // l: fp32 sum; lw: sum of bf16 weights
         bool ok = true;
         int u = 0;
-        for (int t = 0; t < hi; ++t) {
-            if (!tile_visible(mk, qb, t, kvalid)) continue;
+        for (int t = next_vis(0); t < hi; t = next_vis(t + 1)) {
             ok = __all_sync(0xffffffffu, mbar_wait(&s_full[u & 1], (u >> 1) & 1, cx, 35));
             if (!ok) break;
             tc_fence_after();
