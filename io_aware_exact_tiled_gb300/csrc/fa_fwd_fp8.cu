@@ -308,7 +308,8 @@ __device__ __forceinline__ bool fp8_issue_pv(uint32_t leader, int s, Fp8Mma& st,
 
 __global__ void __launch_bounds__(384, 1)
     fa_fwd_fp8_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
-                      const __grid_constant__ CUtensorMap tmVt, const __grid_constant__ Fp8Params p) {
+                      const __grid_constant__ CUtensorMap tmVt, const __grid_constant__ CUtensorMap tmO,
+                      const __grid_constant__ Fp8Params p) {
     using C = Fp8Cfg;
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     uint8_t* sm = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
@@ -358,6 +359,11 @@ __global__ void __launch_bounds__(384, 1)
         }
         mbar_init(drain, 1);
         fence_barrier_init();
+        // both Q tiles are requested before TMEM allocation and the CTA-wide
+        // barrier (the producer lets them land before the CTA exits)
+        mbar_arrive_expect_tx(bar_q, (act1 ? 2 : 1) * C::TILE_BYTES);
+        for (int s = 0; s < (act1 ? 2 : 1); ++s)
+            tma_load_2d(sm + C::Q_OFF + s * C::TILE_BYTES, &tmQ, 0, bh * N + (qb0 + s) * kTile, bar_q);
     }
     if (warp == 0 && lane == 0) {
         tma_prefetch_desc(&tmQ);
@@ -382,9 +388,6 @@ __global__ void __launch_bounds__(384, 1)
     if (warp == 0) {
         // ------------------------------------------------------------ producer
         if (lane == 0) {
-            mbar_arrive_expect_tx(bar_q, (act1 ? 2 : 1) * C::TILE_BYTES);
-            for (int s = 0; s < (act1 ? 2 : 1); ++s)
-                tma_load_2d(sm + C::Q_OFF + s * C::TILE_BYTES, &tmQ, 0, bh * N + (qb0 + s) * kTile, bar_q);
             int nk = 0, nv = 0;
             for (int t = 0; t < hi; ++t) {
                 if (!need_of(t)) continue;
@@ -573,16 +576,28 @@ __global__ void __launch_bounds__(384, 1)
             if (ok) {
                 const float inv = lw > 0.f ? exp2i(p.vexp[bh]) / lw : 0.f;
                 const size_t orow = (static_cast<size_t>(bh) * N + grow) * kD8;
+                // A warp whose query tile saw a key tile stages its 32 rows,
+                // as [32 x 64] swizzled bf16 boxes, in two stages of the K
+                // ring (free once o_done has landed: every GEMM is complete)
+                // and writes them with bulk tensor stores; a tile that saw no
+                // key tile stores its (zero) rows directly.
+                const bool tma_rows = n > 0;
+                uint8_t* ob = sm + C::K_OFF + s * 2 * C::TILE_BYTES + wq * 8192;
+                uint32_t oa[kD8 / 32][32];
+                if (n > 0) {
+#pragma unroll
+                    for (int c = 0; c < kD8 / 32; ++c) tmem_ld32(tl + 128 + c * 32, oa[c]);
+#pragma unroll
+                    for (int c = 0; c < kD8 / 32; ++c) tmem_ld_wait(oa[c]);
+                } else {
+#pragma unroll
+                    for (int c = 0; c < kD8 / 32; ++c)
+#pragma unroll
+                        for (int i = 0; i < 32; ++i) oa[c][i] = 0u;
+                }
 #pragma unroll
                 for (int c = 0; c < kD8 / 32; ++c) {
-                    uint32_t ov[32];
-                    if (n > 0) {
-                        tmem_ld32(tl + 128 + c * 32, ov);
-                        tmem_ld_wait(ov);
-                    } else {
-#pragma unroll
-                        for (int i = 0; i < 32; ++i) ov[i] = 0u;
-                    }
+                    const uint32_t* ov = oa[c];
                     uint4* dst = reinterpret_cast<uint4*>(static_cast<uint16_t*>(p.o) + orow + c * 32);
 #pragma unroll
                     for (int j = 0; j < 4; ++j) {
@@ -591,7 +606,24 @@ __global__ void __launch_bounds__(384, 1)
                         w.y = pack_bf16x2(__uint_as_float(ov[8 * j + 2]) * inv, __uint_as_float(ov[8 * j + 3]) * inv);
                         w.z = pack_bf16x2(__uint_as_float(ov[8 * j + 4]) * inv, __uint_as_float(ov[8 * j + 5]) * inv);
                         w.w = pack_bf16x2(__uint_as_float(ov[8 * j + 6]) * inv, __uint_as_float(ov[8 * j + 7]) * inv);
-                        dst[j] = w;
+                        if (tma_rows) {
+                            const int ch = ((c & 1) << 2) + j;  // 16-byte chunk within the 128-byte row
+                            sts128(smem_u32(ob + (c >> 1) * 4096 + lane * 128 + ((ch ^ (lane & 7)) << 4)), w.x, w.y,
+                                   w.z, w.w);
+                        } else {
+                            dst[j] = w;
+                        }
+                    }
+                }
+                if (tma_rows) {
+                    fence_proxy_async_smem();
+                    __syncwarp();
+                    if (lane == 0) {
+                        const int wrow = bh * N + qb * kTile + wq * 32;
+                        tma_store_2d(&tmO, 0, wrow, ob);
+                        tma_store_2d(&tmO, 64, wrow, ob + 4096);
+                        bulk_commit_group();
+                        bulk_wait_group_read0();  // read out before the CTA exits
                     }
                 }
                 p.lse[static_cast<size_t>(bh) * N + grow] =
@@ -622,8 +654,9 @@ cudaError_t launch_fwd_fp8(const Fp8Args& a, cudaStream_t stream, int* nlaunch) 
     fa_fp8_vmax_kernel<<<dim3(chunks, BH), 256, 0, stream>>>(static_cast<const uint16_t*>(a.v), a.vmax_bits, per_head);
     fa_fp8_v_kernel<<<dim3(T, BH), 256, 0, stream>>>(static_cast<const uint16_t*>(a.v), a.vmax_bits, a.vt8, a.vexp,
                                                       a.N);
-    CUtensorMap tq, tk, tv;
-    if (!make_tmap_2d_sw128(&tq, a.q8, rows, kD8, 1, kTile, 128) ||
+    CUtensorMap tq, tk, tv, to;
+    if (!make_tmap_2d_sw128(&to, a.o, rows, kD8, 2, 32, 64) ||
+        !make_tmap_2d_sw128(&tq, a.q8, rows, kD8, 1, kTile, 128) ||
         !make_tmap_2d_sw128(&tk, a.k8, rows, kD8, 1, kTile, 128) ||
         !make_tmap_2d_sw128(&tv, a.vt8, static_cast<uint64_t>(BH) * kD8, a.N, 1, kD8, 128))
         return cudaErrorInvalidValue;
@@ -650,7 +683,7 @@ cudaError_t launch_fwd_fp8(const Fp8Args& a, cudaStream_t stream, int* nlaunch) 
     p.status = a.status;
     dim3 grid(a.H, a.B, (T + 1) / 2);
     if (a.ev_begin) cudaEventRecord(a.ev_begin, stream);
-    fa_fwd_fp8_kernel<<<grid, C::THREADS, C::SMEM, stream>>>(tq, tk, tv, p);
+    fa_fwd_fp8_kernel<<<grid, C::THREADS, C::SMEM, stream>>>(tq, tk, tv, to, p);
     if (a.ev_end) cudaEventRecord(a.ev_end, stream);
     *nlaunch = 5;
     return cudaGetLastError();
