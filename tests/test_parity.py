@@ -157,3 +157,35 @@ def test_tile_mask_longer_than_the_backward_bitmaps(cuda_device):
         for name, ref in (("dq", dq), ("dk", dk), ("dv", dv)):
             a, b = out[name][0, 0, sl], ref[0, 0, sl]
             assert np.linalg.norm(a - b) / np.linalg.norm(b) <= TOL_G, name
+
+
+def test_causal_head_groups_with_a_partial_last_group(cuda_device):
+    """Causal calls run head groups on a 1D grid: at N = 8192, d = 128 the
+    forward takes 16 heads per group and the backward 8, so 36 heads end on
+    a partial group in both. Whole heads from the first, a middle and the
+    last (partial) group against the oracle."""
+    w = W.Workload("groups", 1, 36, 8192, 128, causal=True)
+    x = W.make_inputs(w, seed=11, device="cuda")
+    x = W.Inputs(*(t.cpu() if torch.is_tensor(t) else t for t in (x.q, x.k, x.v, x.do)), x.kv_len, x.blockmask,
+                 x.scale, x.causal)
+    g = run_gpu(x, cuda_device)
+    check(errors(x, g, heads=[(0, 0), (0, 20), (0, 35)]))
+
+
+def test_causal_tile_mask_longer_than_the_one_tile_bitmap(cuda_device):
+    """Causal tile-masked forwards run one query tile per CTA, which keeps its
+    mask row as a 1,024-tile bitmap at d = 128; 1,025 tiles take the per-tile
+    mask reads. Sampled query tiles against the oracle."""
+    T = 1025
+    N = T * 128
+    w = W.Workload("causal-sparse-long", 1, 1, N, 128, causal=True, backward=False)
+    x = W.make_inputs(w, seed=12)
+    g = torch.Generator().manual_seed(13)
+    bm = (torch.rand(T, T, generator=g) < 0.01).to(torch.uint8)
+    bm.fill_diagonal_(1)
+    x.blockmask = bm
+    out = run_gpu(x, cuda_device, backward=False)
+    for r0 in (0, 512 * 128, N - 128):
+        O, L = oracle.forward(x.q, x.k, x.v, x.scale, causal=True, blockmask=bm, rows=(r0, r0 + 128))
+        assert np.abs(out["o"][0, 0, r0:r0 + 128] - O[0, 0, r0:r0 + 128]).max() <= TOL_O
+        assert np.abs(out["lse"][0, 0, r0:r0 + 128] - L[0, 0, r0:r0 + 128]).max() <= TOL_L
