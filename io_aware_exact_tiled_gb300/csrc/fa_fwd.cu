@@ -90,7 +90,20 @@ struct FwdParams {
     DropoutArgs drop;           // dropout on the probabilities (DROPOUT kernels)
     int head_major;             // grid (pairs, H, B) instead of (H, B, pairs)
     int group;                  // > 0: 1D grid of head groups (heads per group), longest pair first in each
+    int pf_ahead;               // 1D grid: prefetch into L2 the Q tiles of CTA blockIdx.x + pf_ahead (0: off)
 };
+
+// Work item L of the head-group order: groups of `group` heads in turn (the
+// last one may be smaller), and within a group pair rank zq (0 = longest)
+// major, head minor.
+__device__ __forceinline__ void fwd_group_item(int L, int group, int np, int nb, int H, int& b, int& h, int& zq) {
+    const int gi = L / (group * np), r = L - gi * group * np;
+    const int g0 = gi * group, gsz = min(group, nb - g0);
+    zq = r / gsz;
+    const int bhx = g0 + (r - zq * gsz);
+    b = bhx / H;
+    h = bhx - b * H;
+}
 
 // Issue state of the MMA thread, per Q tile s of the CTA.
 struct MmaState {
@@ -182,16 +195,8 @@ __global__ void __launch_bounds__(384, 1)
     // which stays in L2.
     int h = p.head_major ? blockIdx.y : blockIdx.x, b = p.head_major ? blockIdx.z : blockIdx.y;
     int zq = static_cast<int>(p.head_major ? blockIdx.x : blockIdx.z);  // pair rank, longest first
-    if (!VARLEN && p.group > 0) {
-        const int np = (p.mask.T + 1) >> 1, nb = p.B * p.H;
-        const int L = static_cast<int>(blockIdx.x);
-        const int gi = L / (p.group * np), r = L - gi * p.group * np;
-        const int g0 = gi * p.group, gsz = min(p.group, nb - g0);
-        zq = r / gsz;
-        const int bhx = g0 + (r - zq * gsz);
-        b = bhx / p.H;
-        h = bhx - b * p.H;
-    }
+    if (!VARLEN && p.group > 0)
+        fwd_group_item(static_cast<int>(blockIdx.x), p.group, (p.mask.T + 1) >> 1, p.B * p.H, p.H, b, h, zq);
     // A packed variable-length batch puts sequence b at tokens seq0 ..
     // seq0 + N - 1 of [total, H, d] tensors (the grid covers the longest
     // sequence; CTAs past the end of a shorter one leave at once). Otherwise
@@ -217,6 +222,35 @@ __global__ void __launch_bounds__(384, 1)
     int hi = T;
     if (p.mask.causal) hi = min(hi, (act1 ? qb1 : qb0) + 1);
     hi = min(hi, (kvalid + kTile - 1) / kTile);
+
+    // K and V tile loads (producer thread): rows t * 128 .. of this head
+    // (packed: of this sequence) into K stage kst / V stage vst
+    auto load_rows = [&](void* dst, const CUtensorMap* m, int x, int row, uint64_t* bar) {
+        if (varlen)
+            tma_load_3d(dst, m, x, h, seq0 + row, bar);
+        else
+            tma_load_2d(dst, m, x, bh * N + row, bar);
+    };
+    auto load_k = [&](int t, int kst) {
+        uint8_t* sk = sm + C::K_OFF + kst * C::SPLIT * C::TILE_BYTES;
+        mbar_arrive_expect_tx(&k_full[kst], C::SPLIT * C::TILE_BYTES);
+        for (int r = 0; r < C::NREG; ++r) {
+            load_rows(sk + r * 16384, &tmK, r * C::BOXC, t * kTile, &k_full[kst]);
+            if constexpr (TF32)
+                tma_load_2d(sk + C::TILE_BYTES + r * 16384, &tmKlo, r * C::BOXC, bh * N + t * kTile, &k_full[kst]);
+        }
+    };
+    auto load_v = [&](int t, int vst) {
+        uint8_t* sv = sm + C::V_OFF + vst * C::TILE_BYTES;
+        mbar_arrive_expect_tx(&v_full[vst], C::TILE_BYTES);
+        if constexpr (!TF32) {
+            for (int r = 0; r < C::NREG; ++r) load_rows(sv + r * 16384, &tmV, r * C::BOXC, t * kTile, &v_full[vst]);
+        } else {
+            // V^T [d][keys]: four 32-key swizzle regions of [d][32]
+            for (int r = 0; r < 4; ++r) tma_load_2d(sv + r * D * 128, &tmV, t * kTile + r * 32, bh * D, &v_full[vst]);
+        }
+    };
+    int t_early = -1;  // key tile whose K and V the set-up thread requested
 
     if (tid == 0) {
         *abort_flag = 0;
@@ -250,6 +284,28 @@ __global__ void __launch_bounds__(384, 1)
                 if constexpr (TF32)
                     tma_load_2d(dq + C::TILE_BYTES, &tmQlo, r * C::BOXC, bh * N + (qb0 + s) * kTile, bar_q);
             }
+        // ... and so are the first needed tile's K and V (the rings start
+        // empty; tile-masked kernels find that tile in their bitmaps later)
+        if constexpr (!TMASK) {
+            int t0 = 0;
+            while (t0 < hi && !tile_visible(p.mask, qb0, t0, kvalid) && !(act1 && tile_visible(p.mask, qb1, t0, kvalid)))
+                ++t0;
+            if (t0 < hi) {
+                load_k(t0, 0);
+                load_v(t0, 0);
+                t_early = t0;
+            }
+        }
+        // Q is the one operand read from DRAM exactly once; the CTA about a
+        // wave ahead in the 1D order finds its Q tiles in L2
+        if (!VARLEN && p.group > 0 && p.pf_ahead > 0 && blockIdx.x + p.pf_ahead < gridDim.x) {
+            int b2, h2, z2;
+            fwd_group_item(static_cast<int>(blockIdx.x + p.pf_ahead), p.group, npairs, p.B * p.H, p.H, b2, h2, z2);
+            const int qb2 = 2 * (npairs - 1 - z2);
+            for (int s = 0; s < 2 && qb2 + s < T; ++s)
+                for (int r = 0; r < C::NREG; ++r)
+                    tma_prefetch_l2_2d(&tmQ, r * C::BOXC, (b2 * p.H + h2) * N + (qb2 + s) * kTile);
+        }
     }
     if (warp == 0 && lane == 0) {
         tma_prefetch_desc(&tmQ);
@@ -324,39 +380,18 @@ __global__ void __launch_bounds__(384, 1)
     if (warp == 0) {
         // ------------------------------------------------------------ producer
         if (lane == 0) {
-            // rows row .. row + 127 of this head (packed: of this sequence)
-            auto load_rows = [&](void* dst, const CUtensorMap* m, int x, int row, uint64_t* bar) {
-                if (varlen)
-                    tma_load_3d(dst, m, x, h, seq0 + row, bar);
-                else
-                    tma_load_2d(dst, m, x, bh * N + row, bar);
-            };
-            int nk = 0, nv = 0;  // K and V tiles whose loads were issued
-            for (int t = next_tile(0, 3u); t < hi; t = next_tile(t + 1, 3u)) {
+            // K and V tiles whose loads were issued (the first one possibly
+            // by the set-up code above)
+            int nk = t_early >= 0 ? 1 : 0, nv = nk;
+            for (int t = next_tile(t_early + 1, 3u); t < hi; t = next_tile(t + 1, 3u)) {
                 if (!need_of(t)) continue;
                 const int kst = nk % C::KSTAGES;
                 if (!mbar_wait(&k_empty[kst], ((nk / C::KSTAGES) & 1) ^ 1, cx, 1)) break;
-                uint8_t* sk = sm + C::K_OFF + kst * C::SPLIT * C::TILE_BYTES;
-                mbar_arrive_expect_tx(&k_full[kst], C::SPLIT * C::TILE_BYTES);
-                for (int r = 0; r < C::NREG; ++r) {
-                    load_rows(sk + r * 16384, &tmK, r * C::BOXC, t * kTile, &k_full[kst]);
-                    if constexpr (TF32)
-                        tma_load_2d(sk + C::TILE_BYTES + r * 16384, &tmKlo, r * C::BOXC, bh * N + t * kTile,
-                                    &k_full[kst]);
-                }
+                load_k(t, kst);
                 ++nk;
                 const int vst = nv % C::VSTAGES;
                 if (!mbar_wait(&kv_empty[vst], ((nv / C::VSTAGES) & 1) ^ 1, cx, 9)) break;
-                uint8_t* sv = sm + C::V_OFF + vst * C::TILE_BYTES;
-                mbar_arrive_expect_tx(&v_full[vst], C::TILE_BYTES);
-                if constexpr (!TF32) {
-                    for (int r = 0; r < C::NREG; ++r)
-                        load_rows(sv + r * 16384, &tmV, r * C::BOXC, t * kTile, &v_full[vst]);
-                } else {
-                    // V^T [d][keys]: four 32-key swizzle regions of [d][32]
-                    for (int r = 0; r < 4; ++r)
-                        tma_load_2d(sv + r * D * 128, &tmV, t * kTile + r * 32, bh * D, &v_full[vst]);
-                }
+                load_v(t, vst);
                 ++nv;
             }
             // let every copy in flight land before the CTA can exit
@@ -830,6 +865,14 @@ static cudaError_t launch_fwd_t(const FwdArgs& a, cudaStream_t stream, int* nlau
         g = g < 1 ? 1 : g;
         p.group = static_cast<int>(g < a.B * a.H ? g : a.B * a.H);
     }
+    static int nsm = 0;
+    if (nsm == 0) {
+        int dev = 0;
+        if (cudaGetDevice(&dev) != cudaSuccess ||
+            cudaDeviceGetAttribute(&nsm, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+            nsm = 0;
+    }
+    p.pf_ahead = p.group > 0 ? nsm : 0;
     const dim3 grid = p.group > 0     ? dim3(static_cast<unsigned>((T + 1) / 2) * a.H * a.B)
                       : p.head_major ? dim3((T + 1) / 2, a.H, a.B)
                                      : dim3(a.H, a.B, (T + 1) / 2);

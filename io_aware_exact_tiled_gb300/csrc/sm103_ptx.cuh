@@ -194,6 +194,12 @@ __device__ __forceinline__ bool mbar_wait_teardown(uint64_t* bar, uint32_t parit
 // --------------------------------------------------------------------------
 // TMA (bulk tensor copies) and plain bulk copies
 // --------------------------------------------------------------------------
+// Prefetch a tile of a tensor map into L2 (no shared memory, no barrier).
+__device__ __forceinline__ void tma_prefetch_l2_2d(const CUtensorMap* map, int x, int y) {
+    asm volatile("cp.async.bulk.prefetch.tensor.2d.L2.global.tile [%0, {%1, %2}];"
+                 ::"l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y)
+                 : "memory");
+}
 __device__ __forceinline__ void tma_prefetch_desc(const CUtensorMap* map) {
     asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
 }
