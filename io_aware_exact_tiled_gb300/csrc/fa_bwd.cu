@@ -211,6 +211,39 @@ __global__ void __launch_bounds__(512, 1)
         return i;
     };
 
+    // K_j, V_j (once) and the Q_i, dO_i, -L, -D stage loads (producer thread)
+    auto load_kv = [&]() {
+        mbar_arrive_expect_tx(kv_full, 2 * C::TILE_BYTES);
+        for (int r = 0; r < C::NREG; ++r) {
+            if (varlen) {
+                tma_load_3d(sm + C::K_OFF + r * 16384, &tmK, r * 64, h, seq0 + j * kTile, kv_full);
+                tma_load_3d(sm + C::V_OFF + r * 16384, &tmV, r * 64, h, seq0 + j * kTile, kv_full);
+            } else {
+                tma_load_2d(sm + C::K_OFF + r * 16384, &tmK, r * 64, bh * N + j * kTile, kv_full);
+                tma_load_2d(sm + C::V_OFF + r * 16384, &tmV, r * 64, bh * N + j * kTile, kv_full);
+            }
+        }
+    };
+    auto load_stage = [&](int i, int st) {
+        mbar_arrive_expect_tx(&qd_full[st], 2 * C::TILE_BYTES + 1024);
+        const int row = bh * N + i * kTile;
+        for (int r = 0; r < C::NREG; ++r) {
+            uint8_t* dq_s = sm + C::Q_OFF + st * C::TILE_BYTES + r * 16384;
+            uint8_t* ddo_s = sm + C::DO_OFF + st * C::TILE_BYTES + r * 16384;
+            if (varlen) {
+                tma_load_3d(dq_s, &tmQ, r * 64, h, seq0 + i * kTile, &qd_full[st]);
+                tma_load_3d(ddo_s, &tmdO, r * 64, h, seq0 + i * kTile, &qd_full[st]);
+            } else {
+                tma_load_2d(dq_s, &tmQ, r * 64, row, &qd_full[st]);
+                tma_load_2d(ddo_s, &tmdO, r * 64, row, &qd_full[st]);
+            }
+        }
+        const long long lrow = lrow0 + static_cast<long long>(i) * kTile;
+        bulk_load(sm + C::LSE_OFF + st * 512, p.nlse2 + lrow, 512, &qd_full[st]);
+        bulk_load(sm + C::DEL_OFF + st * 512, p.ndelta + lrow, 512, &qd_full[st]);
+    };
+    int i_early = -1;  // query block whose stage the set-up thread requested
+
     if (tid == 0) {
         *abort_flag = 0;
         mbar_init(kv_full, 1);
@@ -227,6 +260,18 @@ __global__ void __launch_bounds__(512, 1)
         mbar_init(dkv_done, 1);
         mbar_init(drain, 1);
         fence_barrier_init();
+        // K, V and the first visible query block's stage are requested before
+        // TMEM allocation and the CTA-wide barrier (the tile-masked kernel
+        // finds its first block in the bitmap built after this)
+        if constexpr (!TMASK) {
+            int i0 = lo;
+            while (i0 < T && !tile_visible(mk, i0, j, kvalid)) ++i0;
+            if (i0 < T) {
+                load_kv();
+                load_stage(i0, 0);
+                i_early = i0;
+            }
+        }
     }
     if (warp == 0 && lane == 0) {
         tma_prefetch_desc(&tmQ);
@@ -255,42 +300,19 @@ __global__ void __launch_bounds__(512, 1)
     if (warp == 0) {
         // ------------------------------------------------------------ producer
         if (lane == 0) {
-            int u = 0;
-            bool kv_issued = false;
-            for (int i = next_i(lo); i < T; i = next_i(i + 1)) {
+            // the set-up code may have requested K, V and the first stage
+            int u = i_early >= 0 ? 1 : 0;
+            bool kv_issued = i_early >= 0;
+            for (int i = next_i(i_early >= 0 ? i_early + 1 : lo); i < T; i = next_i(i + 1)) {
                 if (!visible_i(i)) continue;
                 if (!kv_issued) {
-                    mbar_arrive_expect_tx(kv_full, 2 * C::TILE_BYTES);
-                    for (int r = 0; r < C::NREG; ++r) {
-                        if (varlen) {
-                            tma_load_3d(sm + C::K_OFF + r * 16384, &tmK, r * 64, h, seq0 + j * kTile, kv_full);
-                            tma_load_3d(sm + C::V_OFF + r * 16384, &tmV, r * 64, h, seq0 + j * kTile, kv_full);
-                        } else {
-                            tma_load_2d(sm + C::K_OFF + r * 16384, &tmK, r * 64, bh * N + j * kTile, kv_full);
-                            tma_load_2d(sm + C::V_OFF + r * 16384, &tmV, r * 64, bh * N + j * kTile, kv_full);
-                        }
-                    }
+                    load_kv();
                     kv_issued = true;
                 }
                 const int st = u % C::STAGES;
                 const uint32_t ph = (u / C::STAGES) & 1;
                 if (!mbar_wait(&qd_empty[st], ph ^ 1, cx, 11)) break;
-                mbar_arrive_expect_tx(&qd_full[st], 2 * C::TILE_BYTES + 1024);
-                const int row = bh * N + i * kTile;
-                for (int r = 0; r < C::NREG; ++r) {
-                    uint8_t* dq_s = sm + C::Q_OFF + st * C::TILE_BYTES + r * 16384;
-                    uint8_t* ddo_s = sm + C::DO_OFF + st * C::TILE_BYTES + r * 16384;
-                    if (varlen) {
-                        tma_load_3d(dq_s, &tmQ, r * 64, h, seq0 + i * kTile, &qd_full[st]);
-                        tma_load_3d(ddo_s, &tmdO, r * 64, h, seq0 + i * kTile, &qd_full[st]);
-                    } else {
-                        tma_load_2d(dq_s, &tmQ, r * 64, row, &qd_full[st]);
-                        tma_load_2d(ddo_s, &tmdO, r * 64, row, &qd_full[st]);
-                    }
-                }
-                const long long lrow = lrow0 + static_cast<long long>(i) * kTile;
-                bulk_load(sm + C::LSE_OFF + st * 512, p.nlse2 + lrow, 512, &qd_full[st]);
-                bulk_load(sm + C::DEL_OFF + st * 512, p.ndelta + lrow, 512, &qd_full[st]);
+                load_stage(i, st);
                 ++u;
             }
             if (kv_issued) mbar_wait_teardown(kv_full, 0, 200000000ull);
