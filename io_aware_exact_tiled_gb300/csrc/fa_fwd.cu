@@ -74,7 +74,7 @@ struct FwdCfg {
     // tf32 operands must be K-major, so V arrives transposed ([d][keys]).
     static constexpr uint32_t ID_PV = idesc_make(128, D, TF32 ? kFmtTF32 : kFmtBF16, false, !TF32);
     static_assert(SMEM <= 232448, "shared memory budget");
-    static_assert((1 + 2 * KSTAGES + 2 * VSTAGES + 7) * 8 + 8 <= 512, "barrier area");
+    static_assert((1 + 2 * KSTAGES + 2 * VSTAGES + 9) * 8 + 8 <= 512, "barrier area");
     static_assert(VSTAGES <= 16, "two bits of reader count per V stage");
 };
 
@@ -115,25 +115,32 @@ struct MmaState {
     uint32_t rem = 0;              // 2 bits per stage: Q tiles still to read its V
 };
 
-// O_s += P_s V for Q tile s's pending K/V tile (waits for P_s and V).
+// O_s += P_s V for Q tile s's pending K/V tile, in two halves of 64 keys:
+// the first as soon as the softmax warps have stored P for keys 0-63
+// (p_half), so that it runs while they form P for keys 64-127 (p_full).
 template <bool TF32, int D>
 __device__ __forceinline__ bool fwd_issue_pv(uint32_t leader, int s, MmaState& st, uint32_t tm, uint64_t dV0,
-                                             uint64_t* p_full,
+                                             uint64_t* p_half, uint64_t* p_full,
                                              uint64_t* v_full, uint64_t* kv_empty, const WaitCtx& cx) {
     using C = FwdCfg<TF32, D>;
     const int ps = st.pend_stage[s];
-    if (!mbar_wait_warp(&p_full[s], st.nP[s] & 1, cx, 3)) return false;
-    ++st.nP[s];
+    const uint32_t php = st.nP[s] & 1;
+    if (!mbar_wait_warp(&p_half[s], php, cx, 12)) return false;
     // V comes through its own ring and is normally resident long before P
     if (!mbar_wait_warp(&v_full[ps], st.pend_ph[s], cx, 4)) return false;
     tc_fence_after();
     const uint64_t vst = sdesc_advance(dV0, ps * C::TILE_BYTES);
 #pragma unroll
     for (int kk = 0; kk < C::PV_KSTEPS; ++kk) {
+        if (kk == C::PV_KSTEPS / 2) {
+            if (!mbar_wait_warp(&p_full[s], php, cx, 3)) return false;
+            tc_fence_after();
+        }
         const uint32_t off = TF32 ? (kk / 4) * (D * 128) + (kk % 4) * 32 : kk * 2048;
         umma_ts<TF32>(leader, tm + s * 256 + 128, tm + s * 256 + kk * 8, sdesc_advance(vst, off), C::ID_PV,
                       (st.nPV[s] > 0 || kk > 0) ? 1u : 0u);
     }
+    ++st.nP[s];
     ++st.nPV[s];
     uint32_t r = (st.rem >> (2 * ps)) & 3u;
     r -= 1;
@@ -178,7 +185,8 @@ __global__ void __launch_bounds__(384, 1)
     uint64_t* p_full = s_full + 2;            // [2]
     uint64_t* o_done = p_full + 2;            // [2]
     uint64_t* drain = o_done + 2;
-    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
+    uint64_t* p_half = drain + 1;             // [2] P of keys 0-63 stored
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(p_half + 2);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
     const WaitCtx cx{abort_flag, p.status};
 
@@ -266,6 +274,7 @@ __global__ void __launch_bounds__(384, 1)
         for (int i = 0; i < 2; ++i) {
             mbar_init(&s_full[i], 1);
             mbar_init(&p_full[i], 128);
+            mbar_init(&p_half[i], 128);
             mbar_init(&o_done[i], 1);
         }
         mbar_init(drain, 1);
@@ -419,7 +428,7 @@ __global__ void __launch_bounds__(384, 1)
             // bf16: V MN-major (LBO = distance between 64-column regions);
             // tf32: V^T K-major
             const uint64_t dV0 = sdesc_sw128(smem_u32(sm + C::V_OFF), TF32 ? 16 : 16384, 1024);
-#define issue_pv(S) fwd_issue_pv<TF32, D>(leader, (S), st, tm, dV0, p_full, v_full, kv_empty, cx)
+#define issue_pv(S) fwd_issue_pv<TF32, D>(leader, (S), st, tm, dV0, p_half, p_full, v_full, kv_empty, cx)
             int (&pend_stage)[2] = st.pend_stage;
             uint32_t(&pend_ph)[2] = st.pend_ph;
             uint32_t& rem = st.rem;
@@ -540,6 +549,8 @@ __global__ void __launch_bounds__(384, 1)
                 // two elements per f32x2 instruction: x = s * c2 - mu, the
                 // fp32 row sum and the sum of the bf16-rounded weights
                 const uint64_t c2c2 = f2_make(c2, c2), nmu2 = f2_make(-mu, -mu);
+                // O is rescaled (below) before any P V of this tile may run
+                const bool resc_any = __any_sync(0xffffffffu, resc) && n > 0;
                 uint64_t rs2 = 0ull;
                 uint64_t rr2d = 0ull;  // dropout: bf16-weight sum, formed before the weights are masked
                 uint32_t pk[4][16];  // P as bf16 pairs; kept for the bf16-weight sum
@@ -582,6 +593,11 @@ __global__ void __launch_bounds__(384, 1)
                             }
                         }
                         tmem_st16(tl + c * 16, pk[c]);
+                        if (c == 1 && !resc_any) {
+                            tmem_st_wait();
+                            tc_fence_before();
+                            mbar_arrive(&p_half[s]);
+                        }
                     } else {
                         uint32_t pk[32];
 #pragma unroll
@@ -592,6 +608,11 @@ __global__ void __launch_bounds__(384, 1)
                         }
                         rr = rs;
                         tmem_st32(tl + c * 32, pk);
+                        if (c == 1 && !resc_any) {
+                            tmem_st_wait();
+                            tc_fence_before();
+                            mbar_arrive(&p_half[s]);
+                        }
                     }
                 }
                 if constexpr (TF32) {
@@ -626,7 +647,7 @@ __global__ void __launch_bounds__(384, 1)
             lw += a_ + b_;                                                                                \
         }                                                                                                 \
     } while (0)
-                if (__any_sync(0xffffffffu, resc) && n > 0) {
+                if (resc_any) {
                     FA_ROW_SUMS();
                     // O holds the previous tiles' sum; their last P V was issued
                     // before this tile's S, and MMAs complete in issue order,
@@ -643,6 +664,7 @@ __global__ void __launch_bounds__(384, 1)
                     }
                     tmem_st_wait();
                     tc_fence_before();
+                    mbar_arrive(&p_half[s]);
                     if (!FA_DROP_THIS_ARRIVE(n == 0)) mbar_arrive(&p_full[s]);
                 } else {
                     tc_fence_before();
