@@ -74,7 +74,7 @@ struct FwdCfg {
     // tf32 operands must be K-major, so V arrives transposed ([d][keys]).
     static constexpr uint32_t ID_PV = idesc_make(128, D, TF32 ? kFmtTF32 : kFmtBF16, false, !TF32);
     static_assert(SMEM <= 232448, "shared memory budget");
-    static_assert((1 + 2 * KSTAGES + 2 * VSTAGES + 9) * 8 + 8 <= 512, "barrier area");
+    static_assert((1 + 2 * KSTAGES + 2 * VSTAGES + 13) * 8 + 8 <= 512, "barrier area");
     static_assert(VSTAGES <= 16, "two bits of reader count per V stage");
 };
 
@@ -115,25 +115,27 @@ struct MmaState {
     uint32_t rem = 0;              // 2 bits per stage: Q tiles still to read its V
 };
 
-// O_s += P_s V for Q tile s's pending K/V tile, in two halves of 64 keys:
-// the first as soon as the softmax warps have stored P for keys 0-63
-// (p_half), so that it runs while they form P for keys 64-127 (p_full).
-template <bool TF32, int D>
+// O_s += P_s V for Q tile s's pending K/V tile, in PARTS slices of the
+// keys: each as soon as the softmax warps have stored P for its keys
+// (p_part[s][k] for all slices but the last, p_full for the last), so that
+// the product runs while they form P for the later keys.
+template <bool TF32, int D, int PARTS>
 __device__ __forceinline__ bool fwd_issue_pv(uint32_t leader, int s, MmaState& st, uint32_t tm, uint64_t dV0,
                                              uint64_t* p_half, uint64_t* p_full,
                                              uint64_t* v_full, uint64_t* kv_empty, const WaitCtx& cx) {
     using C = FwdCfg<TF32, D>;
     const int ps = st.pend_stage[s];
     const uint32_t php = st.nP[s] & 1;
-    if (!mbar_wait_warp(&p_half[s], php, cx, 12)) return false;
+    if (!mbar_wait_warp(&p_half[s * 3], php, cx, 12)) return false;  // first slice
     // V comes through its own ring and is normally resident long before P
     if (!mbar_wait_warp(&v_full[ps], st.pend_ph[s], cx, 4)) return false;
     tc_fence_after();
     const uint64_t vst = sdesc_advance(dV0, ps * C::TILE_BYTES);
 #pragma unroll
     for (int kk = 0; kk < C::PV_KSTEPS; ++kk) {
-        if (kk == C::PV_KSTEPS / 2) {
-            if (!mbar_wait_warp(&p_full[s], php, cx, 3)) return false;
+        if (kk > 0 && kk % (C::PV_KSTEPS / PARTS) == 0) {
+            const int q = kk / (C::PV_KSTEPS / PARTS);
+            if (!mbar_wait_warp(q == PARTS - 1 ? &p_full[s] : &p_half[s * 3 + q], php, cx, 3)) return false;
             tc_fence_after();
         }
         const uint32_t off = TF32 ? (kk / 4) * (D * 128) + (kk % 4) * 32 : kk * 2048;
@@ -185,8 +187,13 @@ __global__ void __launch_bounds__(384, 1)
     uint64_t* p_full = s_full + 2;            // [2]
     uint64_t* o_done = p_full + 2;            // [2]
     uint64_t* drain = o_done + 2;
-    uint64_t* p_half = drain + 1;             // [2] P of keys 0-63 stored
-    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(p_half + 2);
+    // P V runs in slices of the keys (four in the plain d = 128 kernel; two
+    // in the others: in the tile-masked and d = 64 kernels the softmax warps
+    // stall more on the extra TMEM-store waits than the earlier slices gain):
+    // p_half[s][k] = P of slices 0..k stored
+    constexpr int PV_PARTS = (!TMASK && !VARLEN && !DROPOUT && !TF32 && D == 128) ? 4 : 2;
+    uint64_t* p_half = drain + 1;             // [2][3]
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(p_half + 6);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
     const WaitCtx cx{abort_flag, p.status};
 
@@ -274,7 +281,7 @@ __global__ void __launch_bounds__(384, 1)
         for (int i = 0; i < 2; ++i) {
             mbar_init(&s_full[i], 1);
             mbar_init(&p_full[i], 128);
-            mbar_init(&p_half[i], 128);
+            for (int k = 0; k < 3; ++k) mbar_init(&p_half[i * 3 + k], 128);
             mbar_init(&o_done[i], 1);
         }
         mbar_init(drain, 1);
@@ -428,7 +435,7 @@ __global__ void __launch_bounds__(384, 1)
             // bf16: V MN-major (LBO = distance between 64-column regions);
             // tf32: V^T K-major
             const uint64_t dV0 = sdesc_sw128(smem_u32(sm + C::V_OFF), TF32 ? 16 : 16384, 1024);
-#define issue_pv(S) fwd_issue_pv<TF32, D>(leader, (S), st, tm, dV0, p_half, p_full, v_full, kv_empty, cx)
+#define issue_pv(S) fwd_issue_pv<TF32, D, PV_PARTS>(leader, (S), st, tm, dV0, p_half, p_full, v_full, kv_empty, cx)
             int (&pend_stage)[2] = st.pend_stage;
             uint32_t(&pend_ph)[2] = st.pend_ph;
             uint32_t& rem = st.rem;
@@ -593,10 +600,10 @@ __global__ void __launch_bounds__(384, 1)
                             }
                         }
                         tmem_st16(tl + c * 16, pk[c]);
-                        if (c == 1 && !resc_any) {
+                        if (c < 3 && (c + 1) % (4 / PV_PARTS) == 0 && !resc_any) {
                             tmem_st_wait();
                             tc_fence_before();
-                            mbar_arrive(&p_half[s]);
+                            mbar_arrive(&p_half[s * 3 + (c + 1) / (4 / PV_PARTS) - 1]);
                         }
                     } else {
                         uint32_t pk[32];
@@ -608,10 +615,10 @@ __global__ void __launch_bounds__(384, 1)
                         }
                         rr = rs;
                         tmem_st32(tl + c * 32, pk);
-                        if (c == 1 && !resc_any) {
+                        if (c < 3 && (c + 1) % (4 / PV_PARTS) == 0 && !resc_any) {
                             tmem_st_wait();
                             tc_fence_before();
-                            mbar_arrive(&p_half[s]);
+                            mbar_arrive(&p_half[s * 3 + (c + 1) / (4 / PV_PARTS) - 1]);
                         }
                     }
                 }
@@ -664,7 +671,7 @@ __global__ void __launch_bounds__(384, 1)
                     }
                     tmem_st_wait();
                     tc_fence_before();
-                    mbar_arrive(&p_half[s]);
+                    for (int k = 0; k < PV_PARTS - 1; ++k) mbar_arrive(&p_half[s * 3 + k]);
                     if (!FA_DROP_THIS_ARRIVE(n == 0)) mbar_arrive(&p_full[s]);
                 } else {
                     tc_fence_before();
