@@ -256,7 +256,7 @@ struct Fp8Cfg {
     static constexpr int THREADS = 384;
     static constexpr uint32_t ID_S = idesc_make(128, 128, kFmtE4M3, false, false);
     static constexpr uint32_t ID_PV = idesc_make(128, kD8, kFmtE4M3, false, false);
-    static_assert((1 + 2 * KSTAGES + 2 * VSTAGES + 7) * 8 + 8 <= 512, "barrier area");
+    static_assert((1 + 2 * KSTAGES + 2 * VSTAGES + 9) * 8 + 8 <= 512, "barrier area");
     static_assert(SMEM <= 232448, "shared memory budget");
 };
 
@@ -283,20 +283,28 @@ struct Fp8Mma {
     uint32_t rem = 0;
 };
 
+// O_s += P_s V in two halves of 64 keys, the first as soon as the softmax
+// warps have stored P of keys 0-63 (p_half), the second after p_full.
 __device__ __forceinline__ bool fp8_issue_pv(uint32_t leader, int s, Fp8Mma& st, uint32_t tm, uint64_t dV0,
-                                             uint64_t* p_full, uint64_t* v_full, uint64_t* kv_empty,
-                                             const WaitCtx& cx) {
+                                             uint64_t* p_half, uint64_t* p_full, uint64_t* v_full,
+                                             uint64_t* kv_empty, const WaitCtx& cx) {
     using C = Fp8Cfg;
     const int ps = st.pend_stage[s];
-    if (!mbar_wait_warp(&p_full[s], st.nP[s] & 1, cx, 3)) return false;
-    ++st.nP[s];
+    const uint32_t php = st.nP[s] & 1;
+    if (!mbar_wait_warp(&p_half[s], php, cx, 12)) return false;
     if (!mbar_wait_warp(&v_full[ps], st.pend_ph[s], cx, 4)) return false;
     tc_fence_after();
     const uint64_t vst = sdesc_advance(dV0, ps * C::TILE_BYTES);
 #pragma unroll
-    for (int kk = 0; kk < 4; ++kk)  // 32 keys (8 TMEM columns of P8) per instruction
+    for (int kk = 0; kk < 4; ++kk) {  // 32 keys (8 TMEM columns of P8) per instruction
+        if (kk == 2) {
+            if (!mbar_wait_warp(&p_full[s], php, cx, 3)) return false;
+            tc_fence_after();
+        }
         umma_ts_f8(leader, tm + s * 256 + 128, tm + s * 256 + kk * 8, sdesc_advance(vst, kk * 32), C::ID_PV,
                    (st.nPV[s] > 0 || kk > 0) ? 1u : 0u);
+    }
+    ++st.nP[s];
     ++st.nPV[s];
     uint32_t r = (st.rem >> (2 * ps)) & 3u;
     r -= 1;
@@ -323,7 +331,8 @@ __global__ void __launch_bounds__(384, 1)
     uint64_t* p_full = s_full + 2;             // [2]
     uint64_t* o_done = p_full + 2;             // [2]
     uint64_t* drain = o_done + 2;
-    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
+    uint64_t* p_half = drain + 1;              // [2] P of keys 0-63 stored
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(p_half + 2);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
     const WaitCtx cx{abort_flag, p.status};
 
@@ -355,6 +364,7 @@ __global__ void __launch_bounds__(384, 1)
         for (int i = 0; i < 2; ++i) {
             mbar_init(&s_full[i], 1);
             mbar_init(&p_full[i], 128);
+            mbar_init(&p_half[i], 128);
             mbar_init(&o_done[i], 1);
         }
         mbar_init(drain, 1);
@@ -422,7 +432,7 @@ __global__ void __launch_bounds__(384, 1)
         const uint64_t dQ0 = sdesc_sw128(smem_u32(sm + C::Q_OFF), 16, 1024);
         const uint64_t dK0 = sdesc_sw128(smem_u32(sm + C::K_OFF), 16, 1024);
         const uint64_t dV0 = sdesc_sw128(smem_u32(sm + C::V_OFF), 16, 1024);
-#define issue_pv8(S) fp8_issue_pv(leader, (S), st, tm, dV0, p_full, v_full, kv_empty, cx)
+#define issue_pv8(S) fp8_issue_pv(leader, (S), st, tm, dV0, p_half, p_full, v_full, kv_empty, cx)
         int u = 0;
         for (int t = 0; ok && t < hi; ++t) {
             const uint32_t nd = need_of(t);
@@ -525,9 +535,11 @@ __global__ void __launch_bounds__(384, 1)
                 const float mu = (m_hat == -CUDART_INF_F) ? 0.f : m_hat;
                 const uint64_t cc = f2_make(c2t, c2t), nmu2 = f2_make(-mu, -mu);
                 uint64_t rs2 = 0ull, rr2 = 0ull;
-                uint32_t pk[32];  // 128 keys, four E4M3 weights per word
+                // O is rescaled (below) before any P V of this tile may run
+                const bool resc_any = __any_sync(0xffffffffu, resc) && n > 0;
+                uint32_t pk[2][16];  // keys 0-63 and 64-127, four E4M3 weights per word
 #pragma unroll
-                for (int c = 0; c < 4; ++c)
+                for (int c = 0; c < 4; ++c) {
 #pragma unroll
                     for (int i = 0; i < 8; ++i) {
                         float x0, x1, x2, x3;
@@ -538,10 +550,19 @@ __global__ void __launch_bounds__(384, 1)
                         const float p0 = ex2_approx(x0), p1 = ex2_approx(x1), p2 = ex2_approx(x2), p3 = ex2_approx(x3);
                         rs2 = f2_add(rs2, f2_add(f2_make(p0, p1), f2_make(p2, p3)));
                         const uint32_t lo = pack_e4m3x2(p0, p1), hi2 = pack_e4m3x2(p2, p3);
-                        pk[c * 8 + i] = lo | (hi2 << 16);
+                        pk[c >> 1][(c & 1) * 8 + i] = lo | (hi2 << 16);
                         rr2 = f2_add(rr2, f2_add(f2_from_e4m3x2(lo), f2_from_e4m3x2(hi2)));
                     }
-                tmem_st32(tl, pk);
+                    if (c == 1) {
+                        tmem_st16(tl, pk[0]);
+                        if (!resc_any) {
+                            tmem_st_wait();
+                            tc_fence_before();
+                            mbar_arrive(&p_half[s]);
+                        }
+                    }
+                }
+                tmem_st16(tl + 16, pk[1]);
                 {
                     float a_, b_;
                     f2_split(rs2, a_, b_);
@@ -550,7 +571,7 @@ __global__ void __launch_bounds__(384, 1)
                     lw += a_ + b_;
                 }
                 tmem_st_wait();
-                if (__any_sync(0xffffffffu, resc) && n > 0) {
+                if (resc_any) {
                     // O holds the previous tiles' sum (their P V was issued
                     // before this tile's S): bring it to the new reference
 #pragma unroll
@@ -565,6 +586,7 @@ __global__ void __launch_bounds__(384, 1)
                     tmem_st_wait();
                 }
                 tc_fence_before();
+                if (resc_any) mbar_arrive(&p_half[s]);
                 if (!FA_DROP_THIS_ARRIVE(n == 0)) mbar_arrive(&p_full[s]);
                 ++n;
             }
