@@ -536,12 +536,21 @@ __global__ void __launch_bounds__(384, 1)
                         for (int i = 0; i < 32; ++i)
                             if (c * 32 + i >= lim) sr[c][i] = __float_as_uint(-CUDART_INF_F);
                 }
-                float mx = -CUDART_INF_F;
+                // row maximum as eight independent chains (one dependent chain
+                // of 64 three-input maxima would sit on the softmax's
+                // critical path), combined at the end
+                float mc[8];
+#pragma unroll
+                for (int k = 0; k < 8; ++k) mc[k] = -CUDART_INF_F;
 #pragma unroll
                 for (int c = 0; c < 4; ++c)
 #pragma unroll
-                    for (int i = 0; i < 32; i += 2)
-                        mx = fmax3(mx, __uint_as_float(sr[c][i]), __uint_as_float(sr[c][i + 1]));
+                    for (int i = 0; i < 32; i += 4) {
+                        const int k = 2 * c + ((i >> 2) & 1);
+                        mc[k] = fmax3(mc[k], __uint_as_float(sr[c][i]), __uint_as_float(sr[c][i + 1]));
+                        mc[k] = fmax3(mc[k], __uint_as_float(sr[c][i + 2]), __uint_as_float(sr[c][i + 3]));
+                    }
+                const float mx = fmaxf(fmax3(mc[0], mc[1], mc[2]), fmaxf(fmax3(mc[3], mc[4], mc[5]), fmax3(mc[6], mc[7], mc[7])));
                 const float m_new = fmaxf(m_hat, mx * c2);
                 const bool resc = (m_new - m_hat) > kRescaleThreshold;
                 float alpha = 1.f;

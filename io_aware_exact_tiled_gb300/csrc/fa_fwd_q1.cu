@@ -273,11 +273,21 @@ __global__ void __launch_bounds__(384, 1)
                     for (int i = 0; i < 32; ++i)
                         if (c * 32 + i >= lim) sr[c][i] = __float_as_uint(-CUDART_INF_F);
             }
-            float mx = -CUDART_INF_F;
+            // row maximum of this group's 64 columns as four independent
+            // chains (one chain of 32 dependent maxima would sit on the
+            // critical path), combined at the end
+            float mc[4];
+#pragma unroll
+            for (int k = 0; k < 4; ++k) mc[k] = -CUDART_INF_F;
 #pragma unroll
             for (int c = 0; c < 2; ++c)
 #pragma unroll
-                for (int i = 0; i < 32; i += 2) mx = fmax3(mx, __uint_as_float(sr[c][i]), __uint_as_float(sr[c][i + 1]));
+                for (int i = 0; i < 32; i += 4) {
+                    const int k = 2 * c + ((i >> 2) & 1);
+                    mc[k] = fmax3(mc[k], __uint_as_float(sr[c][i]), __uint_as_float(sr[c][i + 1]));
+                    mc[k] = fmax3(mc[k], __uint_as_float(sr[c][i + 2]), __uint_as_float(sr[c][i + 3]));
+                }
+            float mx = fmaxf(fmax3(mc[0], mc[1], mc[2]), mc[3]);
             // agree on the row maximum with the other column group
             xbuf[(u & 1) * 256 + g * 128 + r] = mx;
             mbar_arrive(&xch[u & 1]);
