@@ -19,7 +19,8 @@
 //                       stream through a two-stage TMA ring; five tcgen05
 //                       GEMMs per tile with dK_j and dV_j accumulated in TMEM;
 //                       dQ_i = dS K_j is added into the fp32 accumulator with
-//                       TMA bulk reduce-adds staged through shared memory
+//                       TMA bulk reduce-adds staged through shared memory;
+//                       dK_j, dV_j leave through TMA stores at the end
 //   fa_bwd_dq_kernel    fp32 dQ accumulator -> dQ in bf16
 //
 // TMEM columns of fa_bwd_kernel: two 128-column buffers in [0, 256) that
@@ -92,8 +93,12 @@ struct BwdParams {
 constexpr float kLog2e = 1.4426950408889634f;
 
 // Warp roles (512 threads):
-//   warp 0        TMA producer (K_j, V_j once; Q_i, dO_i, L_i, D_i per stage)
-//   warp 1        TMEM allocation; lane 0 issues the MMAs
+//   thread 0      sets up the mbarriers and requests K_j, V_j and the first
+//                 stage before the CTA-wide barrier
+//   warp 0        TMA producer (the remaining Q_i, dO_i, L_i, D_i stages)
+//   warp 1        TMEM allocation; the whole warp runs the issue loop and one
+//                 elected lane issues the MMAs
+//   warps 2-3     tile-masked kernel only: gather the mask column into a bitmap
 //   warps 4-7     compute group 0: thread r owns key r, queries 0-63 of block i
 //   warps 8-11    compute group 1: key r, queries 64-127
 //   warps 12-15   dQ drain: thread r owns query r of block i

@@ -12,15 +12,21 @@
 // IO": block-sparse attention skips masked tiles).
 //
 // GB300 design (one CTA per pair of 128-row query tiles of one head):
-//   warp 0      TMA producer: both Q tiles once, then K/V tiles through a
-//               multi-stage shared-memory ring guarded by mbarriers
-//   warp 1      allocates TMEM; lane 0 issues every tcgen05.mma and commit
+//   thread 0    sets up the mbarriers and requests both Q tiles and the first
+//               K / V tile before the CTA-wide barrier
+//   warp 0      TMA producer: the remaining K and V tiles through separate
+//               multi-stage shared-memory rings guarded by mbarriers
+//   warp 1      allocates TMEM; the whole warp runs the issue loop and one
+//               elected lane issues every tcgen05.mma and commit
+//   warps 2-3   tile-masked kernel only: turn the mask rows into bitmaps
 //   warps 4-7   softmax warpgroup of Q tile 0 (thread r owns row r, which is
 //               TMEM lane r, so row max and row sum are in-thread)
 //   warps 8-11  softmax warpgroup of Q tile 1
 // TMEM (512 columns): per Q tile, S (128 fp32 columns, P overwrites it as
 // bf16) and the O accumulator (d columns). The MMA warp interleaves the two
-// Q tiles so that one tile's softmax overlaps the other tile's GEMMs.
+// Q tiles so that one tile's softmax overlaps the other tile's GEMMs, and
+// issues each P V in slices of the keys as the softmax stores them. The
+// epilogue stages O in the Q tile's buffer and writes it with TMA stores.
 // The online-softmax reference maximum is only moved (and O rescaled) when
 // the row maximum grows by more than 2^8 in the exp2 domain; otherwise the
 // stale maximum is kept, which is exact because o and l always share it.

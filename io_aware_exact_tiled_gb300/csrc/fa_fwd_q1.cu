@@ -8,9 +8,12 @@
 // the maximum grows, and write O = o / l and L = m + log l at the end.
 //
 // Layout of the work on one SM (384 threads):
-//   warp 0      TMA producer: Q once, then K and V tiles through a ring of
-//               STAGES (>= 3) shared-memory stages, one mbarrier per stage
-//   warp 1      TMEM allocation; lane 0 issues all MMAs
+//   thread 0    sets up the mbarriers and requests the Q tile
+//   warp 0      TMA producer: K and V tiles through a ring of STAGES (>= 3)
+//               shared-memory stages, one mbarrier per stage
+//   warp 1      TMEM allocation; the whole warp runs the issue loop and one
+//               elected lane issues all MMAs
+//   warps 2-3   turn the mask row into a bitmap (tile-masked calls)
 //   warps 4-7   softmax group 0: thread r owns row r, key columns 0-63
 //   warps 8-11  softmax group 1: row r, key columns 64-127
 // TMEM: two S buffers (columns 0-127 and 128-255, so that S for tile u+2 is
