@@ -650,9 +650,8 @@ def main():
     args = parse()
     if args.table:
         return run_table(args)
-    rank = int(os.environ.get("RANK", "0"))
-    world = int(os.environ.get("WORLD_SIZE", "1"))
-    local = int(os.environ.get("LOCAL_RANK", "0"))
+    from io_aware_exact_tiled_gb300 import replicas
+    rank, world, local = replicas.env()
     if args.impl == "reference":
         return run_reference(args, rank, world)
     from io_aware_exact_tiled_gb300 import workloads as W_
@@ -666,7 +665,6 @@ def main():
         return run_dropout(args, rank, world)
 
     import torch
-    import torch.distributed as dist
 
     import io_aware_exact_tiled_gb300 as fa
     from io_aware_exact_tiled_gb300 import accounting as acc
@@ -674,7 +672,7 @@ def main():
 
     if world > 1:
         torch.cuda.set_device(local)
-        dist.init_process_group("nccl")
+    replicas.init("nccl", world)
     dev = torch.device("cuda", local)
     torch.cuda.set_device(dev)
     fa.load()
@@ -726,8 +724,7 @@ def main():
     sampler = ClockSampler(uuid)
     if rank == 0:
         sampler.start()
-    if world > 1:
-        dist.barrier()
+    replicas.barrier()
     torch.cuda.synchronize()
     launches[0] = 0
     wall0 = time.time()
@@ -743,8 +740,7 @@ def main():
     fa.set_timing_events(None, None)
     torch.cuda.synchronize()
     wall1 = time.time()
-    if world > 1:
-        dist.barrier()
+    replicas.barrier()
     sampler.stop()
     st_f, st_b = fa.get_status(ws_f), fa.get_status(ws_b)
     if st_f != 0 or st_b != 0:
@@ -752,13 +748,11 @@ def main():
     ms = t_start.elapsed_time(t_stop)
     fwd_ms = sum(a.elapsed_time(b) for a, b in fb_ev) / K
     bwd_ms = sum(a.elapsed_time(b) for a, b in bb_ev) / K
-    if world > 1:
-        t = torch.tensor([ms, fwd_ms, bwd_ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms, fwd_ms, bwd_ms = t.tolist()
+    # the slowest rank's times; every rank did the same work
+    ms, fwd_ms, bwd_ms = replicas.max_over_ranks([ms, fwd_ms, bwd_ms], dev)
     ms_step = ms / K
     total_flop = (fwd_flop + bwd_flop) * world
-    value = total_flop / (ms_step * 1e-3) / 1e12
+    value = replicas.whole_job_rate(fwd_flop + bwd_flop, ms_step * 1e-3, world) / 1e12
 
     # ---------------- end to end through the public API with host buffers
     # Every step copies its inputs in from pinned host memory, runs forward
@@ -811,18 +805,13 @@ def main():
         torch.cuda.synchronize()
         K2 = max(3, min(K, 30))
         e0, e1 = ev(), ev()
-        if world > 1:
-            dist.barrier()
+        replicas.barrier()
         e0.record(s_in)
         for i in range(K2):
             e2e_step(3 + i)
         e1.record(s_out)  # after the last step's results are copied out
         torch.cuda.synchronize()
-        ems = e0.elapsed_time(e1)
-        if world > 1:
-            t = torch.tensor([ems], device=dev)
-            dist.all_reduce(t, op=dist.ReduceOp.MAX)
-            ems = t.item()
+        ems = replicas.max_over_ranks([e0.elapsed_time(e1)], dev)[0]
         h2d = sum(t.numel() * t.element_size() for t in (hq, hk, hv, hdo))
         d2h = sum(t.numel() * t.element_size() for t in hout[0])
         e2e = {"value": total_flop / (ems / K2 * 1e-3) / 1e12, "unit": "TFLOP/s", "h2d_bytes_per_step": h2d,
@@ -832,8 +821,7 @@ def main():
         assert torch.equal(hout[(3 + K2 - 1) % nbuf][0].view(torch.int16), dout[(3 + K2 - 1) % nbuf][0].cpu().view(torch.int16))
 
     if rank != 0:
-        if world > 1:
-            dist.destroy_process_group()
+        replicas.finish()
         return
 
     peaks, peaks_src = load_peaks()
@@ -876,8 +864,7 @@ def main():
         "peak_memory_bytes": torch.cuda.max_memory_allocated(dev),
     }
     print(json.dumps(line), flush=True)
-    if world > 1:
-        dist.destroy_process_group()
+    replicas.finish()
 
 
 if __name__ == "__main__":
