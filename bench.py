@@ -332,15 +332,19 @@ def run_table(args):
 
 # ------------------------------------------------------------------ decoding and packed batches
 def _timed_loop(fn, K, ev, fa):
-    """Run fn K times with the library's main-kernel events; returns
-    (total ms, mean main-kernel ms, launches)."""
+    """Run fn K times with the library's main-kernel events, between barriers
+    over the ranks of a replica run; returns (total ms, mean main-kernel ms,
+    launches)."""
     import torch
+
+    from io_aware_exact_tiled_gb300 import replicas
     pairs = [(ev(), ev()) for _ in range(K)]
     for a, b in pairs:
         a.record()
         b.record()
     t0, t1 = ev(), ev()
     torch.cuda.synchronize()
+    replicas.barrier()
     n = 0
     t0.record()
     for i in range(K):
@@ -349,7 +353,23 @@ def _timed_loop(fn, K, ev, fa):
     t1.record()
     fa.set_timing_events(None, None)
     torch.cuda.synchronize()
+    replicas.barrier()
     return t0.elapsed_time(t1), sum(a.elapsed_time(b) for a, b in pairs) / K, n
+
+
+def _emit(line, rank, world, dev):
+    """Print a workload's JSON line. In a replica run every rank did the same
+    work: the line reports the whole job (the slowest rank's step time, the
+    work of all ranks) and only rank 0 prints it."""
+    from io_aware_exact_tiled_gb300 import replicas
+    if world > 1:
+        ms_max = replicas.max_over_ranks([line["ms_per_step"]], dev)[0]
+        line["value"] = line["value"] * world * line["ms_per_step"] / ms_max
+        line["ms_per_step"] = ms_max
+        line["n_gpus"] = world
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    replicas.finish()
 
 
 def run_decode(args, rank, world):
@@ -449,7 +469,7 @@ def run_decode(args, rank, world):
         "split_kernel_ms": ker_ms, "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": launches,
         "clocks": sampler.summary(wall0, wall1),
     }
-    print(json.dumps(line), flush=True)
+    _emit(line, rank, world, dev)
 
 
 def run_packed(args, rank, world):
@@ -517,7 +537,7 @@ def run_packed(args, rank, world):
                      "peak_source": f"{src} bf16 dense burst"},
         "cpu_baseline": None, "e2e": None, "gpu_launches": nf + nb, "clocks": sampler.summary(wall0, wall1),
     }
-    print(json.dumps(line), flush=True)
+    _emit(line, rank, world, dev)
 
 
 def run_fp8(args, rank, world):
@@ -576,7 +596,7 @@ def run_fp8(args, rank, world):
                      "peak_source": f"{src} bf16 dense burst x 2 (nominal FP8 / BF16 ratio 4.5 / 2.25)"},
         "cpu_baseline": None, "e2e": None, "gpu_launches": launches, "clocks": sampler.summary(wall0, wall1),
     }
-    print(json.dumps(line), flush=True)
+    _emit(line, rank, world, dev)
 
 
 def run_dropout(args, rank, world, p_drop: float = 0.1):
@@ -642,7 +662,7 @@ def run_dropout(args, rank, world, p_drop: float = 0.1):
                      "traffic": None, "kernel": "fa_bwd_kernel (dropout)", "peak_source": f"{src} bf16 dense burst"},
         "cpu_baseline": None, "e2e": None, "gpu_launches": nf + nb, "clocks": sampler.summary(wall0, wall1),
     }
-    print(json.dumps(line), flush=True)
+    _emit(line, rank, world, dev)
 
 
 # ------------------------------------------------------------------ our arm
@@ -655,6 +675,11 @@ def main():
     if args.impl == "reference":
         return run_reference(args, rank, world)
     from io_aware_exact_tiled_gb300 import workloads as W_
+    if world > 1:
+        # replica run: one process per GPU under torchrun
+        import torch
+        torch.cuda.set_device(local)
+        replicas.init("nccl", world)
     if args.workload in W_.DECODE_WORKLOADS:
         return run_decode(args, rank, world)
     if args.workload in W_.PACKED_WORKLOADS:

@@ -30,9 +30,18 @@ def _worker(rank, world, port, q):
     # per-kernel times that disagree in opposite directions
     mx = replicas.max_over_ranks([10.0 * (r + 1), 1.0 + r, 7.0 - r])
     rate = replicas.whole_job_rate(3e12, mx[0] * 1e-3, w)
-    q.put((r, w, loc, mx, rate, replicas.active()))
-    replicas.barrier()
-    replicas.finish()
+    assert replicas.active()
+    # bench.py's JSON line of a replica run: rank 1 is the slower one
+    import contextlib
+    import io
+    import sys
+    sys.path.insert(0, os.path.dirname(os.path.dirname(os.path.abspath(__file__))))
+    import bench
+    line = {"value": 100.0 / (r + 1), "ms_per_step": 1.0 * (r + 1), "n_gpus": 1}
+    buf = io.StringIO()
+    with contextlib.redirect_stdout(buf):
+        bench._emit(line, r, w, "cpu")  # also leaves the process group
+    q.put((r, w, loc, mx, rate, True, buf.getvalue()))
 
 
 def test_two_gloo_ranks_take_the_slowest_time():
@@ -47,11 +56,20 @@ def test_two_gloo_ranks_take_the_slowest_time():
     for p in procs:
         p.join(timeout=60)
         assert p.exitcode == 0
-    for r, (rank, w, loc, mx, rate, act) in enumerate(out):
+    for r, (rank, w, loc, mx, rate, act, printed) in enumerate(out):
         assert (rank, w, loc, act) == (r, world, r, True)
         assert mx == [20.0, 2.0, 7.0]
         # both ranks did 3e12 units; the job took the slower rank's 20 ms
         assert rate == pytest.approx(2 * 3e12 / 0.020)
+        if r == 0:
+            # 100 units/s at 1 ms per step on rank 0, 2 ms on rank 1: the
+            # whole job does 2 x 0.1 units in 2 ms = 100 units/s
+            import json
+            d = json.loads(printed)
+            assert d["n_gpus"] == 2 and d["ms_per_step"] == 2.0
+            assert d["value"] == pytest.approx(100.0)
+        else:
+            assert printed == ""
 
 
 def test_single_process_defaults(monkeypatch):
