@@ -41,7 +41,9 @@
  * kv_len: NULL or a device int32 array [B] with 0 <= kv_len[b] <= N.
  * Ownership: the caller allocates and frees every buffer, including the
  *   workspace; the library allocates no device memory and keeps no pointer
- *   after a call returns.
+ *   after a call returns. The one exception is fa_bwd_noalloc (and its status
+ *   reader), which uses a fixed device array inside the library and caches
+ *   its address per device; its own comment below gives the rules.
  * Streams: `stream` is a cudaStream_t (NULL = legacy default stream). Calls
  *   are asynchronous with respect to the host: argument checks run on the host
  *   and return an error before anything is launched; launch failures return
@@ -258,12 +260,24 @@ fa_status fa_bwd(const void* q, const void* k, const void* v, const void* o, con
  *     serialise them on one stream.
  *   - The first call on each device (with that device current) looks up the
  *     array's device address; make that first call before any stream capture.
- *   - Device-side wait time-outs are recorded in the array's status word,
- *     which this entry point does not expose.
+ *     The address stays cached until the process exits; cudaDeviceReset
+ *     unloads the library's device code, so do not call this entry point on a
+ *     device after resetting it.
+ *   - Device-side wait time-outs are recorded in the array's status word and
+ *     returned by fa_bwd_noalloc_get_status. Each call clears the word when
+ *     it starts, so read it before the next call on that device.
  */
 fa_status fa_bwd_noalloc(const void* q, const void* k, const void* v, const void* o, const float* lse,
                          const void* dout, void* dq, void* dk, void* dv, int B, int H, int N, int d, float scale,
                          int causal, const uint8_t* blockmask, const int32_t* kv_len, fa_dtype dtype, void* stream);
+
+/* Status of the last fa_bwd_noalloc call on the current device, like
+ * fa_get_status for a workspace: synchronises `stream` (the stream of that
+ * call), then reads and clears the status word of the library's fixed
+ * scratch array. Returns FA_OK, FA_ERR_TIMEOUT (a device-side wait gave up;
+ * that call's dQ, dK, dV are invalid) or FA_ERR_CUDA. The pages have no
+ * counterpart of this call. */
+fa_status fa_bwd_noalloc_get_status(void* stream);
 
 /* Synchronises `stream`, then reads and clears the device status word of
  * `workspace` (of the fa_fwd or fa_bwd call that used it). Returns FA_OK or

@@ -394,3 +394,12 @@ def backward_noalloc(q, k, v, o, lse, do, scale: Optional[float] = None, causal:
     if rc != FA_OK:
         raise FAError(rc, "fa_bwd_noalloc")
     return dq, dk, dv
+
+
+def noalloc_status(stream=None) -> int:
+    """Synchronise and read (then clear) the status word of the last
+    fa_bwd_noalloc call on the current device (fa_bwd_noalloc_get_status)."""
+    fn = load().fa_bwd_noalloc_get_status
+    fn.argtypes = [ctypes.c_void_p]
+    fn.restype = ctypes.c_int
+    return fn(_stream_handle(stream))

@@ -24,7 +24,12 @@
 //    give wrong results; order them on one stream.
 //  * The device address of the array is looked up once per device, on the
 //    first call made while that device is current (cudaGetSymbolAddress). Make
-//    that first call on each device before any stream capture begins.
+//    that first call on each device before any stream capture begins. The
+//    address is cached for the life of the process: cudaDeviceReset unloads
+//    the library's device code, so after a reset this entry point must not be
+//    called again on that device.
+//  * A device-side wait that gives up records FA_ERR_TIMEOUT in the array's
+//    status word; fa_bwd_noalloc_get_status reads and clears it.
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -71,4 +76,11 @@ extern "C" fa_status fa_bwd_noalloc(const void* q, const void* k, const void* v,
     if (!scratch) return FA_ERR_CUDA;
     return fa_bwd(q, k, v, o, lse, dout, dq, dk, dv, B, H, N, d, scale, causal, blockmask, kv_len, dtype, scratch,
                   kNoAllocScratchBytes, stream);
+}
+
+extern "C" fa_status fa_bwd_noalloc_get_status(void* stream) {
+    void* scratch = scratch_on_current_device();
+    if (!scratch) return FA_ERR_CUDA;
+    // the status word sits at the start of the scratch, as in any fa_bwd workspace
+    return fa_get_status(scratch, stream);
 }

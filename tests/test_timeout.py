@@ -31,6 +31,10 @@ def dbg():
     lib.fa_get_status.restype = i
     lib.fa_bwd_workspace_size.argtypes = [i, i, i, i]
     lib.fa_bwd_workspace_size.restype = sz
+    lib.fa_bwd_noalloc.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, i, i, i, i, f, i, vp, vp, i, vp]
+    lib.fa_bwd_noalloc.restype = i
+    lib.fa_bwd_noalloc_get_status.argtypes = [vp]
+    lib.fa_bwd_noalloc_get_status.restype = i
     return lib
 
 
@@ -59,6 +63,13 @@ def test_bounded_waits_report_timeout(dbg, cuda_device):
                     scale, 1, None, None, fb.FA_BF16, ptr(ws), ws.numel(), s)
     assert rc == fb.FA_OK
     assert dbg.fa_get_status(ptr(ws), s) == fb.FA_ERR_TIMEOUT
+
+    # the workspace-free backward reports its give-up through its own reader
+    rc = dbg.fa_bwd_noalloc(ptr(q), ptr(k), ptr(v), ptr(o), ptr(lse), ptr(do), ptr(dq), ptr(dk), ptr(dv), B, H, N,
+                            d, scale, 1, None, None, fb.FA_BF16, s)
+    assert rc == fb.FA_OK
+    assert dbg.fa_bwd_noalloc_get_status(s) == fb.FA_ERR_TIMEOUT
+    assert dbg.fa_bwd_noalloc_get_status(s) == fb.FA_OK  # reading clears the word
 
     # the context is still usable: the regular library computes correct results
     o2, lse2 = fa.forward(q, k, v, causal=True)

@@ -61,6 +61,7 @@ def test_noalloc_matches_fa_bwd_two_calls(lib, cuda_device, w):
     for call in range(2):
         got = fb.backward_noalloc(q, k, v, o, lse, do, **kw)
         torch.cuda.synchronize()
+        assert fb.noalloc_status() == fb.FA_OK
         for name, a, b in zip(("dq", "dk", "dv"), got, ref):
             e = rel(a, b)
             assert e <= TOL_G, (call, name, e)
