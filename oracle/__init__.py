@@ -21,5 +21,5 @@ from .attention import (  # noqa: F401
 )
 from .varlen import forward_varlen, backward_varlen  # noqa: F401
 from .decode import decode_forward, split_decode  # noqa: F401
-from .fp8 import fp8_forward, e4m3_round  # noqa: F401
+from .fp8 import fp8_forward, fp8_forward_online, fp8_shift_bound, e4m3_round  # noqa: F401
 from . import dropout  # noqa: F401

@@ -37,20 +37,29 @@ silent:
 4. Scores. S = (scale_attn / d) * deq(Q8) deq(K8)^T with
    deq(x8) = x8 * scale (1/d undoes the sqrt(d) of step 1 on both sides;
    without the rotation it is 1), masked as in the dense oracle.
-5. Probabilities, online. With x = S log2(e), the keys are taken in tiles
-   of 128 in order (the tiling of "Online softmax"). Each row keeps an
-   integer reference exponent m: on the first tile with a visible key, and
-   whenever a tile's maximum exceeds m by more than 7, m becomes
-   floor(tile maximum) and the sums so far are multiplied by 2^(m_old - m)
-   (exact). The weights of a tile are p_j = 2^(x_j - m) (at most 2^8, inside
-   E4M3) rounded to E4M3 (p8_j). Because m is an integer, rounding
-   2^(x_j - m) is the same as rounding relative to any other integer
-   exponent, except for weights in E4M3's subnormal range (below 2^-6 of the
-   reference): there the result depends on m, which is why the procedure,
-   and not only the final maximum, is part of the definition.
+5. Probabilities. With x = S log2(e) and M = floor(max_j x_j) over the
+   row's visible keys, the weights are p_j = 2^(x_j - M) (in [0, 2)),
+   rounded to E4M3 (p8_j). This is the definition `fp8_forward` computes:
+   it depends on the row's scores only, not on the order in which a kernel
+   visits the keys.
 6. Output. O = sum_j p8_j deq(V8_j) / sum_j p8_j (a convex combination of
    the dequantised values), and L = logsumexp_j S_j (natural log) from the
    unrounded weights.
+
+A single-pass kernel cannot know M before it has seen every key, so it
+rounds relative to a running integer reference r instead (the online
+softmax of "Online softmax"). Rounding to E4M3 commutes with multiplication
+by 2^(M - r) except in E4M3's subnormal range (weights below 2^-6), so such a
+kernel differs from the definition only through weights p_j < 2^-6. If every
+key's weight is rounded relative to some integer r <= M (r may differ from
+key to key, as a running reference rises) with 2^(x_j - r) <= 448, each such
+weight moves by at most 2^-9 on the scale of M (half a subnormal step,
+2^-10, on either side), and O moves by at most
+2^-9 sum_{j: p_j < 2^-6} |deq(V8_j) - O| / sum_{j: p_j >= 2^-6} p8_j per
+element; `fp8_shift_bound` returns that bound. `fp8_forward_online` models
+one such procedure (128-key tiles in order; r set on the first visible tile
+and moved to floor(tile maximum) whenever a tile exceeds it by more than 7;
+sums rescaled by 2^(r_old - r_new), exactly).
 """
 
 from __future__ import annotations
@@ -122,34 +131,27 @@ def dequantize_rows(x8, sc, rows: int = BLOCK):
     return x8 * np.repeat(sc, rows)[: x8.shape[0], None]
 
 
-def quantized_inputs(q, k, v, signs, rows: int = BLOCK):
+def quantized_inputs(q, k, v, signs, rows: int = BLOCK, rotate: bool = True):
     """Steps 1-3 for one head ([N, d] arrays): (q8, q scales, k8, k scales,
-    v8, v scale), the values on the E4M3 grid as fp64."""
+    v8, v scale), the values on the E4M3 grid as fp64 (``rotate=False``
+    skips step 1)."""
     q, k, v = _f64(q), _f64(k), _f64(v)
     d = q.shape[-1]
-    T = rotation(signs) * np.sqrt(d)
+    T = rotation(signs) * np.sqrt(d) if rotate else np.eye(d)
     q8, sq = quantize_rows(q @ T, rows)
     k8, sk = quantize_rows(k @ T, rows)
     sv = pow2_scale(float(np.abs(v).max()))
     return q8, sq, k8, sk, e4m3_round(v / sv), sv
 
 
-def fp8_forward(q, k, v, scale: float, signs, causal: bool = False, rotate: bool = True, rows: int = BLOCK,
-                kv_len=None):
-    """FP8 forward of [B, H, N, d] inputs. Returns (O, L) in fp64.
-
-    ``kv_len`` (optional, [B]) masks keys j >= kv_len[b] as in the dense
-    oracle; the quantisation of steps 1-3 still covers every row.
-
-    ``rotate=False`` skips step 1 (plain block-quantised FP8), for comparing
-    the error with and without the rotation."""
+def _heads_fp8(q, k, v, scale, signs, causal, rotate, rows, kv_len):
+    """Steps 1-4 per head: yields (b, h, x = S log2 e [N, N] with -inf on
+    invisible keys, deq(V8) [N, d])."""
     q, k, v = _f64(q), _f64(k), _f64(v)
     B, H, N, d = q.shape
-    # sqrt(d) R = diag(s) H_d: the transform the GPU applies in fp32
+    # sqrt(d) R = diag(s) H_d: the transform applied to Q and K
     T = rotation(signs) * np.sqrt(d) if rotate else np.eye(d)
     s_fold = scale / d if rotate else scale
-    O = np.zeros((B, H, N, d))
-    L = np.zeros((B, H, N))
     kl = None if kv_len is None else np.asarray(kv_len.cpu() if hasattr(kv_len, "cpu") else kv_len)
     for b in range(B):
         vis = visible(N, causal, None if kl is None else int(kl[b]))
@@ -159,35 +161,105 @@ def fp8_forward(q, k, v, scale: float, signs, causal: bool = False, rotate: bool
             sv = pow2_scale(float(np.abs(v[b, h]).max()))
             v8 = e4m3_round(v[b, h] / sv)
             s = s_fold * (dequantize_rows(q8, sq, rows) @ dequantize_rows(k8, sk, rows).T)
-            s = np.where(vis, s, -np.inf)
-            x = s * np.log2(np.e)
-            vd = v8 * sv
-            m = np.full(N, -np.inf)    # integer reference exponent per row
-            l8 = np.zeros(N)           # sum of the rounded weights
-            lx = np.zeros(N)           # sum of the unrounded weights
-            o = np.zeros((N, d))
-            err = np.seterr(invalid="ignore")  # -inf - (-inf) on rows that have seen no key yet
-            for j0 in range(0, N, TILE_KEYS):
-                xt = x[:, j0:j0 + TILE_KEYS]
-                tmax = xt.max(axis=1)
-                first = np.isneginf(m)
-                upd = np.isfinite(tmax) & (first | (tmax - m > RESCALE_LOG2))
-                m_new = np.where(upd, np.floor(np.where(np.isfinite(tmax), tmax, 0.0)), m)
-                alpha = np.where(upd & ~first, np.exp2(np.where(upd & ~first, m - m_new, 0.0)), 1.0)
-                m = m_new
-                l8 *= alpha
-                lx *= alpha
-                o *= alpha[:, None]
-                mu = np.where(np.isfinite(m), m, 0.0)
-                pt = np.exp2(xt - mu[:, None])   # masked keys give 0
-                p8 = e4m3_round(pt)
-                l8 += p8.sum(axis=1)
-                lx += pt.sum(axis=1)
-                o += p8 @ vd[j0:j0 + TILE_KEYS]
-            np.seterr(**err)
-            seen = l8 > 0
-            O[b, h] = np.where(seen[:, None], o / np.where(seen, l8, 1.0)[:, None], 0.0)
-            with np.errstate(divide="ignore"):
-                L[b, h] = np.where(lx > 0, (np.where(np.isfinite(m), m, 0.0) + np.log2(np.where(lx > 0, lx, 1.0)))
-                                   * np.log(2.0), -np.inf)
+            yield b, h, np.where(vis, s, -np.inf) * np.log2(np.e), v8 * sv
+
+
+def _definition_weights(x):
+    """Step 5 for one head: M = floor(row max) (0 on rows with no visible
+    key), unrounded weights w = 2^(x - M) and their E4M3 roundings."""
+    xm = x.max(axis=1)
+    M = np.floor(np.where(np.isfinite(xm), xm, 0.0))
+    w = np.exp2(x - M[:, None])   # invisible keys give 0
+    return M, w, e4m3_round(w)
+
+
+def fp8_forward(q, k, v, scale: float, signs, causal: bool = False, rotate: bool = True, rows: int = BLOCK,
+                kv_len=None):
+    """FP8 forward of [B, H, N, d] inputs by steps 1-6 (the weights rounded
+    relative to the floor of each row's final maximum). Returns (O, L) in
+    fp64.
+
+    ``kv_len`` (optional, [B]) masks keys j >= kv_len[b] as in the dense
+    oracle; the quantisation of steps 1-3 still covers every row.
+
+    ``rotate=False`` skips step 1 (plain block-quantised FP8), for comparing
+    the error with and without the rotation."""
+    B, H, N, d = np.shape(q)
+    O = np.zeros((B, H, N, d))
+    L = np.zeros((B, H, N))
+    for b, h, x, vd in _heads_fp8(q, k, v, scale, signs, causal, rotate, rows, kv_len):
+        M, w, p8 = _definition_weights(x)
+        l8, lx = p8.sum(axis=1), w.sum(axis=1)
+        seen = l8 > 0
+        O[b, h] = np.where(seen[:, None], (p8 @ vd) / np.where(seen, l8, 1.0)[:, None], 0.0)
+        with np.errstate(divide="ignore"):
+            L[b, h] = np.where(lx > 0, (M + np.log2(np.where(lx > 0, lx, 1.0))) * np.log(2.0), -np.inf)
+    return O, L
+
+
+def fp8_shift_bound(q, k, v, scale: float, signs, causal: bool = False, rotate: bool = True, rows: int = BLOCK,
+                    kv_len=None):
+    """Per-element bound [B, H, N, d] on |O' - O| for any computation that
+    differs from `fp8_forward` only in rounding each weight relative to an
+    integer reference r <= M (any r per key, with 2^(x - r) <= 448) instead
+    of M (see the module notes):
+    2^-9 sum_{j: w_j < 2^-6} |deq(V8_j) - O| / sum_{j: w_j >= 2^-6} p8_j."""
+    B, H, N, d = np.shape(q)
+    out = np.zeros((B, H, N, d))
+    for b, h, x, vd in _heads_fp8(q, k, v, scale, signs, causal, rotate, rows, kv_len):
+        M, w, p8 = _definition_weights(x)
+        l8 = p8.sum(axis=1)
+        seen = l8 > 0
+        O = np.where(seen[:, None], (p8 @ vd) / np.where(seen, l8, 1.0)[:, None], 0.0)
+        sub = np.isfinite(x) & (w < 2.0 ** -6)
+        lnorm = np.where(sub, 0.0, p8).sum(axis=1)
+        for i in range(N):
+            if not seen[i]:
+                continue
+            out[b, h, i] = 2.0 ** -9 * np.abs(vd[sub[i]] - O[i]).sum(axis=0) / lnorm[i]
+    return out
+
+
+def fp8_forward_online(q, k, v, scale: float, signs, causal: bool = False, rotate: bool = True, rows: int = BLOCK,
+                       kv_len=None):
+    """Steps 1-6 with step 5 done by one single-pass procedure (a model of
+    how a kernel that visits 128-key tiles in order can round its weights):
+    an integer reference r per row, set to floor(tile maximum) on the first
+    tile with a visible key and moved there whenever a tile's maximum
+    exceeds r by more than 7; the sums so far are multiplied by
+    2^(r_old - r_new) (exact). Weights relative to r are <= 2^8 (inside
+    E4M3). It differs from `fp8_forward` within `fp8_shift_bound`.
+    Returns (O, L) in fp64."""
+    B, H, N, d = np.shape(q)
+    O = np.zeros((B, H, N, d))
+    L = np.zeros((B, H, N))
+    for b, h, x, vd in _heads_fp8(q, k, v, scale, signs, causal, rotate, rows, kv_len):
+        m = np.full(N, -np.inf)    # integer reference exponent r per row
+        l8 = np.zeros(N)           # sum of the rounded weights
+        lx = np.zeros(N)           # sum of the unrounded weights
+        o = np.zeros((N, d))
+        err = np.seterr(invalid="ignore")  # -inf - (-inf) on rows that have seen no key yet
+        for j0 in range(0, N, TILE_KEYS):
+            xt = x[:, j0:j0 + TILE_KEYS]
+            tmax = xt.max(axis=1)
+            first = np.isneginf(m)
+            upd = np.isfinite(tmax) & (first | (tmax - m > RESCALE_LOG2))
+            m_new = np.where(upd, np.floor(np.where(np.isfinite(tmax), tmax, 0.0)), m)
+            alpha = np.where(upd & ~first, np.exp2(np.where(upd & ~first, m - m_new, 0.0)), 1.0)
+            m = m_new
+            l8 *= alpha
+            lx *= alpha
+            o *= alpha[:, None]
+            mu = np.where(np.isfinite(m), m, 0.0)
+            pt = np.exp2(xt - mu[:, None])   # masked keys give 0
+            p8 = e4m3_round(pt)
+            l8 += p8.sum(axis=1)
+            lx += pt.sum(axis=1)
+            o += p8 @ vd[j0:j0 + TILE_KEYS]
+        np.seterr(**err)
+        seen = l8 > 0
+        O[b, h] = np.where(seen[:, None], o / np.where(seen, l8, 1.0)[:, None], 0.0)
+        with np.errstate(divide="ignore"):
+            L[b, h] = np.where(lx > 0, (np.where(np.isfinite(m), m, 0.0) + np.log2(np.where(lx > 0, lx, 1.0)))
+                               * np.log(2.0), -np.inf)
     return O, L

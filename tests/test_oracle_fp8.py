@@ -8,7 +8,10 @@ float8_e4m3fn conversion, the Hadamard matrix to its defining identities,
 the block scales to their bounds, the whole forward to closed forms (values
 already on the FP8 grid, identical keys), to exact attention within the
 format's error, and the rotation to its stated purpose (lower error when Q
-and K carry outlier channels).
+and K carry outlier channels). The weights of the definition are checked
+against torch's own E4M3 conversion, and the single-pass model of step 5
+(`fp8_forward_online`) against the definition: equal when no weight is in
+E4M3's subnormal range, within `fp8_shift_bound` otherwise.
 """
 
 import numpy as np
@@ -136,22 +139,63 @@ def test_key_padding_rows_and_empty_rows():
     assert np.all(O[1] == 0) and np.all(np.isneginf(L[1]))
 
 
-def test_online_reference_matches_global_maximum_away_from_subnormals():
-    """Reading 5: with every weight far from E4M3's subnormal range (scores
-    spread by less than 5 in log2 units and no tile raising the maximum past
-    the threshold) the online rounding equals rounding relative to the
-    integer part of the row maximum."""
+def test_definition_weights_match_torch_float8_conversion():
+    """Step 5 of the definition with the weights rounded by torch's
+    float8_e4m3fn conversion (a library routine the oracle does not use):
+    weights relative to floor(row max), O normalised by their sum."""
+    rng = np.random.default_rng(8)
+    B, H, N, d = 1, 2, 256, 32
+    q, k, v = (rng.standard_normal((B, H, N, d)) for _ in range(3))
+    k *= 2.0   # wide scores: many weights in the subnormal range
+    scale = 1 / np.sqrt(d)
+    signs = np.where(rng.random(d) < 0.5, -1.0, 1.0)
+    O, L = F8.fp8_forward(q, k, v, scale, signs, causal=True)
+    T = np.diag(signs) @ F8.hadamard(d)
+    vis = np.tril(np.ones((N, N), dtype=bool))
+    for h in range(H):
+        q8, sq = F8.quantize_rows(q[0, h] @ T)
+        k8, sk = F8.quantize_rows(k[0, h] @ T)
+        sv = F8.pow2_scale(float(np.abs(v[0, h]).max()))
+        vd = F8.e4m3_round(v[0, h] / sv) * sv
+        x = np.where(vis, scale / d * (F8.dequantize_rows(q8, sq) @ F8.dequantize_rows(k8, sk).T), -np.inf)
+        x = x * np.log2(np.e)
+        w = np.exp2(x - np.floor(x.max(axis=1, keepdims=True)))
+        p8 = torch.from_numpy(w).to(torch.float8_e4m3fn).to(torch.float64).numpy()
+        assert (p8[vis] < 2.0 ** -6).sum() > 1000   # the subnormal range is exercised
+        np.testing.assert_allclose(O[0, h], (p8 @ vd) / p8.sum(axis=1, keepdims=True), atol=1e-13)
+
+
+def test_online_model_equals_definition_away_from_subnormals():
+    """With every weight far from E4M3's subnormal range (scores spread by
+    less than 5 in log2 units, so no tile raises the reference past the
+    threshold either) the single-pass model equals the definition."""
     rng = np.random.default_rng(7)
     B, H, N, d = 1, 1, 384, 16
     q, k, v = (rng.standard_normal((B, H, N, d)) for _ in range(3))
     scale = 0.05
     O, L = F8.fp8_forward(q, k, v, scale, np.ones(d), rotate=False)
-    q8, sq = F8.quantize_rows(q[0, 0])
-    k8, sk = F8.quantize_rows(k[0, 0])
-    sv = F8.pow2_scale(float(np.abs(v[0, 0]).max()))
-    vd = F8.e4m3_round(v[0, 0] / sv) * sv
-    x = scale * (F8.dequantize_rows(q8, sq) @ F8.dequantize_rows(k8, sk).T) * np.log2(np.e)
+    O1, L1 = F8.fp8_forward_online(q, k, v, scale, np.ones(d), rotate=False)
+    x = scale * (q[0, 0] @ k[0, 0].T) * np.log2(np.e)
     assert (x.max(axis=1) - x.min(axis=1)).max() < 5.0
-    p8 = F8.e4m3_round(np.exp2(x - np.floor(x.max(axis=1, keepdims=True))))
-    np.testing.assert_allclose(O[0, 0], (p8 @ vd) / p8.sum(axis=1, keepdims=True), atol=1e-13)
-    np.testing.assert_allclose(L[0, 0], np.log(np.exp(x / np.log2(np.e)).sum(axis=1)), atol=1e-12)
+    assert np.all(F8.fp8_shift_bound(q, k, v, scale, np.ones(d), rotate=False) == 0.0)
+    np.testing.assert_allclose(O1, O, atol=1e-13)
+    np.testing.assert_allclose(L1, L, atol=1e-12)
+
+
+def test_online_model_within_the_shift_bound_on_wide_scores():
+    """Wide scores (K x 2, causal, N = 512): the model's references trail the
+    final maxima, so weights in the subnormal range round differently; every
+    element stays within the derived bound, and the bound is not vacuous."""
+    rng = np.random.default_rng(12)
+    B, H, N, d = 1, 2, 512, 64
+    q, k, v = (rng.standard_normal((B, H, N, d)) for _ in range(3))
+    k *= 2.0
+    scale = 1 / np.sqrt(d)
+    signs = np.where(rng.random(d) < 0.5, -1.0, 1.0)
+    O, _ = F8.fp8_forward(q, k, v, scale, signs, causal=True)
+    O1, _ = F8.fp8_forward_online(q, k, v, scale, signs, causal=True)
+    bound = F8.fp8_shift_bound(q, k, v, scale, signs, causal=True)
+    diff = np.abs(O1 - O)
+    assert diff.max() > 1e-3                      # the two roundings do differ
+    assert np.all(diff <= bound + 1e-12)
+    assert np.median(bound[diff > 0]) < 0.2       # and the bound is informative
