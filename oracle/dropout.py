@@ -84,42 +84,59 @@ def keep_mask(b: int, h: int, rows, N: int, seed: int, p: float) -> np.ndarray:
     return byte >= np.uint64(t)
 
 
-def forward(q, k, v, scale: float, p: float, seed: int, causal: bool = False, kv_len=None):
-    """Attention with dropout on P. Returns (O [B,H,N,d], L [B,H,N]) in fp64."""
+def forward(q, k, v, scale: float, p: float, seed: int, causal: bool = False, kv_len=None, heads=None,
+            chunk: int = 1024):
+    """Attention with dropout on P. Returns (O [B,H,N,d], L [B,H,N]) in fp64.
+    ``heads`` optionally restricts the work to a list of (b, h) pairs (the
+    other heads are left as NaN); query rows are processed in chunks of
+    ``chunk`` rows, each holding whole rows of S, P and Z."""
     q, k, v = _f64(q), _f64(k), _f64(v)
     B, H, N, d = q.shape
     keep = 1.0 - threshold(p) / 256.0
-    O = np.zeros((B, H, N, d))
-    _, L = dense_forward(q, k, v, scale, causal=causal, kv_len=kv_len)
+    O = np.full((B, H, N, d), np.nan)
+    _, L = dense_forward(q, k, v, scale, causal=causal, kv_len=kv_len, heads=heads, chunk=chunk)
     kl = None if kv_len is None else np.asarray(kv_len.cpu() if hasattr(kv_len, "cpu") else kv_len)
-    rows = np.arange(N)
+    want = None if heads is None else set(heads)
     for b in range(B):
-        vis = visible(N, causal, None if kl is None else int(kl[b]), None, rows)
         for h in range(H):
-            P, _, _ = probabilities(scores(q[b, h], k[b, h], scale, vis))
-            Z = keep_mask(b, h, rows, N, seed, p)
-            O[b, h] = (P * Z / keep) @ v[b, h]
+            if want is not None and (b, h) not in want:
+                continue
+            for r0 in range(0, N, chunk):
+                rows = np.arange(r0, min(N, r0 + chunk))
+                vis = visible(N, causal, None if kl is None else int(kl[b]), None, rows)
+                P, _, _ = probabilities(scores(q[b, h, rows], k[b, h], scale, vis))
+                Z = keep_mask(b, h, rows, N, seed, p)
+                O[b, h, rows] = (P * Z / keep) @ v[b, h]
     return O, L
 
 
-def backward(q, k, v, do, scale: float, p: float, seed: int, causal: bool = False, kv_len=None):
-    """Gradients of <dO, O> for the dropout forward. Returns (dQ, dK, dV)."""
+def backward(q, k, v, do, scale: float, p: float, seed: int, causal: bool = False, kv_len=None, heads=None,
+             chunk: int = 1024):
+    """Gradients of <dO, O> for the dropout forward. Returns (dQ, dK, dV);
+    ``heads`` and ``chunk`` as for `forward` (dK and dV sum the chunks'
+    contributions)."""
     q, k, v, do = _f64(q), _f64(k), _f64(v), _f64(do)
     B, H, N, d = q.shape
     keep = 1.0 - threshold(p) / 256.0
-    dq, dk, dv = np.zeros_like(q), np.zeros_like(k), np.zeros_like(v)
+    dq, dk, dv = np.full_like(q, np.nan), np.full_like(k, np.nan), np.full_like(v, np.nan)
     kl = None if kv_len is None else np.asarray(kv_len.cpu() if hasattr(kv_len, "cpu") else kv_len)
-    rows = np.arange(N)
+    want = None if heads is None else set(heads)
     for b in range(B):
-        vis = visible(N, causal, None if kl is None else int(kl[b]), None, rows)
         for h in range(H):
-            P, _, _ = probabilities(scores(q[b, h], k[b, h], scale, vis))
-            Zs = keep_mask(b, h, rows, N, seed, p) / keep
-            dv[b, h] = (P * Zs).T @ do[b, h]
-            dP = (do[b, h] @ v[b, h].T) * Zs
-            dS = P * (dP - (P * dP).sum(axis=1, keepdims=True))
-            dq[b, h] = scale * dS @ k[b, h]
-            dk[b, h] = scale * dS.T @ q[b, h]
+            if want is not None and (b, h) not in want:
+                continue
+            dk_bh, dv_bh = np.zeros((N, d)), np.zeros((N, d))
+            for r0 in range(0, N, chunk):
+                rows = np.arange(r0, min(N, r0 + chunk))
+                vis = visible(N, causal, None if kl is None else int(kl[b]), None, rows)
+                P, _, _ = probabilities(scores(q[b, h, rows], k[b, h], scale, vis))
+                Zs = keep_mask(b, h, rows, N, seed, p) / keep
+                dv_bh += (P * Zs).T @ do[b, h, rows]
+                dP = (do[b, h, rows] @ v[b, h].T) * Zs
+                dS = P * (dP - (P * dP).sum(axis=1, keepdims=True))
+                dq[b, h, rows] = scale * dS @ k[b, h]
+                dk_bh += scale * dS.T @ q[b, h, rows]
+            dk[b, h], dv[b, h] = dk_bh, dv_bh
     return dq, dk, dv
 
 

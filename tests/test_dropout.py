@@ -94,3 +94,23 @@ def test_dropout_rejects(cuda_device):
         run(x, cuda_device, 1.0, 1, False, backward=False)
     with pytest.raises(fb.FAError):
         run(x, cuda_device, -0.1, 1, False, backward=False)
+
+
+@pytest.mark.gpu
+def test_dropout_long8k_sampled_heads(cuda_device):
+    """The benchmarked shape (B 1, H 32, N 8192, d 128, causal, K x 2,
+    p = 0.1): the Philox counters reach query index 8191 and head 31. Whole
+    heads (0, 0) and (0, 31) are compared with the oracle (heads are
+    independent, so the check is exact for them)."""
+    w = W.WORKLOADS["long8k"]
+    x = W.make_inputs(w, seed=0)
+    p, seed = 0.1, 1234
+    o, lse, dq, dk, dv = run(x, cuda_device, p, seed, True)
+    heads = [(0, 0), (0, 31)]
+    O, L = DR.forward(x.q, x.k, x.v, x.scale, p, seed, causal=True, heads=heads)
+    G = DR.backward(x.q, x.k, x.v, x.do, x.scale, p, seed, causal=True, heads=heads)
+    for (b, h) in heads:
+        check_o(o[b, h], O[b, h], p)
+        assert float(np.abs(lse[b, h] - L[b, h]).max()) <= TOL_L
+        e = {n: rel(g[b, h], ref[b, h]) for n, g, ref in zip(("dq", "dk", "dv"), (dq, dk, dv), G)}
+        assert max(e.values()) <= TOL_G, ((b, h), e)

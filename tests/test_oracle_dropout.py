@@ -105,3 +105,19 @@ def test_D_identity_with_dropout():
     Zs = DR.keep_mask(0, 0, np.arange(33), 33, 5, 0.2) / (1 - DR.threshold(0.2) / 256)
     dP = (do[0, 0] @ v[0, 0].T) * Zs
     np.testing.assert_allclose((do[0, 0] * O[0, 0]).sum(axis=1), (P * dP).sum(axis=1), atol=1e-12)
+
+
+def test_row_chunks_and_head_subsets_do_not_change_the_result():
+    """Chunking the query rows and restricting the heads only reorders the
+    sums: the chosen heads equal the whole computation's."""
+    rng = np.random.default_rng(3)
+    B, H, N, d = 1, 3, 100, 8
+    q, k, v, do = (rng.standard_normal((B, H, N, d)) for _ in range(4))
+    full = DR.forward(q, k, v, 0.3, 0.2, 99, causal=True)
+    part = DR.forward(q, k, v, 0.3, 0.2, 99, causal=True, heads=[(0, 2)], chunk=7)
+    np.testing.assert_allclose(part[0][0, 2], full[0][0, 2], rtol=0, atol=1e-12)
+    gf = DR.backward(q, k, v, do, 0.3, 0.2, 99, causal=True)
+    gp = DR.backward(q, k, v, do, 0.3, 0.2, 99, causal=True, heads=[(0, 2)], chunk=7)
+    for a, b in zip(gp, gf):
+        np.testing.assert_allclose(a[0, 2], b[0, 2], rtol=0, atol=1e-12)
+        assert np.isnan(a[0, 0]).all()

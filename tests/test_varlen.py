@@ -159,3 +159,35 @@ def test_backward_status_clear(cuda_device):
     ws = fb.workspace(fb.load().fa_bwd_varlen_workspace_size(3, H, total, d), cuda_device)
     fb.backward_varlen(q, k, v, o, lse, do, cu, x.max_seqlen, causal=True, ws=ws)
     assert fb.get_status(ws) == fb.FA_OK
+
+
+@pytest.mark.gpu
+def test_mix8k_packed_sampled_sequences(cuda_device):
+    """The benchmarked packed batch (16 causal sequences, lengths
+    U{512..8192}, H 32, d 128), run whole on the GPU; the two longest
+    sequences (several thousand tokens each) are compared with the oracle on
+    heads 0 and 31 (sequences and heads are independent, so the oracle runs
+    on each as a packed batch of one)."""
+    w = W.PACKED_WORKLOADS["mix8k_packed"]
+    x = W.make_packed_workload(w, seed=0)
+    dev = cuda_device
+    q, k, v, do = (t.to(dev) for t in (x.q, x.k, x.v, x.do))
+    cu = x.cu_seqlens.to(dev)
+    o, lse = fb.forward_varlen(q, k, v, cu, x.max_seqlen, scale=x.scale, causal=True)
+    dq, dk, dv = fb.backward_varlen(q, k, v, o, lse, do, cu, x.max_seqlen, scale=x.scale, causal=True)
+    torch.cuda.synchronize()
+    o, lse, dq, dk, dv = (t.float().cpu().numpy() for t in (o, lse, dq, dk, dv))
+    cuh = x.cu_seqlens.tolist()
+    order = sorted(range(len(x.lens)), key=lambda b: -x.lens[b])[:2]
+    assert min(x.lens[b] for b in order) >= 4096
+    hs = [0, 31]
+    for b in order:
+        s, e = cuh[b], cuh[b + 1]
+        one = torch.tensor([0, e - s], dtype=torch.int32)
+        sub = lambda t: t[s:e][:, hs]
+        O, L = VL.forward_varlen(sub(x.q), sub(x.k), sub(x.v), one, x.scale, causal=True)
+        G = VL.backward_varlen(sub(x.q), sub(x.k), sub(x.v), sub(x.do), one, x.scale, causal=True)
+        assert float(np.abs(o[s:e][:, hs] - O).max()) <= TOL_O
+        assert float(np.abs(lse[hs][:, s:e] - L).max()) <= TOL_L
+        e_g = {n: rel(g[s:e][:, hs], ref) for n, g, ref in zip(("dq", "dk", "dv"), (dq, dk, dv), G)}
+        assert max(e_g.values()) <= TOL_G, (b, x.lens[b], e_g)
