@@ -167,18 +167,22 @@ fa_status fa_decode(const void* q, const void* k, const void* v, void* o, float*
  *      divided by the power of two 2^ceil(log2(amax / 448)) and rounded to
  *      E4M3 (nearest even, saturating);
  *   3. S and O = softmax(S) V on the FP8 tensor cores; the weights are
- *      rounded to E4M3 relative to an integer exponent, O is normalised by
- *      the sum of the rounded weights and L comes from the unrounded ones.
+ *      rounded to E4M3 relative to a running integer exponent (a weight
+ *      below 2^-6 of the row's final maximum can therefore round differently
+ *      than relative to that maximum), O is normalised by the sum of the
+ *      rounded weights and L comes from the unrounded ones.
  *   q, k, v   in,  device, [B, H, N, 128] bf16
  *   o         out, device, [B, H, N, 128] bf16
  *   lse       out, device, float32 [B, H, N]
- *   signs     in,  device, float32 [128], each +1 or -1 (drawn by the caller)
+ *   signs     in,  device, float32 [128], each +1 or -1 (drawn by the
+ *             caller), or NULL: no rotation (step 1 skipped, Q and K are
+ *             quantised as they are; for measuring what the rotation buys)
  *   causal, kv_len  masks as for fa_fwd (no tile mask)
  *   workspace fa_fwd_fp8_workspace_size(B, H, N, d) bytes: the quantised
- *             Q, K and V^T and their scale exponents
- * d = 128 and N a multiple of 128 only (FA_ERR_UNSUPPORTED otherwise). Runs
- * five kernels: quantisation of Q, of K, V's maximum, V's quantisation, and
- * the attention kernel.
+ *             Q, K and V^T, their scale exponents and V's block maxima
+ * d = 128, N a multiple of 128 and B * H <= 65535 only (FA_ERR_UNSUPPORTED
+ * otherwise). Runs three kernels: quantisation of Q and K together with the
+ * block maxima of V, V's quantisation, and the attention kernel.
  */
 size_t fa_fwd_fp8_workspace_size(int B, int H, int N, int d);
 fa_status fa_fwd_fp8(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int N, int d,

@@ -234,15 +234,16 @@ def backward_varlen(q, k, v, o, lse, do, cu_seqlens, max_seqlen: int, scale: Opt
 def forward_fp8(q, k, v, signs, scale: Optional[float] = None, causal: bool = False, kv_len=None, out=None,
                 lse=None, ws=None, stream=None):
     """O, L = fa_fwd_fp8(...): the FP8 forward pass with a Hadamard rotation
-    (signs: float32 [128] of +-1 on the device) and per-block scales. q, k, v:
-    [B, H, N, 128] bf16. Returns (o bf16, lse fp32 [B, H, N])."""
+    (signs: float32 [128] of +-1 on the device; None skips the rotation) and
+    per-block scales. q, k, v: [B, H, N, 128] bf16. Returns (o bf16, lse fp32
+    [B, H, N])."""
     lib = load()
     dtype = _check_qkv(q, k, v)
     if dtype != FA_BF16:
         raise ValueError("the FP8 path takes bfloat16 inputs")
     B, H, N, d = q.shape
-    if signs.dtype != torch.float32 or signs.shape != (d,) or signs.device != q.device:
-        raise ValueError("signs must be a float32 [d] tensor on the same device")
+    if signs is not None and (signs.dtype != torch.float32 or signs.shape != (d,) or signs.device != q.device):
+        raise ValueError("signs must be None or a float32 [d] tensor on the same device")
     scale = 1.0 / math.sqrt(d) if scale is None else float(scale)
     o = torch.empty_like(q) if out is None else out
     L = torch.empty((B, H, N), dtype=torch.float32, device=q.device) if lse is None else lse

@@ -297,20 +297,20 @@ size_t fa_fwd_fp8_workspace_size(int B, int H, int N, int d) {
     if (B <= 0 || H <= 0 || N <= 0 || d <= 0) return 0;
     const size_t bhn = static_cast<size_t>(B) * H * N, bh = static_cast<size_t>(B) * H;
     const size_t tiles = bh * ((N + 127) / 128);
-    return kStatusBytes + 3 * align256(bhn * d) + 2 * align256(tiles * sizeof(int)) + 2 * align256(bh * sizeof(int));
+    return kStatusBytes + 3 * align256(bhn * d) + 3 * align256(tiles * sizeof(int)) + align256(bh * sizeof(int));
 }
 
 fa_status fa_fwd_fp8(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int N, int d,
                      float scale, int causal, const int32_t* kv_len, const float* signs, void* workspace,
                      size_t ws_bytes, void* stream) {
-    if (!q || !k || !v || !o || !lse || !signs || !workspace) return FA_ERR_INVALID_ARG;
+    if (!q || !k || !v || !o || !lse || !workspace) return FA_ERR_INVALID_ARG;
     if (causal != 0 && causal != 1) return FA_ERR_INVALID_ARG;
     fa_status st = check_shape(B, H, N, d, scale);
     if (st != FA_OK) return st;
     if (d != 128) return FA_ERR_UNSUPPORTED;
-    if (N / 128 > 65535) return FA_ERR_UNSUPPORTED;
+    if (N / 128 > 65535 || static_cast<long long>(B) * H > 65535) return FA_ERR_UNSUPPORTED;  // quantisation grids
     if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(o, 16) || !aligned(lse, 4) ||
-        !aligned(signs, 4) || !aligned(workspace, 256) || (kv_len && !aligned(kv_len, 4)))
+        (signs && !aligned(signs, 4)) || !aligned(workspace, 256) || (kv_len && !aligned(kv_len, 4)))
         return FA_ERR_INVALID_ARG;
     if (ws_bytes < fa_fwd_fp8_workspace_size(B, H, N, d)) return FA_ERR_INVALID_ARG;
     const size_t bhn = static_cast<size_t>(B) * H * N, bh = static_cast<size_t>(B) * H;
@@ -343,7 +343,7 @@ fa_status fa_fwd_fp8(const void* q, const void* k, const void* v, void* o, float
     off += align256(tiles * sizeof(int));
     a.vexp = reinterpret_cast<int*>(ws + off);
     off += align256(bh * sizeof(int));
-    a.vmax_bits = reinterpret_cast<int*>(ws + off);
+    a.vblk_max = reinterpret_cast<float*>(ws + off);
     a.ev_begin = g_ev_begin;
     a.ev_end = g_ev_end;
     cudaStream_t s = static_cast<cudaStream_t>(stream);

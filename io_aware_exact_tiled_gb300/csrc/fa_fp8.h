@@ -14,13 +14,13 @@ struct Fp8Args {
     float scale;
     int causal;
     const int32_t* kv_len;  // [B] or null
-    const float* signs;     // [128] +-1: the random signs of the rotation
+    const float* signs;     // [128] +-1: the random signs of the rotation; null: no rotation
     // workspace
     uint8_t *q8, *k8;       // [B,H,N,128] E4M3 (rotated Q, K)
     uint8_t* vt8;           // [B,H,128,N] E4M3 (V transposed)
     int *qexp, *kexp;       // [B,H,N/128] block scale exponents
     int* vexp;              // [B,H]
-    int* vmax_bits;         // [B,H] scratch
+    float* vblk_max;        // [B,H,N/128] max |v| per 128-row block (scratch)
     int* status;
     cudaEvent_t ev_begin, ev_end;  // optional, recorded around the attention kernel
 };

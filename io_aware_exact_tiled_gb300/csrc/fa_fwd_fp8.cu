@@ -22,11 +22,14 @@
 // do not depend on when the running maximum was last moved: rounding to E4M3
 // commutes with multiplication by powers of two (away from the subnormals).
 //
-// Kernels: fa_fp8_qk_kernel (rotate + quantise Q and K, one CTA per 128-row
-// block), fa_fp8_vmax_kernel and fa_fp8_v_kernel (per-head amax of V, then
-// quantise and transpose it), fa_fwd_fp8_kernel (attention; two 128-row query
-// tiles per CTA, warp 0 TMA, warp 1 MMA, two softmax warpgroups, as in the
-// bf16 kernel). d = 128.
+// Kernels: fa_fp8_prep_kernel (one CTA per 128-row block of Q, of K and of
+// V: rotates and quantises the Q and K blocks and takes the maximum |v| of
+// each V block, in one launch), fa_fp8_v_kernel (the head's V scale from its
+// block maxima, then V quantised and transposed), fa_fwd_fp8_kernel
+// (attention; two 128-row query tiles per CTA, warp 0 TMA, warp 1 MMA, two
+// softmax warpgroups, as in the bf16 kernel). d = 128. Without signs (a null
+// pointer) step 1 is skipped: Q and K are quantised as they are and the 1/d
+// is not folded into the score scale.
 #include <math_constants.h>
 
 #include "fa_common.cuh"
@@ -70,17 +73,25 @@ __device__ __forceinline__ void fwht8_inlane(float (&a)[8]) {
             }
 }
 
-__global__ void __launch_bounds__(256) fa_fp8_qk_kernel(const uint16_t* __restrict__ x, const float* __restrict__ signs,
-                                                        uint8_t* __restrict__ x8, int* __restrict__ exps, int N) {
+// blockIdx.z selects the tensor: 0 = Q, 1 = K (rotated when ROT, block
+// scale, E4M3), 2 = V (only the block's max |v|, for the head's V scale).
+template <bool ROT>
+__global__ void __launch_bounds__(256) fa_fp8_prep_kernel(const uint16_t* __restrict__ q,
+                                                          const uint16_t* __restrict__ k,
+                                                          const uint16_t* __restrict__ v,
+                                                          const float* __restrict__ signs, uint8_t* __restrict__ q8,
+                                                          uint8_t* __restrict__ k8, int* __restrict__ qexp,
+                                                          int* __restrict__ kexp, float* __restrict__ vblk_max, int N) {
     __shared__ float wmax[8];
     __shared__ int e_sh;
     __shared__ float sg_sh[kD8];
-    const int blk = blockIdx.x, bh = blockIdx.y;
+    const int blk = blockIdx.x, bh = blockIdx.y, which = blockIdx.z;
+    const uint16_t* x = which == 0 ? q : (which == 1 ? k : v);
     const int T = N / kTile;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int t = lane & 3, rq = lane >> 2;  // column quarter, row within the warp's 8
     const size_t row0 = static_cast<size_t>(bh) * N + static_cast<size_t>(blk) * kTile;
-    if (threadIdx.x < kD8) sg_sh[threadIdx.x] = signs[threadIdx.x];
+    if (ROT && which < 2 && threadIdx.x < kD8) sg_sh[threadIdx.x] = signs[threadIdx.x];
     // both passes' rows are requested before any arithmetic
     uint4 raw[2][4];
 #pragma unroll
@@ -88,6 +99,28 @@ __global__ void __launch_bounds__(256) fa_fp8_qk_kernel(const uint16_t* __restri
         const uint16_t* src = x + (row0 + warp * 16 + ps * 8 + rq) * kD8;
 #pragma unroll
         for (int k = 0; k < 4; ++k) raw[ps][k] = *reinterpret_cast<const uint4*>(src + 32 * k + 8 * t);
+    }
+    if (which == 2) {  // V: the block's maximum |v| only (uniform branch per CTA)
+        float m = 0.f;
+#pragma unroll
+        for (int ps = 0; ps < 2; ++ps)
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+                const uint32_t u[4] = {raw[ps][k].x, raw[ps][k].y, raw[ps][k].z, raw[ps][k].w};
+#pragma unroll
+                for (int h = 0; h < 4; ++h)
+                    m = fmaxf(m, fmaxf(fabsf(__uint_as_float(u[h] << 16)), fabsf(__uint_as_float(u[h] & 0xFFFF0000u))));
+            }
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, off));
+        if (lane == 0) wmax[warp] = m;
+        __syncthreads();
+        if (threadIdx.x == 0) {
+            float mm = 0.f;
+            for (int w = 0; w < 8; ++w) mm = fmaxf(mm, wmax[w]);
+            vblk_max[static_cast<size_t>(bh) * T + blk] = mm;
+        }
+        return;
     }
     __syncthreads();
     float y[2][4][8];
@@ -100,32 +133,38 @@ __global__ void __launch_bounds__(256) fa_fp8_qk_kernel(const uint16_t* __restri
 #pragma unroll
             for (int h = 0; h < 4; ++h) {
                 const int c = 32 * k + 8 * t + 2 * h;
-                y[ps][k][2 * h] = __uint_as_float(u[h] << 16) * sg_sh[c];
-                y[ps][k][2 * h + 1] = __uint_as_float(u[h] & 0xFFFF0000u) * sg_sh[c + 1];
-            }
-            fwht8_inlane(y[ps][k]);  // column bits 0-2
-        }
-        // column bits 5-6: butterflies across k
-#pragma unroll
-        for (int e = 0; e < 8; ++e) {
-            float b0 = y[ps][0][e] + y[ps][1][e], b1 = y[ps][0][e] - y[ps][1][e];
-            float b2 = y[ps][2][e] + y[ps][3][e], b3 = y[ps][2][e] - y[ps][3][e];
-            y[ps][0][e] = b0 + b2;
-            y[ps][1][e] = b1 + b3;
-            y[ps][2][e] = b0 - b2;
-            y[ps][3][e] = b1 - b3;
-        }
-        // column bits 3-4: partner lanes t ^ 1, t ^ 2
-#pragma unroll
-        for (int m = 1; m < 4; m <<= 1) {
-            const bool upper = (t & m) != 0;
-#pragma unroll
-            for (int k = 0; k < 4; ++k)
-#pragma unroll
-                for (int e = 0; e < 8; ++e) {
-                    const float o = __shfl_xor_sync(0xffffffffu, y[ps][k][e], m);
-                    y[ps][k][e] = upper ? o - y[ps][k][e] : y[ps][k][e] + o;
+                y[ps][k][2 * h] = __uint_as_float(u[h] << 16);
+                y[ps][k][2 * h + 1] = __uint_as_float(u[h] & 0xFFFF0000u);
+                if (ROT) {
+                    y[ps][k][2 * h] *= sg_sh[c];
+                    y[ps][k][2 * h + 1] *= sg_sh[c + 1];
                 }
+            }
+            if (ROT) fwht8_inlane(y[ps][k]);  // column bits 0-2
+        }
+        if (ROT) {
+            // column bits 5-6: butterflies across k
+#pragma unroll
+            for (int e = 0; e < 8; ++e) {
+                float b0 = y[ps][0][e] + y[ps][1][e], b1 = y[ps][0][e] - y[ps][1][e];
+                float b2 = y[ps][2][e] + y[ps][3][e], b3 = y[ps][2][e] - y[ps][3][e];
+                y[ps][0][e] = b0 + b2;
+                y[ps][1][e] = b1 + b3;
+                y[ps][2][e] = b0 - b2;
+                y[ps][3][e] = b1 - b3;
+            }
+            // column bits 3-4: partner lanes t ^ 1, t ^ 2
+#pragma unroll
+            for (int m = 1; m < 4; m <<= 1) {
+                const bool upper = (t & m) != 0;
+#pragma unroll
+                for (int k = 0; k < 4; ++k)
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) {
+                        const float o = __shfl_xor_sync(0xffffffffu, y[ps][k][e], m);
+                        y[ps][k][e] = upper ? o - y[ps][k][e] : y[ps][k][e] + o;
+                    }
+            }
         }
 #pragma unroll
         for (int k = 0; k < 4; ++k)
@@ -141,10 +180,11 @@ __global__ void __launch_bounds__(256) fa_fp8_qk_kernel(const uint16_t* __restri
         for (int w = 0; w < 8; ++w) m = fmaxf(m, wmax[w]);
         const int e = pow2_scale_exp(m);
         e_sh = e;
-        exps[static_cast<size_t>(bh) * T + blk] = e;
+        (which == 0 ? qexp : kexp)[static_cast<size_t>(bh) * T + blk] = e;
     }
     __syncthreads();
     const float inv = exp2i(-e_sh);
+    uint8_t* x8 = which == 0 ? q8 : k8;
 #pragma unroll
     for (int ps = 0; ps < 2; ++ps) {
         uint8_t* dst = x8 + (row0 + warp * 16 + ps * 8 + rq) * kD8;
@@ -158,48 +198,18 @@ __global__ void __launch_bounds__(256) fa_fp8_qk_kernel(const uint16_t* __restri
     }
 }
 
-// Per-head max |v| (as float bits; nonnegative floats order like integers);
-// four independent 16-byte loads in flight per thread.
-__global__ void __launch_bounds__(256) fa_fp8_vmax_kernel(const uint16_t* __restrict__ v, int* __restrict__ vmax_bits,
-                                                          long long per_head) {
-    const int bh = blockIdx.y;
-    const uint4* src = reinterpret_cast<const uint4*>(v + static_cast<size_t>(bh) * per_head);
-    const long long n8 = per_head / 8;
-    const long long stride = static_cast<long long>(gridDim.x) * 256;
-    float m = 0.f;
-    for (long long i0 = static_cast<long long>(blockIdx.x) * 256 + threadIdx.x; i0 < n8; i0 += 4 * stride) {
-        uint4 w[4];
-#pragma unroll
-        for (int q = 0; q < 4; ++q) {
-            const long long i = i0 + q * stride;
-            w[q] = i < n8 ? src[i] : make_uint4(0u, 0u, 0u, 0u);
-        }
-#pragma unroll
-        for (int q = 0; q < 4; ++q) {
-            const uint32_t u[4] = {w[q].x, w[q].y, w[q].z, w[q].w};
-#pragma unroll
-            for (int e = 0; e < 4; ++e)
-                m = fmaxf(m, fmaxf(fabsf(__uint_as_float(u[e] << 16)), fabsf(__uint_as_float(u[e] & 0xFFFF0000u))));
-        }
-    }
-#pragma unroll
-    for (int off = 16; off > 0; off >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, off));
-    if ((threadIdx.x & 31) == 0) atomicMax(vmax_bits + bh, __float_as_int(m));
-}
-
 // V -> E4M3 with the head's scale, transposed to [d][keys] (the P V product
 // needs K-major operands): one CTA per (128-key block, head). Thread (lane,
 // warp) converts keys 4 lane .. 4 lane + 3 of columns 16 warp .. 16 warp + 15,
 // so each column's four key bytes form one 32-bit word of the transposed
 // tile (a warp writes 128 contiguous bytes of a row of it).
 __global__ void __launch_bounds__(256) fa_fp8_v_kernel(const uint16_t* __restrict__ v,
-                                                       const int* __restrict__ vmax_bits, uint8_t* __restrict__ vt8,
+                                                       const float* __restrict__ vblk_max, uint8_t* __restrict__ vt8,
                                                        int* __restrict__ vexp, int N) {
     __shared__ __align__(16) uint32_t t8w[kD8][kTile / 4 + 4];  // [column][key quad]; +4 words keep rows 16-byte aligned
+    __shared__ float wmax[8];
     const int blk = blockIdx.x, bh = blockIdx.y;
-    const int e = pow2_scale_exp(__int_as_float(vmax_bits[bh]));
-    if (blk == 0 && threadIdx.x == 0) vexp[bh] = e;
-    const float inv = exp2i(-e);
+    const int T = N / kTile;
     const size_t row0 = static_cast<size_t>(bh) * N + static_cast<size_t>(blk) * kTile;
     const int kq = threadIdx.x & 31, cg = threadIdx.x >> 5;
     uint4 w[4][2];
@@ -209,6 +219,19 @@ __global__ void __launch_bounds__(256) fa_fp8_v_kernel(const uint16_t* __restric
         w[r][0] = src[0];
         w[r][1] = src[1];
     }
+    // the head's max |v| from its blocks' maxima
+    float hm = 0.f;
+    for (int i = threadIdx.x; i < T; i += 256) hm = fmaxf(hm, vblk_max[static_cast<size_t>(bh) * T + i]);
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) hm = fmaxf(hm, __shfl_xor_sync(0xffffffffu, hm, off));
+    if (kq == 0) wmax[cg] = hm;
+    __syncthreads();
+    hm = wmax[0];
+#pragma unroll
+    for (int i = 1; i < 8; ++i) hm = fmaxf(hm, wmax[i]);
+    const int e = pow2_scale_exp(hm);
+    if (blk == 0 && threadIdx.x == 0) vexp[bh] = e;
+    const float inv = exp2i(-e);
 #pragma unroll
     for (int h = 0; h < 2; ++h) {
         uint32_t u[4][4];
@@ -675,16 +698,18 @@ cudaError_t launch_fwd_fp8(const Fp8Args& a, cudaStream_t stream, int* nlaunch) 
     const int T = a.N / kTile;
     const int BH = a.B * a.H;
     const uint64_t rows = static_cast<uint64_t>(BH) * a.N;
-    // quantisation
-    fa_fp8_qk_kernel<<<dim3(T, BH), 256, 0, stream>>>(static_cast<const uint16_t*>(a.q), a.signs, a.q8, a.qexp, a.N);
-    fa_fp8_qk_kernel<<<dim3(T, BH), 256, 0, stream>>>(static_cast<const uint16_t*>(a.k), a.signs, a.k8, a.kexp, a.N);
-    cudaError_t e = cudaMemsetAsync(a.vmax_bits, 0, sizeof(int) * BH, stream);
-    if (e != cudaSuccess) return e;
-    const long long per_head = static_cast<long long>(a.N) * kD8;
-    const int chunks = static_cast<int>(min(64LL, (per_head / 8 + 255) / 256));
-    fa_fp8_vmax_kernel<<<dim3(chunks, BH), 256, 0, stream>>>(static_cast<const uint16_t*>(a.v), a.vmax_bits, per_head);
-    fa_fp8_v_kernel<<<dim3(T, BH), 256, 0, stream>>>(static_cast<const uint16_t*>(a.v), a.vmax_bits, a.vt8, a.vexp,
-                                                      a.N);
+    // quantisation: Q, K and the V block maxima in one launch, then V
+    const dim3 pgrid(T, BH, 3);
+    const uint16_t *q16 = static_cast<const uint16_t*>(a.q), *k16 = static_cast<const uint16_t*>(a.k),
+                   *v16 = static_cast<const uint16_t*>(a.v);
+    if (a.signs)
+        fa_fp8_prep_kernel<true><<<pgrid, 256, 0, stream>>>(q16, k16, v16, a.signs, a.q8, a.k8, a.qexp, a.kexp,
+                                                             a.vblk_max, a.N);
+    else
+        fa_fp8_prep_kernel<false><<<pgrid, 256, 0, stream>>>(q16, k16, v16, nullptr, a.q8, a.k8, a.qexp, a.kexp,
+                                                              a.vblk_max, a.N);
+    fa_fp8_v_kernel<<<dim3(T, BH), 256, 0, stream>>>(v16, a.vblk_max, a.vt8, a.vexp, a.N);
+    cudaError_t e;
     CUtensorMap tq, tk, tv, to;
     if (!make_tmap_2d_sw128(&to, a.o, rows, kD8, 2, 32, 64) ||
         !make_tmap_2d_sw128(&tq, a.q8, rows, kD8, 1, kTile, 128) ||
@@ -701,7 +726,8 @@ cudaError_t launch_fwd_fp8(const Fp8Args& a, cudaStream_t stream, int* nlaunch) 
     p.B = a.B;
     p.H = a.H;
     p.N = a.N;
-    p.c2 = a.scale * 1.4426950408889634f / static_cast<float>(kD8);
+    // the rotation leaves a factor d in Q' K'^T (diag(s) H_d is sqrt(d) times an orthogonal matrix)
+    p.c2 = a.scale * 1.4426950408889634f / (a.signs ? static_cast<float>(kD8) : 1.f);
     p.mask.blockmask = nullptr;
     p.mask.kv_len = a.kv_len;
     p.mask.causal = a.causal;
@@ -716,7 +742,7 @@ cudaError_t launch_fwd_fp8(const Fp8Args& a, cudaStream_t stream, int* nlaunch) 
     if (a.ev_begin) cudaEventRecord(a.ev_begin, stream);
     fa_fwd_fp8_kernel<<<grid, C::THREADS, C::SMEM, stream>>>(tq, tk, tv, to, p);
     if (a.ev_end) cudaEventRecord(a.ev_end, stream);
-    *nlaunch = 5;
+    *nlaunch = 3;
     return cudaGetLastError();
 }
 
