@@ -85,36 +85,38 @@ def keep_mask(b: int, h: int, rows, N: int, seed: int, p: float) -> np.ndarray:
 
 
 def forward(q, k, v, scale: float, p: float, seed: int, causal: bool = False, kv_len=None, heads=None,
-            chunk: int = 1024):
+            chunk: int = 1024, rows=None):
     """Attention with dropout on P. Returns (O [B,H,N,d], L [B,H,N]) in fp64.
     ``heads`` optionally restricts the work to a list of (b, h) pairs (the
-    other heads are left as NaN); query rows are processed in chunks of
-    ``chunk`` rows, each holding whole rows of S, P and Z."""
+    other heads are left as NaN) and ``rows`` = (r0, r1) to those query
+    rows; query rows are processed in chunks of ``chunk`` rows, each holding
+    whole rows of S, P and Z."""
     q, k, v = _f64(q), _f64(k), _f64(v)
     B, H, N, d = q.shape
     keep = 1.0 - threshold(p) / 256.0
     O = np.full((B, H, N, d), np.nan)
-    _, L = dense_forward(q, k, v, scale, causal=causal, kv_len=kv_len, heads=heads, chunk=chunk)
+    _, L = dense_forward(q, k, v, scale, causal=causal, kv_len=kv_len, heads=heads, chunk=chunk, rows=rows)
+    lo, hi = (0, N) if rows is None else rows
     kl = None if kv_len is None else np.asarray(kv_len.cpu() if hasattr(kv_len, "cpu") else kv_len)
     want = None if heads is None else set(heads)
     for b in range(B):
         for h in range(H):
             if want is not None and (b, h) not in want:
                 continue
-            for r0 in range(0, N, chunk):
-                rows = np.arange(r0, min(N, r0 + chunk))
-                vis = visible(N, causal, None if kl is None else int(kl[b]), None, rows)
-                P, _, _ = probabilities(scores(q[b, h, rows], k[b, h], scale, vis))
-                Z = keep_mask(b, h, rows, N, seed, p)
-                O[b, h, rows] = (P * Z / keep) @ v[b, h]
+            for r0 in range(lo, hi, chunk):
+                rr = np.arange(r0, min(hi, r0 + chunk))
+                vis = visible(N, causal, None if kl is None else int(kl[b]), None, rr)
+                P, _, _ = probabilities(scores(q[b, h, rr], k[b, h], scale, vis))
+                Z = keep_mask(b, h, rr, N, seed, p)
+                O[b, h, rr] = (P * Z / keep) @ v[b, h]
     return O, L
 
 
 def backward(q, k, v, do, scale: float, p: float, seed: int, causal: bool = False, kv_len=None, heads=None,
-             chunk: int = 1024):
+             chunk: int = 1024, rows=None):
     """Gradients of <dO, O> for the dropout forward. Returns (dQ, dK, dV);
-    ``heads`` and ``chunk`` as for `forward` (dK and dV sum the chunks'
-    contributions)."""
+    ``heads``, ``rows`` and ``chunk`` as for `forward` (dK and dV sum the
+    contributions of the rows taken)."""
     q, k, v, do = _f64(q), _f64(k), _f64(v), _f64(do)
     B, H, N, d = q.shape
     keep = 1.0 - threshold(p) / 256.0
@@ -126,16 +128,17 @@ def backward(q, k, v, do, scale: float, p: float, seed: int, causal: bool = Fals
             if want is not None and (b, h) not in want:
                 continue
             dk_bh, dv_bh = np.zeros((N, d)), np.zeros((N, d))
-            for r0 in range(0, N, chunk):
-                rows = np.arange(r0, min(N, r0 + chunk))
-                vis = visible(N, causal, None if kl is None else int(kl[b]), None, rows)
-                P, _, _ = probabilities(scores(q[b, h, rows], k[b, h], scale, vis))
-                Zs = keep_mask(b, h, rows, N, seed, p) / keep
-                dv_bh += (P * Zs).T @ do[b, h, rows]
-                dP = (do[b, h, rows] @ v[b, h].T) * Zs
+            lo, hi = (0, N) if rows is None else rows
+            for r0 in range(lo, hi, chunk):
+                rr = np.arange(r0, min(hi, r0 + chunk))
+                vis = visible(N, causal, None if kl is None else int(kl[b]), None, rr)
+                P, _, _ = probabilities(scores(q[b, h, rr], k[b, h], scale, vis))
+                Zs = keep_mask(b, h, rr, N, seed, p) / keep
+                dv_bh += (P * Zs).T @ do[b, h, rr]
+                dP = (do[b, h, rr] @ v[b, h].T) * Zs
                 dS = P * (dP - (P * dP).sum(axis=1, keepdims=True))
-                dq[b, h, rows] = scale * dS @ k[b, h]
-                dk_bh += scale * dS.T @ q[b, h, rows]
+                dq[b, h, rr] = scale * dS @ k[b, h]
+                dk_bh += scale * dS.T @ q[b, h, rr]
             dk[b, h], dv[b, h] = dk_bh, dv_bh
     return dq, dk, dv
 
