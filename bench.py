@@ -43,6 +43,11 @@ def parse():
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-targets", action="store_true",
+                    help="skip the measurement of the other N >= 4096 workloads (the line's 'targets')")
+    ap.add_argument("--spin-up-s", type=float, default=0.5,
+                    help="untimed calls after the warm-up steps until the GPU has been busy this long (0: none), "
+                         "so that the clocks have settled before the timed region")
     ap.add_argument("--table", action="store_true",
                     help="measure every workload (times, TFLOP/s, errors vs the oracle on sampled heads); "
                          "prints one JSON object per workload instead of the benchmark line")
@@ -443,11 +448,18 @@ def timed_steps(fns, K, fa, flush=None):
     return total, [sum(a.elapsed_time(b) for a, b in row) / K for row in kern], n
 
 
-def spin_up(fn, seconds=0.5, min_calls=3):
+SPIN_UP_S = 0.5
+
+
+def spin_up(fn, seconds=None, min_calls=3):
     """Untimed calls (beyond the warm-up steps) until the GPU has been busy
-    for about `seconds`, so that its clocks have settled under load before
-    the timed region starts."""
+    for about `seconds` (default: the --spin-up-s option), so that its clocks
+    have settled under load before the timed region starts; none when it is
+    0 (deterministic launch counts, e.g. under a profiler)."""
     import torch
+    seconds = SPIN_UP_S if seconds is None else min(seconds, SPIN_UP_S)
+    if seconds <= 0:
+        return
     t0 = time.time()
     n = 0
     while n < min_calls or time.time() - t0 < seconds:
@@ -954,7 +966,9 @@ def target_row(case, ms_step, fwd_ms, bwd_ms, peak):
 
 
 def main():
+    global SPIN_UP_S
     args = parse()
+    SPIN_UP_S = args.spin_up_s
     if args.table:
         return run_table(args)
     from io_aware_exact_tiled_gb300 import replicas
@@ -1087,7 +1101,7 @@ def main():
 
     # ---------------- the other N >= 4096, d = 128 configurations, same protocol
     targets = None
-    if world == 1:
+    if world == 1 and not args.no_targets:
         targets = {w.name: target_row(case, ms_step, fwd_ms, bwd_ms, peak)}
         Kt = max(5, min(K, 50))
         for name in TARGET_WORKLOADS:

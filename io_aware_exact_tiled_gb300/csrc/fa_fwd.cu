@@ -96,7 +96,6 @@ struct FwdParams {
     DropoutArgs drop;           // dropout on the probabilities (DROPOUT kernels)
     int head_major;             // grid (pairs, H, B) instead of (H, B, pairs)
     int group;                  // > 0: 1D grid of head groups (heads per group), longest pair first in each
-    int pf_ahead;               // 1D grid: prefetch into L2 the Q tiles of CTA blockIdx.x + pf_ahead (0: off)
 };
 
 // Work item L of the head-group order: groups of `group` heads in turn (the
@@ -317,16 +316,6 @@ __global__ void __launch_bounds__(384, 1)
                 load_v(t0, 0);
                 t_early = t0;
             }
-        }
-        // Q is the one operand read from DRAM exactly once; the CTA about a
-        // wave ahead in the 1D order finds its Q tiles in L2
-        if (!VARLEN && p.group > 0 && p.pf_ahead > 0 && blockIdx.x + p.pf_ahead < gridDim.x) {
-            int b2, h2, z2;
-            fwd_group_item(static_cast<int>(blockIdx.x + p.pf_ahead), p.group, npairs, p.B * p.H, p.H, b2, h2, z2);
-            const int qb2 = 2 * (npairs - 1 - z2);
-            for (int s = 0; s < 2 && qb2 + s < T; ++s)
-                for (int r = 0; r < C::NREG; ++r)
-                    tma_prefetch_l2_2d(&tmQ, r * C::BOXC, (b2 * p.H + h2) * N + (qb2 + s) * kTile);
         }
     }
     if (warp == 0 && lane == 0) {
@@ -909,14 +898,6 @@ static cudaError_t launch_fwd_t(const FwdArgs& a, cudaStream_t stream, int* nlau
         g = g < 1 ? 1 : g;
         p.group = static_cast<int>(g < a.B * a.H ? g : a.B * a.H);
     }
-    static int nsm = 0;
-    if (nsm == 0) {
-        int dev = 0;
-        if (cudaGetDevice(&dev) != cudaSuccess ||
-            cudaDeviceGetAttribute(&nsm, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
-            nsm = 0;
-    }
-    p.pf_ahead = p.group > 0 ? nsm : 0;
     const dim3 grid = p.group > 0     ? dim3(static_cast<unsigned>((T + 1) / 2) * a.H * a.B)
                       : p.head_major ? dim3((T + 1) / 2, a.H, a.B)
                                      : dim3(a.H, a.B, (T + 1) / 2);
