@@ -22,15 +22,18 @@
 // do not depend on when the running maximum was last moved: rounding to E4M3
 // commutes with multiplication by powers of two (away from the subnormals).
 //
-// Kernels: fa_fp8_prep_kernel (one CTA per 128-row block of Q, of K and of
-// V: rotates and quantises the Q and K blocks and takes the maximum |v| of
-// each V block, in one launch), fa_fp8_v_kernel (the head's V scale from its
+// Kernels: fa_fp8_prep_kernel (persistent, three CTAs per SM walking the
+// 128-row blocks of Q, K and V through double-buffered bulk copies: rotates
+// and quantises the Q and K blocks and takes the maximum |v| of each V block,
+// in one launch), fa_fp8_v_kernel (the head's V scale from its
 // block maxima, then V quantised and transposed), fa_fwd_fp8_kernel
 // (attention; two 128-row query tiles per CTA, warp 0 TMA, warp 1 MMA, two
 // softmax warpgroups, as in the bf16 kernel). d = 128. Without signs (a null
 // pointer) step 1 is skipped: Q and K are quantised as they are and the 1/d
 // is not folded into the score scale.
 #include <math_constants.h>
+
+#include <algorithm>
 
 #include "fa_common.cuh"
 #include "fa_fp8.h"
@@ -73,128 +76,195 @@ __device__ __forceinline__ void fwht8_inlane(float (&a)[8]) {
             }
 }
 
-// blockIdx.z selects the tensor: 0 = Q, 1 = K (rotated when ROT, block
-// scale, E4M3), 2 = V (only the block's max |v|, for the head's V scale).
+// Persistent: each CTA walks the 128-row blocks j = blockIdx.x, + gridDim.x,
+// ... of the three tensors in the order Q, K, V (V's blocks last, so that
+// V is still partly in L2 when fa_fp8_v_kernel reads it again). Q and K
+// blocks are rotated (when ROT), scaled and rounded to E4M3; a V block only
+// gets its maximum |v| (for the head's V scale). Blocks are contiguous 32 KiB
+// and come into two shared-memory buffers by bulk copies, the one after next
+// requested as soon as the current one has been read into registers, so
+// every SM keeps loads in flight while it computes.
+constexpr int kPrepBlockBytes = kTile * kD8 * 2;  // 128 rows of bf16
+constexpr int kPrepCtasPerSm = 3;
+constexpr int kPrepSmem = 2 * kPrepBlockBytes + 64;  // two buffers, two mbarriers, abort flag
+
 template <bool ROT>
-__global__ void __launch_bounds__(256) fa_fp8_prep_kernel(const uint16_t* __restrict__ q,
-                                                          const uint16_t* __restrict__ k,
-                                                          const uint16_t* __restrict__ v,
-                                                          const float* __restrict__ signs, uint8_t* __restrict__ q8,
-                                                          uint8_t* __restrict__ k8, int* __restrict__ qexp,
-                                                          int* __restrict__ kexp, float* __restrict__ vblk_max, int N) {
+__global__ void __launch_bounds__(256, kPrepCtasPerSm)
+    fa_fp8_prep_kernel(const uint16_t* __restrict__ q, const uint16_t* __restrict__ k, const uint16_t* __restrict__ v,
+                       const float* __restrict__ signs, uint8_t* __restrict__ q8, uint8_t* __restrict__ k8,
+                       int* __restrict__ qexp, int* __restrict__ kexp, float* __restrict__ vblk_max, int N, int BH,
+                       int* status) {
+    extern __shared__ __align__(128) uint8_t prep_smem[];
     __shared__ float wmax[8];
     __shared__ int e_sh;
     __shared__ float sg_sh[kD8];
-    const int blk = blockIdx.x, bh = blockIdx.y, which = blockIdx.z;
-    const uint16_t* x = which == 0 ? q : (which == 1 ? k : v);
+    uint64_t* full = reinterpret_cast<uint64_t*>(prep_smem + 2 * kPrepBlockBytes);  // [2]
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(full + 2);
+    const WaitCtx cx{abort_flag, status};
     const int T = N / kTile;
+    const int per_tensor = T * BH;
+    const int nblocks = 3 * per_tensor;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int t = lane & 3, rq = lane >> 2;  // column quarter, row within the warp's 8
-    const size_t row0 = static_cast<size_t>(bh) * N + static_cast<size_t>(blk) * kTile;
-    if (ROT && which < 2 && threadIdx.x < kD8) sg_sh[threadIdx.x] = signs[threadIdx.x];
-    // both passes' rows are requested before any arithmetic
-    uint4 raw[2][4];
-#pragma unroll
-    for (int ps = 0; ps < 2; ++ps) {
-        const uint16_t* src = x + (row0 + warp * 16 + ps * 8 + rq) * kD8;
-#pragma unroll
-        for (int k = 0; k < 4; ++k) raw[ps][k] = *reinterpret_cast<const uint4*>(src + 32 * k + 8 * t);
+    // first row of block j ([B * H * N, 128] view of its tensor)
+    auto block_src = [=](int j) -> const uint16_t* {
+        const int which = j / per_tensor, rem = j - which * per_tensor;
+        const uint16_t* x = which == 0 ? q : (which == 1 ? k : v);
+        return x + static_cast<size_t>(rem) * kTile * kD8;  // rem = bh * T + blk
+    };
+    if (threadIdx.x == 0) {
+        *abort_flag = 0;
+        mbar_init(&full[0], 1);
+        mbar_init(&full[1], 1);
+        fence_barrier_init();
     }
-    if (which == 2) {  // V: the block's maximum |v| only (uniform branch per CTA)
-        float m = 0.f;
-#pragma unroll
-        for (int ps = 0; ps < 2; ++ps)
-#pragma unroll
-            for (int k = 0; k < 4; ++k) {
-                const uint32_t u[4] = {raw[ps][k].x, raw[ps][k].y, raw[ps][k].z, raw[ps][k].w};
-#pragma unroll
-                for (int h = 0; h < 4; ++h)
-                    m = fmaxf(m, fmaxf(fabsf(__uint_as_float(u[h] << 16)), fabsf(__uint_as_float(u[h] & 0xFFFF0000u))));
-            }
-#pragma unroll
-        for (int off = 16; off > 0; off >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, off));
-        if (lane == 0) wmax[warp] = m;
-        __syncthreads();
-        if (threadIdx.x == 0) {
-            float mm = 0.f;
-            for (int w = 0; w < 8; ++w) mm = fmaxf(mm, wmax[w]);
-            vblk_max[static_cast<size_t>(bh) * T + blk] = mm;
-        }
-        return;
-    }
+    if (ROT && threadIdx.x < kD8) sg_sh[threadIdx.x] = signs[threadIdx.x];
     __syncthreads();
-    float y[2][4][8];
-    float amax = 0.f;
+    // thread 0: copies issued into each buffer, and which buffers still have
+    // one outstanding (issued, not yet consumed)
+    int n_issued0 = 0, n_issued1 = 0;
+    uint32_t issued = 0;
+    if (threadIdx.x == 0) {
+        for (int i = 0; i < 2; ++i) {
+            const int j = blockIdx.x + i * gridDim.x;
+            if (j < nblocks) {
+                mbar_arrive_expect_tx(&full[i], kPrepBlockBytes);
+                bulk_load(prep_smem + i * kPrepBlockBytes, block_src(j), kPrepBlockBytes, &full[i]);
+                issued |= 1u << i;
+                if (i) ++n_issued1; else ++n_issued0;
+            }
+        }
+    }
+    int it = 0;
+    for (int j = blockIdx.x; j < nblocks; j += gridDim.x, ++it) {
+        const int buf = it & 1;
+        if (!__syncthreads_and(mbar_wait(&full[buf], (it >> 1) & 1, cx, 31))) break;
+        if (threadIdx.x == 0) issued &= ~(1u << buf);
+        // this thread's two rows (passes) of the block, four 16-byte pieces each
+        uint4 raw[2][4];
 #pragma unroll
-    for (int ps = 0; ps < 2; ++ps) {
+        for (int ps = 0; ps < 2; ++ps) {
+            const uint8_t* src = prep_smem + buf * kPrepBlockBytes + (warp * 16 + ps * 8 + rq) * (kD8 * 2);
 #pragma unroll
-        for (int k = 0; k < 4; ++k) {
-            const uint32_t u[4] = {raw[ps][k].x, raw[ps][k].y, raw[ps][k].z, raw[ps][k].w};
+            for (int kk = 0; kk < 4; ++kk) raw[ps][kk] = *reinterpret_cast<const uint4*>(src + 64 * kk + 16 * t);
+        }
+        __syncthreads();  // buffer read by every thread: request the block after next
+        if (threadIdx.x == 0) {
+            const int j2 = j + 2 * gridDim.x;
+            if (j2 < nblocks) {
+                mbar_arrive_expect_tx(&full[buf], kPrepBlockBytes);
+                bulk_load(prep_smem + buf * kPrepBlockBytes, block_src(j2), kPrepBlockBytes, &full[buf]);
+                issued |= 1u << buf;
+                if (buf) ++n_issued1; else ++n_issued0;
+            }
+        }
+        const int which = j / per_tensor, rem = j - which * per_tensor;  // rem = bh * T + blk
+        const size_t row0 = static_cast<size_t>(rem) * kTile;
+        if (which == 2) {  // V: the block's maximum |v| only (uniform branch per CTA)
+            float m = 0.f;
 #pragma unroll
-            for (int h = 0; h < 4; ++h) {
-                const int c = 32 * k + 8 * t + 2 * h;
-                y[ps][k][2 * h] = __uint_as_float(u[h] << 16);
-                y[ps][k][2 * h + 1] = __uint_as_float(u[h] & 0xFFFF0000u);
-                if (ROT) {
-                    y[ps][k][2 * h] *= sg_sh[c];
-                    y[ps][k][2 * h + 1] *= sg_sh[c + 1];
+            for (int ps = 0; ps < 2; ++ps)
+#pragma unroll
+                for (int kk = 0; kk < 4; ++kk) {
+                    const uint32_t u[4] = {raw[ps][kk].x, raw[ps][kk].y, raw[ps][kk].z, raw[ps][kk].w};
+#pragma unroll
+                    for (int h = 0; h < 4; ++h)
+                        m = fmaxf(m, fmaxf(fabsf(__uint_as_float(u[h] << 16)),
+                                           fabsf(__uint_as_float(u[h] & 0xFFFF0000u))));
+                }
+#pragma unroll
+            for (int off = 16; off > 0; off >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, off));
+            if (lane == 0) wmax[warp] = m;
+            __syncthreads();
+            if (threadIdx.x == 0) {
+                float mm = 0.f;
+                for (int w = 0; w < 8; ++w) mm = fmaxf(mm, wmax[w]);
+                vblk_max[rem] = mm;
+            }
+            continue;
+        }
+        float y[2][4][8];
+        float amax = 0.f;
+#pragma unroll
+        for (int ps = 0; ps < 2; ++ps) {
+#pragma unroll
+            for (int kk = 0; kk < 4; ++kk) {
+                const uint32_t u[4] = {raw[ps][kk].x, raw[ps][kk].y, raw[ps][kk].z, raw[ps][kk].w};
+#pragma unroll
+                for (int h = 0; h < 4; ++h) {
+                    const int c = 32 * kk + 8 * t + 2 * h;
+                    y[ps][kk][2 * h] = __uint_as_float(u[h] << 16);
+                    y[ps][kk][2 * h + 1] = __uint_as_float(u[h] & 0xFFFF0000u);
+                    if (ROT) {
+                        y[ps][kk][2 * h] *= sg_sh[c];
+                        y[ps][kk][2 * h + 1] *= sg_sh[c + 1];
+                    }
+                }
+                if (ROT) fwht8_inlane(y[ps][kk]);  // column bits 0-2
+            }
+            if (ROT) {
+                // column bits 5-6: butterflies across kk
+#pragma unroll
+                for (int e = 0; e < 8; ++e) {
+                    float b0 = y[ps][0][e] + y[ps][1][e], b1 = y[ps][0][e] - y[ps][1][e];
+                    float b2 = y[ps][2][e] + y[ps][3][e], b3 = y[ps][2][e] - y[ps][3][e];
+                    y[ps][0][e] = b0 + b2;
+                    y[ps][1][e] = b1 + b3;
+                    y[ps][2][e] = b0 - b2;
+                    y[ps][3][e] = b1 - b3;
+                }
+                // column bits 3-4: partner lanes t ^ 1, t ^ 2
+#pragma unroll
+                for (int m = 1; m < 4; m <<= 1) {
+                    const bool upper = (t & m) != 0;
+#pragma unroll
+                    for (int kk = 0; kk < 4; ++kk)
+#pragma unroll
+                        for (int e = 0; e < 8; ++e) {
+                            const float o = __shfl_xor_sync(0xffffffffu, y[ps][kk][e], m);
+                            y[ps][kk][e] = upper ? o - y[ps][kk][e] : y[ps][kk][e] + o;
+                        }
                 }
             }
-            if (ROT) fwht8_inlane(y[ps][k]);  // column bits 0-2
-        }
-        if (ROT) {
-            // column bits 5-6: butterflies across k
 #pragma unroll
-            for (int e = 0; e < 8; ++e) {
-                float b0 = y[ps][0][e] + y[ps][1][e], b1 = y[ps][0][e] - y[ps][1][e];
-                float b2 = y[ps][2][e] + y[ps][3][e], b3 = y[ps][2][e] - y[ps][3][e];
-                y[ps][0][e] = b0 + b2;
-                y[ps][1][e] = b1 + b3;
-                y[ps][2][e] = b0 - b2;
-                y[ps][3][e] = b1 - b3;
-            }
-            // column bits 3-4: partner lanes t ^ 1, t ^ 2
+            for (int kk = 0; kk < 4; ++kk)
 #pragma unroll
-            for (int m = 1; m < 4; m <<= 1) {
-                const bool upper = (t & m) != 0;
-#pragma unroll
-                for (int k = 0; k < 4; ++k)
-#pragma unroll
-                    for (int e = 0; e < 8; ++e) {
-                        const float o = __shfl_xor_sync(0xffffffffu, y[ps][k][e], m);
-                        y[ps][k][e] = upper ? o - y[ps][k][e] : y[ps][k][e] + o;
-                    }
-            }
+                for (int e = 0; e < 8; ++e) amax = fmaxf(amax, fabsf(y[ps][kk][e]));
         }
 #pragma unroll
-        for (int k = 0; k < 4; ++k)
+        for (int off = 16; off > 0; off >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, off));
+        if (lane == 0) wmax[warp] = amax;
+        __syncthreads();
+        if (threadIdx.x == 0) {
+            float m = 0.f;
+            for (int w = 0; w < 8; ++w) m = fmaxf(m, wmax[w]);
+            const int e = pow2_scale_exp(m);
+            e_sh = e;
+            (which == 0 ? qexp : kexp)[rem] = e;
+        }
+        __syncthreads();
+        const float inv = exp2i(-e_sh);
+        uint8_t* x8 = which == 0 ? q8 : k8;
 #pragma unroll
-            for (int e = 0; e < 8; ++e) amax = fmaxf(amax, fabsf(y[ps][k][e]));
+        for (int ps = 0; ps < 2; ++ps) {
+            uint8_t* dst = x8 + (row0 + warp * 16 + ps * 8 + rq) * kD8;
+#pragma unroll
+            for (int kk = 0; kk < 4; ++kk) {
+                uint2 w;
+                w.x = pack_e4m3x2(y[ps][kk][0] * inv, y[ps][kk][1] * inv) |
+                      (pack_e4m3x2(y[ps][kk][2] * inv, y[ps][kk][3] * inv) << 16);
+                w.y = pack_e4m3x2(y[ps][kk][4] * inv, y[ps][kk][5] * inv) |
+                      (pack_e4m3x2(y[ps][kk][6] * inv, y[ps][kk][7] * inv) << 16);
+                *reinterpret_cast<uint2*>(dst + 32 * kk + 8 * t) = w;
+            }
+        }
     }
-#pragma unroll
-    for (int off = 16; off > 0; off >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, off));
-    if (lane == 0) wmax[warp] = amax;
-    __syncthreads();
+    // after a give-up, copies still in flight must land before the CTA exits
     if (threadIdx.x == 0) {
-        float m = 0.f;
-        for (int w = 0; w < 8; ++w) m = fmaxf(m, wmax[w]);
-        const int e = pow2_scale_exp(m);
-        e_sh = e;
-        (which == 0 ? qexp : kexp)[static_cast<size_t>(bh) * T + blk] = e;
-    }
-    __syncthreads();
-    const float inv = exp2i(-e_sh);
-    uint8_t* x8 = which == 0 ? q8 : k8;
-#pragma unroll
-    for (int ps = 0; ps < 2; ++ps) {
-        uint8_t* dst = x8 + (row0 + warp * 16 + ps * 8 + rq) * kD8;
-#pragma unroll
-        for (int k = 0; k < 4; ++k) {
-            uint2 w;
-            w.x = pack_e4m3x2(y[ps][k][0] * inv, y[ps][k][1] * inv) | (pack_e4m3x2(y[ps][k][2] * inv, y[ps][k][3] * inv) << 16);
-            w.y = pack_e4m3x2(y[ps][k][4] * inv, y[ps][k][5] * inv) | (pack_e4m3x2(y[ps][k][6] * inv, y[ps][k][7] * inv) << 16);
-            *reinterpret_cast<uint2*>(dst + 32 * k + 8 * t) = w;
-        }
+        // copies into buffer b complete its phases in order; the outstanding
+        // one is the last issued there
+        if (issued & 1u) mbar_wait_teardown(&full[0], (n_issued0 - 1) & 1, 200000000ull);
+        if (issued & 2u) mbar_wait_teardown(&full[1], (n_issued1 - 1) & 1, 200000000ull);
     }
 }
 
@@ -698,16 +768,34 @@ cudaError_t launch_fwd_fp8(const Fp8Args& a, cudaStream_t stream, int* nlaunch) 
     const int T = a.N / kTile;
     const int BH = a.B * a.H;
     const uint64_t rows = static_cast<uint64_t>(BH) * a.N;
-    // quantisation: Q, K and the V block maxima in one launch, then V
-    const dim3 pgrid(T, BH, 3);
+    // quantisation: Q, K and the V block maxima in one persistent launch, then V
+    static int nsm = 0;
+    static bool prep_attr = false;
+    if (nsm == 0) {
+        int dev = 0;
+        if (cudaGetDevice(&dev) != cudaSuccess ||
+            cudaDeviceGetAttribute(&nsm, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || nsm <= 0)
+            return cudaErrorUnknown;
+    }
+    if (!prep_attr) {
+        cudaError_t e0 = cudaFuncSetAttribute(fa_fp8_prep_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                              kPrepSmem);
+        if (e0 == cudaSuccess)
+            e0 = cudaFuncSetAttribute(fa_fp8_prep_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                      kPrepSmem);
+        if (e0 != cudaSuccess) return e0;
+        prep_attr = true;
+    }
+    const long long nblocks = 3LL * T * BH;
+    const unsigned pgrid = static_cast<unsigned>(std::min<long long>(nblocks, static_cast<long long>(nsm) * kPrepCtasPerSm));
     const uint16_t *q16 = static_cast<const uint16_t*>(a.q), *k16 = static_cast<const uint16_t*>(a.k),
                    *v16 = static_cast<const uint16_t*>(a.v);
     if (a.signs)
-        fa_fp8_prep_kernel<true><<<pgrid, 256, 0, stream>>>(q16, k16, v16, a.signs, a.q8, a.k8, a.qexp, a.kexp,
-                                                             a.vblk_max, a.N);
+        fa_fp8_prep_kernel<true><<<pgrid, 256, kPrepSmem, stream>>>(q16, k16, v16, a.signs, a.q8, a.k8, a.qexp,
+                                                                     a.kexp, a.vblk_max, a.N, BH, a.status);
     else
-        fa_fp8_prep_kernel<false><<<pgrid, 256, 0, stream>>>(q16, k16, v16, nullptr, a.q8, a.k8, a.qexp, a.kexp,
-                                                              a.vblk_max, a.N);
+        fa_fp8_prep_kernel<false><<<pgrid, 256, kPrepSmem, stream>>>(q16, k16, v16, nullptr, a.q8, a.k8, a.qexp,
+                                                                      a.kexp, a.vblk_max, a.N, BH, a.status);
     fa_fp8_v_kernel<<<dim3(T, BH), 256, 0, stream>>>(v16, a.vblk_max, a.vt8, a.vexp, a.N);
     cudaError_t e;
     CUtensorMap tq, tk, tv, to;
