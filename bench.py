@@ -591,7 +591,7 @@ def run_decode(args, rank, world):
                          max(3, min(args.steps, 50)), cache_bytes, "GB/s", 1e9)
         e2e["note"] = "the cache stays resident in HBM; q in, o and lse out per step"
     cpu = None
-    if not args.no_cpu_baseline and rank == 0:
+    if not args.no_cpu_baseline and rank == 0 and world == 1:
         from oracle import decode as DEC
         # two requests of the workload's shape and length range, decoded
         # repeatedly until about 10 s of CPU time is spent
@@ -687,7 +687,7 @@ def run_packed(args, rank, world):
         e2e = e2e_simple(hin, din, hout, dout, compute, max(3, min(args.steps, 20)), fwd_flop + bwd_flop,
                          "TFLOP/s")
     cpu = None
-    if not args.no_cpu_baseline and rank == 0:
+    if not args.no_cpu_baseline and rank == 0 and world == 1:
         from oracle import varlen as VL
         xs = W.make_packed_workload(w, seed=0)
         cuh = xs.cu_seqlens.tolist()
@@ -775,7 +775,7 @@ def run_fp8(args, rank, world):
                                                 lse=lse, ws=ws),
                          max(3, min(args.steps, 20)), fwd_flop, "TFLOP/s")
     cpu = None
-    if not args.no_cpu_baseline and rank == 0:
+    if not args.no_cpu_baseline and rank == 0 and world == 1:
         from oracle import fp8 as F8
         xs = W.make_inputs(w, seed=0)
         s_cpu = W.make_signs(w.d, seed=0).numpy()
@@ -869,7 +869,7 @@ def run_dropout(args, rank, world, p_drop: float = 0.1):
         e2e = e2e_simple(hin, din, hout, dout, compute, max(3, min(args.steps, 20)), fwd_flop + bwd_flop,
                          "TFLOP/s")
     cpu = None
-    if not args.no_cpu_baseline and rank == 0:
+    if not args.no_cpu_baseline and rank == 0 and world == 1:
         from oracle import dropout as DR
         from oracle.attention import visible
         import numpy as np
