@@ -919,6 +919,9 @@ static cudaError_t launch_fwd_t(const FwdArgs& a, cudaStream_t stream, int* nlau
 
 cudaError_t launch_fwd(const FwdArgs& a, cudaStream_t stream, int* nlaunch) {
     if (!a.fp32 && a.blockmask && a.causal) return launch_fwd_bf16_q1(a, stream, nlaunch);
+    // tile-masked calls without a causal mask: one query tile per CTA, two
+    // CTAs per SM (fa_fwd_t1.cu)
+    if (!a.fp32 && a.blockmask && !a.cu_seqlens && !a.dropout) return launch_fwd_bf16_t1(a, stream, nlaunch);
     if (a.fp32) {
         if (a.d == 64) return launch_fwd_t<true, 64>(a, stream, nlaunch);
         return cudaErrorInvalidValue;  // fp32 d=128 exceeds the shared-memory budget of this kernel

@@ -29,6 +29,13 @@ for d in (64, 128):
 SWEEP.append(W.Workload("causal-kvlen-sparse-768-128", 2, 2, 768, 128, causal=True, kv_len_range=(200, 700),
                         block_density=0.5))
 SWEEP.append(W.Workload("wide-scores-512-128", 1, 2, 512, 128, causal=True, k_scale=4.0))
+# tile masks without a causal mask run the one-query-tile kernel: ragged key
+# padding inside visible tiles, rows that see most tiles (its K and V rings
+# wrap several times), and a rescale of O (K x 4 widens the scores)
+for d in (64, 128):
+    SWEEP.append(W.Workload(f"sparse-kvlen-640-{d}", 3, 2, 640, d, kv_len_range=(100, 600), block_density=0.5))
+    SWEEP.append(W.Workload(f"sparse-dense-1024-{d}", 1, 2, 1024, d, block_density=0.9))
+SWEEP.append(W.Workload("wide-scores-sparse-1024-128", 1, 2, 1024, 128, k_scale=4.0, block_density=0.6))
 
 
 @pytest.mark.parametrize("w", SWEEP, ids=lambda w: w.name)

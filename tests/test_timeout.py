@@ -59,6 +59,13 @@ def test_bounded_waits_report_timeout(dbg, cuda_device):
     assert dbg.fa_get_status(ptr(ws), s) == fb.FA_ERR_TIMEOUT
     assert dbg.fa_get_status(ptr(ws), s) == fb.FA_OK  # reading clears the word
 
+    # the tile-masked forward without a causal mask (one query tile per CTA)
+    bm = torch.ones(N // 128, N // 128, dtype=torch.uint8, device=cuda_device)
+    rc = dbg.fa_fwd(ptr(q), ptr(k), ptr(v), ptr(o), ptr(lse), B, H, N, d, scale, 0, ptr(bm), None, fb.FA_BF16,
+                    ptr(ws), ws.numel(), s)
+    assert rc == fb.FA_OK
+    assert dbg.fa_get_status(ptr(ws), s) == fb.FA_ERR_TIMEOUT
+
     rc = dbg.fa_bwd(ptr(q), ptr(k), ptr(v), ptr(o), ptr(lse), ptr(do), ptr(dq), ptr(dk), ptr(dv), B, H, N, d,
                     scale, 1, None, None, fb.FA_BF16, ptr(ws), ws.numel(), s)
     assert rc == fb.FA_OK
