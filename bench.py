@@ -200,7 +200,7 @@ KERNEL_SOURCES = {
     "fa_fwd_kernel": ["fa_fwd.cu"],
     "fa_fwd_fp8_kernel": ["fa_fwd_fp8.cu", "fa_fp8.h"],
     "fa_bwd_kernel": ["fa_bwd.cu"],
-    "fa_fwd_q1_kernel": ["fa_fwd_q1.cu"],
+    "fa_fwd_t1_kernel": ["fa_fwd_t1.cu"],
     "fa_decode_split_kernel": ["fa_decode.cu", "fa_decode.h"],
 }
 SHARED_HEADERS = ["fa_common.cuh", "fa_launch.h", "sm103_ptx.cuh", "tmap.h"]
@@ -1125,7 +1125,8 @@ def main():
 
     fwd_tf = fwd_flop / (fwd_ms * 1e-3) / 1e12
     bwd_tf = bwd_flop / (bwd_ms * 1e-3) / 1e12
-    dominant = "fa_bwd_kernel" if bwd_ms >= fwd_ms else "fa_fwd_kernel"
+    # bf16 [B, H, N, d] forwards without dropout run fa_fwd_t1_kernel
+    dominant = "fa_bwd_kernel" if bwd_ms >= fwd_ms else "fa_fwd_t1_kernel"
     dom_tf = bwd_tf if dominant == "fa_bwd_kernel" else fwd_tf
     roofline = {"bound": "tensor", "achieved": dom_tf, "peak": peak, "unit": "TFLOP/s", "frac": dom_tf / peak,
                 "traffic": recorded_traffic(dominant, args.workload), "kernel": dominant,

@@ -18,7 +18,7 @@ CSRC = os.path.join(PKG, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 BUILD_DIR = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libfa.so")
-SOURCES = ["fa_api.cu", "fa_fwd.cu", "fa_fwd_q1.cu", "fa_fwd_t1.cu", "fa_bwd.cu", "fa_noalloc.cu", "fa_decode.cu", "fa_fwd_fp8.cu"]
+SOURCES = ["fa_api.cu", "fa_fwd.cu", "fa_fwd_t1.cu", "fa_bwd.cu", "fa_noalloc.cu", "fa_decode.cu", "fa_fwd_fp8.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "-I" + INCLUDE, "-I" + CSRC]
 

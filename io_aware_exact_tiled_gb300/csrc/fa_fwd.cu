@@ -11,6 +11,10 @@
 // ("FlashAttention-2": tiles above the diagonal are skipped; "Counting the
 // IO": block-sparse attention skips masked tiles).
 //
+// This file's kernel serves fp32 inputs, packed variable-length batches and
+// dropout; bf16 [B, H, N, d] calls without dropout run fa_fwd_t1.cu (one query
+// tile per CTA, two CTAs per SM), which is faster on every measured shape.
+//
 // GB300 design (one CTA per pair of 128-row query tiles of one head):
 //   thread 0    sets up the mbarriers and requests both Q tiles and the first
 //               K / V tile before the CTA-wide barrier
@@ -18,7 +22,7 @@
 //               multi-stage shared-memory rings guarded by mbarriers
 //   warp 1      allocates TMEM; the whole warp runs the issue loop and one
 //               elected lane issues every tcgen05.mma and commit
-//   warps 2-3   tile-masked kernel only: turn the mask rows into bitmaps
+//   warps 2-3   idle after the set-up
 //   warps 4-7   softmax warpgroup of Q tile 0 (thread r owns row r, which is
 //               TMEM lane r, so row max and row sum are in-thread)
 //   warps 8-11  softmax warpgroup of Q tile 1
@@ -43,11 +47,6 @@
 
 namespace fa {
 
-// Key tiles per sequence up to which a tile-masked CTA keeps its visible
-// tiles as bitmaps in shared memory (N <= 524,288); longer sequences read the
-// tile mask in global memory tile by tile.
-constexpr int kVisMaxTiles = 4096;
-
 template <bool TF32, int D>
 struct FwdCfg {
     static constexpr int ELEM = TF32 ? 4 : 2;
@@ -66,10 +65,7 @@ struct FwdCfg {
     static constexpr int K_OFF = Q_OFF + NQ * SPLIT * TILE_BYTES;
     static constexpr int V_OFF = K_OFF + KSTAGES * SPLIT * TILE_BYTES;
     static constexpr int BAR_OFF = V_OFF + VSTAGES * TILE_BYTES;
-    // visible-tile bitmaps of the two Q tiles (tile-masked calls)
-    static constexpr int VIS_OFF = BAR_OFF + 512;
-    static constexpr int VIS_WORDS = kVisMaxTiles / 32;
-    static constexpr int SMEM = VIS_OFF + 2 * VIS_WORDS * 4 + 1024;  // + alignment slack
+    static constexpr int SMEM = BAR_OFF + 512 + 1024;  // + alignment slack
     static constexpr int KSTEP = 32 / ELEM;            // K elements per MMA instruction
     static constexpr int S_KSTEPS = D / KSTEP;
     static constexpr int PV_KSTEPS = kTile / KSTEP;
@@ -164,9 +160,7 @@ constexpr float kLn2 = 0.69314718055994530942f;
 // so that the [B, H, N, d] kernels carry none of its branches.
 // DROPOUT: dropout on the probabilities, with the keep mask regenerated from
 // Philox (fa_philox.cuh); a separate instantiation as well.
-// TMASK: calls with a tile mask (bf16, [B, H, N, d]); the visible-tile
-// bitmaps and the jumps over masked tiles live only in this instantiation.
-template <bool TF32, int D, bool VARLEN, bool DROPOUT = false, bool TMASK = false>
+template <bool TF32, int D, bool VARLEN, bool DROPOUT = false>
 __global__ void __launch_bounds__(384, 1)
     fa_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                   const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmQlo,
@@ -192,11 +186,10 @@ __global__ void __launch_bounds__(384, 1)
     uint64_t* p_full = s_full + 2;            // [2]
     uint64_t* o_done = p_full + 2;            // [2]
     uint64_t* drain = o_done + 2;
-    // P V runs in slices of the keys (four in the plain d = 128 kernel; two
-    // in the others: in the tile-masked and d = 64 kernels the softmax warps
-    // stall more on the extra TMEM-store waits than the earlier slices gain):
+    // P V runs in two slices of the keys (more slices cost the softmax warps
+    // more in TMEM-store waits than the earlier slices gain):
     // p_half[s][k] = P of slices 0..k stored
-    constexpr int PV_PARTS = (!TMASK && !VARLEN && !DROPOUT && !TF32 && D == 128) ? 4 : 2;
+    constexpr int PV_PARTS = 2;
     uint64_t* p_half = drain + 1;             // [2][3]
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(p_half + 6);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
@@ -210,9 +203,9 @@ __global__ void __launch_bounds__(384, 1)
     // its K and V stay in L2 (across all heads the resident CTAs' K and V
     // tiles would span every head and part of them would be read again).
     // Without causal masking every pair of a head costs about the same, and
-    // a tile mask makes the pairs share few key tiles, so the grid is then
-    // head-major instead: the CTAs running together read one head's K and V,
-    // which stays in L2.
+    // a tile mask (here: fp32 inputs) makes the pairs share few key tiles,
+    // so the grid is then head-major instead: the CTAs running together read
+    // one head's K and V, which stays in L2.
     int h = p.head_major ? blockIdx.y : blockIdx.x, b = p.head_major ? blockIdx.z : blockIdx.y;
     int zq = static_cast<int>(p.head_major ? blockIdx.x : blockIdx.z);  // pair rank, longest first
     if (!VARLEN && p.group > 0)
@@ -306,8 +299,8 @@ __global__ void __launch_bounds__(384, 1)
                     tma_load_2d(dq + C::TILE_BYTES, &tmQlo, r * C::BOXC, bh * N + (qb0 + s) * kTile, bar_q);
             }
         // ... and so are the first needed tile's K and V (the rings start
-        // empty; tile-masked kernels find that tile in their bitmaps later)
-        if constexpr (!TMASK) {
+        // empty)
+        {
             int t0 = 0;
             while (t0 < hi && !tile_visible(p.mask, qb0, t0, kvalid) && !(act1 && tile_visible(p.mask, qb1, t0, kvalid)))
                 ++t0;
@@ -331,27 +324,7 @@ __global__ void __launch_bounds__(384, 1)
         tmem_alloc(tmem_slot, 512);
         tmem_relinquish();
     }
-    // With a tile mask, finding the next visible tile by reading the mask in
-    // global memory one tile at a time costs a dependent load per skipped
-    // tile on the issue paths; warps 2 and 3 (otherwise idle) first turn the
-    // two Q tiles' mask rows into bitmaps (bit t of Q tile s: tile t visible),
-    // and every role then jumps to the next visible tile with a find-first-set.
     const MaskArgs mk = p.mask;
-    constexpr bool kVis = TMASK && !TF32 && !VARLEN && !DROPOUT;
-    const bool use_vis = kVis && mk.blockmask != nullptr && hi <= kVisMaxTiles;
-    uint32_t* vis = reinterpret_cast<uint32_t*>(sm + C::VIS_OFF);  // [2][VIS_WORDS]
-    if (use_vis && (warp == 2 || warp == 3)) {
-        const int s = warp - 2;
-        const int qb = s == 0 ? qb0 : qb1;
-        const bool on = s == 0 || act1;
-        const int nw = (hi + 31) >> 5;
-#pragma unroll 4
-        for (int w = 0; w < nw; ++w) {
-            const int t = w * 32 + lane;
-            const uint32_t word = __ballot_sync(0xffffffffu, on && t < hi && tile_visible(mk, qb, t, kvalid));
-            if (lane == 0) vis[s * C::VIS_WORDS + w] = word;
-        }
-    }
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
@@ -361,31 +334,9 @@ __global__ void __launch_bounds__(384, 1)
     // (captured by value: a by-reference capture would give these variables
     // addresses and move them to local memory)
     auto need_of = [=](int t) -> uint32_t {
-        if (kVis && use_vis)
-            return ((vis[t >> 5] >> (t & 31)) & 1u) | (((vis[C::VIS_WORDS + (t >> 5)] >> (t & 31)) & 1u) << 1);
         uint32_t nd = tile_visible(mk, qb0, t, kvalid) ? 1u : 0u;
         if (act1 && tile_visible(mk, qb1, t, kvalid)) nd |= 2u;
         return nd;
-    };
-    // The roles walk the tiles as "for t from next_tile(0) on, skipping tiles
-    // whose need bits are clear": next_tile(t, sides) is t itself except in
-    // the tile-masked kernel, where it jumps to the first tile >= t that a Q
-    // tile in sides (bit s = Q tile s) needs, or to hi.
-    auto next_tile = [=](int t, uint32_t sides) -> int {
-        if constexpr (kVis) {
-            if (use_vis) {
-                while (t < hi) {
-                    uint32_t w = 0;
-                    if (sides & 1u) w |= vis[t >> 5];
-                    if (sides & 2u) w |= vis[C::VIS_WORDS + (t >> 5)];
-                    w >>= (t & 31);
-                    if (w) return t + __ffs(w) - 1;
-                    t = (t | 31) + 1;
-                }
-                return hi;
-            }
-        }
-        return t;
     };
 
     if (warp == 0) {
@@ -394,7 +345,7 @@ __global__ void __launch_bounds__(384, 1)
             // K and V tiles whose loads were issued (the first one possibly
             // by the set-up code above)
             int nk = t_early >= 0 ? 1 : 0, nv = nk;
-            for (int t = next_tile(t_early + 1, 3u); t < hi; t = next_tile(t + 1, 3u)) {
+            for (int t = t_early + 1; t < hi; ++t) {
                 if (!need_of(t)) continue;
                 const int kst = nk % C::KSTAGES;
                 if (!mbar_wait(&k_empty[kst], ((nk / C::KSTAGES) & 1) ^ 1, cx, 1)) break;
@@ -436,7 +387,7 @@ __global__ void __launch_bounds__(384, 1)
             uint32_t& rem = st.rem;
 
             int u = 0;
-            for (int t = next_tile(0, 3u); ok && t < hi; t = next_tile(t + 1, 3u)) {
+            for (int t = 0; ok && t < hi; ++t) {
                 const uint32_t nd = need_of(t);
                 if (!nd) continue;
                 const int kst = u % C::KSTAGES;
@@ -511,7 +462,7 @@ __global__ void __launch_bounds__(384, 1)
         int n = 0;
         bool ok = true;
         if (active) {
-            for (int t = next_tile(0, 1u << s); t < hi; t = next_tile(t + 1, 1u << s)) {
+            for (int t = 0; t < hi; ++t) {
                 const uint32_t nd = need_of(t);
                 if (!(nd & (1u << s))) continue;
                 ok = mbar_wait(&s_full[s], n & 1, cx, 6);
@@ -858,19 +809,22 @@ static cudaError_t launch_fwd_t(const FwdArgs& a, cudaStream_t stream, int* nlau
         tkl = tk;
     }
     if constexpr (TF32) to = tq;  // unused: fp32 O is stored directly
+    // bf16 calls reach this kernel only packed or with dropout; the others
+    // run fa_fwd_t1.cu
+    if (!TF32 && !a.cu_seqlens && !a.dropout) return cudaErrorInvalidValue;
     static bool attr_set = false;
     if (!attr_set) {
-        cudaError_t e = cudaFuncSetAttribute(fa_fwd_kernel<TF32, D, false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             C::SMEM);
-        if (e == cudaSuccess && !TF32)
-            e = cudaFuncSetAttribute(fa_fwd_kernel<TF32, D, !TF32>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+        cudaError_t e;
+        if constexpr (TF32) {
+            e = cudaFuncSetAttribute(fa_fwd_kernel<true, D, false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                      C::SMEM);
-        if (e == cudaSuccess && !TF32)
-            e = cudaFuncSetAttribute(fa_fwd_kernel<TF32, D, false, !TF32>,
-                                     cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
-        if (e == cudaSuccess && !TF32)
-            e = cudaFuncSetAttribute(fa_fwd_kernel<TF32, D, false, false, !TF32>,
-                                     cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
+        } else {
+            e = cudaFuncSetAttribute(fa_fwd_kernel<false, D, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                     C::SMEM);
+            if (e == cudaSuccess)
+                e = cudaFuncSetAttribute(fa_fwd_kernel<false, D, false, true>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
+        }
         if (e != cudaSuccess) return e;
         attr_set = true;
     }
@@ -903,14 +857,12 @@ static cudaError_t launch_fwd_t(const FwdArgs& a, cudaStream_t stream, int* nlau
                                      : dim3(a.H, a.B, (T + 1) / 2);
     if (a.ev_begin) cudaEventRecord(a.ev_begin, stream);
     p.drop = a.drop;
-    if (p.cu_seqlens)
-        fa_fwd_kernel<TF32, D, !TF32><<<grid, C::THREADS, C::SMEM, stream>>>(tq, tk, tv, tql, tkl, to, p);
-    else if (a.dropout && !TF32)
-        fa_fwd_kernel<TF32, D, false, !TF32><<<grid, C::THREADS, C::SMEM, stream>>>(tq, tk, tv, tql, tkl, to, p);
-    else if (a.blockmask && !TF32)
-        fa_fwd_kernel<TF32, D, false, false, !TF32><<<grid, C::THREADS, C::SMEM, stream>>>(tq, tk, tv, tql, tkl, to, p);
+    if constexpr (TF32)
+        fa_fwd_kernel<true, D, false><<<grid, C::THREADS, C::SMEM, stream>>>(tq, tk, tv, tql, tkl, to, p);
+    else if (p.cu_seqlens)
+        fa_fwd_kernel<false, D, true><<<grid, C::THREADS, C::SMEM, stream>>>(tq, tk, tv, tql, tkl, to, p);
     else
-        fa_fwd_kernel<TF32, D, false><<<grid, C::THREADS, C::SMEM, stream>>>(tq, tk, tv, tql, tkl, to, p);
+        fa_fwd_kernel<false, D, false, true><<<grid, C::THREADS, C::SMEM, stream>>>(tq, tk, tv, tql, tkl, to, p);
     if (a.ev_end) cudaEventRecord(a.ev_end, stream);
     ++launches;
     *nlaunch = launches;
@@ -918,10 +870,10 @@ static cudaError_t launch_fwd_t(const FwdArgs& a, cudaStream_t stream, int* nlau
 }
 
 cudaError_t launch_fwd(const FwdArgs& a, cudaStream_t stream, int* nlaunch) {
-    if (!a.fp32 && a.blockmask && a.causal) return launch_fwd_bf16_q1(a, stream, nlaunch);
-    // tile-masked calls without a causal mask: one query tile per CTA, two
-    // CTAs per SM (fa_fwd_t1.cu)
-    if (!a.fp32 && a.blockmask && !a.cu_seqlens && !a.dropout) return launch_fwd_bf16_t1(a, stream, nlaunch);
+    // bf16 [B, H, N, d] calls without dropout: one query tile per CTA, two
+    // CTAs per SM (fa_fwd_t1.cu); this file's pair kernel serves fp32 inputs,
+    // packed batches and dropout
+    if (!a.fp32 && !a.cu_seqlens && !a.dropout) return launch_fwd_bf16_t1(a, stream, nlaunch);
     if (a.fp32) {
         if (a.d == 64) return launch_fwd_t<true, 64>(a, stream, nlaunch);
         return cudaErrorInvalidValue;  // fp32 d=128 exceeds the shared-memory budget of this kernel

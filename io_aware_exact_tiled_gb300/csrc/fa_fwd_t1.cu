@@ -1,5 +1,5 @@
-// Forward pass for tile-masked bf16 calls without a causal mask: one 128-row
-// query tile per CTA and two CTAs per SM.
+// Forward pass for bf16 [B, H, N, d] calls: one 128-row query tile per CTA
+// and two CTAs per SM.
 //
 // Same computation as fa_fwd.cu ("FlashAttention: making attention
 // IO-aware", sections "Tiling: never materialise S" and "Online softmax";
@@ -10,13 +10,16 @@
 // output o (rescaled by exp(m_old - m_new) when the maximum grows), and write
 // O = o / l and L = m + log l at the end.
 //
-// Why a separate kernel: a random tile mask leaves two query tiles few key
-// tiles in common, so in the pair kernel most key tiles feed one query tile,
-// and its single in-order MMA issuer then waits on that tile's chain
-// (S -> softmax -> P V -> next S). Here each CTA owns one query tile with its
+// Why one query tile per CTA: in a CTA that holds two query tiles, one
+// in-order MMA issuer serves both, and a key tile that only one of them needs
+// (the usual case under a random tile mask) waits on that tile's chain
+// S -> softmax -> P V -> next S. Here each CTA owns one query tile with its
 // own producer, issuer and softmax warps, and two CTAs share an SM (256 TMEM
 // columns and under half of the shared memory each): while one CTA's softmax
-// forms P, the other's GEMMs run, and no issue order ties them together.
+// forms P, the other's GEMMs run, and no issue order ties them together. The
+// price is that each K and V tile is loaded once per query tile instead of
+// once per pair: twice the L2-to-shared-memory traffic, well within what TMA
+// sustains from L2.
 //
 // Layout of one CTA (192 threads):
 //   thread 0    sets up the mbarriers and requests Q and the first K / V
@@ -77,6 +80,7 @@ struct T1Params {
     void* o;
     float* lse;
     int* status;
+    int group;  // > 0 (causal): 1D grid of head groups, longest query tile first in each
 };
 
 constexpr float kT1RescaleThreshold = 8.0f;  // log2 units
@@ -112,13 +116,27 @@ __global__ void __launch_bounds__(192, 2)
     volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
     const WaitCtx cx{abort_flag, p.status};
 
+    // Without a causal mask every query tile of a head costs about the same:
     // query tile fastest, so that the CTAs running together read the K and V
-    // of one or two heads, which stay in L2
-    const int qb = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
+    // of one or two heads, which stay in L2. With a causal mask query tile qb
+    // reads qb + 1 key tiles: a 1D grid runs groups of p.group heads in turn
+    // (sized so that a group's K and V stay in L2), longest tile first across
+    // the heads of a group, so that the kernel ends on short CTAs.
+    int qb = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
     const int N = p.N, T = p.mask.T;
+    if (p.group > 0) {
+        const int nb = p.B * p.H, L = static_cast<int>(blockIdx.x);
+        const int gi = L / (p.group * T), rr = L - gi * p.group * T;
+        const int g0 = gi * p.group, gsz = min(p.group, nb - g0);
+        const int zq = rr / gsz, bhx = g0 + (rr - zq * gsz);
+        qb = T - 1 - zq;
+        b = bhx / p.H;
+        h = bhx - b * p.H;
+    }
     const int bh = b * p.H + h;
     const int kvalid = keys_valid(p.mask, b, N);
-    const int hi = min(T, (kvalid + kTile - 1) / kTile);
+    int hi = min(T, (kvalid + kTile - 1) / kTile);
+    if (p.mask.causal) hi = min(hi, qb + 1);
     const MaskArgs mk = p.mask;
     const bool use_vis = mk.blockmask != nullptr && hi <= kT1VisMaxTiles;
     uint32_t* vis = reinterpret_cast<uint32_t*>(sm + C::VIS_OFF);
@@ -306,7 +324,7 @@ __global__ void __launch_bounds__(192, 2)
 #pragma unroll
             for (int c = 0; c < 4; ++c) tmem_ld_wait(sr[c]);
             if (tile_partial(mk, qb, t, kvalid)) {
-                const int lim = kvalid - t * kTile;  // no causal mask in this kernel
+                const int lim = min(kvalid - t * kTile, mk.causal && t == qb ? r + 1 : kTile);
 #pragma unroll
                 for (int c = 0; c < 4; ++c)
 #pragma unroll
@@ -500,12 +518,19 @@ static cudaError_t launch_t1(const FwdArgs& a, cudaStream_t stream, int* nlaunch
     p.scale_log2 = a.scale * 1.4426950408889634f;
     p.mask.blockmask = a.blockmask;
     p.mask.kv_len = a.kv_len;
-    p.mask.causal = 0;
+    p.mask.causal = a.causal;
     p.mask.T = a.N / kTile;
     p.o = a.o;
     p.lse = a.lse;
     p.status = a.status;
-    const dim3 grid(a.N / kTile, a.H, a.B);
+    // causal calls: head groups whose K and V take at most 64 MiB
+    p.group = 0;
+    if (a.causal) {
+        long long g = (64LL << 20) / (4LL * a.N * D);
+        g = g < 1 ? 1 : g;
+        p.group = static_cast<int>(g < a.B * a.H ? g : a.B * a.H);
+    }
+    const dim3 grid = p.group > 0 ? dim3(static_cast<unsigned>(a.N / kTile) * a.H * a.B) : dim3(a.N / kTile, a.H, a.B);
     if (a.ev_begin) cudaEventRecord(a.ev_begin, stream);
     fa_fwd_t1_kernel<D><<<grid, C::THREADS, C::SMEM, stream>>>(tq, tk, tvh, to, p);
     if (a.ev_end) cudaEventRecord(a.ev_end, stream);

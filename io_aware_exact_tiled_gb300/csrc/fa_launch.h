@@ -60,7 +60,6 @@ struct BwdArgs {
 };
 
 cudaError_t launch_fwd(const FwdArgs& a, cudaStream_t stream, int* nlaunch);
-cudaError_t launch_fwd_bf16_q1(const FwdArgs& a, cudaStream_t stream, int* nlaunch);
 cudaError_t launch_fwd_bf16_t1(const FwdArgs& a, cudaStream_t stream, int* nlaunch);
 cudaError_t launch_bwd(const BwdArgs& a, cudaStream_t stream, int* nlaunch);
 

@@ -29,9 +29,9 @@ for d in (64, 128):
 SWEEP.append(W.Workload("causal-kvlen-sparse-768-128", 2, 2, 768, 128, causal=True, kv_len_range=(200, 700),
                         block_density=0.5))
 SWEEP.append(W.Workload("wide-scores-512-128", 1, 2, 512, 128, causal=True, k_scale=4.0))
-# tile masks without a causal mask run the one-query-tile kernel: ragged key
-# padding inside visible tiles, rows that see most tiles (its K and V rings
-# wrap several times), and a rescale of O (K x 4 widens the scores)
+# tile masks: ragged key padding inside visible tiles, rows that see most
+# tiles (the K and V rings wrap several times), and a rescale of O (K x 4
+# widens the scores)
 for d in (64, 128):
     SWEEP.append(W.Workload(f"sparse-kvlen-640-{d}", 3, 2, 640, d, kv_len_range=(100, 600), block_density=0.5))
     SWEEP.append(W.Workload(f"sparse-dense-1024-{d}", 1, 2, 1024, d, block_density=0.9))
@@ -179,10 +179,10 @@ def test_causal_head_groups_with_a_partial_last_group(cuda_device):
     check(errors(x, g, heads=[(0, 0), (0, 20), (0, 35)]))
 
 
-def test_causal_tile_mask_longer_than_the_one_tile_bitmap(cuda_device):
-    """Causal tile-masked forwards run one query tile per CTA, which keeps its
-    mask row as a 1,024-tile bitmap at d = 128; 1,025 tiles take the per-tile
-    mask reads. Sampled query tiles against the oracle."""
+def test_causal_tile_mask_long_rows(cuda_device):
+    """A causal tile mask over 1,025 key tiles: long bitmap rows cut at the
+    diagonal, and causal calls run their query tiles longest first in head
+    groups. Sampled query tiles against the oracle."""
     T = 1025
     N = T * 128
     w = W.Workload("causal-sparse-long", 1, 1, N, 128, causal=True, backward=False)

@@ -31,6 +31,8 @@ def dbg():
     lib.fa_get_status.restype = i
     lib.fa_bwd_workspace_size.argtypes = [i, i, i, i]
     lib.fa_bwd_workspace_size.restype = sz
+    lib.fa_fwd_dropout.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, f, i, vp, f, ctypes.c_ulonglong, vp, sz, vp]
+    lib.fa_fwd_dropout.restype = i
     lib.fa_bwd_noalloc.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, i, i, i, i, f, i, vp, vp, i, vp]
     lib.fa_bwd_noalloc.restype = i
     lib.fa_bwd_noalloc_get_status.argtypes = [vp]
@@ -59,7 +61,13 @@ def test_bounded_waits_report_timeout(dbg, cuda_device):
     assert dbg.fa_get_status(ptr(ws), s) == fb.FA_ERR_TIMEOUT
     assert dbg.fa_get_status(ptr(ws), s) == fb.FA_OK  # reading clears the word
 
-    # the tile-masked forward without a causal mask (one query tile per CTA)
+    # the pair-tile forward kernel (it serves dropout, packed batches and fp32)
+    rc = dbg.fa_fwd_dropout(ptr(q), ptr(k), ptr(v), ptr(o), ptr(lse), B, H, N, d, scale, 1, None, 0.1, 1234,
+                            ptr(ws), ws.numel(), s)
+    assert rc == fb.FA_OK
+    assert dbg.fa_get_status(ptr(ws), s) == fb.FA_ERR_TIMEOUT
+
+    # a tile-masked forward
     bm = torch.ones(N // 128, N // 128, dtype=torch.uint8, device=cuda_device)
     rc = dbg.fa_fwd(ptr(q), ptr(k), ptr(v), ptr(o), ptr(lse), B, H, N, d, scale, 0, ptr(bm), None, fb.FA_BF16,
                     ptr(ws), ws.numel(), s)
