@@ -11,9 +11,9 @@
 // ("FlashAttention-2": tiles above the diagonal are skipped; "Counting the
 // IO": block-sparse attention skips masked tiles).
 //
-// This file's kernel serves fp32 inputs, packed variable-length batches and
-// dropout; bf16 [B, H, N, d] calls without dropout run fa_fwd_t1.cu (one query
-// tile per CTA, two CTAs per SM), which is faster on every measured shape.
+// This file's kernel serves fp32 inputs and dropout; bf16 calls without
+// dropout ([B, H, N, d] or packed) run fa_fwd_t1.cu (one query tile per CTA,
+// two CTAs per SM), which is faster on every measured shape.
 //
 // GB300 design (one CTA per pair of 128-row query tiles of one head):
 //   thread 0    sets up the mbarriers and requests both Q tiles and the first
@@ -87,8 +87,6 @@ struct FwdParams {
     void* o;
     float* lse;
     int* status;
-    const int32_t* cu_seqlens;  // packed variable-length batch (bf16), else null
-    int total;                  // tokens of the packed batch
     DropoutArgs drop;           // dropout on the probabilities (DROPOUT kernels)
     int head_major;             // grid (pairs, H, B) instead of (H, B, pairs)
     int group;                  // > 0: 1D grid of head groups (heads per group), longest pair first in each
@@ -156,11 +154,9 @@ __device__ __forceinline__ bool fwd_issue_pv(uint32_t leader, int s, MmaState& s
 constexpr float kRescaleThreshold = 8.0f;  // log2 units
 constexpr float kLn2 = 0.69314718055994530942f;
 
-// VARLEN: packed variable-length batch (bf16 only); a separate instantiation
-// so that the [B, H, N, d] kernels carry none of its branches.
 // DROPOUT: dropout on the probabilities, with the keep mask regenerated from
-// Philox (fa_philox.cuh); a separate instantiation as well.
-template <bool TF32, int D, bool VARLEN, bool DROPOUT = false>
+// Philox (fa_philox.cuh); a separate instantiation.
+template <bool TF32, int D, bool DROPOUT = false>
 __global__ void __launch_bounds__(384, 1)
     fa_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                   const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmQlo,
@@ -208,23 +204,10 @@ __global__ void __launch_bounds__(384, 1)
     // one head's K and V, which stays in L2.
     int h = p.head_major ? blockIdx.y : blockIdx.x, b = p.head_major ? blockIdx.z : blockIdx.y;
     int zq = static_cast<int>(p.head_major ? blockIdx.x : blockIdx.z);  // pair rank, longest first
-    if (!VARLEN && p.group > 0)
+    if (p.group > 0)
         fwd_group_item(static_cast<int>(blockIdx.x), p.group, (p.mask.T + 1) >> 1, p.B * p.H, p.H, b, h, zq);
-    // A packed variable-length batch puts sequence b at tokens seq0 ..
-    // seq0 + N - 1 of [total, H, d] tensors (the grid covers the longest
-    // sequence; CTAs past the end of a shorter one leave at once). Otherwise
-    // head (b, h) is rows bh * N .. of the [B * H * N, d] view.
-    constexpr bool varlen = VARLEN && !TF32;
-    int N = p.N, T = p.mask.T, seq0 = 0;
-    if (varlen) {
-        const int s0 = min(max(p.cu_seqlens[b], 0), p.total);
-        const int s1 = min(max(p.cu_seqlens[b + 1], s0), p.total);
-        if (s1 - s0 > p.N && tid == 0 && blockIdx.x == 0 && blockIdx.z == 0 && p.status)
-            atomicCAS(p.status, 0, FA_DEV_INVALID | (97 << 8));
-        seq0 = s0;
-        N = min(s1 - s0, p.N);
-        T = (N + kTile - 1) / kTile;
-    }
+    // head (b, h) is rows bh * N .. of the [B * H * N, d] view
+    const int N = p.N, T = p.mask.T;
     const int npairs = (T + 1) >> 1;
     const int qp = npairs - 1 - zq;
     if (qp < 0) return;  // uniform over the CTA, before any barrier or TMEM use
@@ -237,12 +220,9 @@ __global__ void __launch_bounds__(384, 1)
     hi = min(hi, (kvalid + kTile - 1) / kTile);
 
     // K and V tile loads (producer thread): rows t * 128 .. of this head
-    // (packed: of this sequence) into K stage kst / V stage vst
+    // into K stage kst / V stage vst
     auto load_rows = [&](void* dst, const CUtensorMap* m, int x, int row, uint64_t* bar) {
-        if (varlen)
-            tma_load_3d(dst, m, x, h, seq0 + row, bar);
-        else
-            tma_load_2d(dst, m, x, bh * N + row, bar);
+        tma_load_2d(dst, m, x, bh * N + row, bar);
     };
     auto load_k = [&](int t, int kst) {
         uint8_t* sk = sm + C::K_OFF + kst * C::SPLIT * C::TILE_BYTES;
@@ -291,10 +271,7 @@ __global__ void __launch_bounds__(384, 1)
         for (int s = 0; s < (act1 ? 2 : 1); ++s)
             for (int r = 0; r < C::NREG; ++r) {
                 uint8_t* dq = sm + C::Q_OFF + s * C::SPLIT * C::TILE_BYTES + r * 16384;
-                if (varlen)
-                    tma_load_3d(dq, &tmQ, r * C::BOXC, h, seq0 + (qb0 + s) * kTile, bar_q);
-                else
-                    tma_load_2d(dq, &tmQ, r * C::BOXC, bh * N + (qb0 + s) * kTile, bar_q);
+                tma_load_2d(dq, &tmQ, r * C::BOXC, bh * N + (qb0 + s) * kTile, bar_q);
                 if constexpr (TF32)
                     tma_load_2d(dq + C::TILE_BYTES, &tmQlo, r * C::BOXC, bh * N + (qb0 + s) * kTile, bar_q);
             }
@@ -645,21 +622,15 @@ __global__ void __launch_bounds__(384, 1)
             if (ok) {
                 float inv = lw > 0.f ? 1.f / lw : 0.f;
                 if constexpr (DROPOUT) inv *= p.drop.inv_keep;
-                // packed rows past the end of the sequence belong to the next
-                // one: computed (the TMEM loads are warp-wide) but not stored
-                const bool row_ok = !varlen || grow < N;
-                const size_t orow = varlen ? (static_cast<size_t>(seq0 + grow) * p.H + h) * D
-                                           : (static_cast<size_t>(bh) * N + grow) * D;
-                const size_t lrow = varlen ? static_cast<size_t>(h) * p.total + seq0 + grow
-                                           : static_cast<size_t>(bh) * N + grow;
-                // bf16: a warp whose 32 rows all lie in the sequence stages them
-                // in its Q tile's buffer (every S GEMM is complete once o_done
-                // is), in the 128-byte swizzled layout of [32 x 64] boxes, and
-                // stores them with one bulk tensor copy per box; a store per
-                // thread and row would touch 32 rows (cache lines) per
-                // instruction. Other warps store their valid rows directly, and
-                // so does a Q tile that saw no key tile (n == 0: nothing waited
-                // for its Q load, which may still be landing in the buffer).
+                const size_t orow = (static_cast<size_t>(bh) * N + grow) * D;
+                const size_t lrow = static_cast<size_t>(bh) * N + grow;
+                // bf16: a warp stages its 32 rows in its Q tile's buffer (every
+                // S GEMM is complete once o_done is), in the 128-byte swizzled
+                // layout of [32 x 64] boxes, and stores them with one bulk
+                // tensor copy per box; a store per thread and row would touch
+                // 32 rows (cache lines) per instruction. A Q tile that saw no
+                // key tile (n == 0: nothing waited for its Q load, which may
+                // still be landing in the buffer) stores its rows directly.
                 const int wrow0 = qb * kTile + wq * 32;
                 const bool tma_rows = !TF32 && n > 0 && wrow0 + 32 <= N;
                 uint8_t* ob = sm + C::Q_OFF + s * C::SPLIT * C::TILE_BYTES + wq * (C::NREG * 4096);
@@ -692,12 +663,11 @@ __global__ void __launch_bounds__(384, 1)
                                 const int ch = ((c & 1) << 2) + j;  // 16-byte chunk within the 128-byte row
                                 sts128(smem_u32(ob + (c >> 1) * 4096 + lane * 128 + ((ch ^ (lane & 7)) << 4)), w.x, w.y,
                                        w.z, w.w);
-                            } else if (row_ok) {
+                            } else {
                                 dst[j] = w;
                             }
                         }
                     } else {
-                        if (!row_ok) continue;
                         float4* dst = reinterpret_cast<float4*>(static_cast<float*>(p.o) + orow + c * 32);
 #pragma unroll
                         for (int j = 0; j < 8; ++j)
@@ -711,18 +681,14 @@ __global__ void __launch_bounds__(384, 1)
                     __syncwarp();
                     if (lane == 0) {
 #pragma unroll
-                        for (int rg = 0; rg < C::NREG; ++rg) {
-                            if (varlen)
-                                tma_store_3d(&tmO, rg * C::BOXC, h, seq0 + wrow0, ob + rg * 4096);
-                            else
-                                tma_store_2d(&tmO, rg * C::BOXC, bh * N + wrow0, ob + rg * 4096);
-                        }
+                        for (int rg = 0; rg < C::NREG; ++rg)
+                            tma_store_2d(&tmO, rg * C::BOXC, bh * N + wrow0, ob + rg * 4096);
                         bulk_commit_group();
                         // the shared buffer must be read out before the CTA exits
                         bulk_wait_group_read0();
                     }
                 }
-                if (row_ok) p.lse[lrow] = l > 0.f ? (m_hat + log2f(l)) * kLn2 : -CUDART_INF_F;
+                p.lse[lrow] = l > 0.f ? (m_hat + log2f(l)) * kLn2 : -CUDART_INF_F;
             }
         }
     }
@@ -793,25 +759,18 @@ static cudaError_t launch_fwd_t(const FwdArgs& a, cudaStream_t stream, int* nlau
             return cudaErrorInvalidValue;
     } else {
         // O is stored in [32 rows x 64 columns] boxes, one per warp and region
-        if (a.cu_seqlens) {
-            const uint64_t tot = static_cast<uint64_t>(a.total);
-            if (!make_tmap_packed_sw128(&tq, a.q, tot, a.H, D, elem, kTile, C::BOXC) ||
-                !make_tmap_packed_sw128(&tk, a.k, tot, a.H, D, elem, kTile, C::BOXC) ||
-                !make_tmap_packed_sw128(&tv, a.v, tot, a.H, D, elem, kTile, C::BOXC) ||
-                !make_tmap_packed_sw128(&to, a.o, tot, a.H, D, elem, 32, C::BOXC))
-                return cudaErrorInvalidValue;
-        } else if (!make_tmap_2d_sw128(&tq, a.q, rows, D, elem, kTile, C::BOXC) ||
-                   !make_tmap_2d_sw128(&tk, a.k, rows, D, elem, kTile, C::BOXC) ||
-                   !make_tmap_2d_sw128(&tv, a.v, rows, D, elem, kTile, C::BOXC) ||
-                   !make_tmap_2d_sw128(&to, a.o, rows, D, elem, 32, C::BOXC))
+        if (!make_tmap_2d_sw128(&tq, a.q, rows, D, elem, kTile, C::BOXC) ||
+            !make_tmap_2d_sw128(&tk, a.k, rows, D, elem, kTile, C::BOXC) ||
+            !make_tmap_2d_sw128(&tv, a.v, rows, D, elem, kTile, C::BOXC) ||
+            !make_tmap_2d_sw128(&to, a.o, rows, D, elem, 32, C::BOXC))
             return cudaErrorInvalidValue;
         tql = tq;
         tkl = tk;
     }
     if constexpr (TF32) to = tq;  // unused: fp32 O is stored directly
-    // bf16 calls reach this kernel only packed or with dropout; the others
-    // run fa_fwd_t1.cu
-    if (!TF32 && !a.cu_seqlens && !a.dropout) return cudaErrorInvalidValue;
+    // bf16 calls reach this kernel only with dropout ([B, H, N, d]); the
+    // others run fa_fwd_t1.cu
+    if (!TF32 && (a.cu_seqlens || !a.dropout)) return cudaErrorInvalidValue;
     static bool attr_set = false;
     if (!attr_set) {
         cudaError_t e;
@@ -821,9 +780,6 @@ static cudaError_t launch_fwd_t(const FwdArgs& a, cudaStream_t stream, int* nlau
         } else {
             e = cudaFuncSetAttribute(fa_fwd_kernel<false, D, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                      C::SMEM);
-            if (e == cudaSuccess)
-                e = cudaFuncSetAttribute(fa_fwd_kernel<false, D, false, true>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
         }
         if (e != cudaSuccess) return e;
         attr_set = true;
@@ -840,13 +796,11 @@ static cudaError_t launch_fwd_t(const FwdArgs& a, cudaStream_t stream, int* nlau
     p.o = a.o;
     p.lse = a.lse;
     p.status = a.status;
-    p.cu_seqlens = TF32 ? nullptr : a.cu_seqlens;
-    p.total = a.total;
     const int T = (a.N + kTile - 1) / kTile;
-    p.head_major = (a.blockmask && !a.causal && !p.cu_seqlens) ? 1 : 0;
-    // causal [B, H, N, d] calls: head groups whose K and V take at most 64 MiB
+    p.head_major = (a.blockmask && !a.causal) ? 1 : 0;
+    // causal calls: head groups whose K and V take at most 64 MiB
     p.group = 0;
-    if (a.causal && !p.cu_seqlens) {
+    if (a.causal) {
         const long long per_head = 2LL * a.N * D * elem;
         long long g = (64LL << 20) / per_head;
         g = g < 1 ? 1 : g;
@@ -859,10 +813,8 @@ static cudaError_t launch_fwd_t(const FwdArgs& a, cudaStream_t stream, int* nlau
     p.drop = a.drop;
     if constexpr (TF32)
         fa_fwd_kernel<true, D, false><<<grid, C::THREADS, C::SMEM, stream>>>(tq, tk, tv, tql, tkl, to, p);
-    else if (p.cu_seqlens)
-        fa_fwd_kernel<false, D, true><<<grid, C::THREADS, C::SMEM, stream>>>(tq, tk, tv, tql, tkl, to, p);
     else
-        fa_fwd_kernel<false, D, false, true><<<grid, C::THREADS, C::SMEM, stream>>>(tq, tk, tv, tql, tkl, to, p);
+        fa_fwd_kernel<false, D, true><<<grid, C::THREADS, C::SMEM, stream>>>(tq, tk, tv, tql, tkl, to, p);
     if (a.ev_end) cudaEventRecord(a.ev_end, stream);
     ++launches;
     *nlaunch = launches;
@@ -870,10 +822,10 @@ static cudaError_t launch_fwd_t(const FwdArgs& a, cudaStream_t stream, int* nlau
 }
 
 cudaError_t launch_fwd(const FwdArgs& a, cudaStream_t stream, int* nlaunch) {
-    // bf16 [B, H, N, d] calls without dropout: one query tile per CTA, two
-    // CTAs per SM (fa_fwd_t1.cu); this file's pair kernel serves fp32 inputs,
-    // packed batches and dropout
-    if (!a.fp32 && !a.cu_seqlens && !a.dropout) return launch_fwd_bf16_t1(a, stream, nlaunch);
+    // bf16 calls without dropout ([B, H, N, d] or packed): one query tile per
+    // CTA, two CTAs per SM (fa_fwd_t1.cu); this file's pair kernel serves
+    // fp32 inputs and dropout
+    if (!a.fp32 && !a.dropout) return launch_fwd_bf16_t1(a, stream, nlaunch);
     if (a.fp32) {
         if (a.d == 64) return launch_fwd_t<true, 64>(a, stream, nlaunch);
         return cudaErrorInvalidValue;  // fp32 d=128 exceeds the shared-memory budget of this kernel

@@ -1,5 +1,6 @@
-// Forward pass for bf16 [B, H, N, d] calls: one 128-row query tile per CTA
-// and two CTAs per SM.
+// Forward pass for bf16 calls without dropout ([B, H, N, d] tensors or packed
+// variable-length batches): one 128-row query tile per CTA and two CTAs per
+// SM.
 //
 // Same computation as fa_fwd.cu ("FlashAttention: making attention
 // IO-aware", sections "Tiling: never materialise S" and "Online softmax";
@@ -81,12 +82,17 @@ struct T1Params {
     float* lse;
     int* status;
     int group;  // > 0 (causal): 1D grid of head groups, longest query tile first in each
+    const int32_t* cu_seqlens;  // packed variable-length batch, else null
+    int total;                  // tokens of the packed batch
 };
 
 constexpr float kT1RescaleThreshold = 8.0f;  // log2 units
 constexpr float kT1Ln2 = 0.69314718055994530942f;
 
-template <int D>
+// VARLEN: packed variable-length batch ([total, H, d] tensors, sequence b at
+// tokens cu_seqlens[b] .. cu_seqlens[b + 1] - 1, L as [H, total]); a separate
+// instantiation so that the [B, H, N, d] kernel carries none of its branches.
+template <int D, bool VARLEN>
 __global__ void __launch_bounds__(192, 2)
     fa_fwd_t1_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                      const __grid_constant__ CUtensorMap tmVh, const __grid_constant__ CUtensorMap tmO,
@@ -122,9 +128,27 @@ __global__ void __launch_bounds__(192, 2)
     // reads qb + 1 key tiles: a 1D grid runs groups of p.group heads in turn
     // (sized so that a group's K and V stay in L2), longest tile first across
     // the heads of a group, so that the kernel ends on short CTAs.
+    // A packed batch runs a (query tile, H, B) grid over its longest
+    // sequence, query tile fastest so that the CTAs running together share a
+    // head's K and V in L2: CTAs past the end of a shorter sequence leave at
+    // once, and with a causal mask z = 0 is the sequence's last (longest)
+    // query tile.
     int qb = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
-    const int N = p.N, T = p.mask.T;
-    if (p.group > 0) {
+    int N = p.N, T = p.mask.T, seq0 = 0;
+    if constexpr (VARLEN) {
+        h = blockIdx.y;
+        b = blockIdx.z;
+        const int s0 = min(max(p.cu_seqlens[b], 0), p.total);
+        const int s1 = min(max(p.cu_seqlens[b + 1], s0), p.total);
+        if (s1 - s0 > p.N && tid == 0 && h == 0 && blockIdx.x == 0 && p.status)
+            atomicCAS(p.status, 0, FA_DEV_INVALID | (95 << 8));
+        seq0 = s0;
+        N = min(s1 - s0, p.N);
+        T = (N + kTile - 1) / kTile;
+        const int z = static_cast<int>(blockIdx.x);
+        if (z >= T) return;  // uniform over the CTA, before any barrier or TMEM use
+        qb = p.mask.causal ? T - 1 - z : z;
+    } else if (p.group > 0) {
         const int nb = p.B * p.H, L = static_cast<int>(blockIdx.x);
         const int gi = L / (p.group * T), rr = L - gi * p.group * T;
         const int g0 = gi * p.group, gsz = min(p.group, nb - g0);
@@ -134,7 +158,7 @@ __global__ void __launch_bounds__(192, 2)
         h = bhx - b * p.H;
     }
     const int bh = b * p.H + h;
-    const int kvalid = keys_valid(p.mask, b, N);
+    const int kvalid = VARLEN ? N : keys_valid(p.mask, b, N);
     int hi = min(T, (kvalid + kTile - 1) / kTile);
     if (p.mask.causal) hi = min(hi, qb + 1);
     const MaskArgs mk = p.mask;
@@ -158,10 +182,17 @@ __global__ void __launch_bounds__(192, 2)
         return t;
     };
 
+    // rows row .. of this head ([B, H, N, d]) or of this sequence (packed)
+    auto load_rows = [&](void* dst, const CUtensorMap* m, int x, int row, uint64_t* bar) {
+        if constexpr (VARLEN)
+            tma_load_3d(dst, m, x, h, seq0 + row, bar);
+        else
+            tma_load_2d(dst, m, x, bh * N + row, bar);
+    };
     auto load_k = [&](int t, int kst) {
         uint8_t* sk = sm + C::K_OFF + kst * C::TILE_BYTES;
         mbar_arrive_expect_tx(&k_full[kst], C::TILE_BYTES);
-        for (int r = 0; r < C::NREG; ++r) tma_load_2d(sk + r * 16384, &tmK, r * 64, bh * N + t * kTile, &k_full[kst]);
+        for (int r = 0; r < C::NREG; ++r) load_rows(sk + r * 16384, &tmK, r * 64, t * kTile, &k_full[kst]);
     };
     // V half hf (keys 64 hf .. 64 hf + 63) of key tile t into slot vs: NREG
     // swizzled boxes of [64 keys x 64 columns], 8 KiB apart
@@ -169,7 +200,7 @@ __global__ void __launch_bounds__(192, 2)
         uint8_t* sv = sm + C::V_OFF + vs * C::HALF_BYTES;
         mbar_arrive_expect_tx(&v_full[vs], C::HALF_BYTES);
         for (int r = 0; r < C::NREG; ++r)
-            tma_load_2d(sv + r * 8192, &tmVh, r * 64, bh * N + t * kTile + hf * 64, &v_full[vs]);
+            load_rows(sv + r * 8192, &tmVh, r * 64, t * kTile + hf * 64, &v_full[vs]);
     };
 
     if (tid == 0) {
@@ -193,7 +224,7 @@ __global__ void __launch_bounds__(192, 2)
         // TMEM allocation and the CTA-wide barrier
         mbar_arrive_expect_tx(bar_q, C::TILE_BYTES);
         for (int r = 0; r < C::NREG; ++r)
-            tma_load_2d(sm + C::Q_OFF + r * 16384, &tmQ, r * 64, bh * N + qb * kTile, bar_q);
+            load_rows(sm + C::Q_OFF + r * 16384, &tmQ, r * 64, qb * kTile, bar_q);
         tma_prefetch_desc(&tmK);
         tma_prefetch_desc(&tmVh);
     }
@@ -433,14 +464,20 @@ __global__ void __launch_bounds__(192, 2)
         }
         if (ok) {
             const float inv = lw > 0.f ? 1.f / lw : 0.f;
-            const int grow = qb * kTile + r;
-            const size_t orow = (static_cast<size_t>(bh) * N + grow) * D;
-            // a warp stages its 32 rows in the Q buffer (every S GEMM is
-            // complete once o_done is), as [32 x 64] swizzled boxes, and
-            // stores them with one bulk tensor copy per box; a tile that saw
-            // no key tile (n == 0: nothing waited for its Q load, which may
-            // still be landing in the buffer) stores its rows directly
-            const bool tma_rows = n > 0;
+            const int grow = qb * kTile + r;  // query row within the sequence
+            // packed rows past the end of the sequence belong to the next
+            // one: computed (the TMEM loads are warp-wide) but not stored
+            const bool row_ok = !VARLEN || grow < N;
+            const size_t orow = VARLEN ? (static_cast<size_t>(seq0 + grow) * p.H + h) * D
+                                       : (static_cast<size_t>(bh) * N + grow) * D;
+            // a warp whose 32 rows all lie in the sequence stages them in the
+            // Q buffer (every S GEMM is complete once o_done is), as [32 x 64]
+            // swizzled boxes, and stores them with one bulk tensor copy per
+            // box; other warps, and a tile that saw no key tile (n == 0:
+            // nothing waited for its Q load, which may still be landing in the
+            // buffer), store their valid rows directly
+            const int wrow0 = qb * kTile + wq * 32;
+            const bool tma_rows = n > 0 && (!VARLEN || wrow0 + 32 <= N);
             uint8_t* ob = sm + C::Q_OFF + wq * (C::NREG * 4096);
             uint32_t oa[D / 32][32];
             if (n > 0) {
@@ -469,7 +506,7 @@ __global__ void __launch_bounds__(192, 2)
                         const int ch = ((c & 1) << 2) + j;  // 16-byte chunk within the 128-byte row
                         sts128(smem_u32(ob + (c >> 1) * 4096 + lane * 128 + ((ch ^ (lane & 7)) << 4)), w.x, w.y, w.z,
                                w.w);
-                    } else {
+                    } else if (row_ok) {
                         dst[j] = w;
                     }
                 }
@@ -480,13 +517,17 @@ __global__ void __launch_bounds__(192, 2)
                 if (lane == 0) {
 #pragma unroll
                     for (int rg = 0; rg < C::NREG; ++rg)
-                        tma_store_2d(&tmO, rg * 64, bh * N + qb * kTile + wq * 32, ob + rg * 4096);
+                        if constexpr (VARLEN)
+                            tma_store_3d(&tmO, rg * 64, h, seq0 + wrow0, ob + rg * 4096);
+                        else
+                            tma_store_2d(&tmO, rg * 64, bh * N + wrow0, ob + rg * 4096);
                     bulk_commit_group();
                     // the shared buffer must be read out before the CTA exits
                     bulk_wait_group_read0();
                 }
             }
-            p.lse[static_cast<size_t>(bh) * N + grow] = l > 0.f ? (m_hat + log2f(l)) * kT1Ln2 : -CUDART_INF_F;
+            const size_t lrow = VARLEN ? static_cast<size_t>(h) * p.total + seq0 + grow : static_cast<size_t>(bh) * N + grow;
+            if (row_ok) p.lse[lrow] = l > 0.f ? (m_hat + log2f(l)) * kT1Ln2 : -CUDART_INF_F;
         }
     }
     tc_fence_before();
@@ -502,12 +543,25 @@ static cudaError_t launch_t1(const FwdArgs& a, cudaStream_t stream, int* nlaunch
     using C = T1Cfg<D>;
     const uint64_t rows = static_cast<uint64_t>(a.B) * a.H * a.N;
     CUtensorMap tq, tk, tvh, to;
-    if (!make_tmap_2d_sw128(&tq, a.q, rows, D, 2, kTile, 64) || !make_tmap_2d_sw128(&tk, a.k, rows, D, 2, kTile, 64) ||
-        !make_tmap_2d_sw128(&tvh, a.v, rows, D, 2, 64, 64) || !make_tmap_2d_sw128(&to, a.o, rows, D, 2, 32, 64))
+    if (a.cu_seqlens) {
+        const uint64_t tot = static_cast<uint64_t>(a.total);
+        if (!make_tmap_packed_sw128(&tq, a.q, tot, a.H, D, 2, kTile, 64) ||
+            !make_tmap_packed_sw128(&tk, a.k, tot, a.H, D, 2, kTile, 64) ||
+            !make_tmap_packed_sw128(&tvh, a.v, tot, a.H, D, 2, 64, 64) ||
+            !make_tmap_packed_sw128(&to, a.o, tot, a.H, D, 2, 32, 64))
+            return cudaErrorInvalidValue;
+    } else if (!make_tmap_2d_sw128(&tq, a.q, rows, D, 2, kTile, 64) ||
+               !make_tmap_2d_sw128(&tk, a.k, rows, D, 2, kTile, 64) ||
+               !make_tmap_2d_sw128(&tvh, a.v, rows, D, 2, 64, 64) ||
+               !make_tmap_2d_sw128(&to, a.o, rows, D, 2, 32, 64)) {
         return cudaErrorInvalidValue;
+    }
     static bool attr_set = false;
     if (!attr_set) {
-        cudaError_t e = cudaFuncSetAttribute(fa_fwd_t1_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
+        cudaError_t e = cudaFuncSetAttribute(fa_fwd_t1_kernel<D, false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             C::SMEM);
+        if (e == cudaSuccess)
+            e = cudaFuncSetAttribute(fa_fwd_t1_kernel<D, true>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
         if (e != cudaSuccess) return e;
         attr_set = true;
     }
@@ -519,20 +573,26 @@ static cudaError_t launch_t1(const FwdArgs& a, cudaStream_t stream, int* nlaunch
     p.mask.blockmask = a.blockmask;
     p.mask.kv_len = a.kv_len;
     p.mask.causal = a.causal;
-    p.mask.T = a.N / kTile;
+    p.mask.T = (a.N + kTile - 1) / kTile;
     p.o = a.o;
     p.lse = a.lse;
     p.status = a.status;
-    // causal calls: head groups whose K and V take at most 64 MiB
+    p.cu_seqlens = a.cu_seqlens;
+    p.total = a.total;
+    // causal [B, H, N, d] calls: head groups whose K and V take at most 64 MiB
     p.group = 0;
-    if (a.causal) {
+    if (a.causal && !a.cu_seqlens) {
         long long g = (64LL << 20) / (4LL * a.N * D);
         g = g < 1 ? 1 : g;
         p.group = static_cast<int>(g < a.B * a.H ? g : a.B * a.H);
     }
-    const dim3 grid = p.group > 0 ? dim3(static_cast<unsigned>(a.N / kTile) * a.H * a.B) : dim3(a.N / kTile, a.H, a.B);
+    const unsigned T = static_cast<unsigned>(p.mask.T);
+    const dim3 grid = p.group > 0 ? dim3(T * a.H * a.B) : dim3(T, a.H, a.B);
     if (a.ev_begin) cudaEventRecord(a.ev_begin, stream);
-    fa_fwd_t1_kernel<D><<<grid, C::THREADS, C::SMEM, stream>>>(tq, tk, tvh, to, p);
+    if (a.cu_seqlens)
+        fa_fwd_t1_kernel<D, true><<<grid, C::THREADS, C::SMEM, stream>>>(tq, tk, tvh, to, p);
+    else
+        fa_fwd_t1_kernel<D, false><<<grid, C::THREADS, C::SMEM, stream>>>(tq, tk, tvh, to, p);
     if (a.ev_end) cudaEventRecord(a.ev_end, stream);
     *nlaunch = 1;
     return cudaGetLastError();
