@@ -56,80 +56,84 @@ __device__ __forceinline__ int pow2_scale_exp(float amax) {
 }
 
 // ---------------------------------------------------------------------------
-// Q and K: one CTA per (128-row block, head); four lanes per row, eight rows
-// per warp at a time, two passes. Lane t of a row's quad holds columns
-// 32 k + 8 t + e (k, e = 0..3, 0..7), read as four 16-byte pieces (a quad
-// reads 64 contiguous bytes per instruction). The Walsh-Hadamard butterflies
-// over column bits 0-2 (e) and 5-6 (k) stay in the lane; bits 3-4 (t) use
-// two shuffle stages. The stages commute (the Sylvester matrix is the
-// Kronecker power of H_2), so their order is free.
+// Q and K rotation and quantisation, V block maxima: one thread per row of a
+// 128-row block. The block arrives by two tiled bulk copies in the 128-byte
+// swizzled layout (16-byte chunk c of row r at chunk c ^ (r mod 8) of its
+// 128-byte line), so 32 threads reading the same chunk of 32 rows touch all
+// 32 banks. A row's 128 values are 64 (even, odd) column pairs, one f32x2
+// register each; the Walsh-Hadamard butterflies over column bit 0 combine
+// the two halves of a pair, and those over bits 1-6 combine whole pairs, two
+// columns per f32x2 instruction. The seven stages commute (the Sylvester
+// matrix is the Kronecker power of H_2), so their order is free, and every
+// stage stays in the thread.
 // ---------------------------------------------------------------------------
-__device__ __forceinline__ void fwht8_inlane(float (&a)[8]) {
-#pragma unroll
-    for (int m = 1; m < 8; m <<= 1)
-#pragma unroll
-        for (int e = 0; e < 8; ++e)
-            if (!(e & m)) {
-                const float x = a[e], y = a[e + m];
-                a[e] = x + y;
-                a[e + m] = x - y;
-            }
+__device__ __forceinline__ uint64_t f2_sub(uint64_t a, uint64_t b) {
+    uint64_t r;
+    asm("sub.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+    return r;
 }
 
 // Persistent: each CTA walks the 128-row blocks j = blockIdx.x, + gridDim.x,
 // ... of the three tensors in the order Q, K, V (V's blocks last, so that
 // V is still partly in L2 when fa_fp8_v_kernel reads it again). Q and K
 // blocks are rotated (when ROT), scaled and rounded to E4M3; a V block only
-// gets its maximum |v| (for the head's V scale). Blocks are contiguous 32 KiB
-// and come into two shared-memory buffers by bulk copies, the one after next
-// requested as soon as the current one has been read into registers, so
-// every SM keeps loads in flight while it computes.
+// gets its maximum |v| (for the head's V scale). Two shared-memory buffers:
+// the block after next is requested as soon as every thread has read the
+// current one into registers, so every SM keeps loads in flight while it
+// computes.
+constexpr int kPrepThreads = 128;
 constexpr int kPrepBlockBytes = kTile * kD8 * 2;  // 128 rows of bf16
 constexpr int kPrepCtasPerSm = 3;
-constexpr int kPrepSmem = 2 * kPrepBlockBytes + 64;  // two buffers, two mbarriers, abort flag
+constexpr int kPrepSmem = 2 * kPrepBlockBytes + 1024 + 64;  // two buffers, alignment, two mbarriers, abort flag
 
 template <bool ROT>
-__global__ void __launch_bounds__(256, kPrepCtasPerSm)
-    fa_fp8_prep_kernel(const uint16_t* __restrict__ q, const uint16_t* __restrict__ k, const uint16_t* __restrict__ v,
-                       const float* __restrict__ signs, uint8_t* __restrict__ q8, uint8_t* __restrict__ k8,
-                       int* __restrict__ qexp, int* __restrict__ kexp, float* __restrict__ vblk_max, int N, int BH,
-                       int* status) {
-    extern __shared__ __align__(128) uint8_t prep_smem[];
-    __shared__ float wmax[8];
-    __shared__ int e_sh;
-    __shared__ float sg_sh[kD8];
-    uint64_t* full = reinterpret_cast<uint64_t*>(prep_smem + 2 * kPrepBlockBytes);  // [2]
+__global__ void __launch_bounds__(kPrepThreads, kPrepCtasPerSm)
+    fa_fp8_prep_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
+                       const __grid_constant__ CUtensorMap tmV, const float* __restrict__ signs,
+                       uint8_t* __restrict__ q8, uint8_t* __restrict__ k8, int* __restrict__ qexp,
+                       int* __restrict__ kexp, float* __restrict__ vblk_max, int N, int BH, int* status) {
+    extern __shared__ __align__(1024) uint8_t prep_raw[];
+    // 1024-byte aligned base: the swizzle pattern follows address bits 4-9
+    uint8_t* sm = prep_raw + ((1024u - (smem_u32(prep_raw) & 1023u)) & 1023u);
+    __shared__ float wmax[kPrepThreads / 32];
+    __shared__ __align__(16) float sg_sh[kD8];
+    uint64_t* full = reinterpret_cast<uint64_t*>(sm + 2 * kPrepBlockBytes);  // [2]
     volatile int* abort_flag = reinterpret_cast<volatile int*>(full + 2);
     const WaitCtx cx{abort_flag, status};
     const int T = N / kTile;
     const int per_tensor = T * BH;
     const int nblocks = 3 * per_tensor;
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int t = lane & 3, rq = lane >> 2;  // column quarter, row within the warp's 8
-    // first row of block j ([B * H * N, 128] view of its tensor)
-    auto block_src = [=](int j) -> const uint16_t* {
+    const int r = threadIdx.x, warp = r >> 5, lane = r & 31;
+    // block j: tensor j / per_tensor (Q, K, V), rows (j mod per_tensor) * 128 ..
+    // of its [B * H * N, 128] view, as two [128 x 64] swizzled boxes
+    auto request = [&](int j, int buf) {
         const int which = j / per_tensor, rem = j - which * per_tensor;
-        const uint16_t* x = which == 0 ? q : (which == 1 ? k : v);
-        return x + static_cast<size_t>(rem) * kTile * kD8;  // rem = bh * T + blk
+        const CUtensorMap* m = which == 0 ? &tmQ : (which == 1 ? &tmK : &tmV);
+        mbar_arrive_expect_tx(&full[buf], kPrepBlockBytes);
+        tma_load_2d(sm + buf * kPrepBlockBytes, m, 0, rem * kTile, &full[buf]);
+        tma_load_2d(sm + buf * kPrepBlockBytes + kPrepBlockBytes / 2, m, 64, rem * kTile, &full[buf]);
     };
-    if (threadIdx.x == 0) {
+    if ((sm - prep_raw) + 2 * kPrepBlockBytes + 64 > kPrepSmem) {
+        if (r == 0 && status) atomicCAS(status, 0, FA_DEV_TIMEOUT | (94 << 8));
+        return;
+    }
+    if (r == 0) {
         *abort_flag = 0;
         mbar_init(&full[0], 1);
         mbar_init(&full[1], 1);
         fence_barrier_init();
     }
-    if (ROT && threadIdx.x < kD8) sg_sh[threadIdx.x] = signs[threadIdx.x];
+    if (ROT) sg_sh[r] = signs[r];
     __syncthreads();
     // thread 0: copies issued into each buffer, and which buffers still have
     // one outstanding (issued, not yet consumed)
     int n_issued0 = 0, n_issued1 = 0;
     uint32_t issued = 0;
-    if (threadIdx.x == 0) {
+    if (r == 0) {
         for (int i = 0; i < 2; ++i) {
             const int j = blockIdx.x + i * gridDim.x;
             if (j < nblocks) {
-                mbar_arrive_expect_tx(&full[i], kPrepBlockBytes);
-                bulk_load(prep_smem + i * kPrepBlockBytes, block_src(j), kPrepBlockBytes, &full[i]);
+                request(j, i);
                 issued |= 1u << i;
                 if (i) ++n_issued1; else ++n_issued0;
             }
@@ -139,128 +143,101 @@ __global__ void __launch_bounds__(256, kPrepCtasPerSm)
     for (int j = blockIdx.x; j < nblocks; j += gridDim.x, ++it) {
         const int buf = it & 1;
         if (!__syncthreads_and(mbar_wait(&full[buf], (it >> 1) & 1, cx, 31))) break;
-        if (threadIdx.x == 0) issued &= ~(1u << buf);
-        // this thread's two rows (passes) of the block, four 16-byte pieces each
-        uint4 raw[2][4];
+        if (r == 0) issued &= ~(1u << buf);
+        // this thread's row: 16 chunks of 8 columns (chunk c: columns 8 c ..)
+        uint32_t raw[64];
+        {
+            const uint32_t base = smem_u32(sm + buf * kPrepBlockBytes) + r * 128;
 #pragma unroll
-        for (int ps = 0; ps < 2; ++ps) {
-            const uint8_t* src = prep_smem + buf * kPrepBlockBytes + (warp * 16 + ps * 8 + rq) * (kD8 * 2);
-#pragma unroll
-            for (int kk = 0; kk < 4; ++kk) raw[ps][kk] = *reinterpret_cast<const uint4*>(src + 64 * kk + 16 * t);
+            for (int c = 0; c < 16; ++c) {
+                const uint4 w = lds128_u4(base + (c >> 3) * (kPrepBlockBytes / 2) + (((c & 7) ^ (r & 7)) << 4));
+                raw[4 * c] = w.x;
+                raw[4 * c + 1] = w.y;
+                raw[4 * c + 2] = w.z;
+                raw[4 * c + 3] = w.w;
+            }
         }
         __syncthreads();  // buffer read by every thread: request the block after next
-        if (threadIdx.x == 0) {
+        if (r == 0) {
             const int j2 = j + 2 * gridDim.x;
             if (j2 < nblocks) {
-                mbar_arrive_expect_tx(&full[buf], kPrepBlockBytes);
-                bulk_load(prep_smem + buf * kPrepBlockBytes, block_src(j2), kPrepBlockBytes, &full[buf]);
+                request(j2, buf);
                 issued |= 1u << buf;
                 if (buf) ++n_issued1; else ++n_issued0;
             }
         }
         const int which = j / per_tensor, rem = j - which * per_tensor;  // rem = bh * T + blk
-        const size_t row0 = static_cast<size_t>(rem) * kTile;
         if (which == 2) {  // V: the block's maximum |v| only (uniform branch per CTA)
-            float m = 0.f;
+            uint32_t m2 = 0;  // two 16-bit magnitudes; bf16 magnitudes order like integers
 #pragma unroll
-            for (int ps = 0; ps < 2; ++ps)
-#pragma unroll
-                for (int kk = 0; kk < 4; ++kk) {
-                    const uint32_t u[4] = {raw[ps][kk].x, raw[ps][kk].y, raw[ps][kk].z, raw[ps][kk].w};
-#pragma unroll
-                    for (int h = 0; h < 4; ++h)
-                        m = fmaxf(m, fmaxf(fabsf(__uint_as_float(u[h] << 16)),
-                                           fabsf(__uint_as_float(u[h] & 0xFFFF0000u))));
-                }
+            for (int i = 0; i < 64; ++i) m2 = __vmaxu2(m2, raw[i] & 0x7FFF7FFFu);
+            float m = fmaxf(__uint_as_float(m2 << 16), __uint_as_float(m2 & 0xFFFF0000u));
 #pragma unroll
             for (int off = 16; off > 0; off >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, off));
             if (lane == 0) wmax[warp] = m;
             __syncthreads();
-            if (threadIdx.x == 0) {
-                float mm = 0.f;
-                for (int w = 0; w < 8; ++w) mm = fmaxf(mm, wmax[w]);
-                vblk_max[rem] = mm;
-            }
+            if (r == 0) vblk_max[rem] = fmaxf(fmaxf(wmax[0], wmax[1]), fmaxf(wmax[2], wmax[3]));
             continue;
         }
-        float y[2][4][8];
+        // y[i]: columns 2 i and 2 i + 1 as an f32x2 pair
+        uint64_t y[64];
+#pragma unroll
+        for (int i = 0; i < 64; ++i) y[i] = f2_from_bf16x2(raw[i]);
+        if (ROT) {
+            const uint64_t* sg2 = reinterpret_cast<const uint64_t*>(sg_sh);
+#pragma unroll
+            for (int i = 0; i < 64; ++i) y[i] = f2_mul(y[i], sg2[i]);
+            // column bit 0: the two halves of a pair
+#pragma unroll
+            for (int i = 0; i < 64; ++i) {
+                float a, b;
+                f2_split(y[i], a, b);
+                y[i] = f2_make(a + b, a - b);
+            }
+            // column bits 1-6: pairs i and i + M, M = 1 .. 32
+#pragma unroll
+            for (int M = 1; M < 64; M <<= 1)
+#pragma unroll
+                for (int i = 0; i < 64; ++i)
+                    if (!(i & M)) {
+                        const uint64_t u = y[i], v = y[i + M];
+                        y[i] = f2_add(u, v);
+                        y[i + M] = f2_sub(u, v);
+                    }
+        }
         float amax = 0.f;
 #pragma unroll
-        for (int ps = 0; ps < 2; ++ps) {
-#pragma unroll
-            for (int kk = 0; kk < 4; ++kk) {
-                const uint32_t u[4] = {raw[ps][kk].x, raw[ps][kk].y, raw[ps][kk].z, raw[ps][kk].w};
-#pragma unroll
-                for (int h = 0; h < 4; ++h) {
-                    const int c = 32 * kk + 8 * t + 2 * h;
-                    y[ps][kk][2 * h] = __uint_as_float(u[h] << 16);
-                    y[ps][kk][2 * h + 1] = __uint_as_float(u[h] & 0xFFFF0000u);
-                    if (ROT) {
-                        y[ps][kk][2 * h] *= sg_sh[c];
-                        y[ps][kk][2 * h + 1] *= sg_sh[c + 1];
-                    }
-                }
-                if (ROT) fwht8_inlane(y[ps][kk]);  // column bits 0-2
-            }
-            if (ROT) {
-                // column bits 5-6: butterflies across kk
-#pragma unroll
-                for (int e = 0; e < 8; ++e) {
-                    float b0 = y[ps][0][e] + y[ps][1][e], b1 = y[ps][0][e] - y[ps][1][e];
-                    float b2 = y[ps][2][e] + y[ps][3][e], b3 = y[ps][2][e] - y[ps][3][e];
-                    y[ps][0][e] = b0 + b2;
-                    y[ps][1][e] = b1 + b3;
-                    y[ps][2][e] = b0 - b2;
-                    y[ps][3][e] = b1 - b3;
-                }
-                // column bits 3-4: partner lanes t ^ 1, t ^ 2
-#pragma unroll
-                for (int m = 1; m < 4; m <<= 1) {
-                    const bool upper = (t & m) != 0;
-#pragma unroll
-                    for (int kk = 0; kk < 4; ++kk)
-#pragma unroll
-                        for (int e = 0; e < 8; ++e) {
-                            const float o = __shfl_xor_sync(0xffffffffu, y[ps][kk][e], m);
-                            y[ps][kk][e] = upper ? o - y[ps][kk][e] : y[ps][kk][e] + o;
-                        }
-                }
-            }
-#pragma unroll
-            for (int kk = 0; kk < 4; ++kk)
-#pragma unroll
-                for (int e = 0; e < 8; ++e) amax = fmaxf(amax, fabsf(y[ps][kk][e]));
+        for (int i = 0; i < 64; ++i) {
+            float a, b;
+            f2_split(y[i], a, b);
+            amax = fmax3(amax, fabsf(a), fabsf(b));
         }
 #pragma unroll
         for (int off = 16; off > 0; off >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, off));
         if (lane == 0) wmax[warp] = amax;
         __syncthreads();
-        if (threadIdx.x == 0) {
-            float m = 0.f;
-            for (int w = 0; w < 8; ++w) m = fmaxf(m, wmax[w]);
-            const int e = pow2_scale_exp(m);
-            e_sh = e;
-            (which == 0 ? qexp : kexp)[rem] = e;
-        }
-        __syncthreads();
-        const float inv = exp2i(-e_sh);
-        uint8_t* x8 = which == 0 ? q8 : k8;
+        // every thread takes the block's scale from the four warp maxima (the
+        // next write of wmax follows the next block's first barrier)
+        const int e = pow2_scale_exp(fmaxf(fmaxf(wmax[0], wmax[1]), fmaxf(wmax[2], wmax[3])));
+        if (r == 0) (which == 0 ? qexp : kexp)[rem] = e;
+        const float inv = exp2i(-e);
+        const uint64_t inv2 = f2_make(inv, inv);
+        uint8_t* dst = (which == 0 ? q8 : k8) + (static_cast<size_t>(rem) * kTile + r) * kD8;
 #pragma unroll
-        for (int ps = 0; ps < 2; ++ps) {
-            uint8_t* dst = x8 + (row0 + warp * 16 + ps * 8 + rq) * kD8;
+        for (int c = 0; c < 8; ++c) {  // 16 columns = 8 pairs per 16-byte store
+            uint32_t w[4];
 #pragma unroll
-            for (int kk = 0; kk < 4; ++kk) {
-                uint2 w;
-                w.x = pack_e4m3x2(y[ps][kk][0] * inv, y[ps][kk][1] * inv) |
-                      (pack_e4m3x2(y[ps][kk][2] * inv, y[ps][kk][3] * inv) << 16);
-                w.y = pack_e4m3x2(y[ps][kk][4] * inv, y[ps][kk][5] * inv) |
-                      (pack_e4m3x2(y[ps][kk][6] * inv, y[ps][kk][7] * inv) << 16);
-                *reinterpret_cast<uint2*>(dst + 32 * kk + 8 * t) = w;
+            for (int h = 0; h < 4; ++h) {
+                float a0, b0, a1, b1;
+                f2_split(f2_mul(y[8 * c + 2 * h], inv2), a0, b0);
+                f2_split(f2_mul(y[8 * c + 2 * h + 1], inv2), a1, b1);
+                w[h] = pack_e4m3x2(a0, b0) | (pack_e4m3x2(a1, b1) << 16);
             }
+            *reinterpret_cast<uint4*>(dst + 16 * c) = make_uint4(w[0], w[1], w[2], w[3]);
         }
     }
     // after a give-up, copies still in flight must land before the CTA exits
-    if (threadIdx.x == 0) {
+    if (r == 0) {
         // copies into buffer b complete its phases in order; the outstanding
         // one is the last issued there
         if (issued & 1u) mbar_wait_teardown(&full[0], (n_issued0 - 1) & 1, 200000000ull);
@@ -788,14 +765,17 @@ cudaError_t launch_fwd_fp8(const Fp8Args& a, cudaStream_t stream, int* nlaunch) 
     }
     const long long nblocks = 3LL * T * BH;
     const unsigned pgrid = static_cast<unsigned>(std::min<long long>(nblocks, static_cast<long long>(nsm) * kPrepCtasPerSm));
-    const uint16_t *q16 = static_cast<const uint16_t*>(a.q), *k16 = static_cast<const uint16_t*>(a.k),
-                   *v16 = static_cast<const uint16_t*>(a.v);
+    CUtensorMap tq16, tk16, tv16;
+    if (!make_tmap_2d_sw128(&tq16, a.q, rows, kD8, 2, kTile, 64) || !make_tmap_2d_sw128(&tk16, a.k, rows, kD8, 2, kTile, 64) ||
+        !make_tmap_2d_sw128(&tv16, a.v, rows, kD8, 2, kTile, 64))
+        return cudaErrorInvalidValue;
+    const uint16_t* v16 = static_cast<const uint16_t*>(a.v);
     if (a.signs)
-        fa_fp8_prep_kernel<true><<<pgrid, 256, kPrepSmem, stream>>>(q16, k16, v16, a.signs, a.q8, a.k8, a.qexp,
-                                                                     a.kexp, a.vblk_max, a.N, BH, a.status);
+        fa_fp8_prep_kernel<true><<<pgrid, kPrepThreads, kPrepSmem, stream>>>(
+            tq16, tk16, tv16, a.signs, a.q8, a.k8, a.qexp, a.kexp, a.vblk_max, a.N, BH, a.status);
     else
-        fa_fp8_prep_kernel<false><<<pgrid, 256, kPrepSmem, stream>>>(q16, k16, v16, nullptr, a.q8, a.k8, a.qexp,
-                                                                      a.kexp, a.vblk_max, a.N, BH, a.status);
+        fa_fp8_prep_kernel<false><<<pgrid, kPrepThreads, kPrepSmem, stream>>>(
+            tq16, tk16, tv16, nullptr, a.q8, a.k8, a.qexp, a.kexp, a.vblk_max, a.N, BH, a.status);
     fa_fp8_v_kernel<<<dim3(T, BH), 256, 0, stream>>>(v16, a.vblk_max, a.vt8, a.vexp, a.N);
     cudaError_t e;
     CUtensorMap tq, tk, tv, to;
