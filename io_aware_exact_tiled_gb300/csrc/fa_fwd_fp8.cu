@@ -246,39 +246,35 @@ __global__ void __launch_bounds__(kPrepThreads, kPrepCtasPerSm)
 }
 
 // V -> E4M3 with the head's scale, transposed to [d][keys] (the P V product
-// needs K-major operands): one CTA per (128-key block, head). Thread (lane,
-// warp) converts keys 4 lane .. 4 lane + 3 of columns 16 warp .. 16 warp + 15,
-// so each column's four key bytes form one 32-bit word of the transposed
-// tile (a warp writes 128 contiguous bytes of a row of it).
+// needs K-major operands): one CTA per (128-key block, head), one warp per
+// 16 of its columns. Lane l converts keys 4 l .. 4 l + 3, so a column's four
+// key bytes form one 32-bit word, and the warp's 32 words of a column are
+// 128 contiguous bytes of a row of V^T: one full line per store instruction,
+// with no shared memory and no barrier. The prep kernel read V last, so much
+// of it is still in L2.
 __global__ void __launch_bounds__(256) fa_fp8_v_kernel(const uint16_t* __restrict__ v,
                                                        const float* __restrict__ vblk_max, uint8_t* __restrict__ vt8,
                                                        int* __restrict__ vexp, int N) {
-    __shared__ __align__(16) uint32_t t8w[kD8][kTile / 4 + 4];  // [column][key quad]; +4 words keep rows 16-byte aligned
-    __shared__ float wmax[8];
     const int blk = blockIdx.x, bh = blockIdx.y;
     const int T = N / kTile;
+    const int lane = threadIdx.x & 31, g = threadIdx.x >> 5;  // columns 16 g .. 16 g + 15
     const size_t row0 = static_cast<size_t>(bh) * N + static_cast<size_t>(blk) * kTile;
-    const int kq = threadIdx.x & 31, cg = threadIdx.x >> 5;
     uint4 w[4][2];
 #pragma unroll
     for (int r = 0; r < 4; ++r) {
-        const uint4* src = reinterpret_cast<const uint4*>(v + (row0 + 4 * kq + r) * kD8 + 16 * cg);
+        const uint4* src = reinterpret_cast<const uint4*>(v + (row0 + 4 * lane + r) * kD8 + 16 * g);
         w[r][0] = src[0];
         w[r][1] = src[1];
     }
     // the head's max |v| from its blocks' maxima
     float hm = 0.f;
-    for (int i = threadIdx.x; i < T; i += 256) hm = fmaxf(hm, vblk_max[static_cast<size_t>(bh) * T + i]);
+    for (int i = lane; i < T; i += 32) hm = fmaxf(hm, vblk_max[static_cast<size_t>(bh) * T + i]);
 #pragma unroll
     for (int off = 16; off > 0; off >>= 1) hm = fmaxf(hm, __shfl_xor_sync(0xffffffffu, hm, off));
-    if (kq == 0) wmax[cg] = hm;
-    __syncthreads();
-    hm = wmax[0];
-#pragma unroll
-    for (int i = 1; i < 8; ++i) hm = fmaxf(hm, wmax[i]);
     const int e = pow2_scale_exp(hm);
     if (blk == 0 && threadIdx.x == 0) vexp[bh] = e;
     const float inv = exp2i(-e);
+    uint8_t* dst = vt8 + (static_cast<size_t>(bh) * kD8 + 16 * g) * N + static_cast<size_t>(blk) * kTile + 4 * lane;
 #pragma unroll
     for (int h = 0; h < 2; ++h) {
         uint32_t u[4][4];
@@ -293,22 +289,15 @@ __global__ void __launch_bounds__(256) fa_fp8_v_kernel(const uint16_t* __restric
         for (int q = 0; q < 4; ++q) {
 #pragma unroll
             for (int half = 0; half < 2; ++half) {
-                // column 16 cg + 8 h + 2 q + half of keys 4 kq .. 4 kq + 3
+                // column 16 g + 8 h + 2 q + half of keys 4 lane .. 4 lane + 3
                 float x[4];
 #pragma unroll
                 for (int r = 0; r < 4; ++r)
                     x[r] = __uint_as_float(half ? (u[r][q] & 0xFFFF0000u) : (u[r][q] << 16)) * inv;
-                t8w[16 * cg + 8 * h + 2 * q + half][kq] = pack_e4m3x2(x[0], x[1]) | (pack_e4m3x2(x[2], x[3]) << 16);
+                *reinterpret_cast<uint32_t*>(dst + static_cast<size_t>(8 * h + 2 * q + half) * N) =
+                    pack_e4m3x2(x[0], x[1]) | (pack_e4m3x2(x[2], x[3]) << 16);
             }
         }
-    }
-    __syncthreads();
-    // rows of V^T: [bh * d + dd][blk * 128 .. + 127], 16 bytes per thread and step
-    for (int i = threadIdx.x; i < kD8 * 8; i += 256) {
-        const int dd = i >> 3, part = i & 7;
-        const uint4 o = *reinterpret_cast<const uint4*>(&t8w[dd][part * 4]);
-        *reinterpret_cast<uint4*>(vt8 + (static_cast<size_t>(bh) * kD8 + dd) * N + static_cast<size_t>(blk) * kTile +
-                                  part * 16) = o;
     }
 }
 
