@@ -26,8 +26,9 @@ for d in (64, 128):
         SWEEP.append(W.Workload(f"causal-{N}-{d}", 2, 2, N, d, causal=True))
         SWEEP.append(W.Workload(f"kvlen-{N}-{d}", 3, 2, N, d, kv_len_range=(1, N)))
         SWEEP.append(W.Workload(f"sparse-{N}-{d}", 1, 2, N, d, block_density=0.3))
-SWEEP.append(W.Workload("causal-kvlen-sparse-768-128", 2, 2, 768, 128, causal=True, kv_len_range=(200, 700),
-                        block_density=0.5))
+for d in (64, 128):
+    SWEEP.append(W.Workload(f"causal-kvlen-sparse-768-{d}", 2, 2, 768, d, causal=True, kv_len_range=(200, 700),
+                            block_density=0.5))
 SWEEP.append(W.Workload("wide-scores-512-128", 1, 2, 512, 128, causal=True, k_scale=4.0))
 # tile masks: ragged key padding inside visible tiles, rows that see most
 # tiles (the K and V rings wrap several times), and a rescale of O (K x 4
