@@ -146,7 +146,8 @@ __global__ void __launch_bounds__(512, 1)
     uint64_t* dq_free = dq_full + 1;
     uint64_t* dkv_done = dq_free + 1;
     uint64_t* drain = dkv_done + 1;
-    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
+    uint64_t* dk_done = drain + 1;  // (kDqFirst) dK_j += dS^T Q_i of a block complete
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(dk_done + 1);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
     const WaitCtx cx{abort_flag, p.status};
 
@@ -237,6 +238,11 @@ __global__ void __launch_bounds__(512, 1)
     // (+1.5-2.6 %) kernels were measured slower that way and keep one barrier
     // per stage.
     constexpr bool kSplitStage = !TMASK && !VARLEN && !DROPOUT && D == 128;
+    // The same kernel issues dQ_i before dK_i, so that the drain starts one
+    // GEMM earlier: it stages the first half of dQ_i in the dO_i tile (free
+    // once dV is complete) and the second half in the Q_i tile only after dK_i,
+    // which reads Q_i, is complete; and the next dS^T waits for dK_i.
+    constexpr bool kDqFirst = kSplitStage;
     auto load_stage = [&](int i, int st) {
         if constexpr (kSplitStage) {
             mbar_arrive_expect_tx(&qd_full[st], C::TILE_BYTES + 512);
@@ -295,6 +301,7 @@ __global__ void __launch_bounds__(512, 1)
         mbar_init(dq_full, 1);
         mbar_init(dq_free, 128);
         mbar_init(dkv_done, 1);
+        mbar_init(dk_done, 1);
         mbar_init(drain, 1);
         fence_barrier_init();
         // K, V and the first visible query block's stage are requested before
@@ -418,17 +425,30 @@ __global__ void __launch_bounds__(512, 1)
                 // dK_j += dS^T Q_i ; dQ_i = dS K_j
                 if (!(ok = mbar_wait_warp(ds_ready, u & 1, cx, 16))) break;
                 tc_fence_after();
+                auto issue_dk = [&]() {
 #pragma unroll
-                for (int kk = 0; kk < 8; ++kk) {
-                    const uint32_t off = (kk / 4) * 16384 + (kk % 4) * 32;
-                    umma_ss<false>(leader, tm + C::COL_DK, sdesc_advance(dS_k, off), sdesc_advance(dQ_mn, kk * 2048), C::ID_KN,
-                                   (u > 0 || kk > 0) ? 1u : 0u);
+                    for (int kk = 0; kk < 8; ++kk) {
+                        const uint32_t off = (kk / 4) * 16384 + (kk % 4) * 32;
+                        umma_ss<false>(leader, tm + C::COL_DK, sdesc_advance(dS_k, off), sdesc_advance(dQ_mn, kk * 2048),
+                                       C::ID_KN, (u > 0 || kk > 0) ? 1u : 0u);
+                    }
+                };
+                auto issue_dq = [&]() {
+#pragma unroll
+                    for (int kk = 0; kk < 8; ++kk)
+                        umma_ss<false>(leader, tm + col_s, sdesc_advance(dS_mn, kk * 2048), sdesc_advance(dK_mn, kk * 2048),
+                                       C::ID_DQ, kk > 0 ? 1u : 0u);
+                };
+                if constexpr (kDqFirst) {
+                    issue_dq();
+                    umma_commit(leader, dq_full);
+                    issue_dk();
+                    umma_commit(leader, dk_done);
+                } else {
+                    issue_dk();
+                    issue_dq();
+                    umma_commit(leader, dq_full);
                 }
-#pragma unroll
-                for (int kk = 0; kk < 8; ++kk)
-                    umma_ss<false>(leader, tm + col_s, sdesc_advance(dS_mn, kk * 2048), sdesc_advance(dK_mn, kk * 2048),
-                                   C::ID_DQ, kk > 0 ? 1u : 0u);
-                umma_commit(leader, dq_full);
                 ++u;
             }
             if (ok && u > 0) umma_commit(leader, dkv_done);
@@ -547,7 +567,7 @@ __global__ void __launch_bounds__(512, 1)
             // to the drain), so each half is stored as soon as it is formed.
             ok = __all_sync(0xffffffffu, mbar_wait(dp_full, u & 1, cx, 19) &&
                                              (!kSplitStage || mbar_wait(&do_full[st], ph, cx, 24)));
-            if (ok && u > 0) ok = __all_sync(0xffffffffu, mbar_wait(dq_full, (u - 1) & 1, cx, 20));
+            if (ok && u > 0) ok = __all_sync(0xffffffffu, mbar_wait(kDqFirst ? dk_done : dq_full, (u - 1) & 1, cx, 20));
             if (!ok) break;
             tc_fence_after();
 #pragma unroll
@@ -694,6 +714,11 @@ __global__ void __launch_bounds__(512, 1)
             uint8_t* box_do = sm + C::DO_OFF + st * C::TILE_BYTES + wq * (NBH * 4096);
 #pragma unroll
             for (int half = 0; half < D / 64; ++half) {
+                if (kDqFirst && half == 1) {
+                    // the second half goes to the Q_i tile, which dK_i reads
+                    ok = __all_sync(0xffffffffu, mbar_wait(dk_done, u & 1, cx, 25));
+                    if (!ok) break;
+                }
                 uint32_t v[2][32];
                 const uint32_t col_q = (u & 1) ? 128u : 0u;  // dQ_u shares the buffer of S^T_u
                 tmem_ld32(tl + col_q + half * 64, v[0]);
@@ -708,7 +733,8 @@ __global__ void __launch_bounds__(512, 1)
 #pragma unroll
                 for (int bx = 0; bx < 2; ++bx) {
                     const int k = half * 2 + bx;
-                    uint8_t* box = k < NBH ? box_q + k * 4096 : box_do + (k - NBH) * 4096;
+                    uint8_t* box = kDqFirst ? (half == 1 ? box_q : box_do) + bx * 4096
+                                            : (k < NBH ? box_q + k * 4096 : box_do + (k - NBH) * 4096);
                     const uint32_t sb = smem_u32(box);
 #pragma unroll
                     for (int c = 0; c < 8; ++c) {
@@ -722,7 +748,8 @@ __global__ void __launch_bounds__(512, 1)
 #pragma unroll
                     for (int bx = 0; bx < 2; ++bx) {
                         const int k = half * 2 + bx;
-                        const uint8_t* box = k < NBH ? box_q + k * 4096 : box_do + (k - NBH) * 4096;
+                        const uint8_t* box = kDqFirst ? (half == 1 ? box_q : box_do) + bx * 4096
+                                                      : (k < NBH ? box_q + k * 4096 : box_do + (k - NBH) * 4096);
                         if (varlen)
                             tma_reduce_add_3d(&tmdQacc, k * 32, h, seq0 + i * kTile + wq * 32, box);
                         else
@@ -731,6 +758,7 @@ __global__ void __launch_bounds__(512, 1)
                     bulk_commit_group();
                 }
             }
+            if (kDqFirst && !ok) break;  // gave up waiting for dK_i (the reduce-adds in flight land below)
             if (lane == 0) {
                 // the stage may be refilled once the reduce-adds have read it
                 bulk_wait_group_read0();
