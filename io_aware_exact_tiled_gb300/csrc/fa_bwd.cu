@@ -137,8 +137,7 @@ __global__ void __launch_bounds__(512, 1)
     uint64_t* kv_full = bars + 0;
     uint64_t* qd_full = bars + 1;                 // [STAGES]
     uint64_t* qd_empty = qd_full + C::STAGES;     // [STAGES]
-    uint64_t* do_full = qd_empty + C::STAGES;     // [STAGES] (kSplitStage)
-    uint64_t* s_full = do_full + C::STAGES;
+    uint64_t* s_full = qd_empty + C::STAGES;
     uint64_t* dp_full = s_full + 1;
     uint64_t* p_ready = dp_full + 1;
     uint64_t* ds_ready = p_ready + 1;
@@ -146,9 +145,12 @@ __global__ void __launch_bounds__(512, 1)
     uint64_t* dq_free = dq_full + 1;
     uint64_t* dkv_done = dq_free + 1;
     uint64_t* drain = dkv_done + 1;
-    uint64_t* dk_done = drain + 1;  // (kDqFirst) dK_j += dS^T Q_i of a block complete
-    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(dk_done + 1);
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+    // barriers of the plain d = 128 kernel only (kSplitStage, kDqFirst), after
+    // the others so that every instance keeps the same layout for those
+    uint64_t* do_full = reinterpret_cast<uint64_t*>(tmem_slot + 2);  // [STAGES] dO_i and -D of a stage landed
+    uint64_t* dk_done = do_full + C::STAGES;                          // dK_j += dS^T Q_i of a block complete
     const WaitCtx cx{abort_flag, p.status};
 
     // Head-major order: the key blocks of one head are adjacent in the grid
@@ -293,7 +295,7 @@ __global__ void __launch_bounds__(512, 1)
         mbar_init(kv_full, 1);
         for (int s = 0; s < C::STAGES; ++s) {
             mbar_init(&qd_full[s], 1);
-            mbar_init(&do_full[s], 1);
+            if constexpr (kSplitStage) mbar_init(&do_full[s], 1);
             mbar_init(&qd_empty[s], 4);  // the four dQ drain warps, done staging through it
         }
         mbar_init(s_full, 1);
@@ -303,7 +305,7 @@ __global__ void __launch_bounds__(512, 1)
         mbar_init(dq_full, 1);
         mbar_init(dq_free, 128);
         mbar_init(dkv_done, 1);
-        mbar_init(dk_done, 1);
+        if constexpr (kDqFirst) mbar_init(dk_done, 1);
         mbar_init(drain, 1);
         fence_barrier_init();
         // K, V and the first visible query block's stage are requested before
@@ -427,28 +429,30 @@ __global__ void __launch_bounds__(512, 1)
                 // dK_j += dS^T Q_i ; dQ_i = dS K_j
                 if (!(ok = mbar_wait_warp(ds_ready, u & 1, cx, 16))) break;
                 tc_fence_after();
-                auto issue_dk = [&]() {
+                if constexpr (kDqFirst) {
+#pragma unroll
+                    for (int kk = 0; kk < 8; ++kk)
+                        umma_ss<false>(leader, tm + col_s, sdesc_advance(dS_mn, kk * 2048), sdesc_advance(dK_mn, kk * 2048),
+                                       C::ID_DQ, kk > 0 ? 1u : 0u);
+                    umma_commit(leader, dq_full);
 #pragma unroll
                     for (int kk = 0; kk < 8; ++kk) {
                         const uint32_t off = (kk / 4) * 16384 + (kk % 4) * 32;
                         umma_ss<false>(leader, tm + C::COL_DK, sdesc_advance(dS_k, off), sdesc_advance(dQ_mn, kk * 2048),
                                        C::ID_KN, (u > 0 || kk > 0) ? 1u : 0u);
                     }
-                };
-                auto issue_dq = [&]() {
+                    umma_commit(leader, dk_done);
+                } else {
+#pragma unroll
+                    for (int kk = 0; kk < 8; ++kk) {
+                        const uint32_t off = (kk / 4) * 16384 + (kk % 4) * 32;
+                        umma_ss<false>(leader, tm + C::COL_DK, sdesc_advance(dS_k, off), sdesc_advance(dQ_mn, kk * 2048), C::ID_KN,
+                                       (u > 0 || kk > 0) ? 1u : 0u);
+                    }
 #pragma unroll
                     for (int kk = 0; kk < 8; ++kk)
                         umma_ss<false>(leader, tm + col_s, sdesc_advance(dS_mn, kk * 2048), sdesc_advance(dK_mn, kk * 2048),
                                        C::ID_DQ, kk > 0 ? 1u : 0u);
-                };
-                if constexpr (kDqFirst) {
-                    issue_dq();
-                    umma_commit(leader, dq_full);
-                    issue_dk();
-                    umma_commit(leader, dk_done);
-                } else {
-                    issue_dk();
-                    issue_dq();
                     umma_commit(leader, dq_full);
                 }
                 ++u;
