@@ -247,6 +247,10 @@ __global__ void __launch_bounds__(512, 1)
     // dS^T waits for dK_i (3 % faster plain, 1.2 % with dropout; the packed
     // kernel is unchanged by it and the tile-masked one 6 % slower).
     constexpr bool kDqFirst = D == 128 && !TMASK && !VARLEN;
+    // The tile-masked kernel writes dK_j and dV_j out of their shared staging
+    // with coalesced stores instead of bulk tensor stores (2 % faster there;
+    // the other instances were as fast or slower that way).
+    constexpr bool kDirectEpi = TMASK;
     auto load_stage = [&](int i, int st) {
         if constexpr (kSplitStage) {
             mbar_arrive_expect_tx(&qd_full[st], C::TILE_BYTES + 512);
@@ -637,8 +641,9 @@ __global__ void __launch_bounds__(512, 1)
             // A warp whose 32 keys all lie in the sequence stages its rows in
             // the V (dV) or K (dK) tile buffer, free once every GEMM is
             // complete, as [32 x 64] swizzled boxes, and writes them with one
-            // bulk tensor store per box; other warps (and a key tile that saw
-            // no query tile) store their valid rows directly.
+            // bulk tensor store per box (kDirectEpi: with coalesced stores of
+            // its own); other warps (and a key tile that saw no query tile)
+            // store their valid rows directly.
             const int wkey0 = j * kTile + (warp & 3) * 32;
             const bool tma_rows = u > 0 && wkey0 + 32 <= N;
             uint8_t* ob = sm + (g == 0 ? C::V_OFF : C::K_OFF) + (warp & 3) * (C::NREG * 4096);
@@ -678,7 +683,24 @@ __global__ void __launch_bounds__(512, 1)
                     }
                 }
             }
-            if (tma_rows) {
+            if (kDirectEpi && tma_rows) {
+                // the warp copies its boxes out itself, four full 128-byte
+                // rows per store instruction, instead of queueing bulk tensor
+                // stores behind the last block's dQ reduce-adds in the SM's
+                // bulk-copy unit (which drain at the L2 reduction rate)
+                __syncwarp();
+                uint16_t* obase = static_cast<uint16_t*>(g == 0 ? p.dv : p.dk);
+#pragma unroll
+                for (int rg = 0; rg < C::NREG; ++rg)
+#pragma unroll
+                    for (int it = 0; it < 8; ++it) {
+                        const int row = it * 4 + (lane >> 3), ch = lane & 7;
+                        const uint4 w = lds128_u4(smem_u32(ob + rg * 4096 + row * 128 + ((ch ^ (row & 7)) << 4)));
+                        const size_t grow_ = varlen ? (static_cast<size_t>(seq0 + wkey0 + row) * p.H + h) * D
+                                                    : (static_cast<size_t>(bh) * N + wkey0 + row) * D;
+                        *reinterpret_cast<uint4*>(obase + grow_ + rg * 64 + ch * 8) = w;
+                    }
+            } else if (tma_rows) {
                 fence_proxy_async_smem();
                 __syncwarp();
                 if (lane == 0) {
