@@ -195,7 +195,8 @@ class ClockSampler:
 
 # ------------------------------------------------------------------ helpers
 # source files each profiled kernel is compiled from (its .cu plus the shared
-# headers); a recorded DRAM-traffic figure stays valid while they are unchanged
+# headers); a recorded DRAM-traffic figure stays valid while their code (the
+# text without `//` comments and blank lines) is unchanged
 KERNEL_SOURCES = {
     "fa_fwd_kernel": ["fa_fwd.cu"],
     "fa_fwd_fp8_kernel": ["fa_fwd_fp8.cu", "fa_fp8.h"],
@@ -211,7 +212,11 @@ def kernel_source_sha(kernel: str):
     csrc = os.path.join(ROOT, "io_aware_exact_tiled_gb300", "csrc")
     for f in sorted(KERNEL_SOURCES.get(kernel, []) + SHARED_HEADERS):
         h.update(f.encode())
-        h.update(open(os.path.join(csrc, f), "rb").read())
+        with open(os.path.join(csrc, f), encoding="utf-8") as fh:
+            for line in fh:
+                code = line.split("//", 1)[0].rstrip()
+                if code:
+                    h.update(code.encode() + b"\n")
     return h.hexdigest()[:16]
 
 

@@ -20,7 +20,9 @@
 //                       GEMMs per tile with dK_j and dV_j accumulated in TMEM;
 //                       dQ_i = dS K_j is added into the fp32 accumulator with
 //                       TMA bulk reduce-adds staged through shared memory;
-//                       dK_j, dV_j leave through TMA stores at the end
+//                       dK_j, dV_j are staged in shared memory at the end and
+//                       leave through TMA stores (coalesced stores in the
+//                       tile-masked instance)
 //   fa_bwd_dq_kernel    fp32 dQ accumulator -> dQ in bf16
 //
 // TMEM columns of fa_bwd_kernel: two 128-column buffers in [0, 256) that
@@ -106,7 +108,8 @@ constexpr float kLog2e = 1.4426950408889634f;
 //   S^T  = K_j Q_i^T   (into the buffer that held dP^T of the previous block)
 //   dP^T = V_j dO_i^T  (after the drain has read dQ_{i-1} out of its buffer)
 //   dV  += P^T dO_i    (P^T from TMEM, written by the compute groups)
-//   dK  += dS^T Q_i, dQ_i = dS K_j  (dS^T from shared memory)
+//   dK  += dS^T Q_i, dQ_i = dS K_j  (dS^T from shared memory; the d = 128
+//                      kernels without tile mask or packing issue dQ_i first)
 // VARLEN: packed variable-length batch; a separate instantiation so that the
 // [B, H, N, d] kernel carries none of its branches.
 // DROPOUT: the keep mask of the forward pass is regenerated (fa_philox.cuh);
