@@ -84,7 +84,7 @@ __device__ __forceinline__ uint64_t f2_sub(uint64_t a, uint64_t b) {
 constexpr int kPrepThreads = 128;
 constexpr int kPrepBlockBytes = kTile * kD8 * 2;  // 128 rows of bf16
 constexpr int kPrepCtasPerSm = 3;
-constexpr int kPrepSmem = 2 * kPrepBlockBytes + 1024 + 64;  // two buffers, alignment, two mbarriers, abort flag
+constexpr int kPrepSmem = 2 * kPrepBlockBytes + 1024 + 64;  // two buffers, alignment, four mbarriers, abort flag
 
 template <bool ROT>
 __global__ void __launch_bounds__(kPrepThreads, kPrepCtasPerSm)
@@ -97,8 +97,9 @@ __global__ void __launch_bounds__(kPrepThreads, kPrepCtasPerSm)
     uint8_t* sm = prep_raw + ((1024u - (smem_u32(prep_raw) & 1023u)) & 1023u);
     __shared__ float wmax[kPrepThreads / 32];
     __shared__ __align__(16) float sg_sh[kD8];
-    uint64_t* full = reinterpret_cast<uint64_t*>(sm + 2 * kPrepBlockBytes);  // [2]
-    volatile int* abort_flag = reinterpret_cast<volatile int*>(full + 2);
+    uint64_t* full = reinterpret_cast<uint64_t*>(sm + 2 * kPrepBlockBytes);  // [2] copy landed
+    uint64_t* empty = full + 2;                                                 // [2] every thread has read it
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(full + 4);
     const WaitCtx cx{abort_flag, status};
     const int T = N / kTile;
     const int per_tensor = T * BH;
@@ -121,6 +122,8 @@ __global__ void __launch_bounds__(kPrepThreads, kPrepCtasPerSm)
         *abort_flag = 0;
         mbar_init(&full[0], 1);
         mbar_init(&full[1], 1);
+        mbar_init(&empty[0], kPrepThreads);
+        mbar_init(&empty[1], kPrepThreads);
         fence_barrier_init();
     }
     if (ROT) sg_sh[r] = signs[r];
@@ -140,9 +143,10 @@ __global__ void __launch_bounds__(kPrepThreads, kPrepCtasPerSm)
         }
     }
     int it = 0;
+    bool refill_ok = true;
     for (int j = blockIdx.x; j < nblocks; j += gridDim.x, ++it) {
         const int buf = it & 1;
-        if (!__syncthreads_and(mbar_wait(&full[buf], (it >> 1) & 1, cx, 31))) break;
+        if (!__syncthreads_and(refill_ok && mbar_wait(&full[buf], (it >> 1) & 1, cx, 31))) break;
         if (r == 0) issued &= ~(1u << buf);
         // this thread's row: 16 chunks of 8 columns (chunk c: columns 8 c ..)
         uint32_t raw[64];
@@ -150,15 +154,29 @@ __global__ void __launch_bounds__(kPrepThreads, kPrepCtasPerSm)
             const uint32_t base = smem_u32(sm + buf * kPrepBlockBytes) + r * 128;
 #pragma unroll
             for (int c = 0; c < 16; ++c) {
-                const uint4 w = lds128_u4(base + (c >> 3) * (kPrepBlockBytes / 2) + (((c & 7) ^ (r & 7)) << 4));
+                uint4 w;  // a shared load the compiler keeps ahead of the release below
+                asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
+                             : "=r"(w.x), "=r"(w.y), "=r"(w.z), "=r"(w.w)
+                             : "r"(base + (c >> 3) * (kPrepBlockBytes / 2) + (((c & 7) ^ (r & 7)) << 4))
+                             : "memory");
                 raw[4 * c] = w.x;
                 raw[4 * c + 1] = w.y;
                 raw[4 * c + 2] = w.z;
                 raw[4 * c + 3] = w.w;
             }
         }
-        __syncthreads();  // buffer read by every thread: request the block after next
-        if (r == 0) {
+        // The refill is a bulk copy, a write by the async proxy: it may start
+        // only once every thread's reads of the buffer have been performed.
+        // A CTA barrier does not order them with it (the values are used only
+        // after the barrier, so loads can still be in flight there, and runs
+        // raced: a few rows of Q8 / K8 changed from call to call); each
+        // thread's arrival on the buffer's "empty" barrier (release
+        // semantics) does, and thread 0 waits for all of them and fences the
+        // proxies before it requests the block after next.
+        mbar_arrive(&empty[buf]);
+        if (r == 0) refill_ok = mbar_wait(&empty[buf], (it >> 1) & 1, cx, 33);
+        if (r == 0 && refill_ok) {
+            fence_proxy_async_smem();
             const int j2 = j + 2 * gridDim.x;
             if (j2 < nblocks) {
                 request(j2, buf);

@@ -37,6 +37,10 @@ def dbg():
     lib.fa_bwd_noalloc.restype = i
     lib.fa_bwd_noalloc_get_status.argtypes = [vp]
     lib.fa_bwd_noalloc_get_status.restype = i
+    lib.fa_fwd_fp8.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, f, i, vp, vp, vp, sz, vp]
+    lib.fa_fwd_fp8.restype = i
+    lib.fa_fwd_fp8_workspace_size.argtypes = [i, i, i, i]
+    lib.fa_fwd_fp8_workspace_size.restype = sz
     return lib
 
 
@@ -94,3 +98,25 @@ def test_bounded_waits_report_timeout(dbg, cuda_device):
     ref = torch.softmax(x, -1) @ v.double().cpu()[0, 0]
     assert (o2.double().cpu()[0, 0] - ref).abs().max().item() < 1e-2
     assert np.isfinite(lse2.cpu().numpy()).all()
+
+
+def test_fp8_forward_reports_timeout(dbg, cuda_device):
+    """The FP8 path (quantisation kernel, then the FP8 attention kernel,
+    whose MMA thread's wait the debug build makes run out): the call reports
+    FA_ERR_TIMEOUT and the regular library's FP8 call works afterwards."""
+    B, H, N, d = 1, 3, 512, 128
+    g = torch.Generator(device="cpu").manual_seed(1)
+    q, k, v = (torch.randn(B, H, N, d, generator=g).to(torch.bfloat16).to(cuda_device) for _ in range(3))
+    signs = (torch.randint(0, 2, (d,), generator=g) * 2 - 1).float().to(cuda_device)
+    o = torch.empty_like(q)
+    lse = torch.empty(B, H, N, dtype=torch.float32, device=cuda_device)
+    ws = torch.empty(dbg.fa_fwd_fp8_workspace_size(B, H, N, d), dtype=torch.uint8, device=cuda_device)
+    s = ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
+    rc = dbg.fa_fwd_fp8(ptr(q), ptr(k), ptr(v), ptr(o), ptr(lse), B, H, N, d, 1.0 / math.sqrt(d), 1, None,
+                        ptr(signs), ptr(ws), ws.numel(), s)
+    assert rc == fb.FA_OK
+    assert dbg.fa_get_status(ptr(ws), s) == fb.FA_ERR_TIMEOUT
+    assert dbg.fa_get_status(ptr(ws), s) == fb.FA_OK
+    o2, lse2 = fb.forward_fp8(q, k, v, signs, scale=1.0 / math.sqrt(d), causal=True)
+    torch.cuda.synchronize()
+    assert torch.isfinite(o2.float()).all() and torch.isfinite(lse2).all()
