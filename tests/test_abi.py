@@ -102,3 +102,48 @@ def test_missing_library_fails_loudly(tmp_path, monkeypatch):
     monkeypatch.setattr(fb, "_lib", None)
     with pytest.raises(RuntimeError, match="missing"):
         fb.load(str(tmp_path / "nope.so"))
+
+
+def test_other_entry_points_reject_bad_arguments_on_the_host(lib):
+    """Every entry point's argument checks run before anything touches the
+    GPU, so they answer here without one."""
+    vp = ctypes.c_void_p
+    P = vp(FAKE)
+    big = 1 << 30
+
+    def fp8(d=128, N=256, signs=FAKE, q=FAKE, wsb=big, causal=0):
+        return lib.fa_fwd_fp8(vp(q), P, P, P, P, 1, 2, N, d, 0.1, causal, None,
+                              None if signs is None else vp(signs), P, wsb, None)
+    assert fp8(q=0) == fb.FA_ERR_INVALID_ARG
+    assert fp8(d=64) == fb.FA_ERR_UNSUPPORTED
+    assert fp8(N=200) == fb.FA_ERR_UNSUPPORTED
+    assert fp8(causal=3) == fb.FA_ERR_INVALID_ARG
+    assert fp8(signs=FAKE + 2) == fb.FA_ERR_INVALID_ARG
+    assert fp8(wsb=1024) == fb.FA_ERR_INVALID_ARG
+
+    def dec(Nq=1, d=128, splits=0, dtype=fb.FA_BF16, wsb=big, scale=0.1):
+        return lib.fa_decode(P, P, P, P, P, 2, 2, Nq, 4096, d, scale, None, splits, dtype, P, wsb, None)
+    assert dec(Nq=9) == fb.FA_ERR_UNSUPPORTED
+    assert dec(d=32) == fb.FA_ERR_UNSUPPORTED
+    assert dec(dtype=fb.FA_FP32) == fb.FA_ERR_UNSUPPORTED
+    assert dec(splits=-1) == fb.FA_ERR_INVALID_ARG
+    assert dec(scale=float("inf")) == fb.FA_ERR_INVALID_ARG
+    assert dec(wsb=64) == fb.FA_ERR_INVALID_ARG
+
+    def vfwd(cu=FAKE, total=1000, max_seqlen=600, d=64, dtype=fb.FA_BF16, wsb=big):
+        return lib.fa_fwd_varlen(P, P, P, P, P, None if cu is None else vp(cu), 3, 2, total, max_seqlen, d, 0.1, 0,
+                                 dtype, P, wsb, None)
+    assert vfwd(cu=None) == fb.FA_ERR_INVALID_ARG
+    assert vfwd(max_seqlen=1001) == fb.FA_ERR_INVALID_ARG
+    assert vfwd(d=96) == fb.FA_ERR_UNSUPPORTED
+    assert vfwd(dtype=fb.FA_FP32) == fb.FA_ERR_UNSUPPORTED
+    assert vfwd(cu=FAKE + 2) == fb.FA_ERR_INVALID_ARG
+    assert vfwd(wsb=16) == fb.FA_ERR_INVALID_ARG
+
+    def dfwd(p=0.1, d=64, N=256):
+        return lib.fa_fwd_dropout(P, P, P, P, P, 1, 1, N, d, 0.1, 0, None, p, 7, P, big, None)
+    assert dfwd(p=1.0) == fb.FA_ERR_INVALID_ARG
+    assert dfwd(p=-0.1) == fb.FA_ERR_INVALID_ARG
+    assert dfwd(p=float("nan")) == fb.FA_ERR_INVALID_ARG
+    assert dfwd(d=80) == fb.FA_ERR_UNSUPPORTED
+    assert dfwd(N=300) == fb.FA_ERR_UNSUPPORTED
