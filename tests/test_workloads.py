@@ -57,3 +57,50 @@ def test_blockmask_recipe():
     off = int(bm.sum()) - T
     assert off == math.floor(0.125 * (T * T - T)) == 2032
     assert not torch.equal(bm, bm.t())
+
+
+def test_packed_recipe():
+    w = W.PACKED_WORKLOADS["bert_packed"]
+    x = W.make_packed_workload(w, seed=3)
+    g = torch.Generator().manual_seed(3)
+    lens = torch.randint(256, 513, (w.B,), generator=g).tolist()
+    assert x.lens == lens and all(256 <= n <= 512 for n in lens)
+    total = sum(lens)
+    assert x.q.shape == (total, w.H, w.d) and x.q.dtype == torch.bfloat16
+    assert x.cu_seqlens.dtype == torch.int32 and x.cu_seqlens.shape == (w.B + 1,)
+    assert int(x.cu_seqlens[0]) == 0 and int(x.cu_seqlens[-1]) == total
+    assert torch.equal(x.cu_seqlens[1:] - x.cu_seqlens[:-1], torch.tensor(lens, dtype=torch.int32))
+    assert x.max_seqlen == max(lens) and x.scale == 1.0 / math.sqrt(w.d) and not x.causal
+    # Q, K, V, dO drawn in that order from one generator seeded with the same seed
+    g = torch.Generator().manual_seed(3)
+    q = torch.randn(total, w.H, w.d, generator=g)
+    k = torch.randn(total, w.H, w.d, generator=g)
+    v = torch.randn(total, w.H, w.d, generator=g)
+    assert torch.equal(x.q, q.to(torch.bfloat16)) and torch.equal(x.k, k.to(torch.bfloat16))
+    assert torch.equal(x.v, v.to(torch.bfloat16))
+    y = W.make_packed_workload(w, seed=3)
+    assert torch.equal(x.do, y.do) and y.lens == x.lens
+    assert W.make_packed_workload(w, seed=4).lens != x.lens
+    assert W.PACKED_WORKLOADS["mix8k_packed"].causal
+
+
+def test_packed_empty_and_zero_length_sequences():
+    x = W.make_packed([0, 5, 0, 3], H=2, d=64)
+    assert x.cu_seqlens.tolist() == [0, 0, 5, 5, 8] and x.q.shape == (8, 2, 64)
+    assert x.max_seqlen == 5
+    e = W.make_packed([], H=2, d=64)
+    assert e.q.shape == (0, 2, 64) and e.cu_seqlens.tolist() == [0] and e.max_seqlen == 0
+
+
+def test_decode_recipe():
+    x = W.make_decode(B=3, H=2, Nq=1, Nk=256, d=128, len_range=(100, 256), seed=5)
+    assert x.q.shape == (3, 2, 1, 128) and x.k.shape == (3, 2, 256, 128) == x.v.shape
+    assert x.q.dtype == x.k.dtype == torch.bfloat16
+    expect = torch.randint(100, 257, (3,), generator=torch.Generator().manual_seed(6)).to(torch.int32)
+    assert torch.equal(x.cache_len, expect) and x.cache_len.dtype == torch.int32
+    g = torch.Generator().manual_seed(5)
+    q = torch.randn(3, 2, 1, 128, generator=g)
+    k = torch.randn(3, 2, 256, 128, generator=g)
+    assert torch.equal(x.q, q.to(torch.bfloat16)) and torch.equal(x.k, k.to(torch.bfloat16))
+    w = W.DECODE_WORKLOADS["decode16k"]
+    assert (w.Nq, w.Nk, w.d) == (1, 16384, 128) and w.len_range[1] <= w.Nk
