@@ -44,6 +44,9 @@
  *   after a call returns. The one exception is fa_bwd_noalloc (and its status
  *   reader), which uses a fixed device array inside the library and caches
  *   its address per device; its own comment below gives the rules.
+ * Device: kernels run on the calling thread's current CUDA device
+ *   (cudaGetDevice); every buffer must be memory of that device and `stream`
+ *   one of its streams. Buffers of another device are not detected here.
  * Streams: `stream` is a cudaStream_t (NULL = legacy default stream). Calls
  *   are asynchronous with respect to the host: argument checks run on the host
  *   and return an error before anything is launched; launch failures return

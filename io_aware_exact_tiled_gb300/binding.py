@@ -81,6 +81,10 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.fa_last_launch_count.restype = i
     lib.fa_set_timing_events.argtypes = [vp, vp]
     lib.fa_set_timing_events.restype = i
+    lib.fa_bwd_noalloc.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, i, i, i, i, f, i, vp, vp, i, vp]
+    lib.fa_bwd_noalloc.restype = i
+    lib.fa_bwd_noalloc_get_status.argtypes = [vp]
+    lib.fa_bwd_noalloc_get_status.restype = i
     _lib = lib
     return lib
 
@@ -105,11 +109,50 @@ def _stream_handle(stream: Optional[torch.cuda.Stream]):
     return ctypes.c_void_p(s.cuda_stream)
 
 
+def _check_device(q: torch.Tensor):
+    """The kernels run on the current CUDA device: q must live there."""
+    if q.device.type != "cuda":
+        raise ValueError("tensors must be on a CUDA device")
+    if q.device.index != torch.cuda.current_device():
+        raise ValueError(f"tensors are on {q.device} but the current device is cuda:{torch.cuda.current_device()}:"
+                         " call under torch.cuda.device(q.device)")
+
+
+def _in(t: torch.Tensor, shape, dtype, device, name: str) -> torch.Tensor:
+    """Check a buffer the kernels read or write as exactly `shape` contiguous
+    elements of `dtype` on `device` (the library cannot see its size)."""
+    if t.dtype != dtype or tuple(t.shape) != tuple(shape) or t.device != device or not t.is_contiguous():
+        raise ValueError(f"{name} must be a contiguous {dtype} {list(shape)} tensor on {device}")
+    return t
+
+
+def _out(t: Optional[torch.Tensor], shape, dtype, device, name: str) -> torch.Tensor:
+    """A caller-supplied output, checked as in _in, or a new one."""
+    if t is None:
+        return torch.empty(tuple(shape), dtype=dtype, device=device)
+    return _in(t, shape, dtype, device, name)
+
+
+def _ws(ws: Optional[torch.Tensor], nbytes, device) -> torch.Tensor:
+    """A caller-supplied workspace (on the device, contiguous; its size is
+    checked by the library) or a new one of `nbytes`."""
+    if ws is None:
+        return workspace(nbytes() if callable(nbytes) else nbytes, device)
+    if ws.device != device or not ws.is_contiguous():
+        raise ValueError(f"the workspace must be a contiguous tensor on {device}")
+    return ws
+
+
+def _nbytes(t: torch.Tensor) -> int:
+    return t.numel() * t.element_size()
+
+
 def _check_qkv(*ts: torch.Tensor):
     q = ts[0]
+    _check_device(q)
     for t in ts:
-        if t.device.type != "cuda":
-            raise ValueError("tensors must be on a CUDA device")
+        if t.device != q.device:
+            raise ValueError("tensors must be on the same CUDA device")
         if not t.is_contiguous():
             raise ValueError("tensors must be contiguous [B, H, N, d]")
         if t.shape != q.shape or t.dtype != q.dtype:
@@ -156,13 +199,12 @@ def forward(q, k, v, scale: Optional[float] = None, causal: bool = False, blockm
     dtype = _check_qkv(q, k, v)
     B, H, N, d = q.shape
     scale = 1.0 / math.sqrt(d) if scale is None else float(scale)
-    o = torch.empty_like(q) if out is None else out
-    L = torch.empty((B, H, N), dtype=torch.float32, device=q.device) if lse is None else lse
-    if ws is None:
-        ws = workspace(lib.fa_fwd_workspace_size(B, H, N, d) if dtype == FA_FP32 else 256, q.device)
+    o = _out(out, q.shape, q.dtype, q.device, "out")
+    L = _out(lse, (B, H, N), torch.float32, q.device, "lse")
+    ws = _ws(ws, lambda: lib.fa_fwd_workspace_size(B, H, N, d) if dtype == FA_FP32 else 256, q.device)
     bm, kl = _mask_ptrs(blockmask, kv_len, q)
     rc = lib.fa_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(L), B, H, N, d, scale, int(bool(causal)), bm, kl,
-                    dtype, _ptr(ws), ws.numel(), _stream_handle(stream))
+                    dtype, _ptr(ws), _nbytes(ws), _stream_handle(stream))
     if rc != FA_OK:
         raise FAError(rc, "fa_fwd")
     return o, L
@@ -170,9 +212,10 @@ def forward(q, k, v, scale: Optional[float] = None, causal: bool = False, blockm
 
 def _check_packed(cu_seqlens, *ts: torch.Tensor):
     q = ts[0]
+    _check_device(q)
     for t in ts:
-        if t.device.type != "cuda":
-            raise ValueError("tensors must be on a CUDA device")
+        if t.device != q.device:
+            raise ValueError("tensors must be on the same CUDA device")
         if not t.is_contiguous() or t.dim() != 3:
             raise ValueError("packed tensors must be contiguous [total, H, d]")
         if t.shape != q.shape or t.dtype != q.dtype:
@@ -195,12 +238,11 @@ def forward_varlen(q, k, v, cu_seqlens, max_seqlen: int, scale: Optional[float] 
     total, H, d = q.shape
     B = cu_seqlens.numel() - 1
     scale = 1.0 / math.sqrt(d) if scale is None else float(scale)
-    o = torch.empty_like(q) if out is None else out
-    L = torch.empty((H, total), dtype=torch.float32, device=q.device) if lse is None else lse
-    if ws is None:
-        ws = workspace(lib.fa_fwd_varlen_workspace_size(H, total, d), q.device)
+    o = _out(out, q.shape, q.dtype, q.device, "out")
+    L = _out(lse, (H, total), torch.float32, q.device, "lse")
+    ws = _ws(ws, lambda: lib.fa_fwd_varlen_workspace_size(H, total, d), q.device)
     rc = lib.fa_fwd_varlen(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(L), _ptr(cu_seqlens), B, H, total,
-                           int(max_seqlen), d, scale, int(bool(causal)), dtype, _ptr(ws), ws.numel(),
+                           int(max_seqlen), d, scale, int(bool(causal)), dtype, _ptr(ws), _nbytes(ws),
                            _stream_handle(stream))
     if rc != FA_OK:
         raise FAError(rc, "fa_fwd_varlen")
@@ -215,17 +257,15 @@ def backward_varlen(q, k, v, o, lse, do, cu_seqlens, max_seqlen: int, scale: Opt
     dtype = _check_packed(cu_seqlens, q, k, v, o, do)
     total, H, d = q.shape
     B = cu_seqlens.numel() - 1
-    if lse.dtype != torch.float32 or lse.shape != (H, total) or not lse.is_contiguous():
-        raise ValueError("lse must be a contiguous float32 [H, total] tensor")
+    _in(lse, (H, total), torch.float32, q.device, "lse")
     scale = 1.0 / math.sqrt(d) if scale is None else float(scale)
-    dq = torch.empty_like(q) if dq is None else dq
-    dk = torch.empty_like(k) if dk is None else dk
-    dv = torch.empty_like(v) if dv is None else dv
-    if ws is None:
-        ws = workspace(lib.fa_bwd_varlen_workspace_size(B, H, total, d), q.device)
+    dq = _out(dq, q.shape, q.dtype, q.device, "dq")
+    dk = _out(dk, q.shape, q.dtype, q.device, "dk")
+    dv = _out(dv, q.shape, q.dtype, q.device, "dv")
+    ws = _ws(ws, lambda: lib.fa_bwd_varlen_workspace_size(B, H, total, d), q.device)
     rc = lib.fa_bwd_varlen(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), _ptr(do), _ptr(dq), _ptr(dk), _ptr(dv),
                            _ptr(cu_seqlens), B, H, total, int(max_seqlen), d, scale, int(bool(causal)), dtype,
-                           _ptr(ws), ws.numel(), _stream_handle(stream))
+                           _ptr(ws), _nbytes(ws), _stream_handle(stream))
     if rc != FA_OK:
         raise FAError(rc, "fa_bwd_varlen")
     return dq, dk, dv
@@ -245,13 +285,12 @@ def forward_fp8(q, k, v, signs, scale: Optional[float] = None, causal: bool = Fa
     if signs is not None and (signs.dtype != torch.float32 or signs.shape != (d,) or signs.device != q.device):
         raise ValueError("signs must be None or a float32 [d] tensor on the same device")
     scale = 1.0 / math.sqrt(d) if scale is None else float(scale)
-    o = torch.empty_like(q) if out is None else out
-    L = torch.empty((B, H, N), dtype=torch.float32, device=q.device) if lse is None else lse
-    if ws is None:
-        ws = workspace(lib.fa_fwd_fp8_workspace_size(B, H, N, d), q.device)
+    o = _out(out, q.shape, q.dtype, q.device, "out")
+    L = _out(lse, (B, H, N), torch.float32, q.device, "lse")
+    ws = _ws(ws, lambda: lib.fa_fwd_fp8_workspace_size(B, H, N, d), q.device)
     _, kl = _mask_ptrs(None, kv_len, q)
     rc = lib.fa_fwd_fp8(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(L), B, H, N, d, scale, int(bool(causal)), kl,
-                        _ptr(signs), _ptr(ws), ws.numel(), _stream_handle(stream))
+                        _ptr(signs), _ptr(ws), _nbytes(ws), _stream_handle(stream))
     if rc != FA_OK:
         raise FAError(rc, "fa_fwd_fp8")
     return o, L
@@ -266,13 +305,12 @@ def forward_dropout(q, k, v, dropout_p: float, seed: int, scale: Optional[float]
         raise ValueError("dropout takes bfloat16 inputs")
     B, H, N, d = q.shape
     scale = 1.0 / math.sqrt(d) if scale is None else float(scale)
-    o = torch.empty_like(q) if out is None else out
-    L = torch.empty((B, H, N), dtype=torch.float32, device=q.device) if lse is None else lse
-    if ws is None:
-        ws = workspace(256, q.device)
+    o = _out(out, q.shape, q.dtype, q.device, "out")
+    L = _out(lse, (B, H, N), torch.float32, q.device, "lse")
+    ws = _ws(ws, 256, q.device)
     _, kl = _mask_ptrs(None, kv_len, q)
     rc = lib.fa_fwd_dropout(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(L), B, H, N, d, scale, int(bool(causal)), kl,
-                            float(dropout_p), int(seed) & 0xFFFFFFFFFFFFFFFF, _ptr(ws), ws.numel(),
+                            float(dropout_p), int(seed) & 0xFFFFFFFFFFFFFFFF, _ptr(ws), _nbytes(ws),
                             _stream_handle(stream))
     if rc != FA_OK:
         raise FAError(rc, "fa_fwd_dropout")
@@ -286,16 +324,16 @@ def backward_dropout(q, k, v, o, lse, do, dropout_p: float, seed: int, scale: Op
     if _check_qkv(q, k, v, o, do) != FA_BF16:
         raise ValueError("dropout takes bfloat16 inputs")
     B, H, N, d = q.shape
+    _in(lse, (B, H, N), torch.float32, q.device, "lse")
     scale = 1.0 / math.sqrt(d) if scale is None else float(scale)
-    dq = torch.empty_like(q) if dq is None else dq
-    dk = torch.empty_like(k) if dk is None else dk
-    dv = torch.empty_like(v) if dv is None else dv
-    if ws is None:
-        ws = workspace(lib.fa_bwd_workspace_size(B, H, N, d), q.device)
+    dq = _out(dq, q.shape, q.dtype, q.device, "dq")
+    dk = _out(dk, q.shape, q.dtype, q.device, "dk")
+    dv = _out(dv, q.shape, q.dtype, q.device, "dv")
+    ws = _ws(ws, lambda: lib.fa_bwd_workspace_size(B, H, N, d), q.device)
     _, kl = _mask_ptrs(None, kv_len, q)
     rc = lib.fa_bwd_dropout(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), _ptr(do), _ptr(dq), _ptr(dk), _ptr(dv),
                             B, H, N, d, scale, int(bool(causal)), kl, float(dropout_p),
-                            int(seed) & 0xFFFFFFFFFFFFFFFF, _ptr(ws), ws.numel(), _stream_handle(stream))
+                            int(seed) & 0xFFFFFFFFFFFFFFFF, _ptr(ws), _nbytes(ws), _stream_handle(stream))
     if rc != FA_OK:
         raise FAError(rc, "fa_bwd_dropout")
     return dq, dk, dv
@@ -307,9 +345,10 @@ def decode(q, k_cache, v_cache, cache_len=None, scale: Optional[float] = None, n
     [B, H, Nk, d] bf16 cache, keys split across CTAs and merged. Returns
     (o [B, H, Nq, d], lse fp32 [B, H, Nq])."""
     lib = load()
+    _check_device(q)
     for t in (q, k_cache, v_cache):
-        if t.device.type != "cuda" or not t.is_contiguous() or t.dim() != 4 or t.dtype != torch.bfloat16:
-            raise ValueError("q and the cache must be contiguous bf16 [B, H, N, d] CUDA tensors")
+        if t.device != q.device or not t.is_contiguous() or t.dim() != 4 or t.dtype != torch.bfloat16:
+            raise ValueError("q and the cache must be contiguous bf16 [B, H, N, d] tensors on one CUDA device")
     B, H, Nq, d = q.shape
     if k_cache.shape != v_cache.shape or k_cache.shape[:2] != (B, H) or k_cache.shape[3] != d:
         raise ValueError("the cache must be [B, H, Nk, d] with q's B, H and d")
@@ -318,12 +357,11 @@ def decode(q, k_cache, v_cache, cache_len=None, scale: Optional[float] = None, n
                                   or cache_len.device != q.device):
         raise ValueError("cache_len must be an int32 [B] tensor on the same device")
     scale = 1.0 / math.sqrt(d) if scale is None else float(scale)
-    o = torch.empty_like(q) if out is None else out
-    L = torch.empty((B, H, Nq), dtype=torch.float32, device=q.device) if lse is None else lse
-    if ws is None:
-        ws = workspace(lib.fa_decode_workspace_size(B, H, Nq, Nk, d, num_splits), q.device)
+    o = _out(out, q.shape, q.dtype, q.device, "out")
+    L = _out(lse, (B, H, Nq), torch.float32, q.device, "lse")
+    ws = _ws(ws, lambda: lib.fa_decode_workspace_size(B, H, Nq, Nk, d, num_splits), q.device)
     rc = lib.fa_decode(_ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(o), _ptr(L), B, H, Nq, Nk, d, scale,
-                       _ptr(cache_len), int(num_splits), FA_BF16, _ptr(ws), ws.numel(), _stream_handle(stream))
+                       _ptr(cache_len), int(num_splits), FA_BF16, _ptr(ws), _nbytes(ws), _stream_handle(stream))
     if rc != FA_OK:
         raise FAError(rc, "fa_decode")
     return o, L
@@ -335,17 +373,15 @@ def backward(q, k, v, o, lse, do, scale: Optional[float] = None, causal: bool = 
     lib = load()
     dtype = _check_qkv(q, k, v, o, do)
     B, H, N, d = q.shape
-    if lse.dtype != torch.float32 or lse.shape != (B, H, N) or not lse.is_contiguous():
-        raise ValueError("lse must be a contiguous float32 [B, H, N] tensor")
+    _in(lse, (B, H, N), torch.float32, q.device, "lse")
     scale = 1.0 / math.sqrt(d) if scale is None else float(scale)
-    dq = torch.empty_like(q) if dq is None else dq
-    dk = torch.empty_like(k) if dk is None else dk
-    dv = torch.empty_like(v) if dv is None else dv
-    if ws is None:
-        ws = workspace(lib.fa_bwd_workspace_size(B, H, N, d), q.device)
+    dq = _out(dq, q.shape, q.dtype, q.device, "dq")
+    dk = _out(dk, q.shape, q.dtype, q.device, "dk")
+    dv = _out(dv, q.shape, q.dtype, q.device, "dv")
+    ws = _ws(ws, lambda: lib.fa_bwd_workspace_size(B, H, N, d), q.device)
     bm, kl = _mask_ptrs(blockmask, kv_len, q)
     rc = lib.fa_bwd(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), _ptr(do), _ptr(dq), _ptr(dk), _ptr(dv),
-                    B, H, N, d, scale, int(bool(causal)), bm, kl, dtype, _ptr(ws), ws.numel(),
+                    B, H, N, d, scale, int(bool(causal)), bm, kl, dtype, _ptr(ws), _nbytes(ws),
                     _stream_handle(stream))
     if rc != FA_OK:
         raise FAError(rc, "fa_bwd")
@@ -376,19 +412,14 @@ def backward_noalloc(q, k, v, o, lse, do, scale: Optional[float] = None, causal:
     """dQ, dK, dV = fa_bwd_noalloc(...): the backward pass with the library's
     own fixed scratch instead of a workspace (for callers that cannot allocate
     device memory). Outputs are allocated here only if not passed in."""
-    lib = load()
-    fn = lib.fa_bwd_noalloc
-    vp, i, f = ctypes.c_void_p, ctypes.c_int, ctypes.c_float
-    fn.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, i, i, i, i, f, i, vp, vp, i, vp]
-    fn.restype = i
+    fn = load().fa_bwd_noalloc
     dtype = _check_qkv(q, k, v, o, do)
     B, H, N, d = q.shape
-    if lse.dtype != torch.float32 or lse.shape != (B, H, N) or not lse.is_contiguous():
-        raise ValueError("lse must be a contiguous float32 [B, H, N] tensor")
+    _in(lse, (B, H, N), torch.float32, q.device, "lse")
     scale = 1.0 / math.sqrt(d) if scale is None else float(scale)
-    dq = torch.empty_like(q) if dq is None else dq
-    dk = torch.empty_like(k) if dk is None else dk
-    dv = torch.empty_like(v) if dv is None else dv
+    dq = _out(dq, q.shape, q.dtype, q.device, "dq")
+    dk = _out(dk, q.shape, q.dtype, q.device, "dk")
+    dv = _out(dv, q.shape, q.dtype, q.device, "dv")
     bm, kl = _mask_ptrs(blockmask, kv_len, q)
     rc = fn(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), _ptr(do), _ptr(dq), _ptr(dk), _ptr(dv), B, H, N, d,
             scale, int(bool(causal)), bm, kl, dtype, _stream_handle(stream))
@@ -400,7 +431,4 @@ def backward_noalloc(q, k, v, o, lse, do, scale: Optional[float] = None, causal:
 def noalloc_status(stream=None) -> int:
     """Synchronise and read (then clear) the status word of the last
     fa_bwd_noalloc call on the current device (fa_bwd_noalloc_get_status)."""
-    fn = load().fa_bwd_noalloc_get_status
-    fn.argtypes = [ctypes.c_void_p]
-    fn.restype = ctypes.c_int
-    return fn(_stream_handle(stream))
+    return load().fa_bwd_noalloc_get_status(_stream_handle(stream))
