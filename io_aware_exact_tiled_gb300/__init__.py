@@ -14,6 +14,8 @@ from .binding import (  # noqa: F401
     forward_fp8,
     forward_dropout,
     backward_dropout,
+    backward_noalloc,
+    noalloc_status,
     fwd_workspace_size,
     bwd_workspace_size,
     get_status,
@@ -22,3 +24,6 @@ from .binding import (  # noqa: F401
     set_timing_events,
     workspace,
 )
+from .binding import C_NAMES as _C_NAMES
+
+globals().update(_C_NAMES)  # fa_fwd, fa_bwd, ...: the header's names

@@ -187,6 +187,22 @@ def bwd_workspace_size(B, H, N, d) -> int:
     return load().fa_bwd_workspace_size(B, H, N, d)
 
 
+def fwd_varlen_workspace_size(H, total, d) -> int:
+    return load().fa_fwd_varlen_workspace_size(H, total, d)
+
+
+def bwd_varlen_workspace_size(B, H, total, d) -> int:
+    return load().fa_bwd_varlen_workspace_size(B, H, total, d)
+
+
+def decode_workspace_size(B, H, Nq, Nk, d, num_splits: int = 0) -> int:
+    return load().fa_decode_workspace_size(B, H, Nq, Nk, d, num_splits)
+
+
+def fwd_fp8_workspace_size(B, H, N, d) -> int:
+    return load().fa_fwd_fp8_workspace_size(B, H, N, d)
+
+
 def workspace(nbytes: int, device) -> torch.Tensor:
     """A device buffer usable as workspace (256-byte aligned by the allocator)."""
     return torch.empty(max(256, nbytes), dtype=torch.uint8, device=device)
@@ -432,3 +448,30 @@ def noalloc_status(stream=None) -> int:
     """Synchronise and read (then clear) the status word of the last
     fa_bwd_noalloc call on the current device (fa_bwd_noalloc_get_status)."""
     return load().fa_bwd_noalloc_get_status(_stream_handle(stream))
+
+
+# The names of include/fa.h, bound to the wrappers above (same arguments in
+# tensor form; outputs returned rather than passed as pointers).
+C_NAMES = {
+    "fa_fwd": forward,
+    "fa_bwd": backward,
+    "fa_fwd_workspace_size": fwd_workspace_size,
+    "fa_bwd_workspace_size": bwd_workspace_size,
+    "fa_fwd_varlen": forward_varlen,
+    "fa_bwd_varlen": backward_varlen,
+    "fa_fwd_varlen_workspace_size": fwd_varlen_workspace_size,
+    "fa_bwd_varlen_workspace_size": bwd_varlen_workspace_size,
+    "fa_decode": decode,
+    "fa_decode_workspace_size": decode_workspace_size,
+    "fa_fwd_fp8": forward_fp8,
+    "fa_fwd_fp8_workspace_size": fwd_fp8_workspace_size,
+    "fa_fwd_dropout": forward_dropout,
+    "fa_bwd_dropout": backward_dropout,
+    "fa_bwd_noalloc": backward_noalloc,
+    "fa_bwd_noalloc_get_status": noalloc_status,
+    "fa_get_status": get_status,
+    "fa_status_string": status_string,
+    "fa_last_launch_count": last_launch_count,
+    "fa_set_timing_events": set_timing_events,
+}
+globals().update(C_NAMES)

@@ -201,3 +201,22 @@ def test_ctypes_signatures_match_the_header(monkeypatch):
         expect = [ctypes.c_void_p if t == "ptr" else C_TO_CTYPES[t.replace("const ", "")] for t in params]
         assert list(fn.argtypes) == expect, name
         assert fn.restype == C_TO_CTYPES[ret], name
+
+
+def test_python_names_follow_the_header():
+    import io_aware_exact_tiled_gb300 as pkg
+    declared = fb.declared_functions()
+    assert set(fb.C_NAMES) == set(declared)
+    for name in declared:
+        assert getattr(pkg, name) is fb.C_NAMES[name] and getattr(fb, name) is fb.C_NAMES[name]
+
+
+def test_workspace_size_wrappers(lib):
+    assert fb.fa_decode_workspace_size(2, 4, 1, 1000, 128) == 4096
+    assert last(lib, "fa_decode_workspace_size") == [2, 4, 1, 1000, 128, 0]
+    fb.fa_fwd_varlen_workspace_size(2, 300, 64)
+    assert last(lib, "fa_fwd_varlen_workspace_size") == [2, 300, 64]
+    fb.fa_bwd_varlen_workspace_size(3, 2, 300, 64)
+    assert last(lib, "fa_bwd_varlen_workspace_size") == [3, 2, 300, 64]
+    fb.fa_fwd_fp8_workspace_size(1, 2, 256, 128)
+    assert last(lib, "fa_fwd_fp8_workspace_size") == [1, 2, 256, 128]
