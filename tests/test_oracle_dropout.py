@@ -41,10 +41,24 @@ def test_mask_layout_matches_scalar_restatement():
     b, h, N = 2, 5, 40
     Z = DR.keep_mask(b, h, np.arange(N), N, seed, p)
     t = DR.threshold(p)
-    for i, j in [(0, 0), (3, 7), (5, 2), (17, 33), (39, 39), (12, 0)]:
+    # every element of the first 16 x 16 block (all four row words and key
+    # bytes of 16 generator calls) and the last rows and columns
+    points = [(i, j) for i in range(16) for j in range(16)] + [(i, j) for i in (36, 39) for j in range(24, 40)]
+    for i, j in points:
         words = _scalar_philox((i // 4, j // 4, h, b), (seed & 0xFFFFFFFF, seed >> 32))
         byte = (words[i % 4] >> (8 * (j % 4))) & 0xFF
-        assert Z[i, j] == (byte >= t)
+        assert Z[i, j] == (byte >= t), (i, j)
+
+
+def test_threshold_is_the_nearest_byte_rate():
+    """The reading t = round(256 p): the effective rate t / 256 is the byte
+    rate nearest to p (at most half a step, 1/512, away), for p below the
+    last step."""
+    for p in np.linspace(0.0, 0.99, 397):
+        t = DR.threshold(p)
+        assert isinstance(t, int) and 0 <= t <= 255
+        assert abs(t / 256 - p) <= 1 / 512 + 1e-12, (p, t)
+    assert DR.threshold(0.0) == 0 and DR.threshold(1.0) == 255
 
 
 def test_keep_rate_is_binomial():

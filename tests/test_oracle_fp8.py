@@ -64,6 +64,16 @@ def test_hadamard_and_rotation(d):
     np.testing.assert_allclose((q @ R) @ (k @ R).T, q @ k.T, atol=1e-12)
 
 
+@pytest.mark.parametrize("d", [2, 8, 128])
+def test_hadamard_is_the_sylvester_matrix(d):
+    """Reading 1 names Sylvester's construction: its entry (i, j) is
+    (-1)^popcount(i AND j), a closed form independent of the recursion (and
+    the order of the fast Walsh-Hadamard butterflies)."""
+    i, j = np.meshgrid(np.arange(d), np.arange(d), indexing="ij")
+    odd = np.vectorize(lambda x: bin(int(x)).count("1") & 1)(i & j)
+    np.testing.assert_array_equal(F8.hadamard(d), np.where(odd == 1, -1.0, 1.0))
+
+
 def test_block_scales_are_tight_powers_of_two():
     rng = np.random.default_rng(3)
     x = rng.standard_normal((300, 16)) * np.repeat([0.01, 5.0, 900.0], 100)[:, None]
@@ -199,3 +209,25 @@ def test_online_model_within_the_shift_bound_on_wide_scores():
     assert diff.max() > 1e-3                      # the two roundings do differ
     assert np.all(diff <= bound + 1e-12)
     assert np.median(bound[diff > 0]) < 0.2       # and the bound is informative
+
+
+def test_online_model_rescales_within_the_shift_bound():
+    """Keys whose scores grow tile by tile (K x 1, 4, 8 over three 128-key
+    tiles): most rows see a later tile exceed the reference by more than 7,
+    so the model moves its reference and rescales its sums. O stays within
+    the derived bound of the definition, and L (from the unrounded weights)
+    equals the definition's."""
+    rng = np.random.default_rng(13)
+    B, H, N, d = 1, 1, 384, 16
+    q, k, v = (rng.standard_normal((B, H, N, d)) for _ in range(3))
+    k *= np.repeat([1.0, 4.0, 8.0], 128)[None, None, :, None]
+    scale = 0.17
+    x = scale * (q[0, 0] @ k[0, 0].T) * np.log2(np.e)
+    tmax = x.reshape(N, 3, 128).max(axis=2)
+    moved = (tmax[:, 1] - np.floor(tmax[:, 0]) > 7) | (tmax[:, 2] - np.floor(tmax[:, :2].max(axis=1)) > 7)
+    assert moved.mean() > 0.5
+    O, L = F8.fp8_forward(q, k, v, scale, None, rotate=False)
+    O1, L1 = F8.fp8_forward_online(q, k, v, scale, None, rotate=False)
+    bound = F8.fp8_shift_bound(q, k, v, scale, None, rotate=False)
+    assert np.all(np.abs(O1 - O) <= bound + 1e-12)
+    np.testing.assert_allclose(L1, L, atol=1e-12)
