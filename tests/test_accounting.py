@@ -34,7 +34,7 @@ def test_flop_conventions():
     assert fb == 4 * 128 * 5 * 128 * 128 * 2
 
 
-def test_long_context_flops_match_survey_table():
+def test_long_context_flops_in_gflop():
     # causal N = 4096 and 8192, d = 128, 32 heads
     f4, b4 = acc.flops(1, 32, 4096, 128, causal=True)
     assert abs(f4 / 1e9 - 137.4) < 0.1 and abs(b4 / 1e9 - 343.6) < 0.1
