@@ -49,7 +49,8 @@ def errors(x, g, heads=None, backward=True):
     e["o"] = float(np.abs(g["o"][sel] - o_ref).max())
     lg = g["lse"][sel]
     both_inf = np.isneginf(lg) & np.isneginf(l_ref)
-    e["lse"] = float(np.where(both_inf, 0.0, np.abs(lg - l_ref)).max())
+    with np.errstate(invalid="ignore"):  # -inf - -inf on rows that see no key, replaced by 0
+        e["lse"] = float(np.where(both_inf, 0.0, np.abs(lg - l_ref)).max())
     if backward:
         dq, dk, dv = oracle.backward(x.q, x.k, x.v, x.do, x.scale, **kw)
         e["dq"] = rel(g["dq"][sel], dq[sel])
