@@ -304,7 +304,8 @@ def run_reference(args, rank, world):
         "impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": args.gpus,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * total_t / len(times),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": {"workload": describe(w)},
+        "config": {"workload": describe(w), "B": w.B, "H": w.H, "N": w.N, "d": w.d, "causal": bool(w.causal),
+                   "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
         "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
                          "sample": f"each step: fp64 NumPy forward + backward of the last {R} query rows of head "
                                    f"(0, 0) (N={w.N}, d={w.d}) on the host cores (BLAS threads = all cores; exp "

@@ -24,6 +24,9 @@ def test_reference_arm_prints_one_contract_line():
     assert d["n_gpus"] == 1 and d["steps"] == 1 and d["warmup"] == 3
     assert d["value"] > 0 and d["ms_per_step"] > 0
     assert d["config"]["workload"].startswith("sparse16k")
+    # the same workload keys as the GPU arm's line
+    assert {k: d["config"][k] for k in ("B", "H", "N", "d", "causal", "parallelism")} == \
+        {"B": 2, "H": 16, "N": 16384, "d": 128, "causal": False, "parallelism": "single GPU"}
     assert d["cpu_baseline"]["kind"] == "oracle" and d["cpu_baseline"]["value"] == d["value"]
     assert d["cpu_baseline"]["cores"] >= 1
     assert d["e2e"] == {"value": d["value"], "unit": d["unit"], "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}
