@@ -295,14 +295,17 @@ fa_status fa_get_status(void* workspace, void* stream);
 /* Static, human-readable name of a status code. */
 const char* fa_status_string(fa_status s);
 
-/* Number of kernels the last successful fa_fwd / fa_bwd call launched on
- * this host thread (for accounting in benchmarks). */
+/* Number of kernels that the last successful call made by this host thread
+ * to an entry point that launches work (fa_fwd, fa_bwd, their packed,
+ * decoding, FP8 and dropout forms, fa_bwd_noalloc) launched, for accounting
+ * in benchmarks. */
 int fa_last_launch_count(void);
 
-/* Profiling hook: for the following fa_fwd / fa_bwd calls made by this host
- * thread, record the CUDA event `begin` (a cudaEvent_t) on the call's stream
- * immediately before the main attention kernel and `end` immediately after
- * it, so that a caller can time that kernel alone. Passing NULL for both
+/* Profiling hook: for the following calls made by this host thread to the
+ * entry points that launch work, record the CUDA event `begin` (a
+ * cudaEvent_t) on the call's stream immediately before the main attention
+ * kernel and `end` immediately after it, so that a caller can time that
+ * kernel alone. Passing NULL for both
  * turns the hook off. The events are owned by the caller. Returns
  * FA_ERR_INVALID_ARG if exactly one of them is NULL. */
 fa_status fa_set_timing_events(void* begin, void* end);
