@@ -224,8 +224,9 @@ fa_status fa_bwd_dropout(const void* q, const void* k, const void* v, const void
  *                     the status word, the running tile counts of the
  *                     sequences, -L and -D with every sequence starting on a
  *                     128-row boundary, and the fp32 dQ accumulator
- * Launches five kernels: the tile counts, D = rowsum(dO * O), the fused
- * key-block kernel, and the dQ conversion (plus two memsets).
+ * Launches four kernels: the tile counts, D = rowsum(dO * O), the fused
+ * key-block kernel, and the dQ conversion (plus three memsets: the status
+ * word and the -L and -D blocks).
  */
 size_t fa_bwd_varlen_workspace_size(int B, int H, int total, int d);
 fa_status fa_bwd_varlen(const void* q, const void* k, const void* v, const void* o, const float* lse,
