@@ -147,3 +147,13 @@ def test_other_entry_points_reject_bad_arguments_on_the_host(lib):
     assert dfwd(p=float("nan")) == fb.FA_ERR_INVALID_ARG
     assert dfwd(d=80) == fb.FA_ERR_UNSUPPORTED
     assert dfwd(N=300) == fb.FA_ERR_UNSUPPORTED
+
+
+def test_timing_hook_and_launch_counter_on_the_host(lib):
+    vp = ctypes.c_void_p
+    assert lib.fa_set_timing_events(vp(FAKE), None) == fb.FA_ERR_INVALID_ARG
+    assert lib.fa_set_timing_events(None, vp(FAKE)) == fb.FA_ERR_INVALID_ARG
+    assert lib.fa_set_timing_events(None, None) == fb.FA_OK
+    before = lib.fa_last_launch_count()
+    assert fwd(lib, q=0) == fb.FA_ERR_INVALID_ARG    # a refused call launches nothing and keeps the count
+    assert lib.fa_last_launch_count() == before
